@@ -1,0 +1,360 @@
+// q4k_api.cu -- the C ABI of libq4kmoe (declared in include/q4kmoe.h): host-side
+// validation, workspace layout and kernel sequencing. No compute happens here.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "q4k_internal.cuh"
+
+using namespace q4k;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return Q4K_OK;
+    return fail(Q4K_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by the GEMV-style calls (ferrum-kernels batched GEMV preconditions:
+// k % 256 == 0, n % 4 == 0, top_k > 0, m > 0; top_k bounded by the slot limit of 16 of
+// moeflux's MAX_K / BadK).
+int check_gemv_shape(int num_experts, int m, int top_k, int n, int k) {
+    if (m < 0) return fail(Q4K_ERR_SHAPE, "m must be >= 0 (got %d)", m);
+    if (num_experts < 1) return fail(Q4K_ERR_SHAPE, "num_experts must be >= 1 (got %d)", num_experts);
+    if (num_experts > kMaxExperts) return fail(Q4K_ERR_LIMIT, "num_experts must be <= %d (got %d)", kMaxExperts, num_experts);
+    if (top_k < 1 || top_k > Q4K_MAX_TOP_K) return fail(Q4K_ERR_TOPK, "top_k must be in [1, %d] (got %d)", Q4K_MAX_TOP_K, top_k);
+    if (n < 1 || n % 4 != 0) return fail(Q4K_ERR_SHAPE, "n must be a positive multiple of 4 (got %d)", n);
+    if (k < 1 || k % kQK != 0) return fail(Q4K_ERR_SHAPE, "k must be a positive multiple of 256 (got %d)", k);
+    if (k > kMaxK) return fail(Q4K_ERR_LIMIT, "k must be <= %d (got %d)", kMaxK, k);
+    if ((int64_t)m * top_k > (int64_t)1 << 24) return fail(Q4K_ERR_LIMIT, "m*top_k too large (%lld)", (long long)m * top_k);
+    return Q4K_OK;
+}
+
+size_t ffn_scratch(int m, int top_k, int inter) {
+    return align_up((size_t)m * top_k * inter * sizeof(float));
+}
+
+struct LayerScratch {
+    size_t act, act_shared, eout, shared_out, total;
+};
+
+LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_inter) {
+    LayerScratch s{};
+    size_t off = 0;
+    s.act = off;        off += align_up((size_t)m * top_k * inter * sizeof(float));
+    s.act_shared = off; off += align_up((size_t)m * shared_inter * sizeof(float));
+    s.eout = off;       off += align_up((size_t)m * top_k * hidden * sizeof(float));
+    s.shared_out = off; off += align_up((size_t)m * hidden * sizeof(float));
+    s.total = off;
+    return s;
+}
+
+int check_workspace(void* ws, size_t ws_bytes, size_t need) {
+    if (need == 0) return Q4K_OK;
+    if (!ws) return fail(Q4K_ERR_WORKSPACE, "workspace is NULL but %zu bytes are needed", need);
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return fail(Q4K_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need) return fail(Q4K_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+    return Q4K_OK;
+}
+
+// Gate|up + SwiGLU of the routed experts and (when shared_inter > 0) the shared expert, in
+// one launch; then the down projections of both, in one launch.
+int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const float* h_post, const int32_t* ids,
+                int m, int top_k, int hidden, int inter, float* act, const void* ws_gate, const void* ws_up,
+                int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream) {
+    GemvGroup g[2] = {};
+    int ng = 1;
+    g[0] = GemvGroup{static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), ids, h_post,
+                     hidden, 0, act, num_experts, m, top_k, inter, hidden};
+    if (shared_inter > 0) {
+        g[1] = GemvGroup{static_cast<const uint8_t*>(ws_gate), static_cast<const uint8_t*>(ws_up), nullptr, h_post,
+                         hidden, 0, act_shared, 1, m, 1, shared_inter, hidden};
+        ng = 2;
+    }
+    return cuda_status(launch_idgemv(g, ng, true, err_flag, stream), "gate|up launch");
+}
+
+int run_down(const void* w_down, int num_experts, const float* act, const int32_t* ids, int m, int top_k,
+             int hidden, int inter, float* expert_out, const void* ws_down, int shared_inter, const float* act_shared,
+             float* shared_out, int* err_flag, cudaStream_t stream) {
+    GemvGroup g[2] = {};
+    int ng = 1;
+    g[0] = GemvGroup{static_cast<const uint8_t*>(w_down), nullptr, ids, act, (int64_t)top_k * inter, inter,
+                     expert_out, num_experts, m, top_k, hidden, inter};
+    if (shared_inter > 0) {
+        g[1] = GemvGroup{static_cast<const uint8_t*>(ws_down), nullptr, nullptr, act_shared, shared_inter, 0,
+                         shared_out, 1, m, 1, hidden, shared_inter};
+        ng = 2;
+    }
+    return cuda_status(launch_idgemv(g, ng, false, err_flag, stream), "down launch");
+}
+
+int run_ffn(const void* w_gate, const void* w_up, const void* w_down, int num_experts, const float* h_post,
+            const int32_t* ids, int m, int top_k, int hidden, int inter, float* act, float* expert_out,
+            const void* ws_gate, const void* ws_up, const void* ws_down, int shared_inter, float* act_shared,
+            float* shared_out, int* err_flag, cudaStream_t stream) {
+    int st = run_gate_up(w_gate, w_up, num_experts, h_post, ids, m, top_k, hidden, inter, act, ws_gate, ws_up,
+                         shared_inter, act_shared, err_flag, stream);
+    if (st) return st;
+    return run_down(w_down, num_experts, act, ids, m, top_k, hidden, inter, expert_out, ws_down, shared_inter,
+                    act_shared, shared_out, err_flag, stream);
+}
+
+// Validation shared by the layer entry points (shapes of both projections, shared expert).
+int check_layer(const void* w_a, const void* w_b, int num_experts, int shared_inter, const void* s_a,
+                const void* s_b, int m, int top_k, int hidden, int inter) {
+    int st = check_gemv_shape(num_experts, m, top_k, inter, hidden);
+    if (!st) st = check_gemv_shape(num_experts, m, top_k, hidden, inter);
+    if (st) return st;
+    if (shared_inter < 0) return fail(Q4K_ERR_SHAPE, "shared_inter must be >= 0");
+    if (shared_inter > 0) {
+        st = check_gemv_shape(1, m, 1, shared_inter, hidden);
+        if (!st) st = check_gemv_shape(1, m, 1, hidden, shared_inter);
+        if (st) return st;
+        if (!s_a || (s_b == nullptr && w_b != nullptr)) return fail(Q4K_ERR_NULL, "shared expert slab is NULL");
+        if (!aligned16(s_a) || (s_b && !aligned16(s_b))) return fail(Q4K_ERR_ALIGN, "shared slabs must be 16-byte aligned");
+    }
+    if (!w_a) return fail(Q4K_ERR_NULL, "NULL slab");
+    if (!aligned16(w_a) || (w_b && !aligned16(w_b))) return fail(Q4K_ERR_ALIGN, "slabs must be 16-byte aligned");
+    return Q4K_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* q4k_last_error_string(void) { return g_last_error.c_str(); }
+
+const char* q4k_version(void) { return "libq4kmoe 0.1 (sm_103a)"; }
+
+size_t q4k_moe_workspace_size(int m, int top_k, int num_experts, int n_max, int k_max) {
+    if (m < 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || num_experts < 1 || n_max < 1 || k_max < 1) return 0;
+    const int inter = n_max > k_max ? n_max : k_max;
+    return ffn_scratch(m, top_k, inter);
+}
+
+size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
+    if (m < 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || num_experts < 1 || hidden < 1 || inter < 1 || shared_inter < 0)
+        return 0;
+    return layer_scratch(m, top_k, hidden, inter, shared_inter).total;
+}
+
+size_t q4k_moe_layer_host_staging_size(int m, int top_k, int hidden) {
+    if (m < 0 || top_k < 1 || hidden < 1) return 0;
+    return align_up((size_t)m * hidden * 4) * 3 + align_up((size_t)m * top_k * 4) * 2 + align_up((size_t)m * 4);
+}
+
+int q4k_moe_bucket(const int32_t* d_ids, int n_pairs, int num_experts, int32_t* d_counts, int32_t* d_offsets,
+                   int32_t* d_perm, int* d_err_flag, cudaStream_t stream) {
+    if (n_pairs < 0) return fail(Q4K_ERR_SHAPE, "n_pairs must be >= 0 (got %d)", n_pairs);
+    if (num_experts < 1) return fail(Q4K_ERR_SHAPE, "num_experts must be >= 1 (got %d)", num_experts);
+    if (num_experts > kMaxExperts) return fail(Q4K_ERR_LIMIT, "num_experts must be <= %d", kMaxExperts);
+    if (!d_counts || !d_offsets || (n_pairs > 0 && (!d_ids || !d_perm))) return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    return cuda_status(launch_bucket(d_ids, n_pairs, num_experts, d_counts, d_offsets, d_perm, d_err_flag, stream),
+                       "bucket launch");
+}
+
+int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_experts, const float* d_a,
+                    int64_t src1_outer_stride, int64_t src1_inner_stride, const int32_t* d_ids, int m, int top_k,
+                    int n, int k, float* d_out, void* d_workspace, size_t ws_bytes, int* d_err_flag,
+                    cudaStream_t stream) {
+    (void)d_workspace;
+    (void)ws_bytes;
+    int st = check_gemv_shape(num_experts, m, top_k, n, k);
+    if (st) return st;
+    if (!d_w_stacked || !d_a || !d_ids || !d_out) return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    const uint8_t* w = static_cast<const uint8_t*>(d_w_stacked) + w_byte_offset;
+    if (!aligned16(w)) return fail(Q4K_ERR_ALIGN, "weights (base + byte offset) must be 16-byte aligned");
+    if (!aligned16(d_a) || src1_outer_stride % 4 || src1_inner_stride % 4 || src1_outer_stride < 0 ||
+        src1_inner_stride < 0)
+        return fail(Q4K_ERR_ALIGN, "activations must be 16-byte aligned with non-negative strides that are multiples of 4 floats");
+    if (m == 0) return Q4K_OK;
+    GemvGroup g{w, nullptr, d_ids, d_a, src1_outer_stride, src1_inner_stride, d_out, num_experts, m, top_k, n, k};
+    return cuda_status(launch_idgemv(&g, 1, false, d_err_flag, stream), "id-gemv launch");
+}
+
+int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,
+                           const float* d_h_post, const int32_t* d_ids, int m, int top_k, int hidden, int inter,
+                           float* d_expert_out, void* d_workspace, size_t ws_bytes, int* d_err_flag,
+                           cudaStream_t stream) {
+    int st = check_gemv_shape(num_experts, m, top_k, inter, hidden);
+    if (!st) st = check_gemv_shape(num_experts, m, top_k, hidden, inter);
+    if (st) return st;
+    if (!d_w_gate || !d_w_up || !d_w_down || !d_h_post || !d_ids || !d_expert_out)
+        return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (!aligned16(d_w_gate) || !aligned16(d_w_up) || !aligned16(d_w_down) || !aligned16(d_h_post))
+        return fail(Q4K_ERR_ALIGN, "slabs and h_post must be 16-byte aligned");
+    st = check_workspace(d_workspace, ws_bytes, ffn_scratch(m, top_k, inter));
+    if (st) return st;
+    if (m == 0) return Q4K_OK;
+    float* act = static_cast<float*>(d_workspace);
+    return run_ffn(d_w_gate, d_w_up, d_w_down, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act,
+                   d_expert_out, nullptr, nullptr, nullptr, 0, nullptr, nullptr, d_err_flag, stream);
+}
+
+int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const float* d_weights,
+                         const float* d_shared_out, const float* d_shared_gate, int shared_mode, int m, int top_k,
+                         int hidden, float* d_hidden_out, cudaStream_t stream) {
+    if (m < 0) return fail(Q4K_ERR_SHAPE, "m must be >= 0 (got %d)", m);
+    if (top_k < 1 || top_k > Q4K_MAX_TOP_K) return fail(Q4K_ERR_TOPK, "top_k must be in [1, %d] (got %d)", Q4K_MAX_TOP_K, top_k);
+    if (hidden < 4 || hidden % 4 != 0) return fail(Q4K_ERR_SHAPE, "hidden must be a positive multiple of 4 (got %d)", hidden);
+    if (shared_mode < 0 || shared_mode > 2) return fail(Q4K_ERR_MODE, "shared_mode must be 0, 1 or 2 (got %d)", shared_mode);
+    if (!d_h_mid || !d_expert_out || !d_weights || !d_hidden_out) return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (shared_mode != Q4K_SHARED_NONE && !d_shared_out) return fail(Q4K_ERR_NULL, "shared_out is NULL");
+    if (shared_mode == Q4K_SHARED_SIGMOID && !d_shared_gate) return fail(Q4K_ERR_NULL, "shared_gate is NULL");
+    if (!aligned16(d_h_mid) || !aligned16(d_expert_out) || !aligned16(d_hidden_out) ||
+        (d_shared_out && !aligned16(d_shared_out)))
+        return fail(Q4K_ERR_ALIGN, "rows must be 16-byte aligned");
+    if (m == 0) return Q4K_OK;
+    return cuda_status(launch_combine(d_h_mid, d_expert_out, d_weights, d_shared_out, d_shared_gate, shared_mode, m,
+                                      top_k, hidden, d_hidden_out, stream),
+                       "combine launch");
+}
+
+int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,
+                          const void* d_ws_gate, const void* d_ws_up, const void* d_ws_down, int shared_inter,
+                          int shared_mode, const float* d_h_post, const float* d_h_mid, const int32_t* d_ids,
+                          const float* d_weights, const float* d_shared_gate, int m, int top_k, int hidden,
+                          int inter, float* d_y, void* d_workspace, size_t ws_bytes, int* d_err_flag,
+                          cudaStream_t stream) {
+    int st = check_gemv_shape(num_experts, m, top_k, inter, hidden);
+    if (!st) st = check_gemv_shape(num_experts, m, top_k, hidden, inter);
+    if (st) return st;
+    if (shared_mode < 0 || shared_mode > 2) return fail(Q4K_ERR_MODE, "shared_mode must be 0, 1 or 2 (got %d)", shared_mode);
+    if (shared_mode == Q4K_SHARED_NONE) {
+        shared_inter = 0;
+    } else {
+        if (shared_inter < 1) return fail(Q4K_ERR_SHAPE, "shared_inter must be >= 1 with a shared expert");
+        st = check_gemv_shape(1, m, 1, shared_inter, hidden);
+        if (!st) st = check_gemv_shape(1, m, 1, hidden, shared_inter);
+        if (st) return st;
+        if (!d_ws_gate || !d_ws_up || !d_ws_down) return fail(Q4K_ERR_NULL, "shared expert slabs are NULL");
+        if (!aligned16(d_ws_gate) || !aligned16(d_ws_up) || !aligned16(d_ws_down))
+            return fail(Q4K_ERR_ALIGN, "shared slabs must be 16-byte aligned");
+        if (shared_mode == Q4K_SHARED_SIGMOID && !d_shared_gate) return fail(Q4K_ERR_NULL, "shared_gate is NULL");
+    }
+    if (!d_w_gate || !d_w_up || !d_w_down || !d_h_post || !d_h_mid || !d_ids || !d_weights || !d_y)
+        return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (!aligned16(d_w_gate) || !aligned16(d_w_up) || !aligned16(d_w_down) || !aligned16(d_h_post) ||
+        !aligned16(d_h_mid) || !aligned16(d_y))
+        return fail(Q4K_ERR_ALIGN, "slabs and activation rows must be 16-byte aligned");
+    const LayerScratch ls = layer_scratch(m, top_k, hidden, inter, shared_inter);
+    st = check_workspace(d_workspace, ws_bytes, ls.total);
+    if (st) return st;
+    if (m == 0) return Q4K_OK;
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    float* act = reinterpret_cast<float*>(ws + ls.act);
+    float* act_shared = reinterpret_cast<float*>(ws + ls.act_shared);
+    float* eout = reinterpret_cast<float*>(ws + ls.eout);
+    float* sout = reinterpret_cast<float*>(ws + ls.shared_out);
+    st = run_ffn(d_w_gate, d_w_up, d_w_down, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act, eout,
+                 d_ws_gate, d_ws_up, d_ws_down, shared_inter, act_shared, sout, d_err_flag, stream);
+    if (st) return st;
+    return cuda_status(launch_combine(d_h_mid, eout, d_weights, sout, d_shared_gate, shared_mode, m, top_k, hidden,
+                                      d_y, stream),
+                       "combine launch");
+}
+
+int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,
+                          const void* d_ws_up, int shared_inter, const float* d_h_post, const int32_t* d_ids, int m,
+                          int top_k, int hidden, int inter, float* d_act, float* d_act_shared, int* d_err_flag,
+                          cudaStream_t stream) {
+    if (!d_w_up) return fail(Q4K_ERR_NULL, "NULL up slab");
+    if (shared_inter > 0 && !d_ws_up) return fail(Q4K_ERR_NULL, "NULL shared up slab");
+    int st = check_layer(d_w_gate, d_w_up, num_experts, shared_inter, d_ws_gate, d_ws_up, m, top_k, hidden, inter);
+    if (st) return st;
+    if (!d_h_post || !d_ids || !d_act || (shared_inter > 0 && !d_act_shared)) return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (!aligned16(d_h_post)) return fail(Q4K_ERR_ALIGN, "h_post must be 16-byte aligned");
+    if (m == 0) return Q4K_OK;
+    return run_gate_up(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, d_act, d_ws_gate,
+                       d_ws_up, shared_inter, d_act_shared, d_err_flag, stream);
+}
+
+int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_down, int shared_inter,
+                       const float* d_act, const float* d_act_shared, const int32_t* d_ids, int m, int top_k,
+                       int hidden, int inter, float* d_expert_out, float* d_shared_out, int* d_err_flag,
+                       cudaStream_t stream) {
+    int st = check_layer(d_w_down, nullptr, num_experts, shared_inter, d_ws_down, nullptr, m, top_k, hidden, inter);
+    if (st) return st;
+    if (!d_act || !d_ids || !d_expert_out || (shared_inter > 0 && (!d_act_shared || !d_shared_out)))
+        return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (!aligned16(d_act) || (d_act_shared && !aligned16(d_act_shared)))
+        return fail(Q4K_ERR_ALIGN, "act rows must be 16-byte aligned");
+    if (m == 0) return Q4K_OK;
+    return run_down(d_w_down, num_experts, d_act, d_ids, m, top_k, hidden, inter, d_expert_out, d_ws_down,
+                    shared_inter, d_act_shared, d_shared_out, d_err_flag, stream);
+}
+
+int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,
+                               const void* d_ws_gate, const void* d_ws_up, const void* d_ws_down, int shared_inter,
+                               int shared_mode, const float* h_post, const float* h_mid, const int32_t* ids,
+                               const float* weights, const float* shared_gate, int m, int top_k, int hidden,
+                               int inter, float* y, void* d_workspace, size_t ws_bytes, int* d_err_flag,
+                               cudaStream_t stream) {
+    int st = check_gemv_shape(num_experts, m, top_k, inter, hidden);
+    if (st) return st;
+    if (!h_post || !h_mid || !ids || !weights || !y) return fail(Q4K_ERR_NULL, "NULL host pointer argument");
+    if (shared_mode == Q4K_SHARED_SIGMOID && !shared_gate) return fail(Q4K_ERR_NULL, "shared_gate is NULL");
+    const int sh = shared_mode == Q4K_SHARED_NONE ? 0 : shared_inter;
+    const size_t layer_bytes = layer_scratch(m, top_k, hidden, inter, sh).total;
+    const size_t stage_bytes = q4k_moe_layer_host_staging_size(m, top_k, hidden);
+    st = check_workspace(d_workspace, ws_bytes, layer_bytes + stage_bytes);
+    if (st) return st;
+    if (m == 0) return Q4K_OK;
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    uint8_t* stage = ws + layer_bytes;
+    const size_t mh = (size_t)m * hidden * 4, mt = (size_t)m * top_k * 4;
+    float* dh_post = reinterpret_cast<float*>(stage);
+    float* dh_mid = reinterpret_cast<float*>(stage + align_up(mh));
+    float* dy = reinterpret_cast<float*>(stage + 2 * align_up(mh));
+    int32_t* dids = reinterpret_cast<int32_t*>(stage + 3 * align_up(mh));
+    float* dw = reinterpret_cast<float*>(stage + 3 * align_up(mh) + align_up(mt));
+    float* dgate = reinterpret_cast<float*>(stage + 3 * align_up(mh) + 2 * align_up(mt));
+    cudaError_t e = cudaMemcpyAsync(dh_post, h_post, mh, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dh_mid, h_mid, mh, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dids, ids, mt, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dw, weights, mt, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && shared_gate)
+        e = cudaMemcpyAsync(dgate, shared_gate, (size_t)m * 4, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_status(e, "host-to-device copy");
+    st = q4k_moe_layer_forward(d_w_gate, d_w_up, d_w_down, num_experts, d_ws_gate, d_ws_up, d_ws_down, sh,
+                               shared_mode, dh_post, dh_mid, dids, dw, shared_gate ? dgate : nullptr, m, top_k,
+                               hidden, inter, dy, d_workspace, layer_bytes, d_err_flag, stream);
+    if (st) return st;
+    return cuda_status(cudaMemcpyAsync(y, dy, mh, cudaMemcpyDeviceToHost, stream), "device-to-host copy");
+}
+
+int q4k_quantize_rows(const float* d_x, int64_t rows, int k, void* d_out, cudaStream_t stream) {
+    if (rows < 0) return fail(Q4K_ERR_SHAPE, "rows must be >= 0");
+    if (k < 1 || k % kQK != 0) return fail(Q4K_ERR_SHAPE, "k must be a positive multiple of 256 (got %d)", k);
+    if (rows > 0 && (!d_x || !d_out)) return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (!aligned16(d_x) || !aligned16(d_out)) return fail(Q4K_ERR_ALIGN, "x and out must be 16-byte aligned");
+    if (rows == 0) return Q4K_OK;
+    return cuda_status(launch_quantize(d_x, rows, k, static_cast<uint8_t*>(d_out), stream), "quantize launch");
+}
+
+int q4k_stream_ceiling_sink_words(void) { return stream_ceiling_grid(); }
+
+int q4k_stream_ceiling(const void* d_src, uint64_t bytes, uint32_t* d_sink, cudaStream_t stream) {
+    if (!d_src || !d_sink) return fail(Q4K_ERR_NULL, "NULL pointer argument");
+    if (!aligned16(d_src) || bytes % 16) return fail(Q4K_ERR_ALIGN, "source must be 16-byte aligned, bytes % 16 == 0");
+    return cuda_status(launch_stream_ceiling(d_src, bytes, d_sink, stream), "ceiling launch");
+}
+
+}  // extern "C"

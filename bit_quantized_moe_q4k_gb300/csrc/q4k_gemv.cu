@@ -1,0 +1,416 @@
+// q4k_gemv.cu -- the bucketed Q4_K MoE id-GEMV (and its fused gate|up + SwiGLU form).
+//
+// What it computes (ferrum-kernels q4_k_moe_id_gemv_batched.rs,
+// `dispatch_gemv_q4k_moe_id_batched_on_encoder`): for every (token, slot) pair p,
+//   out[p, r] = sum_c W_{ids[p]}[r, c] * a[t*outer + s*inner + c],  t = p / top_k, s = p % top_k.
+// With a second slab (moeflux expert_forward.rs: gate, up, SwiGLU) the launch computes
+//   out[p, r] = silu(Wg . x) * (Wu . x).
+//
+// How (GB300 design):
+//  * Pairs are bucketed by expert inside every CTA (histogram + scan of the ids in shared
+//    memory), so each touched slab row tile is streamed from HBM once per launch no matter
+//    how many pairs of the batch picked that expert. Work item = (group, expert, 32-row
+//    tile, chunk of <= kTB tokens of that expert's bucket); CTAs walk items grid-stride.
+//  * The item's activation rows are staged in shared memory as 16-bit fixed point per
+//    32-element sub-block: X = rint(x / delta), delta = max|x| / 32767, split into a low
+//    byte plane (unsigned) and a high byte plane (signed), with sum(X) per sub-block.
+//  * Weights are read with coalesced 16-byte loads; a lane owns one 64-weight group (32
+//    code bytes = sub-blocks 2c and 2c+1) of one block of one row. The codes are used as
+//    bytes directly (w & 0x0F0F0F0F, (w >> 4) & 0x0F0F0F0F) by dp4a against the two
+//    activation planes, so the integer sum S_j = sum_i q_i X_i of a sub-block is exact.
+//  * Per sub-block the Q4_K algebra folds the minimum into the activation sum:
+//      sum_i w_i x_i = delta_j * (d*sc_j * S_j - dmin*m_j * sum_i X_i).
+//  * Lanes sharing a row reduce with warp shuffles; the epilogue writes the pair's row
+//    (optionally silu(g) * u).
+#include <cuda_fp16.h>
+
+#include "q4k_bucket.cuh"
+#include "q4k_internal.cuh"
+
+namespace q4k {
+
+constexpr int kThreads = 128;               // 4 warps
+constexpr int kRowsPerWarp = 8;             // lanes = 4 groups (c) x 8 rows
+constexpr int kTileRows = kRowsPerWarp * (kThreads / 32);
+constexpr int kTB = 4;                      // max tokens of one bucket per work item
+constexpr int kPairBytes = 144;             // staged planes of 2 sub-blocks + 16 B pad
+constexpr int kMaxGroups = 2;
+
+struct GroupDev {
+    const uint8_t* w;
+    const uint8_t* w2;
+    const int32_t* ids;
+    const float* a;
+    float* out;
+    int64_t outer, inner;
+    int64_t nb01;  // bytes per row
+    int64_t nb02;  // bytes per expert
+    int num_experts, n_pairs, top_k, n, k, tiles;
+};
+
+struct GemvParams {
+    GroupDev g[kMaxGroups];
+    int n_groups;
+    int tb;                 // tokens per work item (<= kTB)
+    int hist_off[kMaxGroups];  // int offsets of each group's tables in shared memory
+    int x_off;              // byte offset of the staged activations
+    int meta_off;           // byte offset of the per-sub-block (delta, sumX) pairs
+    int kmax;               // largest k of the groups (sizes the staging area)
+    int* err_flag;
+};
+
+__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+// (scale, min) of sub-blocks ja = 2c and jb = 2c + 1 from the 16-byte block header
+// (d, dmin, 12 scale bytes; GGML Q4_K placement), multiplied by d and dmin.
+__device__ __forceinline__ void block_scales(uint4 h, int c, float& sa, float& ma, float& sb, float& mb) {
+    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+    const bool hi = c >= 2;  // sub-blocks 4..7 take their low bits from bytes 8..11
+    const int ia = (2 * c) & 3, ib = (2 * c + 1) & 3;
+    const unsigned ya = (h.y >> (8 * ia)) & 0xFFu, yb = (h.y >> (8 * ib)) & 0xFFu;
+    const unsigned za = (h.z >> (8 * ia)) & 0xFFu, zb = (h.z >> (8 * ib)) & 0xFFu;
+    const unsigned wa = (h.w >> (8 * ia)) & 0xFFu, wb = (h.w >> (8 * ib)) & 0xFFu;
+    const unsigned sca = hi ? ((wa & 15u) | ((ya >> 6) << 4)) : (ya & 63u);
+    const unsigned mna = hi ? ((wa >> 4) | ((za >> 6) << 4)) : (za & 63u);
+    const unsigned scb = hi ? ((wb & 15u) | ((yb >> 6) << 4)) : (yb & 63u);
+    const unsigned mnb = hi ? ((wb >> 4) | ((zb >> 6) << 4)) : (zb & 63u);
+    sa = d * (float)sca;
+    ma = dmin * (float)mna;
+    sb = d * (float)scb;
+    mb = dmin * (float)mnb;
+}
+
+// Exact integer dot products of one lane's 64 codes with one token's staged planes.
+// q0, q1: the lane's 32 code bytes; L*/H*: low / high planes of sub-blocks a and b.
+__device__ __forceinline__ void dot64(const uint4& q0, const uint4& q1, const uint4* xp, int& Sa, int& Sb) {
+    const uint4 La0 = xp[0], La1 = xp[1], Ha0 = xp[2], Ha1 = xp[3];
+    const uint4 Lb0 = xp[4], Lb1 = xp[5], Hb0 = xp[6], Hb1 = xp[7];
+    const unsigned qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const unsigned la[8] = {La0.x, La0.y, La0.z, La0.w, La1.x, La1.y, La1.z, La1.w};
+    const unsigned ha[8] = {Ha0.x, Ha0.y, Ha0.z, Ha0.w, Ha1.x, Ha1.y, Ha1.z, Ha1.w};
+    const unsigned lb[8] = {Lb0.x, Lb0.y, Lb0.z, Lb0.w, Lb1.x, Lb1.y, Lb1.z, Lb1.w};
+    const unsigned hb[8] = {Hb0.x, Hb0.y, Hb0.z, Hb0.w, Hb1.x, Hb1.y, Hb1.z, Hb1.w};
+    unsigned sal = 0, sbl = 0;
+    int sah = 0, sbh = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const unsigned lo = qw[i] & 0x0F0F0F0Fu;
+        const unsigned hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
+        sal = __dp4a(lo, la[i], sal);
+        sah = __dp4a((int)lo, (int)ha[i], sah);
+        sbl = __dp4a(hi, lb[i], sbl);
+        sbh = __dp4a((int)hi, (int)hb[i], sbh);
+    }
+    Sa = (int)sal + sah * 256;
+    Sb = (int)sbl + sbh * 256;
+}
+
+// Stage the activation rows of the item's pairs: per 32-element sub-block j of token t,
+// planes at xs + t*tok_bytes + (j/2)*144 + (j%2)*64 (low plane 32 B, high plane 32 B),
+// and (delta, sumX) at meta[t*(k/32) + j]. Thread f handles float4 f of the row; the 8
+// threads of a sub-block reduce max|x| and sum(X) with shuffles. All loads of a pass are
+// issued before any is used.
+constexpr int kStageUnroll = 8;
+
+__device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs, int nt, uint8_t* xs,
+                                           float2* meta) {
+    const int tid = threadIdx.x;
+    const int nf = G.k / 4;
+    const int nsb = G.k / 32;
+    const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
+    for (int t = 0; t < nt; ++t) {
+        const int p = s_pairs[t];
+        const float* row = G.a + (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+        for (int f0 = 0; f0 < nf; f0 += kThreads * kStageUnroll) {
+            float4 v[kStageUnroll];
+#pragma unroll
+            for (int u = 0; u < kStageUnroll; ++u) {
+                const int f = f0 + u * kThreads + tid;
+                v[u] = f < nf ? __ldg(reinterpret_cast<const float4*>(row) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kStageUnroll; ++u) {
+                const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
+                if (f0 + u * kThreads >= nf) break;
+                float mx = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                int X[4] = {0, 0, 0, 0};
+                if (mx > 0.0f) {
+                    const float inv = 32767.0f / mx;
+                    X[0] = max(-32767, min(32767, __float2int_rn(v[u].x * inv)));
+                    X[1] = max(-32767, min(32767, __float2int_rn(v[u].y * inv)));
+                    X[2] = max(-32767, min(32767, __float2int_rn(v[u].z * inv)));
+                    X[3] = max(-32767, min(32767, __float2int_rn(v[u].w * inv)));
+                }
+                int sx = X[0] + X[1] + X[2] + X[3];
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, off);
+                if (f < nf) {
+                    const int j = f >> 3, wi = f & 7;
+                    const uint32_t lo = (uint32_t)(X[0] & 0xFF) | ((uint32_t)(X[1] & 0xFF) << 8) |
+                                        ((uint32_t)(X[2] & 0xFF) << 16) | ((uint32_t)(X[3] & 0xFF) << 24);
+                    const uint32_t hi = (uint32_t)((X[0] >> 8) & 0xFF) | ((uint32_t)((X[1] >> 8) & 0xFF) << 8) |
+                                        ((uint32_t)((X[2] >> 8) & 0xFF) << 16) | ((uint32_t)((X[3] >> 8) & 0xFF) << 24);
+                    uint32_t* planes = reinterpret_cast<uint32_t*>(xs + t * tok_bytes + (j >> 1) * kPairBytes + (j & 1) * 64);
+                    planes[wi] = lo;
+                    planes[8 + wi] = hi;
+                    if (wi == 0) meta[t * nsb + j] = make_float2(mx / 32767.0f, (float)sx);
+                }
+            }
+        }
+    }
+}
+
+constexpr int kDepth = 4;  // blocks of the weight stream in flight per lane
+
+template <bool FUSED>
+__global__ void __launch_bounds__(kThreads, 3)
+idgemv_kernel(const __grid_constant__ GemvParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    int* s_int = reinterpret_cast<int*>(smem);
+    __shared__ int s_warp[33];
+    __shared__ int s_bad[kMaxGroups];
+    __shared__ int s_items[kMaxGroups + 1];
+    __shared__ int s_pairs[kTB];
+    __shared__ int s_item_info[5];  // group, expert, tile, tokens, chunk
+
+    // ---- bucketing prologue: per group, counts then item offsets per expert
+    if (threadIdx.x == 0) s_items[0] = 0;
+    for (int gi = 0; gi < P.n_groups; ++gi) {
+        const GroupDev& G = P.g[gi];
+        int* cnt = s_int + P.hist_off[gi];
+        int* start = cnt + G.num_experts;
+        if (G.ids) {
+            block_histogram(G.ids, G.n_pairs, G.num_experts, cnt, &s_bad[gi]);
+        } else {
+            if (threadIdx.x == 0) { cnt[0] = G.n_pairs; s_bad[gi] = 0; }
+            __syncthreads();
+        }
+        for (int e = threadIdx.x; e < G.num_experts; e += kThreads)
+            start[e] = ((cnt[e] + P.tb - 1) / P.tb) * G.tiles;
+        __syncthreads();
+        const int total = block_exclusive_scan(start, G.num_experts, s_warp);
+        if (threadIdx.x == 0) s_items[gi + 1] = s_items[gi] + total;
+        __syncthreads();
+    }
+    // out-of-range ids: flag and zero their rows (done once, by CTA 0)
+    if (blockIdx.x == 0) {
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const GroupDev& G = P.g[gi];
+            if (!G.ids || s_bad[gi] == 0) continue;
+            if (threadIdx.x == 0) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
+            for (int p = 0; p < G.n_pairs; ++p) {
+                if (id_valid(G.ids[p], G.num_experts)) continue;
+                for (int r = threadIdx.x; r < G.n; r += kThreads) G.out[(int64_t)p * G.n + r] = 0.0f;
+            }
+        }
+    }
+    const int total_items = s_items[P.n_groups];
+    uint8_t* xs = smem + P.x_off;
+    float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = lane & 3, rl = lane >> 2;
+
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        // ---- locate the item: group, expert (search over the item offsets), tile, chunk
+        if (threadIdx.x == 0) {
+            int gi = 0;
+            while (gi + 1 < P.n_groups && item >= s_items[gi + 1]) ++gi;
+            const GroupDev& G = P.g[gi];
+            const int* cnt = s_int + P.hist_off[gi];
+            const int* start = cnt + G.num_experts;
+            const int local = item - s_items[gi];
+            int lo = 0, hi = G.num_experts - 1;  // last e with start[e] <= local (it has pairs)
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (start[mid] <= local) lo = mid; else hi = mid - 1;
+            }
+            const int in_e = local - start[lo];
+            const int chunks = (cnt[lo] + P.tb - 1) / P.tb;
+            const int chunk = in_e % chunks;
+            s_item_info[0] = gi;
+            s_item_info[1] = lo;
+            s_item_info[2] = in_e / chunks;
+            s_item_info[3] = min(P.tb, cnt[lo] - chunk * P.tb);
+            s_item_info[4] = chunk;
+        }
+        __syncthreads();
+        const int gi = s_item_info[0], e = s_item_info[1], tile = s_item_info[2], nt = s_item_info[3];
+        const int chunk = s_item_info[4];
+        const GroupDev& G = P.g[gi];
+
+        // ---- start the weight stream before staging (independent of the activations)
+        const int row = tile * kTileRows + warp * kRowsPerWarp + rl;
+        const bool row_ok = row < G.n;
+        const int nb = G.k / kQK;
+        const int nsb = G.k / 32;
+        const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
+        const uint8_t* wr = G.w + (int64_t)e * G.nb02 + (int64_t)(row_ok ? row : 0) * G.nb01;
+        const uint8_t* wr2 = FUSED ? G.w2 + (int64_t)e * G.nb02 + (int64_t)(row_ok ? row : 0) * G.nb01 : nullptr;
+        uint4 H[kDepth], Q0[kDepth], Q1[kDepth], H2[kDepth], R0[kDepth], R1[kDepth];
+#pragma unroll
+        for (int s = 0; s < kDepth; ++s) {
+            H[s] = Q0[s] = Q1[s] = H2[s] = R0[s] = R1[s] = make_uint4(0, 0, 0, 0);
+            if (row_ok && s < nb) {
+                const uint8_t* p = wr + (int64_t)s * kBlockBytes;
+                H[s] = ldg16(p); Q0[s] = ldg16(p + 16 + 32 * c); Q1[s] = ldg16(p + 32 + 32 * c);
+                if (FUSED) {
+                    const uint8_t* p2 = wr2 + (int64_t)s * kBlockBytes;
+                    H2[s] = ldg16(p2); R0[s] = ldg16(p2 + 16 + 32 * c); R1[s] = ldg16(p2 + 32 + 32 * c);
+                }
+            }
+        }
+
+        if (warp == 0) {
+            if (G.ids) {
+                warp_gather_bucket(G.ids, G.n_pairs, e, chunk * P.tb, nt, s_pairs);
+            } else if (lane < nt) {
+                s_pairs[lane] = chunk * P.tb + lane;
+            }
+        }
+        __syncthreads();
+        stage_rows(G, s_pairs, nt, xs, meta);
+        __syncthreads();
+
+        // ---- main loop: lane (c, rl) streams 64-weight group c of every block of its row
+        float acc[kTB], acc2[kTB];
+#pragma unroll
+        for (int t = 0; t < kTB; ++t) { acc[t] = 0.0f; acc2[t] = 0.0f; }
+        for (int b0 = 0; b0 < nb; b0 += kDepth) {
+#pragma unroll
+            for (int s = 0; s < kDepth; ++s) {
+                const int b = b0 + s;
+                if (b < nb) {
+                    float sa, ma, sb, mb, sa2 = 0.f, ma2 = 0.f, sb2 = 0.f, mb2 = 0.f;
+                    block_scales(H[s], c, sa, ma, sb, mb);
+                    if (FUSED) block_scales(H2[s], c, sa2, ma2, sb2, mb2);
+#pragma unroll
+                    for (int t = 0; t < kTB; ++t) {
+                        if (t < nt) {
+                            const uint4* xp = reinterpret_cast<const uint4*>(xs + t * tok_bytes + (4 * b + c) * kPairBytes);
+                            const float4 mt = *reinterpret_cast<const float4*>(meta + t * nsb + 8 * b + 2 * c);
+                            int Sa, Sb;
+                            dot64(Q0[s], Q1[s], xp, Sa, Sb);
+                            acc[t] += mt.x * (sa * (float)Sa - ma * mt.y) + mt.z * (sb * (float)Sb - mb * mt.w);
+                            if (FUSED) {
+                                dot64(R0[s], R1[s], xp, Sa, Sb);
+                                acc2[t] += mt.x * (sa2 * (float)Sa - ma2 * mt.y) + mt.z * (sb2 * (float)Sb - mb2 * mt.w);
+                            }
+                        }
+                    }
+                    if (row_ok && b + kDepth < nb) {  // refill this slot with block b + kDepth
+                        const uint8_t* p = wr + (int64_t)(b + kDepth) * kBlockBytes;
+                        H[s] = ldg16(p); Q0[s] = ldg16(p + 16 + 32 * c); Q1[s] = ldg16(p + 32 + 32 * c);
+                        if (FUSED) {
+                            const uint8_t* p2 = wr2 + (int64_t)(b + kDepth) * kBlockBytes;
+                            H2[s] = ldg16(p2); R0[s] = ldg16(p2 + 16 + 32 * c); R1[s] = ldg16(p2 + 32 + 32 * c);
+                        }
+                    }
+                }
+            }
+        }
+        // ---- reduce over the 4 lanes of the row and write
+#pragma unroll
+        for (int t = 0; t < kTB; ++t) {
+            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 1);
+            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 2);
+            if (FUSED) {
+                acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], 1);
+                acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], 2);
+            }
+        }
+        if (row_ok && c == 0) {
+#pragma unroll
+            for (int t = 0; t < kTB; ++t) {
+                if (t < nt) {
+                    const float v = FUSED ? silu(acc[t]) * acc2[t] : acc[t];
+                    G.out[(int64_t)s_pairs[t] * G.n + row] = v;
+                }
+            }
+        }
+        __syncthreads();  // s_pairs / staged rows are rewritten by the next item
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+static int g_num_sms = 0;
+constexpr int kMaxDevices = 64;
+constexpr size_t kSmemLimit = 200 * 1024;
+static bool g_smem_attr_set[2][kMaxDevices] = {};
+
+int num_sms() {
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 1;
+    }
+    return g_num_sms;
+}
+
+cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, int* err_flag,
+                          cudaStream_t stream) {
+    GemvParams P{};
+    P.n_groups = n_groups;
+    P.err_flag = err_flag;
+    int ints = 0, kmax = 0;
+    int64_t max_items = 0;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        const GemvGroup& S = groups[gi];
+        GroupDev& G = P.g[gi];
+        G.w = S.w; G.w2 = S.w2; G.ids = S.ids; G.a = S.a; G.out = S.out;
+        G.outer = S.outer; G.inner = S.inner;
+        G.nb01 = (int64_t)(S.k / kQK) * kBlockBytes;
+        G.nb02 = (int64_t)S.n * G.nb01;
+        G.num_experts = S.num_experts; G.n_pairs = S.m * S.top_k; G.top_k = S.top_k;
+        G.n = S.n; G.k = S.k;
+        G.tiles = (S.n + kTileRows - 1) / kTileRows;
+        P.hist_off[gi] = ints;
+        ints += 2 * S.num_experts;
+        kmax = S.k > kmax ? S.k : kmax;
+        max_items += (int64_t)G.n_pairs * G.tiles;
+    }
+    if (max_items == 0) return cudaSuccess;
+    P.kmax = kmax;
+    // tokens per item: keep the staged rows within ~150 KB of shared memory
+    const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
+    int tb = kTB;
+    while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;
+    P.tb = tb;
+    int off = ((ints * 4) + 15) & ~15;
+    P.x_off = off;
+    off += (int)(per_tok * tb - (int64_t)(kmax / 32) * 8 * tb);
+    off = (off + 15) & ~15;
+    P.meta_off = off;
+    off += (kmax / 32) * 8 * tb;
+    const size_t smem = (size_t)off;
+    if (smem > kSmemLimit) return cudaErrorInvalidValue;
+    auto kern = fused_swiglu ? idgemv_kernel<true> : idgemv_kernel<false>;
+    // The dynamic shared memory limit is raised once per device and kernel (outside any
+    // stream capture the caller may start later); launches only query occupancy.
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_smem_attr_set[fused_swiglu ? 1 : 0][dev]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+        if (err != cudaSuccess) return err;
+        g_smem_attr_set[fused_swiglu ? 1 : 0][dev] = true;
+    }
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    if (grid > max_items) grid = max_items;
+    kern<<<(unsigned)grid, kThreads, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace q4k

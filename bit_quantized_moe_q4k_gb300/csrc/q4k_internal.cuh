@@ -1,0 +1,58 @@
+// q4k_internal.cuh -- declarations shared by the CUDA translation units of libq4kmoe.
+// Nothing here is part of the C ABI (that is include/q4kmoe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q4kmoe.h"
+
+namespace q4k {
+
+constexpr int kQK = 256;          // weights per Q4_K super-block
+constexpr int kBlockBytes = 144;  // bytes per super-block
+constexpr int kMaxExperts = 4096; // bucketing bound (shared-memory tables)
+constexpr int kMaxK = 65536;
+
+// Device error flag helper: records the first error code, never traps.
+__device__ __forceinline__ void raise_flag(int* flag, int code) {
+    if (flag) atomicCAS(flag, 0, code);
+}
+
+// -------------------------------------------------------------------------------------------
+// Per-CTA pair bucketing (the map0 step of the layer: bucket (token, slot) pairs by expert).
+// Computed redundantly by every CTA of a GEMV launch from the ids in L2, so no separate
+// launch and no global synchronisation is needed before the weight stream starts.
+struct BucketView {
+    int n_experts_used;  // U: experts with at least one valid pair
+};
+
+// Launchers (defined in q4k_misc.cu / q4k_gemv.cu). All return cudaError_t of the launch.
+cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int* err_flag, cudaStream_t stream);
+cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
+                           const float* shared_out, const float* shared_gate, int shared_mode, int m,
+                           int top_k, int hidden, float* y, cudaStream_t stream);
+cudaError_t launch_quantize(const float* x, int64_t rows, int k, uint8_t* out, cudaStream_t stream);
+cudaError_t launch_stream_ceiling(const void* src, uint64_t bytes, uint32_t* sink, cudaStream_t stream);
+int stream_ceiling_grid();
+
+// One projection group of an id-GEMV launch: a stacked slab and how its pairs read rows.
+struct GemvGroup {
+    const uint8_t* w;        // slab base (16-byte aligned), expert e at w + e * n * row_bytes
+    const uint8_t* w2;       // second slab read with the same rows (up, for the fused gate|up), or null
+    const int32_t* ids;      // [m * top_k] expert ids, or null = every pair uses expert 0
+    const float* a;          // activations
+    int64_t outer, inner;    // src1 walk in floats
+    float* out;              // [m * top_k, n] output rows
+    int num_experts, m, top_k, n, k;
+};
+
+// Launch the bucketed Q4_K id-GEMV over up to two groups in one grid (the routed experts
+// and the shared expert of a layer). fused_swiglu: out = silu(w . x) * (w2 . x).
+cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, int* err_flag,
+                          cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace q4k

@@ -1,0 +1,228 @@
+/*
+ * q4kmoe.h -- C ABI of the GB300 (sm_103a) Q4_K mixture-of-experts layer library.
+ *
+ * The operations follow the studied pages' statement of the problem:
+ *   [P1] ferrum-kernels 0.7.7, src/backend/metal/q4_k_moe_id_gemv_batched.rs
+ *        (`dispatch_gemv_q4k_moe_id_batched_on_encoder`: argument list, the
+ *        preconditions k % 256 == 0, n % 4 == 0, the row and expert strides
+ *        nb01 = (k/256)*144 and nb02 = n*nb01, the src1 outer/inner walk);
+ *   [P2] moeflux 0.1.0-pre.3, src/riir/moe/expert_forward.rs (the expert FFN
+ *        gate -> up -> SwiGLU -> down, `ExpertPayload`, the `MAX_K` = 16 slot
+ *        bound and `BadK`, the sigmoid-gated / unscaled shared expert in
+ *        `combine_kernel_name`, the batched combine
+ *        `encode_moe_combine_residual_n_tokens`, and the expert bucketing of
+ *        `encode_moe_batched_permute_fuse` / `encode_moe_gather_id_fuse`).
+ *
+ * Data formats
+ *   Q4_K block: 256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes of
+ *   packed 6-bit scales and mins (GGML Q4_K placement), 128 bytes of 4-bit
+ *   codes; w = d*sc*q - dmin*m. A projection with n outputs and k inputs is
+ *   n rows of k/256 blocks; a stacked slab is num_experts such matrices back
+ *   to back (expert e starts at byte e*n*(k/256)*144).
+ *   Activations, outputs and routing weights are fp32, ids are int32.
+ *   A (token, slot) pair has index p = token*top_k + slot.
+ *
+ * Conventions of every call
+ *   - Pointers named d_* or documented as device memory are device pointers
+ *     owned by the caller; the library allocates no device memory, holds no
+ *     global device state and keeps no pointer past the call.
+ *   - Calls are asynchronous on `stream` (the last argument) and return a
+ *     q4k_status. Host-side validation happens before anything is enqueued;
+ *     on an error status nothing was enqueued.
+ *   - Expert ids are range-checked on the device: a pair whose id is outside
+ *     [0, num_experts) gets an all-zero output row and, when `err_flag` is
+ *     not NULL, the device int *err_flag is set to Q4K_ERR_EXPERT_ID. No trap,
+ *     no host synchronisation. The caller zeroes *err_flag before the call.
+ *   - Scratch memory comes from a caller-provided device `workspace` of at
+ *     least the size the matching *_workspace_size() returns (256-byte aligned).
+ *   - q4k_last_error_string() describes the last non-OK status of the calling
+ *     thread.
+ *   - m == 0 is an empty batch: the call validates, enqueues nothing and
+ *     returns Q4K_OK.
+ */
+#ifndef Q4KMOE_H
+#define Q4KMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q4K_OK = 0,
+    Q4K_ERR_NULL = 1,      /* a required pointer is NULL                                    */
+    Q4K_ERR_SHAPE = 2,     /* k % 256 != 0, n % 4 != 0, m < 0, num_experts < 1, n or k < 1   */
+    Q4K_ERR_TOPK = 3,      /* top_k outside [1, 16]                                          */
+    Q4K_ERR_WORKSPACE = 4, /* workspace NULL, misaligned or smaller than required            */
+    Q4K_ERR_CUDA = 5,      /* a CUDA runtime call or launch failed                           */
+    Q4K_ERR_EXPERT_ID = 6, /* device flag value: some id was outside [0, num_experts)        */
+    Q4K_ERR_ALIGN = 7,     /* slab not 16-byte aligned, or activation rows not 16-byte aligned */
+    Q4K_ERR_MODE = 8,      /* shared_mode not in {0, 1, 2}                                   */
+    Q4K_ERR_LIMIT = 9      /* a size beyond an implementation limit (see each call)          */
+} q4k_status;
+
+#define Q4K_MAX_TOP_K 16
+#define Q4K_SHARED_NONE 0
+#define Q4K_SHARED_SIGMOID 1  /* g_t = 1 / (1 + exp(-shared_gate[t])) */
+#define Q4K_SHARED_UNSCALED 2 /* g_t = 1                               */
+
+/* Text of the calling thread's last non-OK status (never NULL). */
+const char* q4k_last_error_string(void);
+
+/* Library version string. */
+const char* q4k_version(void);
+
+/* ---------------------------------------------------------------------------------
+ * Workspace sizing. Returns the bytes of device scratch the calls below need for
+ * these sizes (0 on invalid sizes). q4k_moe_workspace_size covers q4k_moe_id_gemv
+ * with n <= n_max, k <= k_max and q4k_expert_ffn_forward with hidden, inter <=
+ * max(n_max, k_max); q4k_moe_layer_workspace_size covers q4k_moe_layer_forward.
+ */
+size_t q4k_moe_workspace_size(int m, int top_k, int num_experts, int n_max, int k_max);
+size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidden, int inter,
+                                    int shared_inter);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_moe_bucket -- pair bucketing [P2: bucket (token, slot) tuples by expert id].
+ * Stable counting sort of the n_pairs pairs by expert id:
+ *   d_counts[e]  = number of pairs with id e                       (num_experts ints)
+ *   d_offsets[e] = exclusive prefix sum of d_counts, d_offsets[E] = valid pairs (E+1 ints)
+ *   d_perm[d_offsets[e] .. d_offsets[e+1]) = the pairs with id e, increasing
+ *   d_perm[d_offsets[E] .. n_pairs) = pairs with an out-of-range id, increasing.
+ * The result is unique, so it is bit-exact with any correct implementation.
+ * Limit: num_experts <= 4096 (Q4K_ERR_LIMIT otherwise).
+ */
+int q4k_moe_bucket(const int32_t* d_ids, int n_pairs, int num_experts, int32_t* d_counts,
+                   int32_t* d_offsets, int32_t* d_perm, int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_moe_id_gemv -- batched MoE indirect-dispatch GEMV [P1].
+ * For every pair p < m*top_k, with t = p / top_k and s = p % top_k:
+ *   out[p, r] = sum_c W_{ids[p]}[r, c] * a[t*src1_outer_stride + s*src1_inner_stride + c]
+ * for r < n, c < k. W_e is the Q4_K [n, k] matrix of expert e in the slab at
+ * d_w_stacked + w_byte_offset. Strides are in floats: gate/up use (k, 0) (the
+ * token's row is broadcast to its slots), down uses (top_k*k, k) (one row per
+ * pair). Pairs are bucketed by expert on the device so each touched slab row
+ * is streamed once per call, whatever the number of pairs sharing it.
+ *   d_w_stacked + w_byte_offset: 16-byte aligned, num_experts*n*(k/256)*144 bytes
+ *   d_a: 16-byte aligned; strides multiples of 4 floats
+ *   d_out: [m*top_k, n] fp32
+ * Limits: num_experts <= 4096, k <= 65536.
+ */
+int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_experts,
+                    const float* d_a, int64_t src1_outer_stride, int64_t src1_inner_stride,
+                    const int32_t* d_ids, int m, int top_k, int n, int k, float* d_out,
+                    void* d_workspace, size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_expert_ffn_forward -- routed expert FFN [P2: gate, up, SwiGLU, down].
+ *   g[p, i] = gemv(W_gate, h_post; strides (hidden, 0))
+ *   u[p, i] = gemv(W_up,   h_post; strides (hidden, 0))
+ *   act[p, i] = silu(g) * u,  silu(x) = x / (1 + exp(-x))   (fused into the gate|up pass)
+ *   expert_out[p, h] = gemv(W_down, act; strides (top_k*inter, inter))
+ * d_w_gate / d_w_up: slabs of [num_experts][inter, hidden]; d_w_down: [num_experts][hidden, inter].
+ * d_h_post: [m, hidden]; d_expert_out: [m*top_k, hidden]. The shared expert is this call
+ * with num_experts = 1, top_k = 1 and all ids 0.
+ */
+int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down,
+                           int num_experts, const float* d_h_post, const int32_t* d_ids, int m,
+                           int top_k, int hidden, int inter, float* d_expert_out,
+                           void* d_workspace, size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * moe_combine_residual -- combine [P2: hidden_out = h_mid + sum_k w_k * expert_out_k
+ * + shared term].
+ *   hidden_out[t, h] = h_mid[t, h] + sum_{s<top_k} weights[t*top_k+s] * expert_out[t*top_k+s, h]
+ *                      + g_t * shared_out[t, h]
+ * with g_t per shared_mode (NONE: no term, shared_out / shared_gate may be NULL;
+ * SIGMOID: g_t = 1/(1+exp(-shared_gate[t])); UNSCALED: g_t = 1, shared_gate may be NULL).
+ * The slot sum runs in slot order (deterministic, no atomics). hidden_out may alias
+ * h_mid. Requires hidden % 4 == 0 and 16-byte aligned rows.
+ */
+int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const float* d_weights,
+                         const float* d_shared_out, const float* d_shared_gate, int shared_mode,
+                         int m, int top_k, int hidden, float* d_hidden_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_moe_layer_forward -- one MoE layer: routed FFN, shared-expert FFN and combine.
+ *   y = moe_combine_residual(h_mid, q4k_expert_ffn_forward(routed),
+ *                            weights, q4k_expert_ffn_forward(shared), shared_gate)
+ * Shared slabs (one expert, intermediate shared_inter) are NULL and shared_inter 0
+ * when shared_mode is NONE. All device pointers; d_y [m, hidden] may alias d_h_mid.
+ * Contains no host synchronisation, so it can be captured in a CUDA graph.
+ */
+int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down,
+                          int num_experts, const void* d_ws_gate, const void* d_ws_up,
+                          const void* d_ws_down, int shared_inter, int shared_mode,
+                          const float* d_h_post, const float* d_h_mid, const int32_t* d_ids,
+                          const float* d_weights, const float* d_shared_gate, int m, int top_k,
+                          int hidden, int inter, float* d_y, void* d_workspace, size_t ws_bytes,
+                          int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * The two halves of q4k_moe_layer_forward, for callers that schedule the layer
+ * themselves (the fused gate + up + SiLU batched id-GEMV of ferrum-kernels'
+ * q4_k_moe_id_gate_up_silu_batched, then the down projection), each running the
+ * routed experts and the shared expert in one launch:
+ *   q4k_moe_layer_gate_up: d_act[p, :] = silu(W_gate . x) * (W_up . x) for the routed pairs
+ *     (x = h_post row of the pair's token) and d_act_shared[t, :] likewise for the shared
+ *     expert (d_act [m*top_k, inter], d_act_shared [m, shared_inter]).
+ *   q4k_moe_layer_down: d_expert_out[p, :] = W_down . d_act[p, :] and
+ *     d_shared_out[t, :] = W_sdown . d_act_shared[t, :].
+ * shared_inter == 0 (and NULL shared pointers) means no shared expert.
+ */
+int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,
+                          const void* d_ws_up, int shared_inter, const float* d_h_post, const int32_t* d_ids,
+                          int m, int top_k, int hidden, int inter, float* d_act, float* d_act_shared,
+                          int* d_err_flag, cudaStream_t stream);
+int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_down, int shared_inter,
+                       const float* d_act, const float* d_act_shared, const int32_t* d_ids, int m, int top_k,
+                       int hidden, int inter, float* d_expert_out, float* d_shared_out, int* d_err_flag,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_moe_layer_forward_host -- the same layer with the per-step inputs and the
+ * output in HOST memory (pinned memory gives asynchronous copies). Weights and the
+ * workspace stay in device memory. Copies h_post, h_mid, ids, weights and
+ * shared_gate into the staging area at the front of the workspace, runs the
+ * layer, copies y back, all on `stream`; the call returns once these are
+ * enqueued, so the caller synchronises `stream` before reading y.
+ * Workspace: q4k_moe_layer_workspace_size(...) + q4k_moe_layer_host_staging_size(...).
+ */
+size_t q4k_moe_layer_host_staging_size(int m, int top_k, int hidden);
+int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const void* d_w_down,
+                               int num_experts, const void* d_ws_gate, const void* d_ws_up,
+                               const void* d_ws_down, int shared_inter, int shared_mode,
+                               const float* h_post, const float* h_mid, const int32_t* ids,
+                               const float* weights, const float* shared_gate, int m, int top_k,
+                               int hidden, int inter, float* y, void* d_workspace,
+                               size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_quantize_rows -- fp32 [rows, k] -> Q4_K bytes [rows, k/256*144] on the device
+ * (weight preparation; not part of the layer). Per 32-weight sub-block:
+ * lo = min(0, min x), hi = max x, scale = (hi-lo)/15, mn = -lo; d = fp16(max scale/63),
+ * dmin = fp16(max mn/63); sc = min(63, rint(scale/d)), m = min(63, rint(mn/dmin));
+ * q = clamp(rint((x + dmin*m)/(d*sc)), 0, 15); every step one IEEE binary32
+ * operation rounded to nearest even, so the bytes are reproducible bit for bit.
+ * d_x 16-byte aligned; k % 256 == 0.
+ */
+int q4k_quantize_rows(const float* d_x, int64_t rows, int k, void* d_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_stream_ceiling -- loads-only kernel over `bytes` of device memory (16-byte
+ * aligned, bytes % 16 == 0): the same coalesced 16-byte loads as the GEMV's weight
+ * stream, reduced to one XOR word per CTA in d_sink (grid-sized, caller-provided,
+ * at least q4k_stream_ceiling_sink_words() ints). A measurement tool: its
+ * bandwidth is the ceiling the weight stream can reach.
+ */
+int q4k_stream_ceiling_sink_words(void);
+int q4k_stream_ceiling(const void* d_src, uint64_t bytes, uint32_t* d_sink, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

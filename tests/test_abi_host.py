@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI (no GPU): the library builds for sm_103a, loads, exports
+every entry point include/q4kmoe.h declares, and rejects invalid arguments with the
+documented status before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_quantized_moe_q4k_gb300 as q4k
+from bit_quantized_moe_q4k_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4kmoe.h")
+
+A16 = 1 << 20          # a fake 16-byte-aligned address; never dereferenced by these calls
+MISALIGNED = A16 + 4
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:q4k|moe)_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_pages_calls():
+    names = declared_functions()
+    for required in ("q4k_moe_id_gemv", "q4k_expert_ffn_forward", "moe_combine_residual"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = q4k.load()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_lib.SIGNATURES) >= set(declared_functions())
+
+
+def _st(fn, *args):
+    lib = q4k.load()
+    return getattr(lib, fn)(*args)
+
+
+def gemv(**kw):
+    a = dict(w=A16, off=0, E=4, a=A16, outer=256, inner=0, ids=A16, m=3, T=2, n=64, k=256, out=A16, ws=None,
+             wsb=0, flag=None, stream=None)
+    a.update(kw)
+    return _st("q4k_moe_id_gemv", a["w"], a["off"], a["E"], a["a"], a["outer"], a["inner"], a["ids"], a["m"],
+               a["T"], a["n"], a["k"], a["out"], a["ws"], a["wsb"], a["flag"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=100), 2), (dict(k=0), 2), (dict(n=6), 2), (dict(n=0), 2), (dict(m=-1), 2), (dict(E=0), 2),
+    (dict(T=0), 3), (dict(T=17), 3), (dict(E=5000), 9), (dict(k=65536 + 256), 9),
+    (dict(w=None), 1), (dict(a=None), 1), (dict(ids=None), 1), (dict(out=None), 1),
+    (dict(w=MISALIGNED), 7), (dict(off=8), 7), (dict(a=MISALIGNED), 7), (dict(outer=255), 7), (dict(inner=2), 7),
+])
+def test_id_gemv_rejects(kw, status):
+    assert gemv(**kw) == status
+    assert q4k.load().q4k_last_error_string()  # a message is recorded
+
+
+def test_empty_batch_is_a_no_op_without_device_work():
+    assert gemv(m=0) == 0
+    assert gemv(off=144 * 16, m=0) == 0
+
+
+def test_ffn_and_layer_workspace_checks():
+    lib = q4k.load()
+    need = lib.q4k_moe_workspace_size(3, 2, 4, 512, 512)
+    assert need >= 3 * 2 * 512 * 4 and need % 256 == 0
+    args = [A16, A16, A16, 4, A16, A16, 3, 2, 256, 512, A16]
+    assert lib.q4k_expert_ffn_forward(*args, None, 0, None, None) == 4
+    assert lib.q4k_expert_ffn_forward(*args, A16, need - 1, None, None) == 4
+    assert lib.q4k_expert_ffn_forward(*args, A16 + 16, need, None, None) == 4  # not 256-byte aligned
+    lw = lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768)
+    assert lw >= (8 * 768 + 768 + 8 * 2048 + 2048) * 4
+    assert lib.q4k_moe_layer_workspace_size(1, 0, 128, 2048, 768, 768) == 0
+
+
+def test_layer_rejects_bad_mode_and_missing_shared():
+    lib = q4k.load()
+    base = [A16, A16, A16, 8]
+    tail_args = [A16, A16, A16, A16, A16, 1, 2, 256, 256, A16, None, 0, None, None]
+    assert lib.q4k_moe_layer_forward(*base, None, None, None, 256, 3, *tail_args) == 8
+    assert lib.q4k_moe_layer_forward(*base, None, None, None, 256, 1, *tail_args) == 1
+    assert lib.q4k_moe_layer_forward(*base, A16, A16, A16, 256, 1, A16, A16, A16, A16, None, 1, 2, 256, 256, A16,
+                                     None, 0, None, None) == 1  # sigmoid gate without logits
+
+
+def test_combine_rejects():
+    lib = q4k.load()
+    ok = [A16, A16, A16, A16, A16]
+    assert lib.moe_combine_residual(*ok, 3, 2, 2, 256, A16, None) == 8
+    assert lib.moe_combine_residual(*ok, 1, 2, 0, 256, A16, None) == 3
+    assert lib.moe_combine_residual(*ok, 1, 2, 2, 258, A16, None) == 2
+    assert lib.moe_combine_residual(A16, A16, A16, None, None, 2, 2, 2, 256, A16, None) == 1
+    assert lib.moe_combine_residual(*ok, 0, 0, 2, 256, A16, None) == 0  # m == 0
+
+
+def test_bucket_and_quantize_reject():
+    lib = q4k.load()
+    assert lib.q4k_moe_bucket(A16, -1, 4, A16, A16, A16, None, None) == 2
+    assert lib.q4k_moe_bucket(A16, 4, 0, A16, A16, A16, None, None) == 2
+    assert lib.q4k_moe_bucket(A16, 4, 4097, A16, A16, A16, None, None) == 9
+    assert lib.q4k_moe_bucket(None, 4, 4, A16, A16, A16, None, None) == 1
+    assert lib.q4k_quantize_rows(A16, 4, 300, A16, None) == 2
+    assert lib.q4k_quantize_rows(MISALIGNED, 4, 256, A16, None) == 7
+    assert lib.q4k_quantize_rows(A16, 0, 256, A16, None) == 0
+
+
+def test_binding_raises_with_status_name():
+    with pytest.raises(q4k.Q4KError) as ei:
+        _lib._check(2)
+    assert "Q4K_ERR_SHAPE" in str(ei.value)
