@@ -263,7 +263,10 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
 
     def graph_event():
         # events recorded inside a captured graph must be "external" to be timestamped
-        return torch.cuda.Event(enable_timing=True, external=True)
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True)
 
     ev_k = [(graph_event(), graph_event()) for _ in range(K)]
     g_warm, g_timed = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()

@@ -87,7 +87,7 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
                          hidden, 0, act_shared, 1, m, 1, shared_inter, hidden};
         ng = 2;
     }
-    return cuda_status(launch_idgemv(g, ng, true, err_flag, stream), "gate|up launch");
+    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream), "gate|up launch");
 }
 
 int run_down(const void* w_down, int num_experts, const float* act, const int32_t* ids, int m, int top_k,
@@ -102,7 +102,7 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
                          shared_out, 1, m, 1, hidden, shared_inter};
         ng = 2;
     }
-    return cuda_status(launch_idgemv(g, ng, false, err_flag, stream), "down launch");
+    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream), "down launch");
 }
 
 int run_ffn(const void* w_gate, const void* w_up, const void* w_down, int num_experts, const float* h_post,
@@ -186,7 +186,7 @@ int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_exp
         return fail(Q4K_ERR_ALIGN, "activations must be 16-byte aligned with non-negative strides that are multiples of 4 floats");
     if (m == 0) return Q4K_OK;
     GemvGroup g{w, nullptr, d_ids, d_a, src1_outer_stride, src1_inner_stride, d_out, num_experts, m, top_k, n, k};
-    return cuda_status(launch_idgemv(&g, 1, false, d_err_flag, stream), "id-gemv launch");
+    return cuda_status(launch_idgemv(&g, 1, false, false, d_err_flag, stream), "id-gemv launch");
 }
 
 int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,
@@ -223,7 +223,7 @@ int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const 
         return fail(Q4K_ERR_ALIGN, "rows must be 16-byte aligned");
     if (m == 0) return Q4K_OK;
     return cuda_status(launch_combine(d_h_mid, d_expert_out, d_weights, d_shared_out, d_shared_gate, shared_mode, m,
-                                      top_k, hidden, d_hidden_out, stream),
+                                      top_k, hidden, d_hidden_out, false, stream),
                        "combine launch");
 }
 
@@ -267,7 +267,7 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
                  d_ws_gate, d_ws_up, d_ws_down, shared_inter, act_shared, sout, d_err_flag, stream);
     if (st) return st;
     return cuda_status(launch_combine(d_h_mid, eout, d_weights, sout, d_shared_gate, shared_mode, m, top_k, hidden,
-                                      d_y, stream),
+                                      d_y, true, stream),
                        "combine launch");
 }
 

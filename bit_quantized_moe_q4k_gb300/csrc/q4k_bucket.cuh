@@ -16,19 +16,16 @@ __device__ __forceinline__ bool id_valid(int32_t e, int num_experts) {
     return e >= 0 && e < num_experts;
 }
 
-// Exclusive prefix sum of s[0..n) in place (n <= 4 * blockDim.x), called by every thread
-// of the block. s_warp: 33 ints of scratch. Returns the total. Ends with a barrier.
+// Exclusive prefix sum of s[0..n) in place, any n >= 0, called by every thread of the
+// block. Thread t owns the contiguous range [t*per, (t+1)*per). s_warp: 33 ints of
+// scratch. Returns the total. Ends with a barrier.
 __device__ __forceinline__ int block_exclusive_scan(int* s, int n, int* s_warp) {
     const int nt = blockDim.x, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = (nt + 31) >> 5;
-    const int per = (n + nt - 1) / nt;  // <= 4
-    int v[4] = {0, 0, 0, 0};
+    const int per = (n + nt - 1) / nt;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
     int local = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int idx = tid * per + i;
-        if (i < per && idx < n) { v[i] = s[idx]; local += v[i]; }
-    }
+    for (int i = lo; i < hi; ++i) local += s[i];
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -51,10 +48,10 @@ __device__ __forceinline__ int block_exclusive_scan(int* s, int n, int* s_warp) 
     __syncthreads();
     int run = s_warp[warp] + incl - local;
     const int total = s_warp[32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int idx = tid * per + i;
-        if (i < per && idx < n) { s[idx] = run; run += v[i]; }
+    for (int i = lo; i < hi; ++i) {
+        const int v = s[i];
+        s[i] = run;
+        run += v;
     }
     __syncthreads();
     return total;

@@ -65,6 +65,12 @@ __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// Programmatic dependent launch: let the next kernel in the stream start its prologue, and
+// wait for the previous kernel's results before reading them (no-ops without the launch
+// attribute).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // (scale, min) of sub-blocks ja = 2c and jb = 2c + 1 from the 16-byte block header
 // (d, dmin, 12 scale bytes; GGML Q4_K placement), multiplied by d and dmin.
 __device__ __forceinline__ void block_scales(uint4 h, int c, float& sa, float& ma, float& sb, float& mb) {
@@ -179,8 +185,13 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     __shared__ int s_items[kMaxGroups + 1];
     __shared__ int s_pairs[kTB];
     __shared__ int s_item_info[5];  // group, expert, tile, tokens, chunk
+    __shared__ int64_t s_rows[kTB];  // activation row offsets currently staged
+    __shared__ int s_staged_group, s_staged_nt, s_restage;
 
-    // ---- bucketing prologue: per group, counts then item offsets per expert
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) { s_staged_group = -1; s_staged_nt = 0; }
+
+    // ---- bucketing prologue (ids are inputs of the layer, not results of the previous kernel): per group, counts then item offsets per expert
     if (threadIdx.x == 0) s_items[0] = 0;
     for (int gi = 0; gi < P.n_groups; ++gi) {
         const GroupDev& G = P.g[gi];
@@ -198,18 +209,6 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         const int total = block_exclusive_scan(start, G.num_experts, s_warp);
         if (threadIdx.x == 0) s_items[gi + 1] = s_items[gi] + total;
         __syncthreads();
-    }
-    // out-of-range ids: flag and zero their rows (done once, by CTA 0)
-    if (blockIdx.x == 0) {
-        for (int gi = 0; gi < P.n_groups; ++gi) {
-            const GroupDev& G = P.g[gi];
-            if (!G.ids || s_bad[gi] == 0) continue;
-            if (threadIdx.x == 0) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
-            for (int p = 0; p < G.n_pairs; ++p) {
-                if (id_valid(G.ids[p], G.num_experts)) continue;
-                for (int r = threadIdx.x; r < G.n; r += kThreads) G.out[(int64_t)p * G.n + r] = 0.0f;
-            }
-        }
     }
     const int total_items = s_items[P.n_groups];
     uint8_t* xs = smem + P.x_off;
@@ -273,9 +272,29 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             } else if (lane < nt) {
                 s_pairs[lane] = chunk * P.tb + lane;
             }
+            __syncwarp();
+            // the same activation rows as the staged ones (e.g. every item of a broadcast
+            // gate/up walk at m = 1) need no restaging
+            bool same = s_staged_group == gi && s_staged_nt == nt;
+            if (lane < nt) {
+                const int p = s_pairs[lane];
+                const int64_t row = (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+                same = same && s_rows[lane] == row;
+            }
+            same = __all_sync(0xffffffffu, same);
+            if (lane == 0) s_restage = same ? 0 : 1;
         }
         __syncthreads();
-        stage_rows(G, s_pairs, nt, xs, meta);
+        const bool restage = s_restage != 0;
+        if (item == (int)blockIdx.x) pdl_wait();  // the activations may come from the previous kernel
+        if (restage) {
+            if (warp == 0 && lane < nt) {
+                const int p = s_pairs[lane];
+                s_rows[lane] = (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+            }
+            if (threadIdx.x == 0) { s_staged_group = gi; s_staged_nt = nt; }
+            stage_rows(G, s_pairs, nt, xs, meta);
+        }
         __syncthreads();
 
         // ---- main loop: lane (c, rl) streams 64-weight group c of every block of its row
@@ -336,6 +355,19 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         }
         __syncthreads();  // s_pairs / staged rows are rewritten by the next item
     }
+    // out-of-range ids: flag and zero their rows (CTA 0, after the previous kernel is done)
+    if (blockIdx.x == 0) {
+        pdl_wait();
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const GroupDev& G = P.g[gi];
+            if (!G.ids || s_bad[gi] == 0) continue;
+            if (threadIdx.x == 0) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
+            for (int p = 0; p < G.n_pairs; ++p) {
+                if (id_valid(G.ids[p], G.num_experts)) continue;
+                for (int r = threadIdx.x; r < G.n; r += kThreads) G.out[(int64_t)p * G.n + r] = 0.0f;
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -354,7 +386,7 @@ int num_sms() {
     return g_num_sms;
 }
 
-cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, int* err_flag,
+cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream) {
     GemvParams P{};
     P.n_groups = n_groups;
@@ -409,8 +441,17 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)num_sms() * per_sm;
     if (grid > max_items) grid = max_items;
-    kern<<<(unsigned)grid, kThreads, smem, stream>>>(P);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
 }  // namespace q4k

@@ -32,7 +32,7 @@ cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int3
                           int32_t* offsets, int32_t* perm, int* err_flag, cudaStream_t stream);
 cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
                            const float* shared_out, const float* shared_gate, int shared_mode, int m,
-                           int top_k, int hidden, float* y, cudaStream_t stream);
+                           int top_k, int hidden, float* y, bool pdl, cudaStream_t stream);
 cudaError_t launch_quantize(const float* x, int64_t rows, int k, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_stream_ceiling(const void* src, uint64_t bytes, uint32_t* sink, cudaStream_t stream);
 int stream_ceiling_grid();
@@ -50,7 +50,9 @@ struct GemvGroup {
 
 // Launch the bucketed Q4_K id-GEMV over up to two groups in one grid (the routed experts
 // and the shared expert of a layer). fused_swiglu: out = silu(w . x) * (w2 . x).
-cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, int* err_flag,
+// pdl: the launch may start while the previous kernel of the stream drains (programmatic
+// dependent launch); the kernel waits for it before reading activations.
+cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream);
 
 int num_sms();

@@ -87,9 +87,12 @@ combine_kernel(const float* h_mid, const float* __restrict__ expert_out, const f
                int top_k, int hidden, float* y) {
     const int t = blockIdx.y;
     const int h4 = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index within the row
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (h4 * 4 >= hidden) return;
     const int64_t row = (int64_t)t * hidden + h4 * 4;
     float4 acc = *reinterpret_cast<const float4*>(h_mid + row);
+    // expert and shared outputs come from the previous kernel (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int s = 0; s < top_k; ++s) {
         const int64_t p = (int64_t)t * top_k + s;
         const float w = weights[p];
@@ -112,12 +115,20 @@ combine_kernel(const float* h_mid, const float* __restrict__ expert_out, const f
 
 cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
                            const float* shared_out, const float* shared_gate, int shared_mode, int m,
-                           int top_k, int hidden, float* y, cudaStream_t stream) {
+                           int top_k, int hidden, float* y, bool pdl, cudaStream_t stream) {
     const int threads = 256;
     dim3 grid((hidden / 4 + threads - 1) / threads, m);
-    combine_kernel<<<grid, threads, 0, stream>>>(h_mid, expert_out, weights, shared_out, shared_gate,
-                                                 shared_mode, top_k, hidden, y);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, h_mid, expert_out, weights, shared_out, shared_gate,
+                              shared_mode, top_k, hidden, y);
 }
 
 // ------------------------------------------------------------------------------------------
