@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--layers", type=int, default=0, help="size of the layer rotation (default: > 3x L2 touched)")
     return ap.parse_args()
 
 
@@ -191,6 +192,8 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     ids0 = inputs.make_ids(W.seed, W.ids, m, T, E)
     per_layer_touched = layer_bytes(W, ids0)["layer"]
     n_layers = int(min(64, max(4, -(-3 * L2_BYTES // per_layer_touched))))
+    if args.layers:
+        n_layers = args.layers
     slab_total = E * (2 * slab_bytes(I, H) + slab_bytes(H, I))
     while n_layers > 2 and n_layers * slab_total > 120e9:
         n_layers -= 1

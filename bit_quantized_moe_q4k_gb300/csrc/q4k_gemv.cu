@@ -56,6 +56,7 @@ struct GemvParams {
     int x_off;              // byte offset of the staged activations
     int meta_off;           // byte offset of the per-sub-block (delta, sumX) pairs
     int kmax;               // largest k of the groups (sizes the staging area)
+    int tc_min;             // > 0: experts with at least this many pairs are left to the tensor-core path
     int* err_flag;
 };
 
@@ -204,7 +205,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             __syncthreads();
         }
         for (int e = threadIdx.x; e < G.num_experts; e += kThreads)
-            start[e] = ((cnt[e] + P.tb - 1) / P.tb) * G.tiles;
+            start[e] = (P.tc_min > 0 && cnt[e] >= P.tc_min) ? 0 : ((cnt[e] + P.tb - 1) / P.tb) * G.tiles;
         __syncthreads();
         const int total = block_exclusive_scan(start, G.num_experts, s_warp);
         if (threadIdx.x == 0) s_items[gi + 1] = s_items[gi] + total;
@@ -387,10 +388,16 @@ int num_sms() {
 }
 
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, int tc_min, uint8_t* const* tc_img) {
+    if (tc_min > 0) {
+        cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
+        if (e != cudaSuccess) return e;
+        pdl = false;  // the tensor-core kernels precede this launch in the stream
+    }
     GemvParams P{};
     P.n_groups = n_groups;
     P.err_flag = err_flag;
+    P.tc_min = tc_min;
     int ints = 0, kmax = 0;
     int64_t max_items = 0;
     for (int gi = 0; gi < n_groups; ++gi) {

@@ -52,8 +52,14 @@ struct GemvGroup {
 // and the shared expert of a layer). fused_swiglu: out = silu(w . x) * (w2 . x).
 // pdl: the launch may start while the previous kernel of the stream drains (programmatic
 // dependent launch); the kernel waits for it before reading activations.
+// tc_min > 0: experts with at least tc_min pairs run on the tensor-core grouped GEMM
+// (q4k_tc.cu) first, using tc_img[g] (tc_image_bytes of the group) as scratch; the rest run on
+// the id-GEMV kernel.
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
-                          cudaStream_t stream);
+                          cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr);
+cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
+                      int* err_flag, cudaStream_t stream);
+size_t tc_image_bytes(int n_pairs, int k, int tc_min);
 
 int num_sms();
 

@@ -153,7 +153,8 @@ quantize_kernel(const float* __restrict__ x, int64_t n_blocks, uint8_t* __restri
 #pragma unroll
     for (int i = 0; i < 32; ++i) { lo = fminf(lo, v[i]); hi = fmaxf(hi, v[i]); }
     const float scale = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-    const float mn = -lo;
+    // -lo, but +0 when lo is zero: the block's dmin = fp16(max mn / 63) must not become -0
+    const float mn = __fsub_rn(0.0f, lo);
     float max_scale = scale, max_mn = mn;
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) {

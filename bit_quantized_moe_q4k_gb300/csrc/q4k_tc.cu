@@ -1,0 +1,557 @@
+// q4k_tc.cu -- tensor-core grouped GEMM (tcgen05) for experts whose bucket holds many tokens.
+//
+// Same result as the id-GEMV for those experts (ferrum-kernels q4_k_moe_id_gemv_batched.rs:
+// out[p, r] = W_{ids[p]}[r, :] . x_p; with two slabs, silu(gate) * up), computed as a dense
+// contraction per (expert, 128-row tile, chunk of 32 tokens of the expert's bucket):
+//   D[r, t] = sum_k A[r, k] * B[t, k]
+// with A in tensor memory and B in shared memory (tcgen05.mma, kind::f16, fp32 accumulation).
+//
+// Exactness of the operands. Q4_K gives per 32-weight sub-block j of a 256-weight block
+//   sum_k w_k x_k = d * sum_j sc_j sum_{k in j} q_k x_k  -  dmin * sum_j m_j sum_{k in j} x_k.
+// A holds the integers sc_j * q_k (<= 945, exact in fp16), so the only rounding in the main
+// product is that of x to fp16. A second, 16-deep MMA per block computes sum_j m_j * sx_j
+// with sx_j = sum_{k in j} x_k split into two fp16 halves (hi + lo), i.e. to ~2^-22. The
+// per-block factors d and dmin are applied in fp32 by the epilogue, which reads each block's
+// two partial accumulators from tensor memory (double-buffered, so the next block's MMAs
+// run meanwhile).
+//
+// Roles (6 warps): warps 0-3 dequantize (thread = weight row = TMEM lane) and run the
+// epilogue; warp 4 issues the bulk copies (raw Q4_K rows of the tile, and the prepared B
+// image of the block); warp 5 owns tensor memory and issues the MMAs. Raw rows -> registers
+// -> A: dequantization writes each row's 256 weights as 128 fp16-pair columns with
+// tcgen05.st (the A operand never touches shared memory). Pipelines of depth 2 on mbarriers;
+// every wait is bounded and an abort flag lets all roles leave together.
+//
+// The B image of a (chunk, block) is built once by tc_prep_kernel in the workspace: the 32
+// tokens' x in fp16, in the k order of the A columns, already laid out as the 128-byte
+// swizzled K-major smem tile, plus the sx hi/lo row of the min-term MMA.
+#include <cuda_fp16.h>
+
+#include "q4k_bucket.cuh"
+#include "q4k_internal.cuh"
+#include "q4k_sm100.cuh"
+
+namespace q4k {
+using namespace sm100;
+
+constexpr int kTcThreads = 192;
+constexpr int kTcRows = 128;                  // M (TMEM lanes)
+constexpr int kTcTok = 32;                    // N (tokens per chunk)
+constexpr int kImgB = 4 * kTcTok * 128;       // 4 panels of [32 tokens x 128 B]
+constexpr int kImgB2 = kTcTok * 128;          // min-term operand [32 tokens x 128 B]
+constexpr int kImgBlock = kImgB + kImgB2;     // bytes of one block's B image
+constexpr int kRawStage = kTcRows * kBlockBytes;
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns: A stages (128 each), min-term A stages (16 each), D1 and D2 (32 each)
+constexpr uint32_t kColA = 0, kColA2 = 256, kColD1 = 288, kColD2 = 352;
+
+struct TcGroup {
+    const uint8_t* w;    // slab [E][n][k/256] blocks
+    const uint8_t* w2;   // second slab (up) for silu(gate)*up, or null
+    const int32_t* ids;  // or null: every pair uses expert 0
+    const float* a;
+    int64_t outer, inner;
+    float* out;
+    uint8_t* img;        // B images [max_chunks][nb][kImgBlock]
+    int64_t nb01, nb02;
+    int num_experts, n_pairs, top_k, n, k, tiles;
+};
+
+struct TcParams {
+    TcGroup g[2];
+    int n_groups;
+    int tc_min;       // experts with at least this many pairs take the tensor-core path
+    int hist_off[2];  // int offsets of each group's tables in shared memory
+    int tab_off;      // byte offset of the tables
+    int* err_flag;
+};
+
+// Per-CTA bucketing for the tensor-core path: cnt[e] pairs per expert and start[e] = first
+// chunk id of expert e (exclusive prefix of ceil(cnt/32) over experts with cnt >= tc_min).
+// Returns the number of chunks.
+__device__ __forceinline__ int tc_chunks(const TcGroup& G, int tc_min, int* cnt, int* start, int* s_warp,
+                                         int* s_bad) {
+    if (G.ids) {
+        block_histogram(G.ids, G.n_pairs, G.num_experts, cnt, s_bad);
+    } else {
+        if (threadIdx.x == 0) { cnt[0] = G.n_pairs; *s_bad = 0; }
+        __syncthreads();
+    }
+    for (int e = threadIdx.x; e < G.num_experts; e += blockDim.x)
+        start[e] = cnt[e] >= tc_min ? (cnt[e] + kTcTok - 1) / kTcTok : 0;
+    __syncthreads();
+    return block_exclusive_scan(start, G.num_experts, s_warp);
+}
+
+// chunk id q -> expert (last e with start[e] <= q; it has chunks)
+__device__ __forceinline__ int tc_expert_of(const int* start, int num_experts, int q) {
+    int lo = 0, hi = num_experts - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (start[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void tc_gather(const TcGroup& G, int e, int chunk, int nt, int* s_pairs) {
+    const int lane = threadIdx.x & 31;
+    if (G.ids) {
+        warp_gather_bucket(G.ids, G.n_pairs, e, chunk * kTcTok, nt, s_pairs);
+    } else if (lane < nt) {
+        s_pairs[lane] = chunk * kTcTok + lane;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// B images: grid (max chunks, groups), 128 threads. Warp w builds tokens t = w, w+4, ...
+__global__ void __launch_bounds__(128)
+tc_prep_kernel(const __grid_constant__ TcParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int s_warp[33];
+    __shared__ int s_bad;
+    __shared__ int s_pairs[kTcTok];
+    __shared__ int s_info[3];
+    const int gi = blockIdx.y;
+    const TcGroup& G = P.g[gi];
+    int* cnt = reinterpret_cast<int*>(smem);
+    int* start = cnt + G.num_experts;
+    const int total = tc_chunks(G, P.tc_min, cnt, start, s_warp, &s_bad);
+    const int q = blockIdx.x;
+    if (q >= total) return;
+    if (threadIdx.x == 0) {
+        const int e = tc_expert_of(start, G.num_experts, q);
+        s_info[0] = e;
+        s_info[1] = q - start[e];
+        s_info[2] = min(kTcTok, cnt[e] - (q - start[e]) * kTcTok);
+    }
+    __syncthreads();
+    const int e = s_info[0], chunk = s_info[1], nt = s_info[2];
+    if (threadIdx.x < 32) tc_gather(G, e, chunk, nt, s_pairs);
+    // the activations may be the previous kernel's output
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c4 = lane >> 3, ip = lane & 7;
+    const int nb = G.k / kQK;
+    uint8_t* img0 = G.img + (int64_t)q * nb * kImgBlock;
+    for (int b = 0; b < nb; ++b) {
+        uint8_t* img = img0 + (int64_t)b * kImgBlock;
+        for (int t = warp; t < kTcTok; t += 4) {
+            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+            if (t < nt) {
+                const int p = s_pairs[t];
+                const float* row = G.a + (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner +
+                                   (int64_t)b * kQK + 64 * c4 + 4 * ip;
+                lo = *reinterpret_cast<const float4*>(row);
+                hi = *reinterpret_cast<const float4*>(row + 32);
+            }
+            // k order of the A columns: elements 4i'+{0,2,1,3} then 32+4i'+{0,2,1,3} of group c4
+            const __half2 h0 = __floats2half2_rn(lo.x, lo.z), h1 = __floats2half2_rn(lo.y, lo.w);
+            const __half2 h2 = __floats2half2_rn(hi.x, hi.z), h3 = __floats2half2_rn(hi.y, hi.w);
+            uint4 chunk16;
+            chunk16.x = *reinterpret_cast<const uint32_t*>(&h0);
+            chunk16.y = *reinterpret_cast<const uint32_t*>(&h1);
+            chunk16.z = *reinterpret_cast<const uint32_t*>(&h2);
+            chunk16.w = *reinterpret_cast<const uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(img + c4 * (kTcTok * 128) + t * 128 + ((ip ^ (t & 7)) << 4)) = chunk16;
+            // sub-block sums (fp32) of sub-blocks 2*c4 (lo) and 2*c4+1 (hi) over the 8 lanes of c4
+            float sl = (lo.x + lo.y) + (lo.z + lo.w), sh = (hi.x + hi.y) + (hi.z + hi.w);
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                sl += __shfl_xor_sync(0xffffffffu, sl, off);
+                sh += __shfl_xor_sync(0xffffffffu, sh, off);
+            }
+            // lane 0 gathers sx_0..7 and writes the min-term row: [hi(sx_0..7) | lo(sx_0..7)]
+            float sx[8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                sx[2 * c] = __shfl_sync(0xffffffffu, sl, 8 * c);
+                sx[2 * c + 1] = __shfl_sync(0xffffffffu, sh, 8 * c);
+            }
+            if (lane == 0) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const __half a0 = __float2half_rn(sx[2 * i]), a1 = __float2half_rn(sx[2 * i + 1]);
+                    const __half b0 = __float2half_rn(sx[2 * i] - __half2float(a0));
+                    const __half b1 = __float2half_rn(sx[2 * i + 1] - __half2float(a1));
+                    hw[i] = (uint32_t)__half_as_ushort(a0) | ((uint32_t)__half_as_ushort(a1) << 16);
+                    lw[i] = (uint32_t)__half_as_ushort(b0) | ((uint32_t)__half_as_ushort(b1) << 16);
+                }
+                uint8_t* r2 = img + kImgB + t * 128;
+                *reinterpret_cast<uint4*>(r2 + ((0 ^ (t & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(r2 + ((1 ^ (t & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+__device__ __forceinline__ __half2 hfma2_bits(uint32_t a, __half2 b, __half2 c) {
+    return __hfma2(*reinterpret_cast<__half2*>(&a), b, c);
+}
+
+// item -> (expert, tile, chunk, tokens): items of expert e are [start[e]*tiles,
+// (start[e] + chunks_e)*tiles), chunk fastest, so the chunks of one row tile run together
+// and share its weight reads in L2
+struct TcItem { int e, tile, chunk, nt; };
+__device__ __forceinline__ TcItem tc_item(const TcGroup& G, const int* cnt, const int* start, int item) {
+    int lo = 0, hi = G.num_experts - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (start[mid] * G.tiles <= item) lo = mid; else hi = mid - 1;
+    }
+    TcItem it;
+    it.e = lo;
+    const int chunks_e = (cnt[lo] + kTcTok - 1) / kTcTok;
+    const int local = item - start[lo] * G.tiles;
+    it.tile = local / chunks_e;
+    it.chunk = local % chunks_e;
+    it.nt = min(kTcTok, cnt[lo] - it.chunk * kTcTok);
+    return it;
+}
+
+__device__ __forceinline__ void producers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Persistent: grid = (SMs, groups); each CTA walks items grid-stride. A global step counter
+// (one step = one Q4_K block of one slab) carries the stage index and mbarrier parity
+// across items; tensor memory is allocated once per CTA.
+template <bool FUSED>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemm_kernel(const __grid_constant__ TcParams P) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* bimg = smem;                          // 2 x kImgBlock (1024-byte aligned stages)
+    uint8_t* raw = smem + 2 * kImgBlock;           // 2 x kRawStage
+    int* tabs = reinterpret_cast<int*>(smem + P.tab_off);
+    __shared__ __align__(8) uint64_t bar_raw_full[2], bar_raw_empty[2], bar_a_full[2], bar_a_empty[2];
+    __shared__ __align__(8) uint64_t bar_b_full[2], bar_b_empty[2], bar_d_full[2], bar_d_empty[2], bar_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_warp[33];
+    __shared__ int s_bad;
+    __shared__ int s_pairs[kTcTok];
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gi = blockIdx.y;
+    const TcGroup& G = P.g[gi];
+    int* cnt = tabs + P.hist_off[gi];
+    int* start = cnt + G.num_experts;
+    const int total_items = tc_chunks(G, P.tc_min, cnt, start, s_warp, &s_bad) * G.tiles;
+    if ((int)blockIdx.x >= total_items) return;  // uniform per CTA: before any allocation
+
+    if (warp == 5) {
+        tmem_alloc(&s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_raw_full[i], 1);
+            mbar_init(&bar_raw_empty[i], 128);
+            mbar_init(&bar_a_full[i], 128);
+            mbar_init(&bar_a_empty[i], 1);
+            mbar_init(&bar_b_full[i], 1);
+            mbar_init(&bar_b_empty[i], 1);
+            mbar_init(&bar_d_full[i], 1);
+            mbar_init(&bar_d_empty[i], 128);
+        }
+        mbar_init(&bar_drain, 1);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const int nb = G.k / kQK;
+    const int nslab = FUSED ? 2 : 1;
+    const int steps = nslab * nb;
+
+    if (warp == 4) {
+        // ---------------- copy producer: raw rows of the tile and the block's B image
+        int gs = 0;  // global step
+        int raw_issued = 0, b_issued = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
+            const TcItem it = tc_item(G, cnt, start, item);
+            const int row0 = it.tile * kTcRows;
+            const int rows_valid = min(kTcRows, G.n - row0);
+            const uint8_t* img = G.img + (int64_t)(start[it.e] + it.chunk) * nb * kImgBlock;
+            for (int s = 0; s < steps; ++s, ++gs) {
+                const int st = gs & 1;
+                const uint32_t ph = (gs >> 1) & 1;
+                const int slab = s / nb, b = s % nb;
+                const uint8_t* w = (slab == 0 ? G.w : G.w2) + (int64_t)it.e * G.nb02 + (int64_t)row0 * G.nb01 +
+                                   (int64_t)b * kBlockBytes;
+                int okl = 1;
+                if (lane == 0) {
+                    okl = mbar_wait(&bar_raw_empty[st], ph ^ 1, &s_abort);
+                    if (okl) mbar_arrive_expect_tx(&bar_raw_full[st], (uint32_t)rows_valid * kBlockBytes);
+                }
+                if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+                for (int r = lane; r < rows_valid; r += 32)
+                    bulk_g2s(raw + st * kRawStage + r * kBlockBytes, w + (int64_t)r * G.nb01, kBlockBytes,
+                             &bar_raw_full[st]);
+                raw_issued = gs + 1;
+                if (lane == 0) {
+                    okl = mbar_wait(&bar_b_empty[st], ph ^ 1, &s_abort);
+                    if (okl) {
+                        mbar_arrive_expect_tx(&bar_b_full[st], kImgBlock);
+                        bulk_g2s(bimg + st * kImgBlock, img + (int64_t)b * kImgBlock, kImgBlock, &bar_b_full[st]);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+                b_issued = gs + 1;
+            }
+        }
+        if (!ok && lane == 0) {
+            // let the copies already issued land before the CTA leaves (bounded)
+            volatile int never = 0;
+            for (int g = max(0, raw_issued - 2); g < raw_issued; ++g) mbar_wait(&bar_raw_full[g & 1], (g >> 1) & 1, &never);
+            for (int g = max(0, b_issued - 2); g < b_issued; ++g) mbar_wait(&bar_b_full[g & 1], (g >> 1) & 1, &never);
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer (one thread)
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kTcRows, kTcTok);
+            const uint32_t bimg_addr = smem_u32(bimg);
+            int gs = 0, issued = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
+                for (int s = 0; s < steps; ++s, ++gs) {
+                    const int st = gs & 1;
+                    const uint32_t ph = (gs >> 1) & 1;
+                    if (!mbar_wait(&bar_a_full[st], ph, &s_abort) || !mbar_wait(&bar_b_full[st], ph, &s_abort) ||
+                        !mbar_wait(&bar_d_empty[st], ph ^ 1, &s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b_addr = bimg_addr + st * kImgBlock;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const uint64_t bd = desc_sw128_kmajor(b_addr + (kk >> 2) * (kTcTok * 128) + (kk & 3) * 32);
+                        mma_f16_ts(tmem + kColD1 + st * 32, tmem + kColA + st * 128 + 8 * kk, bd, idesc, kk > 0);
+                    }
+                    mma_f16_ts(tmem + kColD2 + st * 32, tmem + kColA2 + st * 16, desc_sw128_kmajor(b_addr + kImgB),
+                               idesc, 0);
+                    mma_commit(&bar_a_empty[st]);
+                    mma_commit(&bar_b_empty[st]);
+                    mma_commit(&bar_d_full[st]);
+                    issued = gs + 1;
+                }
+            }
+            if (!ok) {
+                s_abort = 1;
+                raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+                if (issued > 0) {  // outstanding MMAs finish before tensor memory is freed
+                    volatile int never = 0;
+                    mma_commit(&bar_drain);
+                    mbar_wait(&bar_drain, 0, &never);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- dequantize (thread = row = TMEM lane) and epilogue
+        const int r = tid;  // 0..127
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        int gs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
+            const TcItem it = tc_item(G, cnt, start, item);
+            const int row0 = it.tile * kTcRows;
+            const int rows_valid = min(kTcRows, G.n - row0);
+            producers_sync();  // the previous item's outputs are written
+            if (warp == 0) tc_gather(G, it.e, it.chunk, it.nt, s_pairs);
+            producers_sync();
+            float acc[kTcTok], accg[kTcTok];
+#pragma unroll
+            for (int t = 0; t < kTcTok; ++t) { acc[t] = 0.f; accg[t] = 0.f; }
+            float d_prev = 0.f, dmin_prev = 0.f;
+            for (int s = 0; s <= steps; ++s) {
+                const int g_cur = gs + s;
+                const int st = g_cur & 1;
+                const uint32_t ph = (g_cur >> 1) & 1;
+                float d_cur = 0.f, dmin_cur = 0.f;
+                if (s < steps) {
+                    if (!mbar_wait(&bar_raw_full[st], ph, &s_abort)) { ok = false; break; }
+                    const uint4* rp = reinterpret_cast<const uint4*>(raw + st * kRawStage + r * kBlockBytes);
+                    uint4 hq[9];
+#pragma unroll
+                    for (int i = 0; i < 9; ++i) hq[i] = rp[i];
+                    mbar_arrive(&bar_raw_empty[st]);
+                    const uint4 h = hq[0];
+                    d_cur = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
+                    dmin_cur = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                    int sc[8], mn[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const unsigned y = (h.y >> (8 * j)) & 0xFFu, z = (h.z >> (8 * j)) & 0xFFu;
+                        const unsigned w = (h.w >> (8 * j)) & 0xFFu;
+                        sc[j] = y & 63u;
+                        mn[j] = z & 63u;
+                        sc[j + 4] = (w & 15u) | ((y >> 6) << 4);
+                        mn[j + 4] = (w >> 4) | ((z >> 6) << 4);
+                    }
+                    if (!mbar_wait(&bar_a_empty[st], ph ^ 1, &s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                    // A columns: code word i -> columns 4i..4i+3 = low nibbles of bytes (0,2), (1,3),
+                    // high nibbles of bytes (0,2), (1,3), each the exact fp16 pair sc_j * q
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {  // 32 columns = 8 code words = 64-weight group g
+                        const __half2 klo = __half2half2(__int2half_rn(sc[2 * g]));
+                        const __half2 clo = __half2half2(__int2half_rn(-1024 * sc[2 * g]));
+                        const __half2 khi = __half2half2(__float2half_rn((float)sc[2 * g + 1] * 0.0625f));
+                        const __half2 chi = __half2half2(__int2half_rn(-64 * sc[2 * g + 1]));
+                        uint32_t col[32];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int wi = 8 * g + i;
+                            const uint4 qv = hq[1 + (wi >> 2)];
+                            const uint32_t wq = (wi & 3) == 0 ? qv.x : (wi & 3) == 1 ? qv.y : (wi & 3) == 2 ? qv.z : qv.w;
+                            const uint32_t w8 = wq >> 8;
+                            col[4 * i + 0] = h2_bits(hfma2_bits((wq & 0x000F000Fu) | 0x64006400u, klo, clo));
+                            col[4 * i + 1] = h2_bits(hfma2_bits((w8 & 0x000F000Fu) | 0x64006400u, klo, clo));
+                            col[4 * i + 2] = h2_bits(hfma2_bits((wq & 0x00F000F0u) | 0x64006400u, khi, chi));
+                            col[4 * i + 3] = h2_bits(hfma2_bits((w8 & 0x00F000F0u) | 0x64006400u, khi, chi));
+                        }
+                        tmem_st32(tmem + lane_base + kColA + st * 128 + 32 * g, col);
+                    }
+                    uint32_t a2[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __half2 mm = __halves2half2(__int2half_rn(mn[2 * i]), __int2half_rn(mn[2 * i + 1]));
+                        a2[i] = a2[i + 4] = h2_bits(mm);
+                    }
+                    tmem_st8(tmem + lane_base + kColA2 + st * 16, a2);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bar_a_full[st]);
+                }
+                if (s >= 1) {
+                    // epilogue of step s-1: acc += d * D1 - dmin * D2
+                    const int pg = g_cur - 1;
+                    const int ps = pg & 1;
+                    const uint32_t pph = (pg >> 1) & 1;
+                    if (!mbar_wait(&bar_d_full[ps], pph, &s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t d1[32], d2[32];
+                    tmem_ld32(tmem + lane_base + kColD1 + ps * 32, d1);
+                    tmem_ld32(tmem + lane_base + kColD2 + ps * 32, d2);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&bar_d_empty[ps]);
+#pragma unroll
+                    for (int t = 0; t < kTcTok; ++t)
+                        acc[t] = fmaf(d_prev, __uint_as_float(d1[t]), fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[t]));
+                    if (FUSED && s - 1 == nb - 1) {  // the gate slab is complete
+#pragma unroll
+                        for (int t = 0; t < kTcTok; ++t) { accg[t] = acc[t]; acc[t] = 0.f; }
+                    }
+                }
+                d_prev = d_cur;
+                dmin_prev = dmin_cur;
+            }
+            if (!ok) break;
+            gs += steps;
+            if (r < rows_valid) {
+#pragma unroll
+                for (int t = 0; t < kTcTok; ++t) {
+                    if (t < it.nt) {
+                        float v = acc[t];
+                        if (FUSED) v = (accg[t] / (1.0f + __expf(-accg[t]))) * acc[t];
+                        G.out[(int64_t)s_pairs[t] * G.n + row0 + r] = v;
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            s_abort = 1;
+            raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------------------------------
+int64_t tc_max_chunks(int n_pairs, int tc_min) {
+    // sum over experts with >= tc_min pairs of ceil(cnt/32) <= n_pairs/32 + n_pairs/tc_min
+    return (int64_t)n_pairs / kTcTok + (int64_t)n_pairs / tc_min + 1;
+}
+
+size_t tc_image_bytes(int n_pairs, int k, int tc_min) {
+    return (size_t)tc_max_chunks(n_pairs, tc_min) * (size_t)(k / kQK) * kImgBlock;
+}
+
+static bool g_tc_attr_set[2][64] = {};
+
+cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
+                      int* err_flag, cudaStream_t stream) {
+    TcParams P{};
+    P.n_groups = n_groups;
+    P.tc_min = tc_min;
+    P.err_flag = err_flag;
+    int ints = 0;
+    int64_t max_chunks = 0;
+    int max_tiles = 0;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        const GemvGroup& S = groups[gi];
+        TcGroup& G = P.g[gi];
+        G.w = S.w; G.w2 = S.w2; G.ids = S.ids; G.a = S.a; G.out = S.out; G.img = img[gi];
+        G.outer = S.outer; G.inner = S.inner;
+        G.nb01 = (int64_t)(S.k / kQK) * kBlockBytes;
+        G.nb02 = (int64_t)S.n * G.nb01;
+        G.num_experts = S.num_experts; G.n_pairs = S.m * S.top_k; G.top_k = S.top_k; G.n = S.n; G.k = S.k;
+        G.tiles = (S.n + kTcRows - 1) / kTcRows;
+        P.hist_off[gi] = ints;
+        ints += 2 * S.num_experts;
+        const int64_t mc = tc_max_chunks(G.n_pairs, tc_min);
+        max_chunks = mc > max_chunks ? mc : max_chunks;
+        max_tiles = G.tiles > max_tiles ? G.tiles : max_tiles;
+    }
+    if (max_chunks == 0) return cudaSuccess;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    // prep: B images
+    {
+        const size_t smem = (size_t)ints * 4;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)max_chunks, n_groups);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, tc_prep_kernel, P);
+        if (err != cudaSuccess) return err;
+    }
+    P.tab_off = 2 * kImgBlock + 2 * kRawStage;
+    // every CTA holds all 512 tensor-memory columns: ask for enough shared memory that only
+    // one CTA fits on an SM
+    size_t smem = 1024 + (size_t)P.tab_off + (size_t)ints * 4;
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    auto kern = fused ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!g_tc_attr_set[fused ? 1 : 0][dev]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (err != cudaSuccess) return err;
+        g_tc_attr_set[fused ? 1 : 0][dev] = true;
+    }
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    int64_t grid = (int64_t)max_chunks * max_tiles;
+    if (grid > num_sms()) grid = num_sms();
+    kern<<<dim3((unsigned)grid, n_groups), kTcThreads, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace q4k

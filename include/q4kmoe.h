@@ -61,7 +61,8 @@ typedef enum {
     Q4K_ERR_EXPERT_ID = 6, /* device flag value: some id was outside [0, num_experts)        */
     Q4K_ERR_ALIGN = 7,     /* slab not 16-byte aligned, or activation rows not 16-byte aligned */
     Q4K_ERR_MODE = 8,      /* shared_mode not in {0, 1, 2}                                   */
-    Q4K_ERR_LIMIT = 9      /* a size beyond an implementation limit (see each call)          */
+    Q4K_ERR_LIMIT = 9,     /* a size beyond an implementation limit (see each call)          */
+    Q4K_ERR_TIMEOUT = 10   /* device flag value: a pipeline wait in a kernel gave up (bounded) */
 } q4k_status;
 
 #define Q4K_MAX_TOP_K 16
