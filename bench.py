@@ -243,15 +243,20 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    ws_gu_bytes = q4k.q4k_moe_layer_half_workspace_size(m, T, H, Is, H)
+    ws_dn_bytes = q4k.q4k_moe_layer_half_workspace_size(m, T, I, Is, Is)
+    ws_gu = torch.empty(max(256, ws_gu_bytes), dtype=torch.uint8, device=dev)
+    ws_dn = torch.empty(max(256, ws_dn_bytes), dtype=torch.uint8, device=dev)
+
     def step(L, ev=None):
         if ev is not None:
             ev[0].record(stream)
         q4k.q4k_moe_layer_gate_up(L["wg"], L["wu"], E, L["sg"], L["su"], Is, L["x"], L["ids"], m, T, H, I, act,
-                                  act_s if Is else None, flag, stream)
+                                  act_s if Is else None, ws_gu, ws_gu_bytes, flag, stream)
         if ev is not None:
             ev[1].record(stream)
         q4k.q4k_moe_layer_down(L["wd"], E, L["sd"], Is, act, act_s if Is else None, L["ids"], m, T, H, I, eout,
-                               sout if Is else None, flag, stream)
+                               sout if Is else None, ws_dn, ws_dn_bytes, flag, stream)
         q4k.moe_combine_residual(L["hm"], eout, L["rw"], sout if Is else None, L["gl"] if W.shared_mode == 1 else None,
                                  W.shared_mode, m, T, H, y, stream)
 

@@ -20,6 +20,7 @@ Q4K_OK = 0
 STATUS_NAMES = {
     0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_TOPK", 4: "Q4K_ERR_WORKSPACE",
     5: "Q4K_ERR_CUDA", 6: "Q4K_ERR_EXPERT_ID", 7: "Q4K_ERR_ALIGN", 8: "Q4K_ERR_MODE", 9: "Q4K_ERR_LIMIT",
+    10: "Q4K_ERR_TIMEOUT",
 }
 SHARED_NONE, SHARED_SIGMOID, SHARED_UNSCALED = 0, 1, 2
 
@@ -39,8 +40,9 @@ SIGNATURES = {
                                    _P, _SZ, _P, _P]),
     "q4k_moe_layer_forward_host": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                         _P, _P, _SZ, _P, _P]),
-    "q4k_moe_layer_gate_up": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
-    "q4k_moe_layer_down": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "q4k_moe_layer_gate_up": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
+    "q4k_moe_layer_down": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
+    "q4k_moe_layer_half_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "q4k_quantize_rows": (_I, [_P, _I64, _I, _P, _P]),
     "q4k_stream_ceiling_sink_words": (_I, []),
     "q4k_stream_ceiling": (_I, [_P, _U64, _P, _P]),
@@ -178,20 +180,25 @@ def q4k_moe_layer_forward_host(w_gate, w_up, w_down, num_experts, ws_gate, ws_up
                                              _stream(stream)))
 
 
+def q4k_moe_layer_half_workspace_size(m, top_k, k_routed, shared_inter, k_shared) -> int:
+    return int(load().q4k_moe_layer_half_workspace_size(m, top_k, k_routed, shared_inter, k_shared))
+
+
 def q4k_moe_layer_gate_up(w_gate, w_up, num_experts, ws_gate, ws_up, shared_inter, h_post, ids, m, top_k, hidden,
-                          inter, act, act_shared, err_flag=None, stream=None):
-    _cuda(w_gate, w_up, ws_gate, ws_up, h_post, ids, act, act_shared, err_flag)
+                          inter, act, act_shared, workspace=None, ws_bytes=0, err_flag=None, stream=None):
+    _cuda(w_gate, w_up, ws_gate, ws_up, h_post, ids, act, act_shared, workspace, err_flag)
     _check(load().q4k_moe_layer_gate_up(_ptr(w_gate), _ptr(w_up), num_experts, _ptr(ws_gate), _ptr(ws_up),
                                         shared_inter, _ptr(h_post), _ptr(ids), m, top_k, hidden, inter, _ptr(act),
-                                        _ptr(act_shared), _ptr(err_flag), _stream(stream)))
+                                        _ptr(act_shared), _ptr(workspace), ws_bytes, _ptr(err_flag),
+                                        _stream(stream)))
 
 
 def q4k_moe_layer_down(w_down, num_experts, ws_down, shared_inter, act, act_shared, ids, m, top_k, hidden, inter,
-                       expert_out, shared_out, err_flag=None, stream=None):
-    _cuda(w_down, ws_down, act, act_shared, ids, expert_out, shared_out, err_flag)
+                       expert_out, shared_out, workspace=None, ws_bytes=0, err_flag=None, stream=None):
+    _cuda(w_down, ws_down, act, act_shared, ids, expert_out, shared_out, workspace, err_flag)
     _check(load().q4k_moe_layer_down(_ptr(w_down), num_experts, _ptr(ws_down), shared_inter, _ptr(act),
                                      _ptr(act_shared), _ptr(ids), m, top_k, hidden, inter, _ptr(expert_out),
-                                     _ptr(shared_out), _ptr(err_flag), _stream(stream)))
+                                     _ptr(shared_out), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream(stream)))
 
 
 def q4k_quantize_rows(x, rows, k, out, stream=None):

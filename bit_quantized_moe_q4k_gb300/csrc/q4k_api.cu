@@ -2,6 +2,7 @@
 // validation, workspace layout and kernel sequencing. No compute happens here.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <string>
 
 #include "q4k_internal.cuh"
@@ -46,12 +47,37 @@ int check_gemv_shape(int num_experts, int m, int top_k, int n, int k) {
     return Q4K_OK;
 }
 
-size_t ffn_scratch(int m, int top_k, int inter) {
-    return align_up((size_t)m * top_k * inter * sizeof(float));
+// Tensor-core path policy: experts whose bucket holds at least tc_min pairs run on the
+// tcgen05 grouped GEMM (q4k_tc.cu), the others on the id-GEMV kernel. tc_min comes from the
+// environment variable Q4K_TC_MIN (default 16, 0 disables). A launch uses the path only when
+// some bucket can reach tc_min (n_pairs >= tc_min and n_pairs / num_experts >= tc_min / 4)
+// and the caller's workspace holds the activation images.
+int tc_min_setting() {
+    static int v = [] {
+        const char* s = getenv("Q4K_TC_MIN");
+        return s ? atoi(s) : 16;
+    }();
+    return v;
+}
+
+bool tc_wanted(int n_pairs, int num_experts) {
+    const int t = tc_min_setting();
+    return t > 0 && n_pairs >= t && (int64_t)n_pairs * 4 >= (int64_t)t * num_experts;
+}
+
+size_t tc_scratch(int n_pairs, int k) {
+    const int t = tc_min_setting();
+    return t > 0 ? align_up(tc_image_bytes(n_pairs, k, t)) : 0;
+}
+
+// FFN scratch: act [m*top_k, inter], then tensor-core images of gate|up (k = hidden) and down (k = inter)
+size_t ffn_scratch(int m, int top_k, int hidden, int inter) {
+    return align_up((size_t)m * top_k * inter * sizeof(float)) + tc_scratch(m * top_k, hidden) +
+           tc_scratch(m * top_k, inter);
 }
 
 struct LayerScratch {
-    size_t act, act_shared, eout, shared_out, total;
+    size_t act, act_shared, eout, shared_out, tc_gu, tc_dn, total;
 };
 
 LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_inter) {
@@ -61,6 +87,8 @@ LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_i
     s.act_shared = off; off += align_up((size_t)m * shared_inter * sizeof(float));
     s.eout = off;       off += align_up((size_t)m * top_k * hidden * sizeof(float));
     s.shared_out = off; off += align_up((size_t)m * hidden * sizeof(float));
+    s.tc_gu = off;      off += tc_scratch(m * top_k, hidden) + (shared_inter > 0 ? tc_scratch(m, hidden) : 0);
+    s.tc_dn = off;      off += tc_scratch(m * top_k, inter) + (shared_inter > 0 ? tc_scratch(m, shared_inter) : 0);
     s.total = off;
     return s;
 }
@@ -77,7 +105,7 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
 // one launch; then the down projections of both, in one launch.
 int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const float* h_post, const int32_t* ids,
                 int m, int top_k, int hidden, int inter, float* act, const void* ws_gate, const void* ws_up,
-                int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream) {
+                int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr) {
     GemvGroup g[2] = {};
     int ng = 1;
     g[0] = GemvGroup{static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), ids, h_post,
@@ -87,12 +115,19 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
                          hidden, 0, act_shared, 1, m, 1, shared_inter, hidden};
         ng = 2;
     }
-    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream), "gate|up launch");
+    int tc = 0;
+    uint8_t* img[2] = {nullptr, nullptr};
+    if (tc_ws && (tc_wanted(m * top_k, num_experts) || (shared_inter > 0 && tc_wanted(m, 1)))) {
+        tc = tc_min_setting();
+        img[0] = tc_ws;
+        img[1] = tc_ws + tc_scratch(m * top_k, hidden);
+    }
+    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream, tc, img), "gate|up launch");
 }
 
 int run_down(const void* w_down, int num_experts, const float* act, const int32_t* ids, int m, int top_k,
              int hidden, int inter, float* expert_out, const void* ws_down, int shared_inter, const float* act_shared,
-             float* shared_out, int* err_flag, cudaStream_t stream) {
+             float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr) {
     GemvGroup g[2] = {};
     int ng = 1;
     g[0] = GemvGroup{static_cast<const uint8_t*>(w_down), nullptr, ids, act, (int64_t)top_k * inter, inter,
@@ -102,18 +137,31 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
                          shared_out, 1, m, 1, hidden, shared_inter};
         ng = 2;
     }
-    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream), "down launch");
+    int tc = 0;
+    uint8_t* img[2] = {nullptr, nullptr};
+    if (tc_ws && (tc_wanted(m * top_k, num_experts) || (shared_inter > 0 && tc_wanted(m, 1)))) {
+        tc = tc_min_setting();
+        img[0] = tc_ws;
+        img[1] = tc_ws + tc_scratch(m * top_k, inter);
+    }
+    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream, tc, img), "down launch");
 }
 
 int run_ffn(const void* w_gate, const void* w_up, const void* w_down, int num_experts, const float* h_post,
             const int32_t* ids, int m, int top_k, int hidden, int inter, float* act, float* expert_out,
             const void* ws_gate, const void* ws_up, const void* ws_down, int shared_inter, float* act_shared,
-            float* shared_out, int* err_flag, cudaStream_t stream) {
+            float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_gu = nullptr,
+            uint8_t* tc_dn = nullptr) {
     int st = run_gate_up(w_gate, w_up, num_experts, h_post, ids, m, top_k, hidden, inter, act, ws_gate, ws_up,
-                         shared_inter, act_shared, err_flag, stream);
+                         shared_inter, act_shared, err_flag, stream, tc_gu);
     if (st) return st;
     return run_down(w_down, num_experts, act, ids, m, top_k, hidden, inter, expert_out, ws_down, shared_inter,
-                    act_shared, shared_out, err_flag, stream);
+                    act_shared, shared_out, err_flag, stream, tc_dn);
+}
+
+// Tensor-core image scratch of one half of the layer: routed group then shared group.
+size_t tc_half_scratch(int m, int top_k, int k_routed, int shared_inter, int k_shared) {
+    return tc_scratch(m * top_k, k_routed) + (shared_inter > 0 ? tc_scratch(m, k_shared) : 0);
 }
 
 // Validation shared by the layer entry points (shapes of both projections, shared expert).
@@ -145,14 +193,19 @@ const char* q4k_version(void) { return "libq4kmoe 0.1 (sm_103a)"; }
 
 size_t q4k_moe_workspace_size(int m, int top_k, int num_experts, int n_max, int k_max) {
     if (m < 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || num_experts < 1 || n_max < 1 || k_max < 1) return 0;
-    const int inter = n_max > k_max ? n_max : k_max;
-    return ffn_scratch(m, top_k, inter);
+    const int mx = n_max > k_max ? n_max : k_max;
+    return ffn_scratch(m, top_k, mx, mx);
 }
 
 size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     if (m < 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || num_experts < 1 || hidden < 1 || inter < 1 || shared_inter < 0)
         return 0;
     return layer_scratch(m, top_k, hidden, inter, shared_inter).total;
+}
+
+size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int shared_inter, int k_shared) {
+    if (m < 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || k_routed < 1 || shared_inter < 0) return 0;
+    return tc_half_scratch(m, top_k, k_routed, shared_inter, k_shared);
 }
 
 size_t q4k_moe_layer_host_staging_size(int m, int top_k, int hidden) {
@@ -174,8 +227,6 @@ int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_exp
                     int64_t src1_outer_stride, int64_t src1_inner_stride, const int32_t* d_ids, int m, int top_k,
                     int n, int k, float* d_out, void* d_workspace, size_t ws_bytes, int* d_err_flag,
                     cudaStream_t stream) {
-    (void)d_workspace;
-    (void)ws_bytes;
     int st = check_gemv_shape(num_experts, m, top_k, n, k);
     if (st) return st;
     if (!d_w_stacked || !d_a || !d_ids || !d_out) return fail(Q4K_ERR_NULL, "NULL pointer argument");
@@ -186,7 +237,15 @@ int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_exp
         return fail(Q4K_ERR_ALIGN, "activations must be 16-byte aligned with non-negative strides that are multiples of 4 floats");
     if (m == 0) return Q4K_OK;
     GemvGroup g{w, nullptr, d_ids, d_a, src1_outer_stride, src1_inner_stride, d_out, num_experts, m, top_k, n, k};
-    return cuda_status(launch_idgemv(&g, 1, false, false, d_err_flag, stream), "id-gemv launch");
+    // the workspace is optional: with room for the activation images, large buckets take
+    // the tensor-core path
+    int tc = 0;
+    uint8_t* img[1] = {static_cast<uint8_t*>(d_workspace)};
+    const size_t need = tc_scratch(m * top_k, k);
+    if (d_workspace && need > 0 && ws_bytes >= need && (reinterpret_cast<uintptr_t>(d_workspace) & 255) == 0 &&
+        tc_wanted(m * top_k, num_experts))
+        tc = tc_min_setting();
+    return cuda_status(launch_idgemv(&g, 1, false, false, d_err_flag, stream, tc, img), "id-gemv launch");
 }
 
 int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,
@@ -200,12 +259,14 @@ int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void*
         return fail(Q4K_ERR_NULL, "NULL pointer argument");
     if (!aligned16(d_w_gate) || !aligned16(d_w_up) || !aligned16(d_w_down) || !aligned16(d_h_post))
         return fail(Q4K_ERR_ALIGN, "slabs and h_post must be 16-byte aligned");
-    st = check_workspace(d_workspace, ws_bytes, ffn_scratch(m, top_k, inter));
+    st = check_workspace(d_workspace, ws_bytes, ffn_scratch(m, top_k, hidden, inter));
     if (st) return st;
     if (m == 0) return Q4K_OK;
     float* act = static_cast<float*>(d_workspace);
+    uint8_t* tc_gu = static_cast<uint8_t*>(d_workspace) + align_up((size_t)m * top_k * inter * sizeof(float));
+    uint8_t* tc_dn = tc_gu + tc_scratch(m * top_k, hidden);
     return run_ffn(d_w_gate, d_w_up, d_w_down, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act,
-                   d_expert_out, nullptr, nullptr, nullptr, 0, nullptr, nullptr, d_err_flag, stream);
+                   d_expert_out, nullptr, nullptr, nullptr, 0, nullptr, nullptr, d_err_flag, stream, tc_gu, tc_dn);
 }
 
 int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const float* d_weights,
@@ -264,7 +325,8 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
     float* eout = reinterpret_cast<float*>(ws + ls.eout);
     float* sout = reinterpret_cast<float*>(ws + ls.shared_out);
     st = run_ffn(d_w_gate, d_w_up, d_w_down, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act, eout,
-                 d_ws_gate, d_ws_up, d_ws_down, shared_inter, act_shared, sout, d_err_flag, stream);
+                 d_ws_gate, d_ws_up, d_ws_down, shared_inter, act_shared, sout, d_err_flag, stream, ws + ls.tc_gu,
+                 ws + ls.tc_dn);
     if (st) return st;
     return cuda_status(launch_combine(d_h_mid, eout, d_weights, sout, d_shared_gate, shared_mode, m, top_k, hidden,
                                       d_y, true, stream),
@@ -273,8 +335,8 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
 
 int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,
                           const void* d_ws_up, int shared_inter, const float* d_h_post, const int32_t* d_ids, int m,
-                          int top_k, int hidden, int inter, float* d_act, float* d_act_shared, int* d_err_flag,
-                          cudaStream_t stream) {
+                          int top_k, int hidden, int inter, float* d_act, float* d_act_shared, void* d_workspace,
+                          size_t ws_bytes, int* d_err_flag, cudaStream_t stream) {
     if (!d_w_up) return fail(Q4K_ERR_NULL, "NULL up slab");
     if (shared_inter > 0 && !d_ws_up) return fail(Q4K_ERR_NULL, "NULL shared up slab");
     int st = check_layer(d_w_gate, d_w_up, num_experts, shared_inter, d_ws_gate, d_ws_up, m, top_k, hidden, inter);
@@ -282,14 +344,17 @@ int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_expe
     if (!d_h_post || !d_ids || !d_act || (shared_inter > 0 && !d_act_shared)) return fail(Q4K_ERR_NULL, "NULL pointer argument");
     if (!aligned16(d_h_post)) return fail(Q4K_ERR_ALIGN, "h_post must be 16-byte aligned");
     if (m == 0) return Q4K_OK;
+    const size_t need = tc_half_scratch(m, top_k, hidden, shared_inter, hidden);
+    uint8_t* tc_ws = (d_workspace && ws_bytes >= need && (reinterpret_cast<uintptr_t>(d_workspace) & 255) == 0)
+                         ? static_cast<uint8_t*>(d_workspace) : nullptr;
     return run_gate_up(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, d_act, d_ws_gate,
-                       d_ws_up, shared_inter, d_act_shared, d_err_flag, stream);
+                       d_ws_up, shared_inter, d_act_shared, d_err_flag, stream, tc_ws);
 }
 
 int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_down, int shared_inter,
                        const float* d_act, const float* d_act_shared, const int32_t* d_ids, int m, int top_k,
-                       int hidden, int inter, float* d_expert_out, float* d_shared_out, int* d_err_flag,
-                       cudaStream_t stream) {
+                       int hidden, int inter, float* d_expert_out, float* d_shared_out, void* d_workspace,
+                       size_t ws_bytes, int* d_err_flag, cudaStream_t stream) {
     int st = check_layer(d_w_down, nullptr, num_experts, shared_inter, d_ws_down, nullptr, m, top_k, hidden, inter);
     if (st) return st;
     if (!d_act || !d_ids || !d_expert_out || (shared_inter > 0 && (!d_act_shared || !d_shared_out)))
@@ -297,8 +362,11 @@ int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_d
     if (!aligned16(d_act) || (d_act_shared && !aligned16(d_act_shared)))
         return fail(Q4K_ERR_ALIGN, "act rows must be 16-byte aligned");
     if (m == 0) return Q4K_OK;
+    const size_t need = tc_half_scratch(m, top_k, inter, shared_inter, shared_inter);
+    uint8_t* tc_ws = (d_workspace && ws_bytes >= need && (reinterpret_cast<uintptr_t>(d_workspace) & 255) == 0)
+                         ? static_cast<uint8_t*>(d_workspace) : nullptr;
     return run_down(d_w_down, num_experts, d_act, d_ids, m, top_k, hidden, inter, d_expert_out, d_ws_down,
-                    shared_inter, d_act_shared, d_shared_out, d_err_flag, stream);
+                    shared_inter, d_act_shared, d_shared_out, d_err_flag, stream, tc_ws);
 }
 
 int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,

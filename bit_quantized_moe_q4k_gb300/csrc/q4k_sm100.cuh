@@ -40,15 +40,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity. Gives up after `limit` polls or once *abort is
-// set (another role gave up), returning false; the caller then raises an error and leaves.
-constexpr uint32_t kWaitLimit = 1u << 22;
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity. Gives up after kWaitNs of wall time or once
+// *abort is set (another role gave up), returning false; the caller then raises an error
+// and leaves. (try_wait may suspend the thread for a while, so the bound is on time.)
+constexpr uint64_t kWaitNs = 2000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
+        if ((i & 63) == 0 && global_timer_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 // ---- bulk async copy global -> shared, completing on an mbarrier (16-byte aligned, size % 16 == 0)

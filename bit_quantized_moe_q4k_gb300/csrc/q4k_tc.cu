@@ -213,8 +213,6 @@ __device__ __forceinline__ TcItem tc_item(const TcGroup& G, const int* cnt, cons
     return it;
 }
 
-__device__ __forceinline__ void producers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 // Persistent: grid = (SMs, groups); each CTA walks items grid-stride. A global step counter
 // (one step = one Q4_K block of one slab) carries the stage index and mbarrier parity
 // across items; tensor memory is allocated once per CTA.
@@ -231,7 +229,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     __shared__ uint32_t s_tmem;
     __shared__ int s_warp[33];
     __shared__ int s_bad;
-    __shared__ int s_pairs[kTcTok];
+    __shared__ int s_pairs_w[4][kTcTok];  // each producer warp keeps its own copy (no cross-warp barrier)
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -364,9 +362,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             const TcItem it = tc_item(G, cnt, start, item);
             const int row0 = it.tile * kTcRows;
             const int rows_valid = min(kTcRows, G.n - row0);
-            producers_sync();  // the previous item's outputs are written
-            if (warp == 0) tc_gather(G, it.e, it.chunk, it.nt, s_pairs);
-            producers_sync();
+            int* s_pairs = s_pairs_w[warp];
+            __syncwarp();  // this warp's previous outputs are written
+            tc_gather(G, it.e, it.chunk, it.nt, s_pairs);
+            __syncwarp();
             float acc[kTcTok], accg[kTcTok];
 #pragma unroll
             for (int t = 0; t < kTcTok; ++t) { acc[t] = 0.f; accg[t] = 0.f; }

@@ -111,6 +111,10 @@ int q4k_moe_bucket(const int32_t* d_ids, int n_pairs, int num_experts, int32_t* 
  *   d_w_stacked + w_byte_offset: 16-byte aligned, num_experts*n*(k/256)*144 bytes
  *   d_a: 16-byte aligned; strides multiples of 4 floats
  *   d_out: [m*top_k, n] fp32
+ * d_workspace is optional here: when it holds at least q4k_moe_workspace_size(m, top_k,
+ * num_experts, n, k) bytes (256-byte aligned), experts whose bucket holds at least
+ * Q4K_TC_MIN pairs (environment variable, default 16, 0 disables) run on the tcgen05
+ * tensor-core grouped GEMM; all others on the id-GEMV kernel.
  * Limits: num_experts <= 4096, k <= 65536.
  */
 int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_experts,
@@ -178,11 +182,15 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
 int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,
                           const void* d_ws_up, int shared_inter, const float* d_h_post, const int32_t* d_ids,
                           int m, int top_k, int hidden, int inter, float* d_act, float* d_act_shared,
-                          int* d_err_flag, cudaStream_t stream);
+                          void* d_workspace, size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
 int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_down, int shared_inter,
                        const float* d_act, const float* d_act_shared, const int32_t* d_ids, int m, int top_k,
-                       int hidden, int inter, float* d_expert_out, float* d_shared_out, int* d_err_flag,
-                       cudaStream_t stream);
+                       int hidden, int inter, float* d_expert_out, float* d_shared_out, void* d_workspace,
+                       size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
+/* Optional workspace of one half (k_routed = hidden for gate|up, inter for down; k_shared =
+ * hidden / shared_inter): with at least this many bytes (256-byte aligned), experts whose
+ * bucket holds many tokens run on the tensor-core grouped GEMM. 0 when that path is off. */
+size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int shared_inter, int k_shared);
 
 /* ---------------------------------------------------------------------------------
  * q4k_moe_layer_forward_host -- the same layer with the per-step inputs and the

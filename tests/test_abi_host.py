@@ -69,7 +69,7 @@ def test_ffn_and_layer_workspace_checks():
     lib = q4k.load()
     need = lib.q4k_moe_workspace_size(3, 2, 4, 512, 512)
     assert need >= 3 * 2 * 512 * 4 and need % 256 == 0
-    args = [A16, A16, A16, 4, A16, A16, 3, 2, 256, 512, A16]
+    args = [A16, A16, A16, 4, A16, A16, 3, 2, 512, 512, A16]  # hidden = inter: need is exact
     assert lib.q4k_expert_ffn_forward(*args, None, 0, None, None) == 4
     assert lib.q4k_expert_ffn_forward(*args, A16, need - 1, None, None) == 4
     assert lib.q4k_expert_ffn_forward(*args, A16 + 16, need, None, None) == 4  # not 256-byte aligned

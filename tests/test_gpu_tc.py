@@ -1,0 +1,116 @@
+"""GPU parity of the tensor-core grouped GEMM (tcgen05) path against the CPU oracle.
+
+Buckets of at least 16 pairs (the default Q4K_TC_MIN) run on the tensor-core path when the
+caller provides the workspace; without it the same calls run on the id-GEMV kernel. Both
+must meet the per-row acceptance; their results differ in rounding (fp16 activations in the
+tensor-core products vs 16-bit fixed point), which shows the tensor-core path did run.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from bit_quantized_moe_q4k_gb300 import inputs
+import bit_quantized_moe_q4k_gb300 as q4k
+
+from helpers import dev, err_flag, host, oracle_slab, rows_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _ws(nbytes):
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda"), nbytes
+
+
+def _gemv(w, E, a, outer, inner, ids, m, T, n, k, workspace):
+    out = torch.empty((m * T, n), dtype=torch.float32, device="cuda")
+    f = err_flag()
+    if workspace:
+        ws, nbytes = _ws(q4k.q4k_moe_workspace_size(m, T, E, n, k))
+        q4k.q4k_moe_id_gemv(dev(w), 0, E, dev(a), outer, inner, dev(ids), m, T, n, k, out, ws, nbytes, f)
+    else:
+        q4k.q4k_moe_id_gemv(dev(w), 0, E, dev(a), outer, inner, dev(ids), m, T, n, k, out, err_flag=f)
+    got = host(out)
+    assert int(host(f)[0]) == 0
+    return got
+
+
+@pytest.mark.parametrize("mode", ["gate_up", "down"])
+@pytest.mark.parametrize("E,n,k,m,T", [(4, 288, 512, 48, 2),     # ~24 pairs per expert, ragged 3rd row tile
+                                       (2, 128, 1024, 40, 2),    # 40 pairs per expert: 2 chunks
+                                       (3, 256, 256, 70, 1)])    # one block per row
+def test_tc_id_gemv_matches_oracle(mode, E, n, k, m, T):
+    seed = 500 + n + k
+    w = oracle_slab(seed, "tc", E, n, k)
+    ids = inputs.ids_uniform_distinct(seed, m, T, E)
+    if mode == "gate_up":
+        a = inputs.normal(seed, "a", (m, k))
+        outer, inner = k, 0
+    else:
+        a = inputs.normal(seed, "a", (m, T, k))
+        outer, inner = T * k, k
+    ref, _ = oracle.moe_id_gemv(w, E, a, outer, inner, ids, m, T, n, k)
+    got_tc = _gemv(w, E, a, outer, inner, ids, m, T, n, k, workspace=True)
+    got_gemv = _gemv(w, E, a, outer, inner, ids, m, T, n, k, workspace=False)
+    rows_close(got_tc, ref, what="tensor-core path")
+    rows_close(got_gemv, ref, what="id-gemv path")
+    assert not np.array_equal(got_tc, got_gemv), "the tensor-core path did not run"
+
+
+def test_tc_mixed_bucket_sizes_zipf():
+    """Zipf ids: the head experts take the tensor-core path, the tail the id-GEMV kernel."""
+    E, n, k, m, T = 16, 160, 768, 48, 4
+    seed = 611
+    w = oracle_slab(seed, "tc", E, n, k)
+    ids = inputs.ids_zipf_distinct(seed, m, T, E)
+    counts = np.bincount(ids, minlength=E)
+    assert counts.max() >= 16 and (counts[counts > 0] < 16).any()
+    a = inputs.normal(seed, "a", (m, k))
+    ref, _ = oracle.moe_id_gemv(w, E, a, k, 0, ids, m, T, n, k)
+    rows_close(_gemv(w, E, a, k, 0, ids, m, T, n, k, workspace=True), ref, what="mixed")
+
+
+def test_tc_ffn_fused_gate_up_matches_oracle():
+    E, H, I, m, T = 4, 512, 512, 40, 2
+    seed = 621
+    wg, wu = oracle_slab(seed, "gate", E, I, H), oracle_slab(seed, "up", E, I, H)
+    wd = oracle_slab(seed, "down", E, H, I)
+    ids = inputs.ids_uniform_distinct(seed, m, T, E)
+    x = inputs.normal(seed, "h_post", (m, H))
+    ref, _ = oracle.expert_ffn(wg, wu, wd, E, x, ids, m, T, H, I)
+    nbytes = q4k.q4k_moe_workspace_size(m, T, E, max(H, I), max(H, I))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((m * T, H), dtype=torch.float32, device="cuda")
+    f = err_flag()
+    q4k.q4k_expert_ffn_forward(dev(wg), dev(wu), dev(wd), E, dev(x), dev(ids), m, T, H, I, out, ws, nbytes, f)
+    got = host(out)
+    assert int(host(f)[0]) == 0
+    rows_close(got, ref, what="tc ffn")
+
+
+def test_tc_layer_shared_expert_takes_tensor_cores():
+    """m >= 16: the shared expert's bucket holds every token and runs on the tensor-core path."""
+    from bit_quantized_moe_q4k_gb300.workloads import Workload
+    W = Workload("tc_layer", 512, 256, 32, 2, 24, "uniform", 512, 2, 631)
+    seed = W.seed
+    ids = inputs.make_ids(seed, W.ids, W.m, W.top_k, W.num_experts)
+    wg = oracle_slab(seed, "gate", W.num_experts, W.inter, W.hidden)
+    wu = oracle_slab(seed, "up", W.num_experts, W.inter, W.hidden)
+    wd = oracle_slab(seed, "down", W.num_experts, W.hidden, W.inter)
+    sh = (oracle_slab(seed, "sgate", 1, W.shared_inter, W.hidden), oracle_slab(seed, "sup", 1, W.shared_inter, W.hidden),
+          oracle_slab(seed, "sdown", 1, W.hidden, W.shared_inter))
+    x = inputs.normal(seed, "h_post", (W.m, W.hidden))
+    hm = inputs.normal(seed, "h_mid", (W.m, W.hidden))
+    rw = inputs.routing_weights(seed, W.m, W.top_k)
+    ref, _ = oracle.moe_layer(wg, wu, wd, W.num_experts, sh, W.shared_inter, W.shared_mode, x, hm, ids, rw, None,
+                              W.m, W.top_k, W.hidden, W.inter)
+    nbytes = q4k.q4k_moe_layer_workspace_size(W.m, W.top_k, W.num_experts, W.hidden, W.inter, W.shared_inter)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    y = torch.empty((W.m, W.hidden), dtype=torch.float32, device="cuda")
+    f = err_flag()
+    q4k.q4k_moe_layer_forward(dev(wg), dev(wu), dev(wd), W.num_experts, dev(sh[0]), dev(sh[1]), dev(sh[2]),
+                              W.shared_inter, W.shared_mode, dev(x), dev(hm), dev(ids), dev(rw), None, W.m, W.top_k,
+                              W.hidden, W.inter, y, ws, nbytes, f)
+    got = host(y)
+    assert int(host(f)[0]) == 0
+    rows_close(got, ref, what="tc layer")
