@@ -8,8 +8,11 @@
 //
 // Exactness of the operands. Q4_K gives per 32-weight sub-block j of a 256-weight block
 //   sum_k w_k x_k = d * sum_j sc_j sum_{k in j} q_k x_k  -  dmin * sum_j m_j sum_{k in j} x_k.
-// A holds the integers sc_j * q_k (<= 945, exact in fp16), so the only rounding in the main
-// product is that of x to fp16. A second, 16-deep MMA per block computes sum_j m_j * sx_j
+// A holds the integers sc_j * q_k (<= 945, exact in fp16). x is split into two fp16 parts,
+// x = hi + lo with hi = fp16(x), lo = fp16(x - hi), and both are multiplied by the same A
+// (two MMAs per k step into one accumulator), so the main product carries x to ~2^-22
+// instead of fp16's 2^-11 (which alone put FFN outputs at the edge of the 1e-3 acceptance).
+// A second, 16-deep MMA per block computes sum_j m_j * sx_j
 // with sx_j = sum_{k in j} x_k split into two fp16 halves (hi + lo), i.e. to ~2^-22. The
 // per-block factors d and dmin are applied in fp32 by the epilogue, which reads each block's
 // two partial accumulators from tensor memory (double-buffered, so the next block's MMAs
@@ -37,9 +40,11 @@ using namespace sm100;
 constexpr int kTcThreads = 192;
 constexpr int kTcRows = 128;                  // M (TMEM lanes)
 constexpr int kTcTok = 32;                    // N (tokens per chunk)
-constexpr int kImgB = 4 * kTcTok * 128;       // 4 panels of [32 tokens x 128 B]
+constexpr int kImgB = 4 * kTcTok * 128;       // 4 panels of [32 tokens x 128 B] (x rounded to fp16)
+constexpr int kImgLo = kImgB;                 // offset of the residual panels (x - fp16(x), in fp16)
 constexpr int kImgB2 = kTcTok * 128;          // min-term operand [32 tokens x 128 B]
-constexpr int kImgBlock = kImgB + kImgB2;     // bytes of one block's B image
+constexpr int kImgMin = 2 * kImgB;            // offset of the min-term operand
+constexpr int kImgBlock = 2 * kImgB + kImgB2; // bytes of one block's B image
 constexpr int kRawStage = kTcRows * kBlockBytes;
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: A stages (128 each), min-term A stages (16 each), D1 and D2 (32 each)
@@ -146,14 +151,19 @@ tc_prep_kernel(const __grid_constant__ TcParams P) {
                 hi = *reinterpret_cast<const float4*>(row + 32);
             }
             // k order of the A columns: elements 4i'+{0,2,1,3} then 32+4i'+{0,2,1,3} of group c4
-            const __half2 h0 = __floats2half2_rn(lo.x, lo.z), h1 = __floats2half2_rn(lo.y, lo.w);
-            const __half2 h2 = __floats2half2_rn(hi.x, hi.z), h3 = __floats2half2_rn(hi.y, hi.w);
-            uint4 chunk16;
-            chunk16.x = *reinterpret_cast<const uint32_t*>(&h0);
-            chunk16.y = *reinterpret_cast<const uint32_t*>(&h1);
-            chunk16.z = *reinterpret_cast<const uint32_t*>(&h2);
-            chunk16.w = *reinterpret_cast<const uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(img + c4 * (kTcTok * 128) + t * 128 + ((ip ^ (t & 7)) << 4)) = chunk16;
+            const float xv[8] = {lo.x, lo.z, lo.y, lo.w, hi.x, hi.z, hi.y, hi.w};
+            uint32_t hw8[4], lw8[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half a = __float2half_rn(xv[2 * i]), b = __float2half_rn(xv[2 * i + 1]);
+                const __half ra = __float2half_rn(xv[2 * i] - __half2float(a));
+                const __half rb = __float2half_rn(xv[2 * i + 1] - __half2float(b));
+                hw8[i] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+                lw8[i] = (uint32_t)__half_as_ushort(ra) | ((uint32_t)__half_as_ushort(rb) << 16);
+            }
+            const int off = c4 * (kTcTok * 128) + t * 128 + ((ip ^ (t & 7)) << 4);
+            *reinterpret_cast<uint4*>(img + off) = make_uint4(hw8[0], hw8[1], hw8[2], hw8[3]);
+            *reinterpret_cast<uint4*>(img + kImgLo + off) = make_uint4(lw8[0], lw8[1], lw8[2], lw8[3]);
             // sub-block sums (fp32) of sub-blocks 2*c4 (lo) and 2*c4+1 (hi) over the 8 lanes of c4
             float sl = (lo.x + lo.y) + (lo.z + lo.w), sh = (hi.x + hi.y) + (hi.z + hi.w);
 #pragma unroll
@@ -178,7 +188,7 @@ tc_prep_kernel(const __grid_constant__ TcParams P) {
                     hw[i] = (uint32_t)__half_as_ushort(a0) | ((uint32_t)__half_as_ushort(a1) << 16);
                     lw[i] = (uint32_t)__half_as_ushort(b0) | ((uint32_t)__half_as_ushort(b1) << 16);
                 }
-                uint8_t* r2 = img + kImgB + t * 128;
+                uint8_t* r2 = img + kImgMin + t * 128;
                 *reinterpret_cast<uint4*>(r2 + ((0 ^ (t & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(r2 + ((1 ^ (t & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
@@ -330,10 +340,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     const uint32_t b_addr = bimg_addr + st * kImgBlock;
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk) {
-                        const uint64_t bd = desc_sw128_kmajor(b_addr + (kk >> 2) * (kTcTok * 128) + (kk & 3) * 32);
-                        mma_f16_ts(tmem + kColD1 + st * 32, tmem + kColA + st * 128 + 8 * kk, bd, idesc, kk > 0);
+                        const uint32_t koff = (kk >> 2) * (kTcTok * 128) + (kk & 3) * 32;
+                        const uint32_t a_col = tmem + kColA + st * 128 + 8 * kk;
+                        mma_f16_ts(tmem + kColD1 + st * 32, a_col, desc_sw128_kmajor(b_addr + koff), idesc, kk > 0);
+                        mma_f16_ts(tmem + kColD1 + st * 32, a_col, desc_sw128_kmajor(b_addr + kImgLo + koff), idesc, 1);
                     }
-                    mma_f16_ts(tmem + kColD2 + st * 32, tmem + kColA2 + st * 16, desc_sw128_kmajor(b_addr + kImgB),
+                    mma_f16_ts(tmem + kColD2 + st * 32, tmem + kColA2 + st * 16, desc_sw128_kmajor(b_addr + kImgMin),
                                idesc, 0);
                     mma_commit(&bar_a_empty[st]);
                     mma_commit(&bar_b_empty[st]);
@@ -539,6 +551,7 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
     // one CTA fits on an SM
     size_t smem = 1024 + (size_t)P.tab_off + (size_t)ints * 4;
     if (smem < 120 * 1024) smem = 120 * 1024;
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
     auto kern = fused ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!g_tc_attr_set[fused ? 1 : 0][dev]) {

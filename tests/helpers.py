@@ -17,7 +17,7 @@ def rows_close(got, ref, rel=ROW_REL_MAX, cos_min=ROW_COS_MIN, what=""):
     ref = np.asarray(ref, np.float64).reshape(len(ref), -1)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
-    worst = (0.0, None)
+    worst = 0.0
     for i in range(ref.shape[0]):
         r, g = ref[i], got[i]
         mx = np.abs(r).max()
@@ -27,8 +27,8 @@ def rows_close(got, ref, rel=ROW_REL_MAX, cos_min=ROW_COS_MIN, what=""):
         d = np.abs(g - r).max() / mx
         cos = float(np.dot(g, r) / (np.linalg.norm(g) * np.linalg.norm(r)))
         assert d <= rel and cos >= cos_min, f"{what}: row {i}: max_abs_diff/max|out| = {d:.3e}, cosine = {cos:.7f}"
-        worst = max(worst, (d, i))
-    return worst[0]
+        worst = max(worst, d)
+    return worst
 
 
 def oracle_slab(seed, proj, num_experts, n, k, experts=None):
