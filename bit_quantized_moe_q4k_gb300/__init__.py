@@ -15,6 +15,8 @@ from ._lib import (  # noqa: F401
     lib_path,
     moe_combine_residual,
     q4k_expert_ffn_forward,
+    q4k_expert_ffn_forward_noalloc,
+    q4k_expert_ffn_noalloc_max_scratch_bytes,
     q4k_moe_bucket,
     q4k_moe_id_gemv,
     q4k_moe_layer_forward,

@@ -35,6 +35,8 @@ SIGNATURES = {
     "q4k_moe_bucket": (_I, [_P, _I, _I, _P, _P, _P, _P, _P]),
     "q4k_moe_id_gemv": (_I, [_P, _U64, _I, _P, _I64, _I64, _P, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "q4k_expert_ffn_forward": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "q4k_expert_ffn_noalloc_max_scratch_bytes": (_SZ, []),
+    "q4k_expert_ffn_forward_noalloc": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "moe_combine_residual": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "q4k_moe_layer_forward": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P,
                                    _P, _SZ, _P, _P]),
@@ -147,6 +149,19 @@ def q4k_expert_ffn_forward(w_gate, w_up, w_down, num_experts, h_post, ids, m, to
     _check(load().q4k_expert_ffn_forward(_ptr(w_gate), _ptr(w_up), _ptr(w_down), num_experts, _ptr(h_post), _ptr(ids),
                                          m, top_k, hidden, inter, _ptr(expert_out), _ptr(workspace), ws_bytes,
                                          _ptr(err_flag), _stream(stream)))
+
+
+def q4k_expert_ffn_noalloc_max_scratch_bytes() -> int:
+    return int(load().q4k_expert_ffn_noalloc_max_scratch_bytes())
+
+
+def q4k_expert_ffn_forward_noalloc(w_gate, w_up, w_down, num_experts, h_post, ids, m, top_k, hidden, inter,
+                                   expert_out, err_flag=None, stream=None):
+    """The routed FFN with its scratch in the library's static device array (no allocation)."""
+    _cuda(w_gate, w_up, w_down, h_post, ids, expert_out, err_flag)
+    _check(load().q4k_expert_ffn_forward_noalloc(_ptr(w_gate), _ptr(w_up), _ptr(w_down), num_experts, _ptr(h_post),
+                                                 _ptr(ids), m, top_k, hidden, inter, _ptr(expert_out),
+                                                 _ptr(err_flag), _stream(stream)))
 
 
 def moe_combine_residual(h_mid, expert_out, weights, shared_out, shared_gate, shared_mode, m, top_k, hidden,

@@ -185,6 +185,8 @@ int check_layer(const void* w_a, const void* w_b, int num_experts, int shared_in
 
 }  // namespace
 
+void q4k::set_last_error(int status, const char* message) { fail(status, "%s", message); }
+
 extern "C" {
 
 const char* q4k_last_error_string(void) { return g_last_error.c_str(); }

@@ -63,4 +63,7 @@ size_t tc_image_bytes(int n_pairs, int k, int tc_min);
 
 int num_sms();
 
+// Record the calling thread's last error text (read back by q4k_last_error_string).
+void set_last_error(int status, const char* message);
+
 }  // namespace q4k

@@ -138,6 +138,30 @@ int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void*
                            void* d_workspace, size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * q4k_expert_ffn_forward_noalloc -- q4k_expert_ffn_forward for callers that cannot allocate
+ * device memory (no counterpart in the studied pages; an addition of this library).
+ * Same computation, arguments and errors as q4k_expert_ffn_forward without the workspace:
+ * the gate|up activations live in a 4 MiB array that the library keeps in every device's
+ * global memory for the life of the process. The call allocates nothing. It serves code
+ * that runs where it may not call cudaMalloc: a plugin inside an application that owns all
+ * device allocations, a latency-critical loop that must not take the synchronisation an
+ * allocation can cause, or a process whose device memory is fully reserved in advance.
+ *   - Limit: m*top_k*inter*4 bytes <= q4k_expert_ffn_noalloc_max_scratch_bytes() (4 MiB);
+ *     larger sizes return Q4K_ERR_LIMIT.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and keeps it; make that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents behind; the call
+ *     overwrites all it reads, so nothing needs clearing. Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it and must be serialised by the caller.
+ *   - Large buckets do not take the tensor-core path here (it needs workspace images).
+ */
+size_t q4k_expert_ffn_noalloc_max_scratch_bytes(void);
+int q4k_expert_ffn_forward_noalloc(const void* d_w_gate, const void* d_w_up, const void* d_w_down,
+                                   int num_experts, const float* d_h_post, const int32_t* d_ids, int m,
+                                   int top_k, int hidden, int inter, float* d_expert_out, int* d_err_flag,
+                                   cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * moe_combine_residual -- combine [P2: hidden_out = h_mid + sum_k w_k * expert_out_k
  * + shared term].
  *   hidden_out[t, h] = h_mid[t, h] + sum_{s<top_k} weights[t*top_k+s] * expert_out[t*top_k+s, h]
