@@ -30,8 +30,7 @@
 namespace q4k {
 
 constexpr int kThreads = 128;               // 4 warps
-constexpr int kRowsPerWarp = 8;             // lanes = 4 groups (c) x 8 rows
-constexpr int kTileRows = kRowsPerWarp * (kThreads / 32);
+constexpr int kWarps = kThreads / 32;
 constexpr int kTB = 4;                      // max tokens of one bucket per work item
 constexpr int kPairBytes = 144;             // staged planes of 2 sub-blocks + 16 B pad
 constexpr int kMaxGroups = 2;
@@ -46,6 +45,7 @@ struct GroupDev {
     int64_t nb01;  // bytes per row
     int64_t nb02;  // bytes per expert
     int num_experts, n_pairs, top_k, n, k, tiles;
+    int lg_split;  // log2 of the lanes splitting one row's blocks (rows per warp = 8 >> lg_split)
 };
 
 struct GemvParams {
@@ -176,8 +176,14 @@ __device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs
 
 constexpr int kDepth = 4;  // blocks of the weight stream in flight per lane
 
-template <bool FUSED>
-__global__ void __launch_bounds__(kThreads, 3)
+// Lane layout: lane = c | s << 2 | r << (2 + lg_split). c (0..3) picks the 64-weight group of
+// a block (code bytes 32c..32c+31 = sub-blocks 2c, 2c+1); s picks which blocks of the row the
+// lane streams (b = s, s + S, ...; S = 1 << lg_split lanes share a row's blocks); r is the row
+// within the warp (8 / S rows per warp). Splitting the row's blocks over more lanes keeps
+// each lane's share within the kDepth-deep register ring, so all of an item's weight loads
+// are in flight at once, and spreads the work over more warps.
+template <bool FUSED, int TB>
+__global__ void __launch_bounds__(kThreads, FUSED ? 3 : 4)
 idgemv_kernel(const __grid_constant__ GemvParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
     int* s_int = reinterpret_cast<int*>(smem);
@@ -192,7 +198,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     pdl_launch_dependents();
     if (threadIdx.x == 0) { s_staged_group = -1; s_staged_nt = 0; }
 
-    // ---- bucketing prologue (ids are inputs of the layer, not results of the previous kernel): per group, counts then item offsets per expert
+    // ---- bucketing prologue (ids are inputs of the layer, not results of the previous kernel)
     if (threadIdx.x == 0) s_items[0] = 0;
     for (int gi = 0; gi < P.n_groups; ++gi) {
         const GroupDev& G = P.g[gi];
@@ -205,7 +211,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             __syncthreads();
         }
         for (int e = threadIdx.x; e < G.num_experts; e += kThreads)
-            start[e] = (P.tc_min > 0 && cnt[e] >= P.tc_min) ? 0 : ((cnt[e] + P.tb - 1) / P.tb) * G.tiles;
+            start[e] = (P.tc_min > 0 && cnt[e] >= P.tc_min) ? 0 : ((cnt[e] + TB - 1) / TB) * G.tiles;
         __syncthreads();
         const int total = block_exclusive_scan(start, G.num_experts, s_warp);
         if (threadIdx.x == 0) s_items[gi + 1] = s_items[gi] + total;
@@ -215,7 +221,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     uint8_t* xs = smem + P.x_off;
     float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int c = lane & 3, rl = lane >> 2;
+    const int c = lane & 3;
 
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         // ---- locate the item: group, expert (search over the item offsets), tile, chunk
@@ -226,18 +232,18 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             const int* cnt = s_int + P.hist_off[gi];
             const int* start = cnt + G.num_experts;
             const int local = item - s_items[gi];
-            int lo = 0, hi = G.num_experts - 1;  // last e with start[e] <= local (it has pairs)
+            int lo = 0, hi = G.num_experts - 1;  // last e with start[e] <= local (it has items)
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (start[mid] <= local) lo = mid; else hi = mid - 1;
             }
             const int in_e = local - start[lo];
-            const int chunks = (cnt[lo] + P.tb - 1) / P.tb;
+            const int chunks = (cnt[lo] + TB - 1) / TB;
             const int chunk = in_e % chunks;
             s_item_info[0] = gi;
             s_item_info[1] = lo;
             s_item_info[2] = in_e / chunks;
-            s_item_info[3] = min(P.tb, cnt[lo] - chunk * P.tb);
+            s_item_info[3] = min(TB, cnt[lo] - chunk * TB);
             s_item_info[4] = chunk;
         }
         __syncthreads();
@@ -246,32 +252,36 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         const GroupDev& G = P.g[gi];
 
         // ---- start the weight stream before staging (independent of the activations)
-        const int row = tile * kTileRows + warp * kRowsPerWarp + rl;
+        const int lgS = G.lg_split, S = 1 << lgS;
+        const int sl = (lane >> 2) & (S - 1);
+        const int rows_per_warp = 8 >> lgS;
+        const int row = (tile * kWarps + warp) * rows_per_warp + (lane >> (2 + lgS));
         const bool row_ok = row < G.n;
         const int nb = G.k / kQK;
+        const int nbl = sl < nb ? (nb - sl + S - 1) / S : 0;  // blocks b = sl + S*i of this lane
         const int nsb = G.k / 32;
         const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
         const uint8_t* wr = G.w + (int64_t)e * G.nb02 + (int64_t)(row_ok ? row : 0) * G.nb01;
         const uint8_t* wr2 = FUSED ? G.w2 + (int64_t)e * G.nb02 + (int64_t)(row_ok ? row : 0) * G.nb01 : nullptr;
         uint4 H[kDepth], Q0[kDepth], Q1[kDepth], H2[kDepth], R0[kDepth], R1[kDepth];
 #pragma unroll
-        for (int s = 0; s < kDepth; ++s) {
-            H[s] = Q0[s] = Q1[s] = H2[s] = R0[s] = R1[s] = make_uint4(0, 0, 0, 0);
-            if (row_ok && s < nb) {
-                const uint8_t* p = wr + (int64_t)s * kBlockBytes;
-                H[s] = ldg16(p); Q0[s] = ldg16(p + 16 + 32 * c); Q1[s] = ldg16(p + 32 + 32 * c);
+        for (int i = 0; i < kDepth; ++i) {
+            H[i] = Q0[i] = Q1[i] = H2[i] = R0[i] = R1[i] = make_uint4(0, 0, 0, 0);
+            if (row_ok && i < nbl) {
+                const uint8_t* p = wr + (int64_t)(sl + S * i) * kBlockBytes;
+                H[i] = ldg16(p); Q0[i] = ldg16(p + 16 + 32 * c); Q1[i] = ldg16(p + 32 + 32 * c);
                 if (FUSED) {
-                    const uint8_t* p2 = wr2 + (int64_t)s * kBlockBytes;
-                    H2[s] = ldg16(p2); R0[s] = ldg16(p2 + 16 + 32 * c); R1[s] = ldg16(p2 + 32 + 32 * c);
+                    const uint8_t* p2 = wr2 + (int64_t)(sl + S * i) * kBlockBytes;
+                    H2[i] = ldg16(p2); R0[i] = ldg16(p2 + 16 + 32 * c); R1[i] = ldg16(p2 + 32 + 32 * c);
                 }
             }
         }
 
         if (warp == 0) {
             if (G.ids) {
-                warp_gather_bucket(G.ids, G.n_pairs, e, chunk * P.tb, nt, s_pairs);
+                warp_gather_bucket(G.ids, G.n_pairs, e, chunk * TB, nt, s_pairs);
             } else if (lane < nt) {
-                s_pairs[lane] = chunk * P.tb + lane;
+                s_pairs[lane] = chunk * TB + lane;
             }
             __syncwarp();
             // the same activation rows as the staged ones (e.g. every item of a broadcast
@@ -279,8 +289,8 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             bool same = s_staged_group == gi && s_staged_nt == nt;
             if (lane < nt) {
                 const int p = s_pairs[lane];
-                const int64_t row = (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
-                same = same && s_rows[lane] == row;
+                const int64_t arow = (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+                same = same && s_rows[lane] == arow;
             }
             same = __all_sync(0xffffffffu, same);
             if (lane == 0) s_restage = same ? 0 : 1;
@@ -298,56 +308,55 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         }
         __syncthreads();
 
-        // ---- main loop: lane (c, rl) streams 64-weight group c of every block of its row
-        float acc[kTB], acc2[kTB];
+        // ---- main loop over this lane's blocks, kDepth of them in flight
+        float acc[TB], acc2[TB];
 #pragma unroll
-        for (int t = 0; t < kTB; ++t) { acc[t] = 0.0f; acc2[t] = 0.0f; }
-        for (int b0 = 0; b0 < nb; b0 += kDepth) {
+        for (int t = 0; t < TB; ++t) { acc[t] = 0.0f; acc2[t] = 0.0f; }
+        for (int i0 = 0; i0 < nbl; i0 += kDepth) {
 #pragma unroll
-            for (int s = 0; s < kDepth; ++s) {
-                const int b = b0 + s;
-                if (b < nb) {
+            for (int j = 0; j < kDepth; ++j) {
+                const int i = i0 + j;
+                if (i < nbl) {
+                    const int b = sl + S * i;
                     float sa, ma, sb, mb, sa2 = 0.f, ma2 = 0.f, sb2 = 0.f, mb2 = 0.f;
-                    block_scales(H[s], c, sa, ma, sb, mb);
-                    if (FUSED) block_scales(H2[s], c, sa2, ma2, sb2, mb2);
+                    block_scales(H[j], c, sa, ma, sb, mb);
+                    if (FUSED) block_scales(H2[j], c, sa2, ma2, sb2, mb2);
 #pragma unroll
-                    for (int t = 0; t < kTB; ++t) {
+                    for (int t = 0; t < TB; ++t) {
                         if (t < nt) {
                             const uint4* xp = reinterpret_cast<const uint4*>(xs + t * tok_bytes + (4 * b + c) * kPairBytes);
                             const float4 mt = *reinterpret_cast<const float4*>(meta + t * nsb + 8 * b + 2 * c);
                             int Sa, Sb;
-                            dot64(Q0[s], Q1[s], xp, Sa, Sb);
+                            dot64(Q0[j], Q1[j], xp, Sa, Sb);
                             acc[t] += mt.x * (sa * (float)Sa - ma * mt.y) + mt.z * (sb * (float)Sb - mb * mt.w);
                             if (FUSED) {
-                                dot64(R0[s], R1[s], xp, Sa, Sb);
+                                dot64(R0[j], R1[j], xp, Sa, Sb);
                                 acc2[t] += mt.x * (sa2 * (float)Sa - ma2 * mt.y) + mt.z * (sb2 * (float)Sb - mb2 * mt.w);
                             }
                         }
                     }
-                    if (row_ok && b + kDepth < nb) {  // refill this slot with block b + kDepth
-                        const uint8_t* p = wr + (int64_t)(b + kDepth) * kBlockBytes;
-                        H[s] = ldg16(p); Q0[s] = ldg16(p + 16 + 32 * c); Q1[s] = ldg16(p + 32 + 32 * c);
+                    if (row_ok && i + kDepth < nbl) {  // refill this slot with block b + S*kDepth
+                        const uint8_t* p = wr + (int64_t)(b + S * kDepth) * kBlockBytes;
+                        H[j] = ldg16(p); Q0[j] = ldg16(p + 16 + 32 * c); Q1[j] = ldg16(p + 32 + 32 * c);
                         if (FUSED) {
-                            const uint8_t* p2 = wr2 + (int64_t)(b + kDepth) * kBlockBytes;
-                            H2[s] = ldg16(p2); R0[s] = ldg16(p2 + 16 + 32 * c); R1[s] = ldg16(p2 + 32 + 32 * c);
+                            const uint8_t* p2 = wr2 + (int64_t)(b + S * kDepth) * kBlockBytes;
+                            H2[j] = ldg16(p2); R0[j] = ldg16(p2 + 16 + 32 * c); R1[j] = ldg16(p2 + 32 + 32 * c);
                         }
                     }
                 }
             }
         }
-        // ---- reduce over the 4 lanes of the row and write
+        // ---- reduce over the 4*S lanes of the row (c bits, then s bits) and write
 #pragma unroll
-        for (int t = 0; t < kTB; ++t) {
-            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 1);
-            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 2);
-            if (FUSED) {
-                acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], 1);
-                acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], 2);
+        for (int t = 0; t < TB; ++t) {
+            for (int off = 1; off < (4 << lgS); off <<= 1) {
+                acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+                if (FUSED) acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], off);
             }
         }
-        if (row_ok && c == 0) {
+        if (row_ok && (lane & ((4 << lgS) - 1)) == 0) {
 #pragma unroll
-            for (int t = 0; t < kTB; ++t) {
+            for (int t = 0; t < TB; ++t) {
                 if (t < nt) {
                     const float v = FUSED ? silu(acc[t]) * acc2[t] : acc[t];
                     G.out[(int64_t)s_pairs[t] * G.n + row] = v;
@@ -375,7 +384,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
 static int g_num_sms = 0;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 200 * 1024;
-static bool g_smem_attr_set[2][kMaxDevices] = {};
+static bool g_smem_attr_set[4][kMaxDevices] = {};
 
 int num_sms() {
     if (g_num_sms == 0) {
@@ -398,6 +407,14 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     P.n_groups = n_groups;
     P.err_flag = err_flag;
     P.tc_min = tc_min;
+    // Tokens per work item: 1 when every bucket this kernel handles holds about one pair
+    // (decode with distinct experts), which keeps the inner loop small; else up to 4.
+    int tb = 1;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        const int64_t pairs = (int64_t)groups[gi].m * groups[gi].top_k;
+        const bool to_tc = tc_min > 0 && pairs >= (int64_t)tc_min * groups[gi].num_experts;
+        if (!to_tc && pairs > groups[gi].num_experts) tb = kTB;
+    }
     int ints = 0, kmax = 0;
     int64_t max_items = 0;
     for (int gi = 0; gi < n_groups; ++gi) {
@@ -409,7 +426,12 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         G.nb02 = (int64_t)S.n * G.nb01;
         G.num_experts = S.num_experts; G.n_pairs = S.m * S.top_k; G.top_k = S.top_k;
         G.n = S.n; G.k = S.k;
-        G.tiles = (S.n + kTileRows - 1) / kTileRows;
+        // split a row's blocks over up to 4 lanes so that a lane's share fits the kDepth-deep
+        // ring where possible (k = 2048: 2 lanes x 4 blocks; k = 4096: 4 x 4; k = 768: 1 x 3)
+        const int nb = S.k / kQK;
+        G.lg_split = nb >= 4 * kDepth ? 2 : (nb >= 2 * kDepth ? 1 : 0);
+        const int tile_rows = kWarps * (8 >> G.lg_split);
+        G.tiles = (S.n + tile_rows - 1) / tile_rows;
         P.hist_off[gi] = ints;
         ints += 2 * S.num_experts;
         kmax = S.k > kmax ? S.k : kmax;
@@ -417,10 +439,10 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     }
     if (max_items == 0) return cudaSuccess;
     P.kmax = kmax;
-    // tokens per item: keep the staged rows within ~150 KB of shared memory
+    // tokens per item also bounded so the staged rows fit in ~150 KB of shared memory
     const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
-    int tb = kTB;
     while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;
+    if (tb != 1 && tb != kTB) tb = 1;
     P.tb = tb;
     int off = ((ints * 4) + 15) & ~15;
     P.x_off = off;
@@ -430,17 +452,24 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     off += (kmax / 32) * 8 * tb;
     const size_t smem = (size_t)off;
     if (smem > kSmemLimit) return cudaErrorInvalidValue;
-    auto kern = fused_swiglu ? idgemv_kernel<true> : idgemv_kernel<false>;
+    const int kind = (fused_swiglu ? 2 : 0) + (tb == 1 ? 0 : 1);
+    void (*kern)(GemvParams) = nullptr;
+    switch (kind) {
+        case 0: kern = idgemv_kernel<false, 1>; break;
+        case 1: kern = idgemv_kernel<false, kTB>; break;
+        case 2: kern = idgemv_kernel<true, 1>; break;
+        default: kern = idgemv_kernel<true, kTB>; break;
+    }
     // The dynamic shared memory limit is raised once per device and kernel (outside any
     // stream capture the caller may start later); launches only query occupancy.
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!g_smem_attr_set[fused_swiglu ? 1 : 0][dev]) {
+    if (!g_smem_attr_set[kind][dev]) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
         if (err != cudaSuccess) return err;
-        g_smem_attr_set[fused_swiglu ? 1 : 0][dev] = true;
+        g_smem_attr_set[kind][dev] = true;
     }
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
