@@ -45,6 +45,7 @@ SIGNATURES = {
     "q4k_moe_layer_gate_up": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
     "q4k_moe_layer_down": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
     "q4k_moe_layer_half_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "q4k_moe_layer_launch_count": (_I, [_I, _I, _I, _I, _I, _I]),
     "q4k_quantize_rows": (_I, [_P, _I64, _I, _P, _P]),
     "q4k_stream_ceiling_sink_words": (_I, []),
     "q4k_stream_ceiling": (_I, [_P, _U64, _P, _P]),
@@ -193,6 +194,10 @@ def q4k_moe_layer_forward_host(w_gate, w_up, w_down, num_experts, ws_gate, ws_up
                                              _ptr(h_mid), _ptr(ids), _ptr(weights), _ptr(shared_gate), m, top_k,
                                              hidden, inter, _ptr(y), _ptr(workspace), ws_bytes, _ptr(err_flag),
                                              _stream(stream)))
+
+
+def q4k_moe_layer_launch_count(m, top_k, num_experts, hidden, inter, shared_inter) -> int:
+    return int(load().q4k_moe_layer_launch_count(m, top_k, num_experts, hidden, inter, shared_inter))
 
 
 def q4k_moe_layer_half_workspace_size(m, top_k, k_routed, shared_inter, k_shared) -> int:

@@ -60,9 +60,13 @@ int tc_min_setting() {
     return v;
 }
 
-bool tc_wanted(int n_pairs, int num_experts) {
+// Worth it only with enough work to spread over the SMs: at least ~64 items of 128 weight
+// rows x 32 tokens (a single shared expert with a few row tiles stays on the id-GEMV kernel).
+bool tc_wanted(int n_pairs, int num_experts, int n_rows) {
     const int t = tc_min_setting();
-    return t > 0 && n_pairs >= t && (int64_t)n_pairs * 4 >= (int64_t)t * num_experts;
+    if (t <= 0 || n_pairs < t || (int64_t)n_pairs * 4 < (int64_t)t * num_experts) return false;
+    const int64_t items = (int64_t)((n_pairs + 31) / 32) * ((n_rows + 127) / 128);
+    return items >= 64;
 }
 
 size_t tc_scratch(int n_pairs, int k) {
@@ -77,7 +81,8 @@ size_t ffn_scratch(int m, int top_k, int hidden, int inter) {
 }
 
 struct LayerScratch {
-    size_t act, act_shared, eout, shared_out, tc_gu, tc_dn, total;
+    size_t act, act_shared, eout, shared_out, tc_gu, tc_dn, counters, total;
+    int n_counters;
 };
 
 LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_inter) {
@@ -89,6 +94,9 @@ LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_i
     s.shared_out = off; off += align_up((size_t)m * hidden * sizeof(float));
     s.tc_gu = off;      off += tc_scratch(m * top_k, hidden) + (shared_inter > 0 ? tc_scratch(m, hidden) : 0);
     s.tc_dn = off;      off += tc_scratch(m * top_k, inter) + (shared_inter > 0 ? tc_scratch(m, shared_inter) : 0);
+    // combine counters of the down launch: one per row tile of hidden
+    s.n_counters = (hidden + idgemv_tile_rows(inter) - 1) / idgemv_tile_rows(inter);
+    s.counters = off;   off += align_up((size_t)s.n_counters * sizeof(unsigned));
     s.total = off;
     return s;
 }
@@ -105,7 +113,8 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
 // one launch; then the down projections of both, in one launch.
 int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const float* h_post, const int32_t* ids,
                 int m, int top_k, int hidden, int inter, float* act, const void* ws_gate, const void* ws_up,
-                int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr) {
+                int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr,
+                unsigned* zero = nullptr, int n_zero = 0) {
     GemvGroup g[2] = {};
     int ng = 1;
     g[0] = GemvGroup{static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), ids, h_post,
@@ -117,17 +126,19 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
     }
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
-    if (tc_ws && (tc_wanted(m * top_k, num_experts) || (shared_inter > 0 && tc_wanted(m, 1)))) {
+    if (tc_ws && (tc_wanted(m * top_k, num_experts, inter) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter)))) {
         tc = tc_min_setting();
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, hidden);
     }
-    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream, tc, img), "gate|up launch");
+    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream, tc, img, nullptr, zero, n_zero),
+                       "gate|up launch");
 }
 
 int run_down(const void* w_down, int num_experts, const float* act, const int32_t* ids, int m, int top_k,
              int hidden, int inter, float* expert_out, const void* ws_down, int shared_inter, const float* act_shared,
-             float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr) {
+             float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr,
+             const CombineSpec* combine = nullptr) {
     GemvGroup g[2] = {};
     int ng = 1;
     g[0] = GemvGroup{static_cast<const uint8_t*>(w_down), nullptr, ids, act, (int64_t)top_k * inter, inter,
@@ -139,12 +150,12 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
     }
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
-    if (tc_ws && (tc_wanted(m * top_k, num_experts) || (shared_inter > 0 && tc_wanted(m, 1)))) {
+    if (tc_ws && (tc_wanted(m * top_k, num_experts, hidden) || (shared_inter > 0 && tc_wanted(m, 1, hidden)))) {
         tc = tc_min_setting();
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, inter);
     }
-    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream, tc, img), "down launch");
+    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream, tc, img, combine), "down launch");
 }
 
 int run_ffn(const void* w_gate, const void* w_up, const void* w_down, int num_experts, const float* h_post,
@@ -205,6 +216,13 @@ size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidde
     return layer_scratch(m, top_k, hidden, inter, shared_inter).total;
 }
 
+int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
+    if (m <= 0 || top_k < 1 || num_experts < 1) return 0;
+    const bool tc_gu = tc_wanted(m * top_k, num_experts, inter) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter));
+    const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden) || (shared_inter > 0 && tc_wanted(m, 1, hidden));
+    return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0);
+}
+
 size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int shared_inter, int k_shared) {
     if (m < 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || k_routed < 1 || shared_inter < 0) return 0;
     return tc_half_scratch(m, top_k, k_routed, shared_inter, k_shared);
@@ -245,7 +263,7 @@ int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_exp
     uint8_t* img[1] = {static_cast<uint8_t*>(d_workspace)};
     const size_t need = tc_scratch(m * top_k, k);
     if (d_workspace && need > 0 && ws_bytes >= need && (reinterpret_cast<uintptr_t>(d_workspace) & 255) == 0 &&
-        tc_wanted(m * top_k, num_experts))
+        tc_wanted(m * top_k, num_experts, n))
         tc = tc_min_setting();
     return cuda_status(launch_idgemv(&g, 1, false, false, d_err_flag, stream, tc, img), "id-gemv launch");
 }
@@ -326,13 +344,15 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
     float* act_shared = reinterpret_cast<float*>(ws + ls.act_shared);
     float* eout = reinterpret_cast<float*>(ws + ls.eout);
     float* sout = reinterpret_cast<float*>(ws + ls.shared_out);
-    st = run_ffn(d_w_gate, d_w_up, d_w_down, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act, eout,
-                 d_ws_gate, d_ws_up, d_ws_down, shared_inter, act_shared, sout, d_err_flag, stream, ws + ls.tc_gu,
-                 ws + ls.tc_dn);
+    // two launches: gate|up + SwiGLU (routed and shared; it also zeroes the combine counters),
+    // then down (routed and shared) with the combine fused into its last CTA per row tile
+    unsigned* counters = reinterpret_cast<unsigned*>(ws + ls.counters);
+    st = run_gate_up(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act, d_ws_gate, d_ws_up,
+                     shared_inter, act_shared, d_err_flag, stream, ws + ls.tc_gu, counters, ls.n_counters);
     if (st) return st;
-    return cuda_status(launch_combine(d_h_mid, eout, d_weights, sout, d_shared_gate, shared_mode, m, top_k, hidden,
-                                      d_y, true, stream),
-                       "combine launch");
+    CombineSpec cb{d_y, d_h_mid, d_weights, d_shared_gate, shared_mode, counters};
+    return run_down(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,
+                    act_shared, sout, d_err_flag, stream, ws + ls.tc_dn, &cb);
 }
 
 int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,

@@ -58,6 +58,10 @@ struct GemvParams {
     int kmax;               // largest k of the groups (sizes the staging area)
     int tc_min;             // > 0: experts with at least this many pairs are left to the tensor-core path
     int* err_flag;
+    int has_combine;        // fuse the combine (group 0 routed, group 1 shared) into this launch
+    CombineSpec cb;
+    unsigned* zero;         // CTA 0 zeroes zero[0..n_zero) first
+    int n_zero;
 };
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
@@ -176,6 +180,31 @@ __device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs
 
 constexpr int kDepth = 4;  // blocks of the weight stream in flight per lane
 
+// Combine of rows [r0, r1) of every token (moeflux expert_forward.rs, the batched combine:
+// hidden_out = h_mid + sum_k w_k * expert_out_k + shared term), run by the last CTA of a row
+// tile. Expert rows were written by other CTAs: read them from L2. A pair whose id is out of
+// range contributes nothing (its row is zero by definition).
+__device__ void combine_rows(const GemvParams& P, int r0, int r1) {
+    const GroupDev& R = P.g[0];
+    const int H = R.n, T = R.top_k, m = R.n_pairs / T;
+    const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
+    const int span = r1 - r0;
+    for (int idx = threadIdx.x; idx < m * span; idx += blockDim.x) {
+        const int t = idx / span, r = r0 + idx % span;
+        const int64_t o = (int64_t)t * H + r;
+        float acc = P.cb.h_mid[o];
+        for (int s = 0; s < T; ++s) {
+            const int p = t * T + s;
+            if (id_valid(R.ids[p], R.num_experts)) acc = fmaf(P.cb.weights[p], __ldcg(R.out + (int64_t)p * H + r), acc);
+        }
+        if (shared) {
+            const float g = P.cb.shared_mode == Q4K_SHARED_SIGMOID ? 1.0f / (1.0f + expf(-P.cb.shared_gate[t])) : 1.0f;
+            acc = fmaf(g, __ldcg(P.g[1].out + o), acc);
+        }
+        P.cb.y[o] = acc;
+    }
+}
+
 // Lane layout: lane = c | s << 2 | r << (2 + lg_split). c (0..3) picks the 64-weight group of
 // a block (code bytes 32c..32c+31 = sub-blocks 2c, 2c+1); s picks which blocks of the row the
 // lane streams (b = s, s + S, ...; S = 1 << lg_split lanes share a row's blocks); r is the row
@@ -194,9 +223,13 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     __shared__ int s_item_info[5];  // group, expert, tile, tokens, chunk
     __shared__ int64_t s_rows[kTB];  // activation row offsets currently staged
     __shared__ int s_staged_group, s_staged_nt, s_restage;
+    __shared__ int s_pairs_key[3];  // (group, expert, chunk) whose pairs are in s_pairs
 
     pdl_launch_dependents();
     if (threadIdx.x == 0) { s_staged_group = -1; s_staged_nt = 0; }
+    if (P.zero && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < P.n_zero; i += kThreads) P.zero[i] = 0u;
+    __shared__ int s_last;
 
     // ---- bucketing prologue (ids are inputs of the layer, not results of the previous kernel)
     if (threadIdx.x == 0) s_items[0] = 0;
@@ -223,7 +256,13 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = lane & 3;
 
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+    // each CTA takes a contiguous range of items: consecutive row tiles of one expert and
+    // chunk, so the staged activation rows and the bucket's pair list carry over
+    const int per_cta = (total_items + gridDim.x - 1) / gridDim.x;
+    const int item_begin = blockIdx.x * per_cta;
+    const int item_end = min(total_items, item_begin + per_cta);
+    if (threadIdx.x == 0) { s_pairs_key[0] = -1; }
+    for (int item = item_begin; item < item_end; ++item) {
         // ---- locate the item: group, expert (search over the item offsets), tile, chunk
         if (threadIdx.x == 0) {
             int gi = 0;
@@ -278,10 +317,15 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         }
 
         if (warp == 0) {
-            if (G.ids) {
-                warp_gather_bucket(G.ids, G.n_pairs, e, chunk * TB, nt, s_pairs);
-            } else if (lane < nt) {
-                s_pairs[lane] = chunk * TB + lane;
+            const bool have = s_pairs_key[0] == gi && s_pairs_key[1] == e && s_pairs_key[2] == chunk;
+            if (!have) {
+                if (G.ids) {
+                    warp_gather_bucket(G.ids, G.n_pairs, e, chunk * TB, nt, s_pairs);
+                } else if (lane < nt) {
+                    s_pairs[lane] = chunk * TB + lane;
+                }
+                __syncwarp();
+                if (lane == 0) { s_pairs_key[0] = gi; s_pairs_key[1] = e; s_pairs_key[2] = chunk; }
             }
             __syncwarp();
             // the same activation rows as the staged ones (e.g. every item of a broadcast
@@ -297,7 +341,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         }
         __syncthreads();
         const bool restage = s_restage != 0;
-        if (item == (int)blockIdx.x) pdl_wait();  // the activations may come from the previous kernel
+        if (item == item_begin) pdl_wait();  // the activations may come from the previous kernel
         if (restage) {
             if (warp == 0 && lane < nt) {
                 const int p = s_pairs[lane];
@@ -364,6 +408,30 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             }
         }
         __syncthreads();  // s_pairs / staged rows are rewritten by the next item
+        if (P.has_combine) {
+            // every item of this row tile, from either group, counts once; the last one combines
+            if (threadIdx.x == 0) {
+                __threadfence();
+                const unsigned expected = (unsigned)(total_items / G.tiles);
+                const unsigned prev = atomicAdd(&P.cb.counters[tile], 1u);
+                s_last = prev + 1u == expected;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                const int tr = G.n > 0 ? kWarps * (8 >> G.lg_split) : 0;
+                combine_rows(P, tile * tr, min(G.n, (tile + 1) * tr));
+                if (threadIdx.x == 0) P.cb.counters[tile] = 0u;
+            }
+            __syncthreads();
+        }
+    }
+    // every expert went to the tensor-core path: no item here counts, so combine every tile
+    if (P.has_combine && total_items == 0) {
+        pdl_wait();
+        const GroupDev& G = P.g[0];
+        const int tr = kWarps * (8 >> G.lg_split);
+        for (int tile = blockIdx.x; tile < G.tiles; tile += gridDim.x) combine_rows(P, tile * tr, min(G.n, (tile + 1) * tr));
     }
     // out-of-range ids: flag and zero their rows (CTA 0, after the previous kernel is done)
     if (blockIdx.x == 0) {
@@ -396,8 +464,16 @@ int num_sms() {
     return g_num_sms;
 }
 
+int idgemv_tile_rows(int k) {
+    const int nb = k / kQK;
+    const int lg = nb >= 4 * kDepth ? 2 : (nb >= 2 * kDepth ? 1 : 0);
+    return kWarps * (8 >> lg);
+}
+
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
-                          cudaStream_t stream, int tc_min, uint8_t* const* tc_img) {
+                          cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
+                          unsigned* zero, int n_zero) {
+    if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
     if (tc_min > 0) {
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
         if (e != cudaSuccess) return e;
@@ -407,6 +483,12 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     P.n_groups = n_groups;
     P.err_flag = err_flag;
     P.tc_min = tc_min;
+    P.zero = zero;
+    P.n_zero = zero ? n_zero : 0;
+    if (combine) {
+        P.has_combine = 1;
+        P.cb = *combine;
+    }
     // Tokens per work item: 1 when every bucket this kernel handles holds about one pair
     // (decode with distinct experts), which keeps the inner loop small; else up to 4.
     int tb = 1;
@@ -430,6 +512,8 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         // ring where possible (k = 2048: 2 lanes x 4 blocks; k = 4096: 4 x 4; k = 768: 1 x 3)
         const int nb = S.k / kQK;
         G.lg_split = nb >= 4 * kDepth ? 2 : (nb >= 2 * kDepth ? 1 : 0);
+        // with the combine fused, every group uses group 0's row tiles (one counter per tile)
+        if (combine && gi > 0) G.lg_split = P.g[0].lg_split;
         const int tile_rows = kWarps * (8 >> G.lg_split);
         G.tiles = (S.n + tile_rows - 1) / tile_rows;
         P.hist_off[gi] = ints;
@@ -437,7 +521,8 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         kmax = S.k > kmax ? S.k : kmax;
         max_items += (int64_t)G.n_pairs * G.tiles;
     }
-    if (max_items == 0) return cudaSuccess;
+    if (max_items == 0 && !combine) return cudaSuccess;
+    if (max_items == 0) max_items = 1;
     P.kmax = kmax;
     // tokens per item also bounded so the staged rows fit in ~150 KB of shared memory
     const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;

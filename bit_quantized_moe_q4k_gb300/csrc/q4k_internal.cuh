@@ -52,14 +52,33 @@ struct GemvGroup {
 // and the shared expert of a layer). fused_swiglu: out = silu(w . x) * (w2 . x).
 // pdl: the launch may start while the previous kernel of the stream drains (programmatic
 // dependent launch); the kernel waits for it before reading activations.
+// The combine fused into a down launch (group 0 = routed experts, group 1 = shared expert):
+// the last CTA to finish a row tile forms, for those rows of every token,
+//   y = h_mid + sum_s weights[t*top_k+s] * out0[t*top_k+s] + g_t * out1[t]
+// in slot order (deterministic). counters: one per row tile, zero on entry, left zero.
+struct CombineSpec {
+    float* y;
+    const float* h_mid;
+    const float* weights;
+    const float* shared_gate;
+    int shared_mode;
+    unsigned* counters;
+};
+
 // tc_min > 0: experts with at least tc_min pairs run on the tensor-core grouped GEMM
 // (q4k_tc.cu) first, using tc_img[g] (tc_image_bytes of the group) as scratch; the rest run on
-// the id-GEMV kernel.
+// the id-GEMV kernel. combine: fuse the combine into this (down) launch. zero / n_zero: CTA 0
+// zeroes these words before anything else (the gate|up launch prepares the counters the
+// following down launch uses).
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
-                          cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr);
+                          cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr,
+                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0);
+// rows per id-GEMV work item for a given k (the combine counters need ceil(n / rows) words)
+int idgemv_tile_rows(int k);
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
                       int* err_flag, cudaStream_t stream);
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);
+bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel's shared memory plan fits
 
 int num_sms();
 

@@ -46,6 +46,8 @@ constexpr int kImgB2 = kTcTok * 128;          // min-term operand [32 tokens x 1
 constexpr int kImgMin = 2 * kImgB;            // offset of the min-term operand
 constexpr int kImgBlock = 2 * kImgB + kImgB2; // bytes of one block's B image
 constexpr int kRawStage = kTcRows * kBlockBytes;
+constexpr int kNRaw = 4;   // raw Q4_K row stages in shared memory (copies run this far ahead)
+constexpr int kNImg = 3;   // activation image stages in shared memory
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: A stages (128 each), min-term A stages (16 each), D1 and D2 (32 each)
 constexpr uint32_t kColA = 0, kColA2 = 256, kColD1 = 288, kColD2 = 352;
@@ -231,11 +233,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* bimg = smem;                          // 2 x kImgBlock (1024-byte aligned stages)
-    uint8_t* raw = smem + 2 * kImgBlock;           // 2 x kRawStage
+    uint8_t* bimg = smem;                          // kNImg x kImgBlock (1024-byte aligned stages)
+    uint8_t* raw = smem + kNImg * kImgBlock;       // kNRaw x kRawStage
     int* tabs = reinterpret_cast<int*>(smem + P.tab_off);
-    __shared__ __align__(8) uint64_t bar_raw_full[2], bar_raw_empty[2], bar_a_full[2], bar_a_empty[2];
-    __shared__ __align__(8) uint64_t bar_b_full[2], bar_b_empty[2], bar_d_full[2], bar_d_empty[2], bar_drain;
+    __shared__ __align__(8) uint64_t bar_raw_full[kNRaw], bar_raw_empty[kNRaw], bar_a_full[2], bar_a_empty[2];
+    __shared__ __align__(8) uint64_t bar_b_full[kNImg], bar_b_empty[kNImg], bar_d_full[2], bar_d_empty[2], bar_drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_warp[33];
     __shared__ int s_bad;
@@ -255,13 +257,17 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNRaw; ++i) {
             mbar_init(&bar_raw_full[i], 1);
             mbar_init(&bar_raw_empty[i], 128);
-            mbar_init(&bar_a_full[i], 128);
-            mbar_init(&bar_a_empty[i], 1);
+        }
+        for (int i = 0; i < kNImg; ++i) {
             mbar_init(&bar_b_full[i], 1);
             mbar_init(&bar_b_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_a_full[i], 128);
+            mbar_init(&bar_a_empty[i], 1);
             mbar_init(&bar_d_full[i], 1);
             mbar_init(&bar_d_empty[i], 128);
         }
@@ -288,26 +294,28 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             const int rows_valid = min(kTcRows, G.n - row0);
             const uint8_t* img = G.img + (int64_t)(start[it.e] + it.chunk) * nb * kImgBlock;
             for (int s = 0; s < steps; ++s, ++gs) {
-                const int st = gs & 1;
-                const uint32_t ph = (gs >> 1) & 1;
+                const int rst = gs % kNRaw;
+                const uint32_t rph = (gs / kNRaw) & 1;
+                const int bst = gs % kNImg;
+                const uint32_t bph = (gs / kNImg) & 1;
                 const int slab = s / nb, b = s % nb;
                 const uint8_t* w = (slab == 0 ? G.w : G.w2) + (int64_t)it.e * G.nb02 + (int64_t)row0 * G.nb01 +
                                    (int64_t)b * kBlockBytes;
                 int okl = 1;
                 if (lane == 0) {
-                    okl = mbar_wait(&bar_raw_empty[st], ph ^ 1, &s_abort);
-                    if (okl) mbar_arrive_expect_tx(&bar_raw_full[st], (uint32_t)rows_valid * kBlockBytes);
+                    okl = mbar_wait(&bar_raw_empty[rst], rph ^ 1, &s_abort);
+                    if (okl) mbar_arrive_expect_tx(&bar_raw_full[rst], (uint32_t)rows_valid * kBlockBytes);
                 }
                 if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
                 for (int r = lane; r < rows_valid; r += 32)
-                    bulk_g2s(raw + st * kRawStage + r * kBlockBytes, w + (int64_t)r * G.nb01, kBlockBytes,
-                             &bar_raw_full[st]);
+                    bulk_g2s(raw + rst * kRawStage + r * kBlockBytes, w + (int64_t)r * G.nb01, kBlockBytes,
+                             &bar_raw_full[rst]);
                 raw_issued = gs + 1;
                 if (lane == 0) {
-                    okl = mbar_wait(&bar_b_empty[st], ph ^ 1, &s_abort);
+                    okl = mbar_wait(&bar_b_empty[bst], bph ^ 1, &s_abort);
                     if (okl) {
-                        mbar_arrive_expect_tx(&bar_b_full[st], kImgBlock);
-                        bulk_g2s(bimg + st * kImgBlock, img + (int64_t)b * kImgBlock, kImgBlock, &bar_b_full[st]);
+                        mbar_arrive_expect_tx(&bar_b_full[bst], kImgBlock);
+                        bulk_g2s(bimg + bst * kImgBlock, img + (int64_t)b * kImgBlock, kImgBlock, &bar_b_full[bst]);
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
@@ -317,8 +325,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         if (!ok && lane == 0) {
             // let the copies already issued land before the CTA leaves (bounded)
             volatile int never = 0;
-            for (int g = max(0, raw_issued - 2); g < raw_issued; ++g) mbar_wait(&bar_raw_full[g & 1], (g >> 1) & 1, &never);
-            for (int g = max(0, b_issued - 2); g < b_issued; ++g) mbar_wait(&bar_b_full[g & 1], (g >> 1) & 1, &never);
+            for (int g = max(0, raw_issued - kNRaw); g < raw_issued; ++g)
+                mbar_wait(&bar_raw_full[g % kNRaw], (g / kNRaw) & 1, &never);
+            for (int g = max(0, b_issued - kNImg); g < b_issued; ++g)
+                mbar_wait(&bar_b_full[g % kNImg], (g / kNImg) & 1, &never);
         }
     } else if (warp == 5) {
         // ---------------- MMA issuer (one thread)
@@ -331,13 +341,15 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 for (int s = 0; s < steps; ++s, ++gs) {
                     const int st = gs & 1;
                     const uint32_t ph = (gs >> 1) & 1;
-                    if (!mbar_wait(&bar_a_full[st], ph, &s_abort) || !mbar_wait(&bar_b_full[st], ph, &s_abort) ||
+                    const int bst = gs % kNImg;
+                    const uint32_t bph = (gs / kNImg) & 1;
+                    if (!mbar_wait(&bar_a_full[st], ph, &s_abort) || !mbar_wait(&bar_b_full[bst], bph, &s_abort) ||
                         !mbar_wait(&bar_d_empty[st], ph ^ 1, &s_abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_addr = bimg_addr + st * kImgBlock;
+                    const uint32_t b_addr = bimg_addr + bst * kImgBlock;
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk) {
                         const uint32_t koff = (kk >> 2) * (kTcTok * 128) + (kk & 3) * 32;
@@ -348,7 +360,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     mma_f16_ts(tmem + kColD2 + st * 32, tmem + kColA2 + st * 16, desc_sw128_kmajor(b_addr + kImgMin),
                                idesc, 0);
                     mma_commit(&bar_a_empty[st]);
-                    mma_commit(&bar_b_empty[st]);
+                    mma_commit(&bar_b_empty[bst]);
                     mma_commit(&bar_d_full[st]);
                     issued = gs + 1;
                 }
@@ -388,12 +400,14 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 const uint32_t ph = (g_cur >> 1) & 1;
                 float d_cur = 0.f, dmin_cur = 0.f;
                 if (s < steps) {
-                    if (!mbar_wait(&bar_raw_full[st], ph, &s_abort)) { ok = false; break; }
-                    const uint4* rp = reinterpret_cast<const uint4*>(raw + st * kRawStage + r * kBlockBytes);
+                    const int rst = g_cur % kNRaw;
+                    const uint32_t rph = (g_cur / kNRaw) & 1;
+                    if (!mbar_wait(&bar_raw_full[rst], rph, &s_abort)) { ok = false; break; }
+                    const uint4* rp = reinterpret_cast<const uint4*>(raw + rst * kRawStage + r * kBlockBytes);
                     uint4 hq[9];
 #pragma unroll
                     for (int i = 0; i < 9; ++i) hq[i] = rp[i];
-                    mbar_arrive(&bar_raw_empty[st]);
+                    mbar_arrive(&bar_raw_empty[rst]);
                     const uint4 h = hq[0];
                     d_cur = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
                     dmin_cur = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
@@ -502,6 +516,12 @@ size_t tc_image_bytes(int n_pairs, int k, int tc_min) {
 
 static bool g_tc_attr_set[2][64] = {};
 
+bool tc_fits(const GemvGroup* groups, int n_groups) {
+    int ints = 0;
+    for (int gi = 0; gi < n_groups; ++gi) ints += 2 * groups[gi].num_experts;
+    return 1024 + (size_t)(kNImg * kImgBlock + kNRaw * kRawStage) + (size_t)ints * 4 <= 200 * 1024;
+}
+
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
                       int* err_flag, cudaStream_t stream) {
     TcParams P{};
@@ -546,7 +566,7 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
         err = cudaLaunchKernelEx(&cfg, tc_prep_kernel, P);
         if (err != cudaSuccess) return err;
     }
-    P.tab_off = 2 * kImgBlock + 2 * kRawStage;
+    P.tab_off = kNImg * kImgBlock + kNRaw * kRawStage;
     // every CTA holds all 512 tensor-memory columns: ask for enough shared memory that only
     // one CTA fits on an SM
     size_t smem = 1024 + (size_t)P.tab_off + (size_t)ints * 4;

@@ -216,6 +216,10 @@ int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_d
  * bucket holds many tokens run on the tensor-core grouped GEMM. 0 when that path is off. */
 size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int shared_inter, int k_shared);
 
+/* Number of kernels one q4k_moe_layer_forward call with its full workspace launches for these
+ * sizes (2, plus 2 per half that takes the tensor-core path). 0 on invalid sizes. */
+int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
+
 /* ---------------------------------------------------------------------------------
  * q4k_moe_layer_forward_host -- the same layer with the per-step inputs and the
  * output in HOST memory (pinned memory gives asynchronous copies). Weights and the

@@ -36,9 +36,10 @@ def _gemv(w, E, a, outer, inner, ids, m, T, n, k, workspace):
 
 
 @pytest.mark.parametrize("mode", ["gate_up", "down"])
-@pytest.mark.parametrize("E,n,k,m,T", [(4, 288, 512, 48, 2),     # ~24 pairs per expert, ragged 3rd row tile
-                                       (2, 128, 1024, 40, 2),    # 40 pairs per expert: 2 chunks
-                                       (3, 256, 256, 70, 1)])    # one block per row
+# sizes give the path enough work (>= 64 items of 128 rows x 32 tokens) to be chosen
+@pytest.mark.parametrize("E,n,k,m,T", [(4, 2148, 512, 64, 2),    # ~32 pairs per expert, ragged last row tile
+                                       (2, 4096, 1024, 40, 2),   # 40 pairs per expert: 2 chunks
+                                       (3, 3072, 256, 70, 1)])   # one block per row
 def test_tc_id_gemv_matches_oracle(mode, E, n, k, m, T):
     seed = 500 + n + k
     w = oracle_slab(seed, "tc", E, n, k)
@@ -59,7 +60,7 @@ def test_tc_id_gemv_matches_oracle(mode, E, n, k, m, T):
 
 def test_tc_mixed_bucket_sizes_zipf():
     """Zipf ids: the head experts take the tensor-core path, the tail the id-GEMV kernel."""
-    E, n, k, m, T = 16, 160, 768, 48, 4
+    E, n, k, m, T = 16, 4096, 512, 48, 4
     seed = 611
     w = oracle_slab(seed, "tc", E, n, k)
     ids = inputs.ids_zipf_distinct(seed, m, T, E)
@@ -71,7 +72,7 @@ def test_tc_mixed_bucket_sizes_zipf():
 
 
 def test_tc_ffn_fused_gate_up_matches_oracle():
-    E, H, I, m, T = 4, 512, 512, 40, 2
+    E, H, I, m, T = 4, 512, 4096, 40, 2  # gate|up on tensor cores, down (512 rows) on the id-GEMV kernel
     seed = 621
     wg, wu = oracle_slab(seed, "gate", E, I, H), oracle_slab(seed, "up", E, I, H)
     wd = oracle_slab(seed, "down", E, H, I)
@@ -91,7 +92,7 @@ def test_tc_ffn_fused_gate_up_matches_oracle():
 def test_tc_layer_shared_expert_takes_tensor_cores():
     """m >= 16: the shared expert's bucket holds every token and runs on the tensor-core path."""
     from bit_quantized_moe_q4k_gb300.workloads import Workload
-    W = Workload("tc_layer", 512, 256, 32, 2, 24, "uniform", 512, 2, 631)
+    W = Workload("tc_layer", 512, 256, 32, 2, 48, "uniform", 4096, 2, 631)
     seed = W.seed
     ids = inputs.make_ids(seed, W.ids, W.m, W.top_k, W.num_experts)
     wg = oracle_slab(seed, "gate", W.num_experts, W.inter, W.hidden)
