@@ -28,6 +28,7 @@
 // The B image of a (chunk, block) is built once by tc_prep_kernel in the workspace: the 32
 // tokens' x in fp16, in the k order of the A columns, already laid out as the 128-byte
 // swizzled K-major smem tile, plus the sx hi/lo row of the min-term MMA.
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "q4k_bucket.cuh"
@@ -65,6 +66,7 @@ struct TcGroup {
 };
 
 struct TcParams {
+    CUtensorMap tmap[2][2];  // [group][slab]: the slab as a 2-D byte tensor [E*n rows, nb01 bytes]
     TcGroup g[2];
     int n_groups;
     int tc_min;       // experts with at least this many pairs take the tensor-core path
@@ -299,17 +301,17 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 const int bst = gs % kNImg;
                 const uint32_t bph = (gs / kNImg) & 1;
                 const int slab = s / nb, b = s % nb;
-                const uint8_t* w = (slab == 0 ? G.w : G.w2) + (int64_t)it.e * G.nb02 + (int64_t)row0 * G.nb01 +
-                                   (int64_t)b * kBlockBytes;
                 int okl = 1;
                 if (lane == 0) {
                     okl = mbar_wait(&bar_raw_empty[rst], rph ^ 1, &s_abort);
-                    if (okl) mbar_arrive_expect_tx(&bar_raw_full[rst], (uint32_t)rows_valid * kBlockBytes);
+                    if (okl) {
+                        // one tensor load: 128 rows x 144 bytes of block b (rows past the slab read as zero)
+                        mbar_arrive_expect_tx(&bar_raw_full[rst], kRawStage);
+                        tma_load_2d(raw + rst * kRawStage, &P.tmap[gi][slab], b * kBlockBytes, it.e * G.n + row0,
+                                    &bar_raw_full[rst]);
+                    }
                 }
                 if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
-                for (int r = lane; r < rows_valid; r += 32)
-                    bulk_g2s(raw + rst * kRawStage + r * kBlockBytes, w + (int64_t)r * G.nb01, kBlockBytes,
-                             &bar_raw_full[rst]);
                 raw_issued = gs + 1;
                 if (lane == 0) {
                     okl = mbar_wait(&bar_b_empty[bst], bph ^ 1, &s_abort);
@@ -516,6 +518,37 @@ size_t tc_image_bytes(int n_pairs, int k, int tc_min) {
 
 static bool g_tc_attr_set[2][64] = {};
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The slab as a 2-D uint8 tensor: rows = num_experts * n, row length = nb01 bytes; one box is
+// one Q4_K block (144 bytes) of 128 consecutive rows.
+static cudaError_t encode_slab_map(CUtensorMap* map, const uint8_t* w, int num_experts, int n, int64_t nb01) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)nb01, (cuuint64_t)num_experts * (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)nb01};
+    const cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)kTcRows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool tc_fits(const GemvGroup* groups, int n_groups) {
     int ints = 0;
     for (int gi = 0; gi < n_groups; ++gi) ints += 2 * groups[gi].num_experts;
@@ -542,6 +575,9 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
         G.tiles = (S.n + kTcRows - 1) / kTcRows;
         P.hist_off[gi] = ints;
         ints += 2 * S.num_experts;
+        cudaError_t me = encode_slab_map(&P.tmap[gi][0], S.w, S.num_experts, S.n, G.nb01);
+        if (me == cudaSuccess && fused) me = encode_slab_map(&P.tmap[gi][1], S.w2, S.num_experts, S.n, G.nb01);
+        if (me != cudaSuccess) return me;
         const int64_t mc = tc_max_chunks(G.n_pairs, tc_min);
         max_chunks = mc > max_chunks ? mc : max_chunks;
         max_tiles = G.tiles > max_tiles ? G.tiles : max_tiles;
