@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--layers", type=int, default=0, help="size of the layer rotation (default: > 3x L2 touched)")
+    ap.add_argument("--separate-inputs", action="store_true",
+                    help="one allocation per layer for its activations, ids and weights instead of stacked tensors")
     return ap.parse_args()
 
 
@@ -230,16 +232,27 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
                    "hm": inputs.normal(seed, "h_mid", (m, H)), "rw": inputs.routing_weights(seed, m, T),
                    "gl": inputs.normal(seed, "shared_gate", (m,))}
         L["ids_np"] = L["np"]["ids"]
-        for key, val in L["np"].items():
-            L[key] = torch.from_numpy(val).to(dev)
         layers.append(L)
+    # Per-layer activations, ids and routing weights: one stacked tensor per kind (as an
+    # inference engine keeps them in a few reused buffers), each layer reading its own slice;
+    # only the weights rotate through HBM. --separate-inputs gives each its own allocation.
+    for key in layers[0]["np"]:
+        if args.separate_inputs:
+            for L in layers:
+                L[key] = torch.from_numpy(L["np"][key]).to(dev)
+        else:
+            stacked = torch.from_numpy(np.stack([L["np"][key] for L in layers])).to(dev)
+            for li, L in enumerate(layers):
+                L[key] = stacked[li]
     torch.cuda.synchronize()
 
     act = torch.empty(P * I, dtype=torch.float32, device=dev)
     act_s = torch.empty(max(1, m * Is), dtype=torch.float32, device=dev)
     eout = torch.empty(P * H, dtype=torch.float32, device=dev)
     sout = torch.empty(m * H, dtype=torch.float32, device=dev)
-    y = torch.empty(m * H, dtype=torch.float32, device=dev)
+    # Layers are chained as in a model: step i reads h_post from xy[i % 2] and writes its output
+    # y to xy[(i + 1) % 2], which the next step reads (--separate-inputs: each layer's own x).
+    xy = [layers[0]["x"].clone().reshape(-1), torch.empty(m * H, dtype=torch.float32, device=dev)]
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -248,23 +261,28 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     ws_gu = torch.empty(max(256, ws_gu_bytes), dtype=torch.uint8, device=dev)
     ws_dn = torch.empty(max(256, ws_dn_bytes), dtype=torch.uint8, device=dev)
 
-    def gate_up(L):
-        q4k.q4k_moe_layer_gate_up(L["wg"], L["wu"], E, L["sg"], L["su"], Is, L["x"], L["ids"], m, T, H, I, act,
+    def x_of(L, i):
+        return L["x"] if args.separate_inputs else xy[i % 2]
+
+    def gate_up(L, i):
+        q4k.q4k_moe_layer_gate_up(L["wg"], L["wu"], E, L["sg"], L["su"], Is, x_of(L, i), L["ids"], m, T, H, I, act,
                                   act_s if Is else None, ws_gu, ws_gu_bytes, flag, stream)
 
     layer_ws_bytes = q4k.q4k_moe_layer_workspace_size(m, T, E, H, I, Is)
     layer_ws = torch.empty(layer_ws_bytes, dtype=torch.uint8, device=dev)
 
-    def step(L):
+    def step(L, i):
         # the public layer call: gate|up + SwiGLU (routed and shared) then down with the combine fused
-        q4k.q4k_moe_layer_forward(L["wg"], L["wu"], L["wd"], E, L["sg"], L["su"], L["sd"], Is, W.shared_mode, L["x"],
-                                  L["hm"], L["ids"], L["rw"], L["gl"], m, T, H, I, y, layer_ws, layer_ws_bytes, flag,
+        y = xy[(i + 1) % 2]
+        q4k.q4k_moe_layer_forward(L["wg"], L["wu"], L["wd"], E, L["sg"], L["su"], L["sd"], Is, W.shared_mode,
+                                  x_of(L, i), L["hm"], L["ids"], L["rw"], L["gl"], m, T, H, I, y, layer_ws,
+                                  layer_ws_bytes, flag,
                                   stream)
 
     # eager warm-up (first launches set kernel attributes), then capture
     with torch.cuda.stream(stream):
         for i in range(max(1, min(args.warmup, n_layers))):
-            step(layers[i % n_layers])
+            step(layers[i % n_layers], i)
     stream.synchronize()
     assert int(flag.item()) == 0, "device error flag raised"
 
@@ -276,13 +294,13 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g_warm, stream=stream, capture_error_mode="thread_local"):
             for i in range(Wm):
-                step(layers[i % n_layers])
+                step(layers[i % n_layers], i)
         with torch.cuda.graph(g_timed, stream=stream, capture_error_mode="thread_local"):
             for i in range(K):
-                step(layers[(Wm + i) % n_layers])
+                step(layers[(Wm + i) % n_layers], Wm + i)
         with torch.cuda.graph(g_kernel, stream=stream, capture_error_mode="thread_local"):
             for i in range(K):
-                gate_up(layers[(Wm + i) % n_layers])
+                gate_up(layers[(Wm + i) % n_layers], Wm + i)
     stream.synchronize()
 
     dist = None
@@ -450,7 +468,10 @@ def main():
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "q4k weights, fp32 activations (exact int dp4a sums)", "data": "synthetic",
         "config": dict(config, l2=f"rotating {r['n_layers']} layers' weights, "
-                                  f"{r['per_layer_touched'] / 1e6:.1f} MB touched per step (> L2 between reuses)"),
+                                  f"{r['per_layer_touched'] / 1e6:.1f} MB touched per step (> L2 between reuses)",
+                    inputs="separate allocations per layer" if args.separate_inputs else
+                    "layers chained (each step's h_post is the previous step's output); per-layer "
+                    "h_mid/ids/routing weights as slices of stacked tensors"),
         "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / peak,
         "experts_touched_per_step": r["experts_touched"],
         "roofline": {"kernel": "idgemv_kernel<fused gate|up+SwiGLU> (routed + shared)", "bound": "hbm",

@@ -22,18 +22,12 @@
 //      sum_i w_i x_i = delta_j * (d*sc_j * S_j - dmin*m_j * sum_i X_i).
 //  * Lanes sharing a row reduce with warp shuffles; the epilogue writes the pair's row
 //    (optionally silu(g) * u).
-#include <cuda_fp16.h>
+#include <algorithm>
+#include <cstdlib>
 
-#include "q4k_bucket.cuh"
-#include "q4k_internal.cuh"
+#include "q4k_gemv_common.cuh"
 
 namespace q4k {
-
-constexpr int kThreads = 128;               // 4 warps
-constexpr int kWarps = kThreads / 32;
-constexpr int kTB = 4;                      // max tokens of one bucket per work item
-constexpr int kPairBytes = 144;             // staged planes of 2 sub-blocks + 16 B pad
-constexpr int kMaxGroups = 2;
 
 struct GroupDev {
     const uint8_t* w;
@@ -62,72 +56,13 @@ struct GemvParams {
     CombineSpec cb;
     unsigned* zero;         // CTA 0 zeroes zero[0..n_zero) first
     int n_zero;
+    int fast;               // every group has at most 32 pairs: bucket with one warp per group
+    L2Prefetch pf[kMaxGroups];  // rows of the next launch to start into L2 (fast mode), by group bucket
+    int n_pf;
 };
 
-__device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
-
-// Programmatic dependent launch: let the next kernel in the stream start its prologue, and
-// wait for the previous kernel's results before reading them (no-ops without the launch
-// attribute).
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// (scale, min) of sub-blocks ja = 2c and jb = 2c + 1 from the 16-byte block header
-// (d, dmin, 12 scale bytes; GGML Q4_K placement), multiplied by d and dmin.
-__device__ __forceinline__ void block_scales(uint4 h, int c, float& sa, float& ma, float& sb, float& mb) {
-    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-    const bool hi = c >= 2;  // sub-blocks 4..7 take their low bits from bytes 8..11
-    const int ia = (2 * c) & 3, ib = (2 * c + 1) & 3;
-    const unsigned ya = (h.y >> (8 * ia)) & 0xFFu, yb = (h.y >> (8 * ib)) & 0xFFu;
-    const unsigned za = (h.z >> (8 * ia)) & 0xFFu, zb = (h.z >> (8 * ib)) & 0xFFu;
-    const unsigned wa = (h.w >> (8 * ia)) & 0xFFu, wb = (h.w >> (8 * ib)) & 0xFFu;
-    const unsigned sca = hi ? ((wa & 15u) | ((ya >> 6) << 4)) : (ya & 63u);
-    const unsigned mna = hi ? ((wa >> 4) | ((za >> 6) << 4)) : (za & 63u);
-    const unsigned scb = hi ? ((wb & 15u) | ((yb >> 6) << 4)) : (yb & 63u);
-    const unsigned mnb = hi ? ((wb >> 4) | ((zb >> 6) << 4)) : (zb & 63u);
-    sa = d * (float)sca;
-    ma = dmin * (float)mna;
-    sb = d * (float)scb;
-    mb = dmin * (float)mnb;
-}
-
-// Exact integer dot products of one lane's 64 codes with one token's staged planes.
-// q0, q1: the lane's 32 code bytes; L*/H*: low / high planes of sub-blocks a and b.
-__device__ __forceinline__ void dot64(const uint4& q0, const uint4& q1, const uint4* xp, int& Sa, int& Sb) {
-    const uint4 La0 = xp[0], La1 = xp[1], Ha0 = xp[2], Ha1 = xp[3];
-    const uint4 Lb0 = xp[4], Lb1 = xp[5], Hb0 = xp[6], Hb1 = xp[7];
-    const unsigned qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const unsigned la[8] = {La0.x, La0.y, La0.z, La0.w, La1.x, La1.y, La1.z, La1.w};
-    const unsigned ha[8] = {Ha0.x, Ha0.y, Ha0.z, Ha0.w, Ha1.x, Ha1.y, Ha1.z, Ha1.w};
-    const unsigned lb[8] = {Lb0.x, Lb0.y, Lb0.z, Lb0.w, Lb1.x, Lb1.y, Lb1.z, Lb1.w};
-    const unsigned hb[8] = {Hb0.x, Hb0.y, Hb0.z, Hb0.w, Hb1.x, Hb1.y, Hb1.z, Hb1.w};
-    unsigned sal = 0, sbl = 0;
-    int sah = 0, sbh = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const unsigned lo = qw[i] & 0x0F0F0F0Fu;
-        const unsigned hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
-        sal = __dp4a(lo, la[i], sal);
-        sah = __dp4a((int)lo, (int)ha[i], sah);
-        sbl = __dp4a(hi, lb[i], sbl);
-        sbh = __dp4a((int)hi, (int)hb[i], sbh);
-    }
-    Sa = (int)sal + sah * 256;
-    Sb = (int)sbl + sbh * 256;
-}
-
-// Stage the activation rows of the item's pairs: per 32-element sub-block j of token t,
-// planes at xs + t*tok_bytes + (j/2)*144 + (j%2)*64 (low plane 32 B, high plane 32 B),
-// and (delta, sumX) at meta[t*(k/32) + j]. Thread f handles float4 f of the row; the 8
-// threads of a sub-block reduce max|x| and sum(X) with shuffles. All loads of a pass are
-// issued before any is used.
-constexpr int kStageUnroll = 8;
-
+// Stage the activation rows of the item's pairs (token t at xs + t*tok_bytes, meta + t*(k/32)).
+// Thread f handles float4 f of the row; all loads of a pass are issued before any is used.
 __device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs, int nt, uint8_t* xs,
                                            float2* meta) {
     const int tid = threadIdx.x;
@@ -148,61 +83,18 @@ __device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs
             for (int u = 0; u < kStageUnroll; ++u) {
                 const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
                 if (f0 + u * kThreads >= nf) break;
-                float mx = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-#pragma unroll
-                for (int off = 1; off < 8; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                int X[4] = {0, 0, 0, 0};
-                if (mx > 0.0f) {
-                    const float inv = 32767.0f / mx;
-                    X[0] = max(-32767, min(32767, __float2int_rn(v[u].x * inv)));
-                    X[1] = max(-32767, min(32767, __float2int_rn(v[u].y * inv)));
-                    X[2] = max(-32767, min(32767, __float2int_rn(v[u].z * inv)));
-                    X[3] = max(-32767, min(32767, __float2int_rn(v[u].w * inv)));
-                }
-                int sx = X[0] + X[1] + X[2] + X[3];
-#pragma unroll
-                for (int off = 1; off < 8; off <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, off);
-                if (f < nf) {
-                    const int j = f >> 3, wi = f & 7;
-                    const uint32_t lo = (uint32_t)(X[0] & 0xFF) | ((uint32_t)(X[1] & 0xFF) << 8) |
-                                        ((uint32_t)(X[2] & 0xFF) << 16) | ((uint32_t)(X[3] & 0xFF) << 24);
-                    const uint32_t hi = (uint32_t)((X[0] >> 8) & 0xFF) | ((uint32_t)((X[1] >> 8) & 0xFF) << 8) |
-                                        ((uint32_t)((X[2] >> 8) & 0xFF) << 16) | ((uint32_t)((X[3] >> 8) & 0xFF) << 24);
-                    uint32_t* planes = reinterpret_cast<uint32_t*>(xs + t * tok_bytes + (j >> 1) * kPairBytes + (j & 1) * 64);
-                    planes[wi] = lo;
-                    planes[8 + wi] = hi;
-                    if (wi == 0) meta[t * nsb + j] = make_float2(mx / 32767.0f, (float)sx);
-                }
+                stage_quad(v[u], f, f < nf, xs + t * tok_bytes, meta + t * nsb);
             }
         }
     }
 }
 
-constexpr int kDepth = 4;  // blocks of the weight stream in flight per lane
-
-// Combine of rows [r0, r1) of every token (moeflux expert_forward.rs, the batched combine:
-// hidden_out = h_mid + sum_k w_k * expert_out_k + shared term), run by the last CTA of a row
-// tile. Expert rows were written by other CTAs: read them from L2. A pair whose id is out of
-// range contributes nothing (its row is zero by definition).
+// Combine of rows [r0, r1) of every token, run by the last CTA of a row tile.
 __device__ void combine_rows(const GemvParams& P, int r0, int r1) {
     const GroupDev& R = P.g[0];
-    const int H = R.n, T = R.top_k, m = R.n_pairs / T;
     const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
-    const int span = r1 - r0;
-    for (int idx = threadIdx.x; idx < m * span; idx += blockDim.x) {
-        const int t = idx / span, r = r0 + idx % span;
-        const int64_t o = (int64_t)t * H + r;
-        float acc = P.cb.h_mid[o];
-        for (int s = 0; s < T; ++s) {
-            const int p = t * T + s;
-            if (id_valid(R.ids[p], R.num_experts)) acc = fmaf(P.cb.weights[p], __ldcg(R.out + (int64_t)p * H + r), acc);
-        }
-        if (shared) {
-            const float g = P.cb.shared_mode == Q4K_SHARED_SIGMOID ? 1.0f / (1.0f + expf(-P.cb.shared_gate[t])) : 1.0f;
-            acc = fmaf(g, __ldcg(P.g[1].out + o), acc);
-        }
-        P.cb.y[o] = acc;
-    }
+    combine_span(P.cb, R.out, R.ids, R.num_experts, R.n_pairs, R.top_k, R.n, shared ? P.g[1].out : nullptr, r0, r1,
+                 threadIdx.x, blockDim.x);
 }
 
 // Lane layout: lane = c | s << 2 | r << (2 + lg_split). c (0..3) picks the 64-weight group of
@@ -231,9 +123,34 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         for (int i = threadIdx.x; i < P.n_zero; i += kThreads) P.zero[i] = 0u;
     __shared__ int s_last;
 
+    __shared__ FastGroup s_fast[kMaxGroups];
     // ---- bucketing prologue (ids are inputs of the layer, not results of the previous kernel)
     if (threadIdx.x == 0) s_items[0] = 0;
-    for (int gi = 0; gi < P.n_groups; ++gi) {
+    if (P.fast) {
+        if (warp_id_of_thread() < P.n_groups) {
+            const int gi = warp_id_of_thread();
+            const GroupDev& G = P.g[gi];
+            fast_bucket(G.ids, G.n_pairs, G.num_experts, G.tiles, TB, P.tc_min, s_fast[gi], &s_bad[gi]);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            for (int gi = 0; gi < P.n_groups; ++gi) s_items[gi + 1] = s_items[gi] + s_fast[gi].start[s_fast[gi].U];
+        // The following launch's rows for the experts of this batch (known now) go to L2 while
+        // this launch streams its own: pieces of kPfPiece bytes spread over the CTAs.
+        const int64_t pc0 = P.n_pf > 0 ? (P.pf[0].expert_bytes + kPfPiece - 1) / kPfPiece : 0;
+        const int64_t pc1 = P.n_pf > 1 ? (P.pf[1].expert_bytes + kPfPiece - 1) / kPfPiece : 0;
+        const int64_t n0 = pc0 * s_fast[0].U, n_all = n0 + (P.n_pf > 1 ? pc1 * s_fast[1].U : 0);
+        for (int64_t q = blockIdx.x + (int64_t)gridDim.x * threadIdx.x; q < n_all; q += (int64_t)gridDim.x * kThreads) {
+            const int i = q < n0 ? 0 : 1;
+            const int64_t qq = i == 0 ? q : q - n0, pc = i == 0 ? pc0 : pc1;
+            const int e = s_fast[i].e[qq / pc];
+            const int64_t off = (qq % pc) * kPfPiece;
+            const int64_t bytes = min((int64_t)kPfPiece, P.pf[i].expert_bytes - off);
+            bulk_prefetch_l2(P.pf[i].base + (int64_t)e * P.pf[i].expert_bytes + off, (uint32_t)bytes);
+        }
+        __syncthreads();
+    }
+    for (int gi = 0; gi < P.n_groups && !P.fast; ++gi) {
         const GroupDev& G = P.g[gi];
         int* cnt = s_int + P.hist_off[gi];
         int* start = cnt + G.num_experts;
@@ -264,7 +181,45 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     if (threadIdx.x == 0) { s_pairs_key[0] = -1; }
     for (int item = item_begin; item < item_end; ++item) {
         // ---- locate the item: group, expert (search over the item offsets), tile, chunk
-        if (threadIdx.x == 0) {
+        if (P.fast) {
+            if (warp == 0) {
+                int gi = 0;
+                while (gi + 1 < P.n_groups && item >= s_items[gi + 1]) ++gi;
+                const FastGroup& F = s_fast[gi];
+                const int local = item - s_items[gi];
+                const bool mine = lane < F.U && F.start[lane] <= local && local < F.start[lane + 1];
+                const unsigned hit = __ballot_sync(0xffffffffu, mine);
+                const int r = __ffs(hit) - 1;
+                const unsigned mask = F.mask[r];
+                const int cnt = __popc(mask);
+                const int chunks = (cnt + TB - 1) / TB;
+                const int in_e = local - F.start[r];
+                const int chunk = in_e % chunks;
+                const int nt = min(TB, cnt - chunk * TB);
+                // pair `lane` is a member: its place in the bucket is the members below it
+                const int q = __popc(mask & ((1u << lane) - 1u)) - chunk * TB;
+                if (((mask >> lane) & 1u) && q >= 0 && q < nt) s_pairs[q] = lane;
+                if (lane == 0) {
+                    s_item_info[0] = gi;
+                    s_item_info[1] = F.e[r];
+                    s_item_info[2] = in_e / chunks;
+                    s_item_info[3] = nt;
+                    s_item_info[4] = chunk;
+                    s_pairs_key[0] = gi; s_pairs_key[1] = F.e[r]; s_pairs_key[2] = chunk;
+                }
+                __syncwarp();
+                // the same activation rows as the staged ones need no restaging
+                const GroupDev& G = P.g[gi];
+                bool same = s_staged_group == gi && s_staged_nt == nt;
+                if (lane < nt) {
+                    const int p = s_pairs[lane];
+                    const int64_t arow = (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+                    same = same && s_rows[lane] == arow;
+                }
+                same = __all_sync(0xffffffffu, same);
+                if (lane == 0) s_restage = same ? 0 : 1;
+            }
+        } else if (threadIdx.x == 0) {
             int gi = 0;
             while (gi + 1 < P.n_groups && item >= s_items[gi + 1]) ++gi;
             const GroupDev& G = P.g[gi];
@@ -290,10 +245,11 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         const int chunk = s_item_info[4];
         const GroupDev& G = P.g[gi];
 
-        // ---- start the weight stream before staging (independent of the activations)
         const int lgS = G.lg_split, S = 1 << lgS;
-        const int sl = (lane >> 2) & (S - 1);
         const int rows_per_warp = 8 >> lgS;
+
+        // ---- start the weight stream before staging (independent of the activations)
+        const int sl = (lane >> 2) & (S - 1);
         const int row = (tile * kWarps + warp) * rows_per_warp + (lane >> (2 + lgS));
         const bool row_ok = row < G.n;
         const int nb = G.k / kQK;
@@ -316,7 +272,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             }
         }
 
-        if (warp == 0) {
+        if (!P.fast && warp == 0) {
             const bool have = s_pairs_key[0] == gi && s_pairs_key[1] == e && s_pairs_key[2] == chunk;
             if (!have) {
                 if (G.ids) {
@@ -339,7 +295,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
             same = __all_sync(0xffffffffu, same);
             if (lane == 0) s_restage = same ? 0 : 1;
         }
-        __syncthreads();
+        if (!P.fast) __syncthreads();
         const bool restage = s_restage != 0;
         if (item == item_begin) pdl_wait();  // the activations may come from the previous kernel
         if (restage) {
@@ -453,6 +409,15 @@ static int g_num_sms = 0;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 200 * 1024;
 static bool g_smem_attr_set[4][kMaxDevices] = {};
+// Switches (environment, read at every launch): Q4K_NEXT_PREFETCH=0 turns off the L2
+// prefetch of the next launch's rows (default on); Q4K_STREAM=1 sends small batches to the
+// bulk-copy kernel (q4k_stream.cu) instead of this one (default off: slower on GB300 at m = 1).
+static int env_flag(const char* name, int dflt) {
+    const char* s = getenv(name);
+    return s ? (atoi(s) != 0 ? 1 : 0) : dflt;
+}
+int next_prefetch_setting() { return env_flag("Q4K_NEXT_PREFETCH", 1); }
+int stream_setting() { return env_flag("Q4K_STREAM", 0); }
 
 int num_sms() {
     if (g_num_sms == 0) {
@@ -472,12 +437,17 @@ int idgemv_tile_rows(int k) {
 
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
-                          unsigned* zero, int n_zero) {
+                          unsigned* zero, int n_zero, const L2Prefetch* pf, int n_pf) {
     if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
     if (tc_min > 0) {
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
         if (e != cudaSuccess) return e;
         pdl = false;  // the tensor-core kernels precede this launch in the stream
+    }
+    if (stream_setting()) {
+        const cudaError_t se = launch_idgemv_stream(groups, n_groups, fused_swiglu, pdl, err_flag, stream, tc_min,
+                                                    combine, zero, n_zero, pf, n_pf);
+        if (se != cudaErrorNotSupported) return se;
     }
     GemvParams P{};
     P.n_groups = n_groups;
@@ -521,9 +491,30 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         kmax = S.k > kmax ? S.k : kmax;
         max_items += (int64_t)G.n_pairs * G.tiles;
     }
+    if (combine && P.g[0].tiles > combine->n_counters) return cudaErrorInvalidValue;
     if (max_items == 0 && !combine) return cudaSuccess;
     if (max_items == 0) max_items = 1;
     P.kmax = kmax;
+    // at most 32 pairs per group: one warp per group buckets them in registers, and the
+    // histogram tables are not needed
+    P.fast = n_groups <= kWarps ? 1 : 0;
+    for (int gi = 0; gi < n_groups; ++gi) P.fast &= P.g[gi].n_pairs <= 32 ? 1 : 0;
+    if (P.fast) ints = 0;
+    // the next launch's rows, when they are few enough to sit in L2 beside this launch's
+    if (P.fast && pf && n_pf > 0 && n_pf <= n_groups && next_prefetch_setting()) {
+        int64_t bytes = 0;
+        for (int i = 0; i < n_pf; ++i) {
+            const int64_t experts = std::min<int64_t>(P.g[i].n_pairs, groups[i].num_experts);
+            bytes += experts * pf[i].expert_bytes;
+        }
+        if (bytes <= kPfMaxBytes) {
+            for (int i = 0; i < n_pf; ++i) P.pf[i] = pf[i];
+            P.n_pf = n_pf;
+        }
+    }
+    // Without a programmatic launch the activations are complete when the kernel starts:
+    // small activation regions (<= 64 KB) are then pulled towards L1 before the prologue, so
+    // that staging finds them there. (With one, the previous kernel may still be writing them.)
     // tokens per item also bounded so the staged rows fit in ~150 KB of shared memory
     const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
     while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;

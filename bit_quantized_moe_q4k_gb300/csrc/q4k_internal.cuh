@@ -55,7 +55,8 @@ struct GemvGroup {
 // The combine fused into a down launch (group 0 = routed experts, group 1 = shared expert):
 // the last CTA to finish a row tile forms, for those rows of every token,
 //   y = h_mid + sum_s weights[t*top_k+s] * out0[t*top_k+s] + g_t * out1[t]
-// in slot order (deterministic). counters: one per row tile, zero on entry, left zero.
+// in slot order (deterministic). counters: one per row tile (n_counters words; the launch
+// fails with cudaErrorInvalidValue if its tiling needs more), zero on entry, left zero.
 struct CombineSpec {
     float* y;
     const float* h_mid;
@@ -63,6 +64,14 @@ struct CombineSpec {
     const float* shared_gate;
     int shared_mode;
     unsigned* counters;
+    int n_counters;
+};
+
+// Rows a later launch will read for the experts of group `g`'s bucket (the down slabs while
+// the gate|up launch runs): expert e's rows are [base + e*expert_bytes, + expert_bytes).
+struct L2Prefetch {
+    const uint8_t* base;
+    int64_t expert_bytes;
 };
 
 // tc_min > 0: experts with at least tc_min pairs run on the tensor-core grouped GEMM
@@ -70,11 +79,21 @@ struct CombineSpec {
 // the id-GEMV kernel. combine: fuse the combine into this (down) launch. zero / n_zero: CTA 0
 // zeroes these words before anything else (the gate|up launch prepares the counters the
 // following down launch uses).
+// pf / n_pf: rows the next launch reads for this launch's experts (group i's bucket selects
+// the experts of pf[i]); a small batch (<= 32 pairs per group) starts them into L2.
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr,
-                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0);
-// rows per id-GEMV work item for a given k (the combine counters need ceil(n / rows) words)
+                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0,
+                          const L2Prefetch* pf = nullptr, int n_pf = 0);
+// rows per id-GEMV work item for a given k (bucketed kernel)
 int idgemv_tile_rows(int k);
+// The bulk-copy id-GEMV for small batches (q4k_stream.cu): cudaErrorNotSupported, before
+// launching anything, when a group holds more than 32 pairs or its rows do not fit.
+cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
+                                 cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
+                                 int n_zero, const L2Prefetch* pf, int n_pf);
+constexpr int64_t kPfMaxBytes = 40ll << 20;  // next-launch rows started into L2 at most
+int next_prefetch_setting();
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
                       int* err_flag, cudaStream_t stream);
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);

@@ -21,6 +21,14 @@ from helpers import dev, err_flag, host, oracle_slab, rows_close
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(params=["bulk_copy", "bucketed"])
+def kernel_path(request, monkeypatch):
+    """Small batches run on the bulk-copy kernel by default; Q4K_STREAM=0 sends them to the
+    bucketed kernel, so both are compared with the oracle."""
+    monkeypatch.setenv("Q4K_STREAM", "1" if request.param == "bulk_copy" else "0")
+    return request.param
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -92,8 +100,11 @@ def _run_gemv(w, E, a, outer, inner, ids, m, T, n, k, flag=None):
 @pytest.mark.parametrize("E,n,k,m,T", [(4, 64, 256, 3, 2),      # the pages' tiny case shape
                                        (8, 68, 768, 5, 3),      # ragged rows, 3 blocks per row
                                        (6, 100, 1280, 7, 2),    # 4 row tiles, ragged
-                                       (3, 32, 2048, 9, 3)])    # buckets of 9 pairs -> 3 chunks
-def test_id_gemv_matches_oracle(mode, E, n, k, m, T):
+                                       (3, 32, 2048, 9, 3),     # buckets of 9 pairs -> 3 chunks
+                                       (2, 24, 4096, 2, 2),     # 64 threads per row: cross-warp sums
+                                       (1, 40, 7168, 2, 1),     # 112 of 128 threads per row, ragged tile
+                                       (2, 20, 10240, 1, 2)])   # two 64-weight groups per thread
+def test_id_gemv_matches_oracle(mode, E, n, k, m, T, kernel_path):
     w, ids, a, outer, inner = _gemv_case(100 + n, E, n, k, m, T, mode)
     ref, _ = oracle.moe_id_gemv(w, E, a, outer, inner, ids, m, T, n, k)
     got = _run_gemv(w, E, a, outer, inner, ids, m, T, n, k)
@@ -101,7 +112,7 @@ def test_id_gemv_matches_oracle(mode, E, n, k, m, T):
 
 
 @pytest.mark.parametrize("mode", ["gate_up", "down"])
-def test_pages_tiny_case(mode):
+def test_pages_tiny_case(mode, kernel_path):
     """The ferrum-kernels tiny case: its ids and input recipes, against the oracle, and
     batched == per-token calls on the GPU bit for bit."""
     with open(os.path.join(GOLDEN, "ferrum_tiny_case.json")) as f:
@@ -129,7 +140,7 @@ def test_pages_tiny_case(mode):
     assert np.array_equal(batched, np.concatenate(per_token))
 
 
-def test_id_gemv_weight_byte_offset_and_duplicates():
+def test_id_gemv_weight_byte_offset_and_duplicates(kernel_path):
     E, n, k, m, T = 5, 64, 512, 4, 3
     w, _, a, outer, inner = _gemv_case(7, E, n, k, m, T, "gate_up")
     ids = np.array([1, 1, 4, 0, 0, 0, 2, 1, 2, 3, 3, 3], np.int32)  # same expert twice in one token
@@ -142,7 +153,7 @@ def test_id_gemv_weight_byte_offset_and_duplicates():
     rows_close(host(out), ref, what="offset+duplicates")
 
 
-def test_id_gemv_out_of_range_ids_flag_and_zero_rows():
+def test_id_gemv_out_of_range_ids_flag_and_zero_rows(kernel_path):
     E, n, k, m, T = 4, 64, 256, 3, 2
     w, _, a, outer, inner = _gemv_case(9, E, n, k, m, T, "gate_up")
     ids = np.array([0, 9, -1, 2, 3, 1], np.int32)
@@ -154,14 +165,14 @@ def test_id_gemv_out_of_range_ids_flag_and_zero_rows():
     rows_close(got, ref, what="invalid ids")
 
 
-def test_id_gemv_empty_batch():
+def test_id_gemv_empty_batch(kernel_path):
     w, ids, a, outer, inner = _gemv_case(10, 4, 64, 256, 1, 2, "gate_up")
     out = torch.full((2, 64), 7.0, device="cuda")
     q4k.q4k_moe_id_gemv(dev(w), 0, 4, dev(a), outer, inner, dev(ids), 0, 2, 64, 256, out)
     assert np.all(host(out) == 7.0)
 
 
-def test_id_gemv_skewed_bucket_many_chunks():
+def test_id_gemv_skewed_bucket_many_chunks(kernel_path):
     """One expert takes every pair (a Zipf head): 20 pairs -> 5 chunks over the same tiles."""
     E, n, k, m, T = 16, 96, 1024, 20, 1
     w, _, a, outer, inner = _gemv_case(11, E, n, k, m, T, "gate_up")
@@ -182,7 +193,7 @@ def _ffn_case(seed, E, H, I, m, T):
 
 
 @pytest.mark.parametrize("E,H,I,m,T", [(8, 512, 256, 5, 2), (16, 1024, 768, 3, 4), (4, 256, 512, 9, 2)])
-def test_expert_ffn_matches_oracle(E, H, I, m, T):
+def test_expert_ffn_matches_oracle(E, H, I, m, T, kernel_path):
     wg, wu, wd, ids, x = _ffn_case(40 + E, E, H, I, m, T)
     ref, _ = oracle.expert_ffn(wg, wu, wd, E, x, ids, m, T, H, I)
     ws_bytes = q4k.q4k_moe_workspace_size(m, T, E, max(H, I), max(H, I))
@@ -193,7 +204,7 @@ def test_expert_ffn_matches_oracle(E, H, I, m, T):
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
-def test_combine_matches_oracle(mode):
+def test_combine_matches_oracle(mode, kernel_path):
     m, T, H = 5, 3, 520
     rng = np.random.default_rng(mode)
     eo = rng.standard_normal((m * T, H)).astype(np.float32)
@@ -241,7 +252,7 @@ def _run_layer_device(W, wg, wu, wd, shared, ids, x, hm, rw, gl):
 
 
 @pytest.mark.parametrize("name", ["qwen3moe_h2048_i768_e128_t8_m1", "qwen3moe_h2048_i768_e128_t8_m16_zipf"])
-def test_layer_full_size_qwen3_like(name):
+def test_layer_full_size_qwen3_like(name, kernel_path):
     """The Qwen3-MoE-like layer at its full size (m=1 and m=16 Zipf), in the launch
     configuration the benchmark times, against the oracle's whole layer."""
     from bit_quantized_moe_q4k_gb300.workloads import WORKLOADS
@@ -254,7 +265,7 @@ def test_layer_full_size_qwen3_like(name):
     rows_close(got, ref, what=name)
 
 
-def test_layer_small_all_shared_modes_and_host_variant():
+def test_layer_small_all_shared_modes_and_host_variant(kernel_path):
     from bit_quantized_moe_q4k_gb300.workloads import Workload
     for mode in (0, 1, 2):
         W = Workload("small", 512, 256, 12, 3, 6, "uniform", 0 if mode == 0 else 512, mode, 900 + mode)
