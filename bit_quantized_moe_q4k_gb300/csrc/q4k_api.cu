@@ -49,13 +49,13 @@ int check_gemv_shape(int num_experts, int m, int top_k, int n, int k) {
 
 // Tensor-core path policy: experts whose bucket holds at least tc_min pairs run on the
 // tcgen05 grouped GEMM (q4k_tc.cu), the others on the id-GEMV kernel. tc_min comes from the
-// environment variable Q4K_TC_MIN (default 16, 0 disables). A launch uses the path only when
+// environment variable Q4K_TC_MIN (default 4, 0 disables). A launch uses the path only when
 // some bucket can reach tc_min (n_pairs >= tc_min and n_pairs / num_experts >= tc_min / 4)
 // and the caller's workspace holds the activation images.
 int tc_min_setting() {
     static int v = [] {
         const char* s = getenv("Q4K_TC_MIN");
-        return s ? atoi(s) : 16;
+        return s ? atoi(s) : 4;
     }();
     return v;
 }

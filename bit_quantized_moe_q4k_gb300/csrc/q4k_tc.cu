@@ -10,7 +10,8 @@
 //   sum_k w_k x_k = d * sum_j sc_j sum_{k in j} q_k x_k  -  dmin * sum_j m_j sum_{k in j} x_k.
 // A holds the integers sc_j * q_k (<= 945, exact in fp16). x is split into two fp16 parts,
 // x = hi + lo with hi = fp16(x), lo = fp16(x - hi), and both are multiplied by the same A
-// (two MMAs per k step into one accumulator), so the main product carries x to ~2^-22
+// (the 32 tokens' hi rows and their lo rows side by side in one N = 64 operand, so one MMA
+// per k step forms both; the epilogue adds the two halves), so the product carries x to ~2^-22
 // instead of fp16's 2^-11 (which alone put FFN outputs at the edge of the 1e-3 acceptance).
 // A second, 16-deep MMA per block computes sum_j m_j * sx_j
 // with sx_j = sum_{k in j} x_k split into two fp16 halves (hi + lo), i.e. to ~2^-22. The
@@ -18,12 +19,14 @@
 // two partial accumulators from tensor memory (double-buffered, so the next block's MMAs
 // run meanwhile).
 //
-// Roles (6 warps): warps 0-3 dequantize (thread = weight row = TMEM lane) and run the
-// epilogue; warp 4 issues the bulk copies (raw Q4_K rows of the tile, and the prepared B
-// image of the block); warp 5 owns tensor memory and issues the MMAs. Raw rows -> registers
-// -> A: dequantization writes each row's 256 weights as 128 fp16-pair columns with
-// tcgen05.st (the A operand never touches shared memory). Pipelines of depth 2 on mbarriers;
-// every wait is bounded and an abort flag lets all roles leave together.
+// Roles (10 warps): warps 0-7 dequantize and run the epilogue, two warps per TMEM lane
+// quarter (thread = weight row = TMEM lane): warp w < 4 takes the 64-weight groups 0-1 of
+// the block and tokens 0-15 of the epilogue, warp w + 4 groups 2-3 and tokens 16-31; warp 8
+// issues the bulk copies (raw Q4_K rows of the tile, and the prepared B image of the
+// block); warp 9 owns tensor memory and issues the MMAs. Raw rows -> registers -> A:
+// dequantization writes each row's 256 weights as 128 fp16-pair columns with tcgen05.st
+// (the A operand never touches shared memory). Pipelines on mbarriers; every wait is
+// bounded and an abort flag lets all roles leave together.
 //
 // The B image of a (chunk, block) is built once by tc_prep_kernel in the workspace: the 32
 // tokens' x in fp16, in the k order of the A columns, already laid out as the 128-byte
@@ -38,20 +41,25 @@
 namespace q4k {
 using namespace sm100;
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
+constexpr int kTcWorkers = 256;               // dequant + epilogue threads (warps 0-7)
+constexpr int kTcCopyWarp = 8, kTcMmaWarp = 9;
 constexpr int kTcRows = 128;                  // M (TMEM lanes)
 constexpr int kTcTok = 32;                    // N (tokens per chunk)
-constexpr int kImgB = 4 * kTcTok * 128;       // 4 panels of [32 tokens x 128 B] (x rounded to fp16)
-constexpr int kImgLo = kImgB;                 // offset of the residual panels (x - fp16(x), in fp16)
-constexpr int kImgB2 = kTcTok * 128;          // min-term operand [32 tokens x 128 B]
-constexpr int kImgMin = 2 * kImgB;            // offset of the min-term operand
-constexpr int kImgBlock = 2 * kImgB + kImgB2; // bytes of one block's B image
+// One block's B image: 4 K-panels of 64 rows x 128 B, rows 0-31 the 32 tokens' x rounded to
+// fp16 and rows 32-63 their residuals x - fp16(x); then the min-term operand.
+constexpr int kPanel = 2 * kTcTok * 128;       // one K-panel: 64 rows x 128 B
+constexpr int kImgLoRow = kTcTok;              // first residual row of a panel
+constexpr int kImgB2 = kTcTok * 128;           // min-term operand [32 tokens x 128 B]
+constexpr int kImgMin = 4 * kPanel;            // offset of the min-term operand
+constexpr int kImgBlock = 4 * kPanel + kImgB2; // bytes of one block's B image
 constexpr int kRawStage = kTcRows * kBlockBytes;
 constexpr int kNRaw = 4;   // raw Q4_K row stages in shared memory (copies run this far ahead)
 constexpr int kNImg = 3;   // activation image stages in shared memory
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: A stages (128 each), min-term A stages (16 each), D1 and D2 (32 each)
-constexpr uint32_t kColA = 0, kColA2 = 256, kColD1 = 288, kColD2 = 352;
+// tensor-memory columns: A stages (128 each), min-term A stages (16 each), D1 stages (64
+// each: 32 tokens' fp16 part, then their residual part), D2 stages (32 each: min term)
+constexpr uint32_t kColA = 0, kColA2 = 256, kColD1 = 288, kColD2 = 416;
 
 struct TcGroup {
     const uint8_t* w;    // slab [E][n][k/256] blocks
@@ -165,9 +173,11 @@ tc_prep_kernel(const __grid_constant__ TcParams P) {
                 hw8[i] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
                 lw8[i] = (uint32_t)__half_as_ushort(ra) | ((uint32_t)__half_as_ushort(rb) << 16);
             }
-            const int off = c4 * (kTcTok * 128) + t * 128 + ((ip ^ (t & 7)) << 4);
+            // 128-byte swizzle: 16-byte chunk ip of row rr sits at chunk ip ^ (rr & 7); rows t and
+            // 32 + t share the pattern
+            const int off = c4 * kPanel + t * 128 + ((ip ^ (t & 7)) << 4);
             *reinterpret_cast<uint4*>(img + off) = make_uint4(hw8[0], hw8[1], hw8[2], hw8[3]);
-            *reinterpret_cast<uint4*>(img + kImgLo + off) = make_uint4(lw8[0], lw8[1], lw8[2], lw8[3]);
+            *reinterpret_cast<uint4*>(img + off + kImgLoRow * 128) = make_uint4(lw8[0], lw8[1], lw8[2], lw8[3]);
             // sub-block sums (fp32) of sub-blocks 2*c4 (lo) and 2*c4+1 (hi) over the 8 lanes of c4
             float sl = (lo.x + lo.y) + (lo.z + lo.w), sh = (hi.x + hi.y) + (hi.z + hi.w);
 #pragma unroll
@@ -243,7 +253,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     __shared__ uint32_t s_tmem;
     __shared__ int s_warp[33];
     __shared__ int s_bad;
-    __shared__ int s_pairs_w[4][kTcTok];  // each producer warp keeps its own copy (no cross-warp barrier)
+    __shared__ int s_pairs_w[8][kTcTok];  // each worker warp keeps its own copy (no cross-warp barrier)
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -254,24 +264,24 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     const int total_items = tc_chunks(G, P.tc_min, cnt, start, s_warp, &s_bad) * G.tiles;
     if ((int)blockIdx.x >= total_items) return;  // uniform per CTA: before any allocation
 
-    if (warp == 5) {
+    if (warp == kTcMmaWarp) {
         tmem_alloc(&s_tmem, kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
         for (int i = 0; i < kNRaw; ++i) {
             mbar_init(&bar_raw_full[i], 1);
-            mbar_init(&bar_raw_empty[i], 128);
+            mbar_init(&bar_raw_empty[i], kTcWorkers);
         }
         for (int i = 0; i < kNImg; ++i) {
             mbar_init(&bar_b_full[i], 1);
             mbar_init(&bar_b_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar_a_full[i], 128);
+            mbar_init(&bar_a_full[i], kTcWorkers);
             mbar_init(&bar_a_empty[i], 1);
             mbar_init(&bar_d_full[i], 1);
-            mbar_init(&bar_d_empty[i], 128);
+            mbar_init(&bar_d_empty[i], kTcWorkers);
         }
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
@@ -285,7 +295,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     const int nslab = FUSED ? 2 : 1;
     const int steps = nslab * nb;
 
-    if (warp == 4) {
+    if (warp == kTcCopyWarp) {
         // ---------------- copy producer: raw rows of the tile and the block's B image
         int gs = 0;  // global step
         int raw_issued = 0, b_issued = 0;
@@ -332,10 +342,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             for (int g = max(0, b_issued - kNImg); g < b_issued; ++g)
                 mbar_wait(&bar_b_full[g % kNImg], (g / kNImg) & 1, &never);
         }
-    } else if (warp == 5) {
+    } else if (warp == kTcMmaWarp) {
         // ---------------- MMA issuer (one thread)
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kTcRows, kTcTok);
+            const uint32_t idesc = idesc_f16_f32(kTcRows, 2 * kTcTok);   // fp16 part | residual
+            const uint32_t idesc_min = idesc_f16_f32(kTcRows, kTcTok);
             const uint32_t bimg_addr = smem_u32(bimg);
             int gs = 0, issued = 0;
             bool ok = true;
@@ -354,13 +365,12 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     const uint32_t b_addr = bimg_addr + bst * kImgBlock;
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * (kTcTok * 128) + (kk & 3) * 32;
+                        const uint32_t koff = (kk >> 2) * kPanel + (kk & 3) * 32;
                         const uint32_t a_col = tmem + kColA + st * 128 + 8 * kk;
-                        mma_f16_ts(tmem + kColD1 + st * 32, a_col, desc_sw128_kmajor(b_addr + koff), idesc, kk > 0);
-                        mma_f16_ts(tmem + kColD1 + st * 32, a_col, desc_sw128_kmajor(b_addr + kImgLo + koff), idesc, 1);
+                        mma_f16_ts(tmem + kColD1 + st * 64, a_col, desc_sw128_kmajor(b_addr + koff), idesc, kk > 0);
                     }
                     mma_f16_ts(tmem + kColD2 + st * 32, tmem + kColA2 + st * 16, desc_sw128_kmajor(b_addr + kImgMin),
-                               idesc, 0);
+                               idesc_min, 0);
                     mma_commit(&bar_a_empty[st]);
                     mma_commit(&bar_b_empty[bst]);
                     mma_commit(&bar_d_full[st]);
@@ -380,8 +390,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         __syncwarp();
     } else {
         // ---------------- dequantize (thread = row = TMEM lane) and epilogue
-        const int r = tid;  // 0..127
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const int quarter = warp & 3, half = warp >> 2;
+        const int r = 32 * quarter + lane;  // 0..127
+        const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+        constexpr int kHalfTok = kTcTok / 2;
         int gs = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
@@ -392,9 +404,9 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             __syncwarp();  // this warp's previous outputs are written
             tc_gather(G, it.e, it.chunk, it.nt, s_pairs);
             __syncwarp();
-            float acc[kTcTok], accg[kTcTok];
+            float acc[kHalfTok], accg[kHalfTok];
 #pragma unroll
-            for (int t = 0; t < kTcTok; ++t) { acc[t] = 0.f; accg[t] = 0.f; }
+            for (int t = 0; t < kHalfTok; ++t) { acc[t] = 0.f; accg[t] = 0.f; }
             float d_prev = 0.f, dmin_prev = 0.f;
             for (int s = 0; s <= steps; ++s) {
                 const int g_cur = gs + s;
@@ -405,12 +417,13 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     const int rst = g_cur % kNRaw;
                     const uint32_t rph = (g_cur / kNRaw) & 1;
                     if (!mbar_wait(&bar_raw_full[rst], rph, &s_abort)) { ok = false; break; }
+                    // this half's code bytes: 64-weight groups 2*half, 2*half + 1 (bytes 64*half ..)
                     const uint4* rp = reinterpret_cast<const uint4*>(raw + rst * kRawStage + r * kBlockBytes);
-                    uint4 hq[9];
+                    const uint4 h = rp[0];
+                    uint4 hq[4];
 #pragma unroll
-                    for (int i = 0; i < 9; ++i) hq[i] = rp[i];
+                    for (int i = 0; i < 4; ++i) hq[i] = rp[1 + 4 * half + i];
                     mbar_arrive(&bar_raw_empty[rst]);
-                    const uint4 h = hq[0];
                     d_cur = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFFu)));
                     dmin_cur = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
                     int sc[8], mn[8];
@@ -428,17 +441,20 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     // A columns: code word i -> columns 4i..4i+3 = low nibbles of bytes (0,2), (1,3),
                     // high nibbles of bytes (0,2), (1,3), each the exact fp16 pair sc_j * q
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {  // 32 columns = 8 code words = 64-weight group g
-                        const __half2 klo = __half2half2(__int2half_rn(sc[2 * g]));
-                        const __half2 clo = __half2half2(__int2half_rn(-1024 * sc[2 * g]));
-                        const __half2 khi = __half2half2(__float2half_rn((float)sc[2 * g + 1] * 0.0625f));
-                        const __half2 chi = __half2half2(__int2half_rn(-64 * sc[2 * g + 1]));
+                    for (int gl = 0; gl < 2; ++gl) {  // 32 columns = 8 code words = 64-weight group g
+                        const int g = 2 * half + gl;
+                        // sub-blocks 2g (low nibbles) and 2g + 1 (high nibbles)
+                        const int sca = half ? sc[4 + 2 * gl] : sc[2 * gl];
+                        const int scb = half ? sc[5 + 2 * gl] : sc[1 + 2 * gl];
+                        const __half2 klo = __half2half2(__int2half_rn(sca));
+                        const __half2 clo = __half2half2(__int2half_rn(-1024 * sca));
+                        const __half2 khi = __half2half2(__float2half_rn((float)scb * 0.0625f));
+                        const __half2 chi = __half2half2(__int2half_rn(-64 * scb));
                         uint32_t col[32];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const int wi = 8 * g + i;
-                            const uint4 qv = hq[1 + (wi >> 2)];
-                            const uint32_t wq = (wi & 3) == 0 ? qv.x : (wi & 3) == 1 ? qv.y : (wi & 3) == 2 ? qv.z : qv.w;
+                            const uint4 qv = hq[2 * gl + (i >> 2)];
+                            const uint32_t wq = (i & 3) == 0 ? qv.x : (i & 3) == 1 ? qv.y : (i & 3) == 2 ? qv.z : qv.w;
                             const uint32_t w8 = wq >> 8;
                             col[4 * i + 0] = h2_bits(hfma2_bits((wq & 0x000F000Fu) | 0x64006400u, klo, clo));
                             col[4 * i + 1] = h2_bits(hfma2_bits((w8 & 0x000F000Fu) | 0x64006400u, klo, clo));
@@ -447,36 +463,40 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                         }
                         tmem_st32(tmem + lane_base + kColA + st * 128 + 32 * g, col);
                     }
-                    uint32_t a2[8];
+                    if (half == 0) {
+                        uint32_t a2[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const __half2 mm = __halves2half2(__int2half_rn(mn[2 * i]), __int2half_rn(mn[2 * i + 1]));
-                        a2[i] = a2[i + 4] = h2_bits(mm);
+                        for (int i = 0; i < 4; ++i) {
+                            const __half2 mm = __halves2half2(__int2half_rn(mn[2 * i]), __int2half_rn(mn[2 * i + 1]));
+                            a2[i] = a2[i + 4] = h2_bits(mm);
+                        }
+                        tmem_st8(tmem + lane_base + kColA2 + st * 16, a2);
                     }
-                    tmem_st8(tmem + lane_base + kColA2 + st * 16, a2);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(&bar_a_full[st]);
                 }
                 if (s >= 1) {
-                    // epilogue of step s-1: acc += d * D1 - dmin * D2
+                    // epilogue of step s-1 for this half's tokens: acc += d * (D1 hi + D1 lo) - dmin * D2
                     const int pg = g_cur - 1;
                     const int ps = pg & 1;
                     const uint32_t pph = (pg >> 1) & 1;
                     if (!mbar_wait(&bar_d_full[ps], pph, &s_abort)) { ok = false; break; }
                     tc_fence_after();
-                    uint32_t d1[32], d2[32];
-                    tmem_ld32(tmem + lane_base + kColD1 + ps * 32, d1);
-                    tmem_ld32(tmem + lane_base + kColD2 + ps * 32, d2);
+                    uint32_t d1[kHalfTok], d2[kHalfTok], d3[kHalfTok];
+                    tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kHalfTok * half, d1);
+                    tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kTcTok + kHalfTok * half, d3);
+                    tmem_ld16(tmem + lane_base + kColD2 + ps * 32 + kHalfTok * half, d2);
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(&bar_d_empty[ps]);
 #pragma unroll
-                    for (int t = 0; t < kTcTok; ++t)
-                        acc[t] = fmaf(d_prev, __uint_as_float(d1[t]), fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[t]));
+                    for (int t = 0; t < kHalfTok; ++t)
+                        acc[t] = fmaf(d_prev, __uint_as_float(d1[t]) + __uint_as_float(d3[t]),
+                                      fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[t]));
                     if (FUSED && s - 1 == nb - 1) {  // the gate slab is complete
 #pragma unroll
-                        for (int t = 0; t < kTcTok; ++t) { accg[t] = acc[t]; acc[t] = 0.f; }
+                        for (int t = 0; t < kHalfTok; ++t) { accg[t] = acc[t]; acc[t] = 0.f; }
                     }
                 }
                 d_prev = d_cur;
@@ -486,10 +506,11 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             gs += steps;
             if (r < rows_valid) {
 #pragma unroll
-                for (int t = 0; t < kTcTok; ++t) {
+                for (int j = 0; j < kHalfTok; ++j) {
+                    const int t = kHalfTok * half + j;
                     if (t < it.nt) {
-                        float v = acc[t];
-                        if (FUSED) v = (accg[t] / (1.0f + __expf(-accg[t]))) * acc[t];
+                        float v = acc[j];
+                        if (FUSED) v = (accg[j] / (1.0f + __expf(-accg[j]))) * acc[j];
                         G.out[(int64_t)s_pairs[t] * G.n + row0 + r] = v;
                     }
                 }
@@ -503,7 +524,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kTcMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------------------------------

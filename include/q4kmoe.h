@@ -113,7 +113,7 @@ int q4k_moe_bucket(const int32_t* d_ids, int n_pairs, int num_experts, int32_t* 
  *   d_out: [m*top_k, n] fp32
  * d_workspace is optional here: when it holds at least q4k_moe_workspace_size(m, top_k,
  * num_experts, n, k) bytes (256-byte aligned), experts whose bucket holds at least
- * Q4K_TC_MIN pairs (environment variable, default 16, 0 disables) run on the tcgen05
+ * Q4K_TC_MIN pairs (environment variable, default 4, 0 disables) run on the tcgen05
  * tensor-core grouped GEMM; all others on the id-GEMV kernel.
  * Limits: num_experts <= 4096, k <= 65536.
  */

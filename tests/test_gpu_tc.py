@@ -1,6 +1,6 @@
 """GPU parity of the tensor-core grouped GEMM (tcgen05) path against the CPU oracle.
 
-Buckets of at least 16 pairs (the default Q4K_TC_MIN) run on the tensor-core path when the
+Buckets of at least 4 pairs (the default Q4K_TC_MIN) run on the tensor-core path when the
 caller provides the workspace; without it the same calls run on the id-GEMV kernel. Both
 must meet the per-row acceptance; their results differ in rounding (fp16 activations in the
 tensor-core products vs 16-bit fixed point), which shows the tensor-core path did run.
@@ -37,7 +37,8 @@ def _gemv(w, E, a, outer, inner, ids, m, T, n, k, workspace):
 
 @pytest.mark.parametrize("mode", ["gate_up", "down"])
 # sizes give the path enough work (>= 64 items of 128 rows x 32 tokens) to be chosen
-@pytest.mark.parametrize("E,n,k,m,T", [(4, 2148, 512, 64, 2),    # ~32 pairs per expert, ragged last row tile
+@pytest.mark.parametrize("E,n,k,m,T", [(32, 2048, 512, 48, 4),   # ~6 pairs per expert: small buckets
+                                       (4, 2148, 512, 64, 2),    # ~32 pairs per expert, ragged last row tile
                                        (2, 4096, 1024, 40, 2),   # 40 pairs per expert: 2 chunks
                                        (3, 3072, 256, 70, 1)])   # one block per row
 def test_tc_id_gemv_matches_oracle(mode, E, n, k, m, T):
