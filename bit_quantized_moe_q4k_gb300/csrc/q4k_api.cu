@@ -1,5 +1,6 @@
 // q4k_api.cu -- the C ABI of libq4kmoe (declared in include/q4kmoe.h): host-side
 // validation, workspace layout and kernel sequencing. No compute happens here.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -61,11 +62,14 @@ int tc_min_setting() {
 }
 
 // Worth it only with enough work to spread over the SMs: at least ~64 items of 128 weight
-// rows x 32 tokens (a single shared expert with a few row tiles stays on the id-GEMV kernel).
+// rows x a chunk of <= 32 tokens (a single shared expert with a few row tiles stays on the
+// id-GEMV kernel). Chunks: at least ceil(pairs / 32), and up to one per expert that can
+// reach t pairs when the buckets are spread (min(experts, pairs / t)).
 bool tc_wanted(int n_pairs, int num_experts, int n_rows) {
     const int t = tc_min_setting();
     if (t <= 0 || n_pairs < t || (int64_t)n_pairs * 4 < (int64_t)t * num_experts) return false;
-    const int64_t items = (int64_t)((n_pairs + 31) / 32) * ((n_rows + 127) / 128);
+    const int64_t chunks = std::max<int64_t>((n_pairs + 31) / 32, std::min<int64_t>(num_experts, n_pairs / t));
+    const int64_t items = chunks * ((n_rows + 127) / 128);
     return items >= 64;
 }
 
