@@ -120,7 +120,8 @@ __device__ __forceinline__ void tc_gather(const TcGroup& G, int e, int chunk, in
 }
 
 // ------------------------------------------------------------------------------------------
-// B images: grid (max chunks, groups), 128 threads. Warp w builds tokens t = w, w+4, ...
+// B images: grid (max chunks, groups, block slices), 128 threads. CTA z builds the blocks
+// b = z, z + gridDim.z, ... of its chunk; warp w builds tokens t = w, w+4, ...
 __global__ void __launch_bounds__(128)
 tc_prep_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -151,7 +152,7 @@ tc_prep_kernel(const __grid_constant__ TcParams P) {
     const int c4 = lane >> 3, ip = lane & 7;
     const int nb = G.k / kQK;
     uint8_t* img0 = G.img + (int64_t)q * nb * kImgBlock;
-    for (int b = 0; b < nb; ++b) {
+    for (int b = blockIdx.z; b < nb; b += gridDim.z) {
         uint8_t* img = img0 + (int64_t)b * kImgBlock;
         for (int t = warp; t < kTcTok; t += 4) {
             float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
@@ -611,7 +612,10 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
     {
         const size_t smem = (size_t)ints * 4;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)max_chunks, n_groups);
+        int kmax = 0;
+        for (int gi = 0; gi < n_groups; ++gi) kmax = groups[gi].k > kmax ? groups[gi].k : kmax;
+        const int slices = kmax / kQK < 16 ? kmax / kQK : 16;
+        cfg.gridDim = dim3((unsigned)max_chunks, n_groups, (unsigned)slices);
         cfg.blockDim = dim3(128);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
