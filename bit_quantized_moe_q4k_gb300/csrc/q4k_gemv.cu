@@ -9,8 +9,10 @@
 // How (GB300 design):
 //  * Pairs are bucketed by expert inside every CTA (histogram + scan of the ids in shared
 //    memory), so each touched slab row tile is streamed from HBM once per launch no matter
-//    how many pairs of the batch picked that expert. Work item = (group, expert, 32-row
-//    tile, chunk of <= kTB tokens of that expert's bucket); CTAs walk items grid-stride.
+//    how many pairs of the batch picked that expert. Work item = (group, expert, row tile,
+//    chunk of <= kTB tokens of that expert's bucket), row tiles of one chunk consecutive;
+//    each CTA takes a contiguous range of items, so its staged rows carry over, and CTAs on
+//    other chunks of the same expert read the same tiles at about the same time (L2 hits).
 //  * The item's activation rows are staged in shared memory as 16-bit fixed point per
 //    32-element sub-block: X = rint(x / delta), delta = max|x| / 32767, split into a low
 //    byte plane (unsigned) and a high byte plane (signed), with sum(X) per sub-block.
@@ -192,9 +194,9 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
                 const int r = __ffs(hit) - 1;
                 const unsigned mask = F.mask[r];
                 const int cnt = __popc(mask);
-                const int chunks = (cnt + TB - 1) / TB;
                 const int in_e = local - F.start[r];
-                const int chunk = in_e % chunks;
+                const int tiles = P.g[gi].tiles;
+                const int chunk = in_e / tiles;  // tiles of one chunk run together (no restaging)
                 const int nt = min(TB, cnt - chunk * TB);
                 // pair `lane` is a member: its place in the bucket is the members below it
                 const int q = __popc(mask & ((1u << lane) - 1u)) - chunk * TB;
@@ -202,7 +204,7 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
                 if (lane == 0) {
                     s_item_info[0] = gi;
                     s_item_info[1] = F.e[r];
-                    s_item_info[2] = in_e / chunks;
+                    s_item_info[2] = in_e % tiles;
                     s_item_info[3] = nt;
                     s_item_info[4] = chunk;
                     s_pairs_key[0] = gi; s_pairs_key[1] = F.e[r]; s_pairs_key[2] = chunk;
@@ -232,11 +234,10 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
                 if (start[mid] <= local) lo = mid; else hi = mid - 1;
             }
             const int in_e = local - start[lo];
-            const int chunks = (cnt[lo] + TB - 1) / TB;
-            const int chunk = in_e % chunks;
+            const int chunk = in_e / G.tiles;  // tiles of one chunk run together (no restaging)
             s_item_info[0] = gi;
             s_item_info[1] = lo;
-            s_item_info[2] = in_e / chunks;
+            s_item_info[2] = in_e % G.tiles;
             s_item_info[3] = min(TB, cnt[lo] - chunk * TB);
             s_item_info[4] = chunk;
         }
