@@ -118,8 +118,7 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
 int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const float* h_post, const int32_t* ids,
                 int m, int top_k, int hidden, int inter, float* act, const void* ws_gate, const void* ws_up,
                 int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr,
-                unsigned* zero = nullptr, int n_zero = 0, const void* w_down_next = nullptr,
-                const void* ws_down_next = nullptr) {
+                unsigned* zero = nullptr, int n_zero = 0) {
     GemvGroup g[2] = {};
     int ng = 1;
     g[0] = GemvGroup{static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), ids, h_post,
@@ -136,16 +135,7 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, hidden);
     }
-    // the down launch that follows reads, for the same experts, hidden rows of inter/256 blocks
-    L2Prefetch pf[2] = {};
-    int npf = 0;
-    if (w_down_next) {
-        pf[npf++] = L2Prefetch{static_cast<const uint8_t*>(w_down_next), (int64_t)hidden * (inter / kQK) * kBlockBytes};
-        if (shared_inter > 0 && ws_down_next)
-            pf[npf++] = L2Prefetch{static_cast<const uint8_t*>(ws_down_next),
-                                   (int64_t)hidden * (shared_inter / kQK) * kBlockBytes};
-    }
-    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream, tc, img, nullptr, zero, n_zero, pf, npf),
+    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream, tc, img, nullptr, zero, n_zero),
                        "gate|up launch");
 }
 
@@ -178,7 +168,7 @@ int run_ffn(const void* w_gate, const void* w_up, const void* w_down, int num_ex
             float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_gu = nullptr,
             uint8_t* tc_dn = nullptr) {
     int st = run_gate_up(w_gate, w_up, num_experts, h_post, ids, m, top_k, hidden, inter, act, ws_gate, ws_up,
-                         shared_inter, act_shared, err_flag, stream, tc_gu, nullptr, 0, w_down, ws_down);
+                         shared_inter, act_shared, err_flag, stream, tc_gu);
     if (st) return st;
     return run_down(w_down, num_experts, act, ids, m, top_k, hidden, inter, expert_out, ws_down, shared_inter,
                     act_shared, shared_out, err_flag, stream, tc_dn);
@@ -362,8 +352,7 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
     // then down (routed and shared) with the combine fused into its last CTA per row tile
     unsigned* counters = reinterpret_cast<unsigned*>(ws + ls.counters);
     st = run_gate_up(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act, d_ws_gate, d_ws_up,
-                     shared_inter, act_shared, d_err_flag, stream, ws + ls.tc_gu, counters, ls.n_counters, d_w_down,
-                     d_ws_down);
+                     shared_inter, act_shared, d_err_flag, stream, ws + ls.tc_gu, counters, ls.n_counters);
     if (st) return st;
     CombineSpec cb{d_y, d_h_mid, d_weights, d_shared_gate, shared_mode, counters, ls.n_counters};
     return run_down(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,

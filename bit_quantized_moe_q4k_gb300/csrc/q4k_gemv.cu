@@ -59,8 +59,6 @@ struct GemvParams {
     unsigned* zero;         // CTA 0 zeroes zero[0..n_zero) first
     int n_zero;
     int fast;               // every group has at most 32 pairs: bucket with one warp per group
-    L2Prefetch pf[kMaxGroups];  // rows of the next launch to start into L2 (fast mode), by group bucket
-    int n_pf;
 };
 
 // Stage the activation rows of the item's pairs (token t at xs + t*tok_bytes, meta + t*(k/32)).
@@ -137,19 +135,6 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         __syncthreads();
         if (threadIdx.x == 0)
             for (int gi = 0; gi < P.n_groups; ++gi) s_items[gi + 1] = s_items[gi] + s_fast[gi].start[s_fast[gi].U];
-        // The following launch's rows for the experts of this batch (known now) go to L2 while
-        // this launch streams its own: pieces of kPfPiece bytes spread over the CTAs.
-        const int64_t pc0 = P.n_pf > 0 ? (P.pf[0].expert_bytes + kPfPiece - 1) / kPfPiece : 0;
-        const int64_t pc1 = P.n_pf > 1 ? (P.pf[1].expert_bytes + kPfPiece - 1) / kPfPiece : 0;
-        const int64_t n0 = pc0 * s_fast[0].U, n_all = n0 + (P.n_pf > 1 ? pc1 * s_fast[1].U : 0);
-        for (int64_t q = blockIdx.x + (int64_t)gridDim.x * threadIdx.x; q < n_all; q += (int64_t)gridDim.x * kThreads) {
-            const int i = q < n0 ? 0 : 1;
-            const int64_t qq = i == 0 ? q : q - n0, pc = i == 0 ? pc0 : pc1;
-            const int e = s_fast[i].e[qq / pc];
-            const int64_t off = (qq % pc) * kPfPiece;
-            const int64_t bytes = min((int64_t)kPfPiece, P.pf[i].expert_bytes - off);
-            bulk_prefetch_l2(P.pf[i].base + (int64_t)e * P.pf[i].expert_bytes + off, (uint32_t)bytes);
-        }
         __syncthreads();
     }
     for (int gi = 0; gi < P.n_groups && !P.fast; ++gi) {
@@ -410,14 +395,12 @@ static int g_num_sms = 0;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 200 * 1024;
 static bool g_smem_attr_set[4][kMaxDevices] = {};
-// Switches (environment, read at every launch): Q4K_NEXT_PREFETCH=0 turns off the L2
-// prefetch of the next launch's rows (default on); Q4K_STREAM=1 sends small batches to the
+// Switch (environment, read at every launch): Q4K_STREAM=1 sends small batches to the
 // bulk-copy kernel (q4k_stream.cu) instead of this one (default off: slower on GB300 at m = 1).
 static int env_flag(const char* name, int dflt) {
     const char* s = getenv(name);
     return s ? (atoi(s) != 0 ? 1 : 0) : dflt;
 }
-int next_prefetch_setting() { return env_flag("Q4K_NEXT_PREFETCH", 1); }
 int stream_setting() { return env_flag("Q4K_STREAM", 0); }
 
 int num_sms() {
@@ -438,7 +421,7 @@ int idgemv_tile_rows(int k) {
 
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
-                          unsigned* zero, int n_zero, const L2Prefetch* pf, int n_pf) {
+                          unsigned* zero, int n_zero) {
     if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
     if (tc_min > 0) {
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
@@ -447,7 +430,7 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     }
     if (stream_setting()) {
         const cudaError_t se = launch_idgemv_stream(groups, n_groups, fused_swiglu, pdl, err_flag, stream, tc_min,
-                                                    combine, zero, n_zero, pf, n_pf);
+                                                    combine, zero, n_zero);
         if (se != cudaErrorNotSupported) return se;
     }
     GemvParams P{};
@@ -501,21 +484,6 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     P.fast = n_groups <= kWarps ? 1 : 0;
     for (int gi = 0; gi < n_groups; ++gi) P.fast &= P.g[gi].n_pairs <= 32 ? 1 : 0;
     if (P.fast) ints = 0;
-    // the next launch's rows, when they are few enough to sit in L2 beside this launch's
-    if (P.fast && pf && n_pf > 0 && n_pf <= n_groups && next_prefetch_setting()) {
-        int64_t bytes = 0;
-        for (int i = 0; i < n_pf; ++i) {
-            const int64_t experts = std::min<int64_t>(P.g[i].n_pairs, groups[i].num_experts);
-            bytes += experts * pf[i].expert_bytes;
-        }
-        if (bytes <= kPfMaxBytes) {
-            for (int i = 0; i < n_pf; ++i) P.pf[i] = pf[i];
-            P.n_pf = n_pf;
-        }
-    }
-    // Without a programmatic launch the activations are complete when the kernel starts:
-    // small activation regions (<= 64 KB) are then pulled towards L1 before the prologue, so
-    // that staging finds them there. (With one, the previous kernel may still be writing them.)
     // tokens per item also bounded so the staged rows fit in ~150 KB of shared memory
     const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
     while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;

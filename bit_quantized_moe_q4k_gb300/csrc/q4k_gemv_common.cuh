@@ -22,7 +22,6 @@ constexpr int kPairBytes = 144;             // staged planes of 2 sub-blocks + 1
 constexpr int kMaxGroups = 2;
 
 constexpr int kStageUnroll = 8;            // float4 loads in flight per thread while staging
-constexpr int kPfPiece = 32 * 1024;        // bytes per L2 bulk prefetch
 
 __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));

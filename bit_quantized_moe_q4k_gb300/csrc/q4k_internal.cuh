@@ -67,33 +67,21 @@ struct CombineSpec {
     int n_counters;
 };
 
-// Rows a later launch will read for the experts of group `g`'s bucket (the down slabs while
-// the gate|up launch runs): expert e's rows are [base + e*expert_bytes, + expert_bytes).
-struct L2Prefetch {
-    const uint8_t* base;
-    int64_t expert_bytes;
-};
-
 // tc_min > 0: experts with at least tc_min pairs run on the tensor-core grouped GEMM
 // (q4k_tc.cu) first, using tc_img[g] (tc_image_bytes of the group) as scratch; the rest run on
 // the id-GEMV kernel. combine: fuse the combine into this (down) launch. zero / n_zero: CTA 0
 // zeroes these words before anything else (the gate|up launch prepares the counters the
 // following down launch uses).
-// pf / n_pf: rows the next launch reads for this launch's experts (group i's bucket selects
-// the experts of pf[i]); a small batch (<= 32 pairs per group) starts them into L2.
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr,
-                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0,
-                          const L2Prefetch* pf = nullptr, int n_pf = 0);
+                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0);
 // rows per id-GEMV work item for a given k (bucketed kernel)
 int idgemv_tile_rows(int k);
 // The bulk-copy id-GEMV for small batches (q4k_stream.cu): cudaErrorNotSupported, before
 // launching anything, when a group holds more than 32 pairs or its rows do not fit.
 cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                                  cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
-                                 int n_zero, const L2Prefetch* pf, int n_pf);
-constexpr int64_t kPfMaxBytes = 40ll << 20;  // next-launch rows started into L2 at most
-int next_prefetch_setting();
+                                 int n_zero);
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
                       int* err_flag, cudaStream_t stream);
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);

@@ -64,8 +64,6 @@ struct SParams {
     CombineSpec cb;
     unsigned* zero;
     int n_zero;
-    L2Prefetch pf[kMaxGroups];
-    int n_pf;
     int stage_bytes;        // bytes per stage (both slabs)
     int xs_off, meta_off;   // staged activation planes and (delta, sumX) pairs
 };
@@ -198,21 +196,6 @@ idgemv_stream_kernel(const __grid_constant__ SParams P) {
     }
     if (warp == 0)
         for (int j = 0; j < kSStages && ib + j < ie; ++j) issue(ib + j, j);
-
-    // ---- the following launch's rows for the experts of this batch: start them into L2
-    {
-        const int64_t pc0 = P.n_pf > 0 ? (P.pf[0].expert_bytes + kPfPiece - 1) / kPfPiece : 0;
-        const int64_t pc1 = P.n_pf > 1 ? (P.pf[1].expert_bytes + kPfPiece - 1) / kPfPiece : 0;
-        const int64_t n0 = pc0 * s_fast[0].U, n_all = n0 + (P.n_pf > 1 ? pc1 * s_fast[1].U : 0);
-        for (int64_t q = blockIdx.x + (int64_t)gridDim.x * tid; q < n_all; q += (int64_t)gridDim.x * kSThreads) {
-            const int i = q < n0 ? 0 : 1;
-            const int64_t qq = i == 0 ? q : q - n0, pc = i == 0 ? pc0 : pc1;
-            const int e = s_fast[i].e[qq / pc];
-            const int64_t off = (qq % pc) * kPfPiece;
-            const int64_t bytes = min((int64_t)kPfPiece, P.pf[i].expert_bytes - off);
-            bulk_prefetch_l2(P.pf[i].base + (int64_t)e * P.pf[i].expert_bytes + off, (uint32_t)bytes);
-        }
-    }
 
     uint8_t* xs = smem + P.xs_off;
     float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
@@ -415,7 +398,7 @@ int pow2_at_least(int v) {
 
 cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                                  cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
-                                 int n_zero, const L2Prefetch* pf, int n_pf) {
+                                 int n_zero) {
     if (n_groups < 1 || n_groups > kMaxGroups) return cudaErrorNotSupported;
     SParams P{};
     P.n_groups = n_groups;
@@ -474,16 +457,6 @@ cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fus
     P.meta_off = P.xs_off + ((kmax / 64) * kPairBytes + 15) / 16 * 16;
     const size_t smem = (size_t)P.meta_off + (size_t)(kmax / 32) * 8;
     if (smem > kSSmemMax) return cudaErrorNotSupported;
-    // the next launch's rows, when they are few enough to sit in L2 beside this launch's
-    if (pf && n_pf > 0 && n_pf <= n_groups && next_prefetch_setting()) {
-        int64_t bytes = 0;
-        for (int i = 0; i < n_pf; ++i)
-            bytes += std::min<int64_t>(P.g[i].n_pairs, groups[i].num_experts) * pf[i].expert_bytes;
-        if (bytes <= kPfMaxBytes) {
-            for (int i = 0; i < n_pf; ++i) P.pf[i] = pf[i];
-            P.n_pf = n_pf;
-        }
-    }
     void (*kern)(SParams) = fused_swiglu ? idgemv_stream_kernel<true> : idgemv_stream_kernel<false>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
