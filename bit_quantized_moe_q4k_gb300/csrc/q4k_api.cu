@@ -48,25 +48,35 @@ int check_gemv_shape(int num_experts, int m, int top_k, int n, int k) {
     return Q4K_OK;
 }
 
-// Tensor-core path policy: experts whose bucket holds at least tc_min pairs run on the
-// tcgen05 grouped GEMM (q4k_tc.cu), the others on the id-GEMV kernel. tc_min comes from the
-// environment variable Q4K_TC_MIN (default 4, 0 disables). A launch uses the path only when
-// some bucket can reach tc_min (n_pairs >= tc_min and n_pairs / num_experts >= tc_min / 4)
+// Tensor-core path policy: experts whose bucket holds at least t pairs run on the tcgen05
+// grouped GEMM (q4k_tc.cu), the others on the id-GEMV kernel, the tensor-core launch first.
+// t is the environment variable Q4K_TC_MIN when set (0 disables the path); otherwise 2 when
+// the batch averages at least two pairs per expert or there are at least 64 experts (many
+// short tensor-core items), else 4 (few experts, about one pair each: the few long
+// tensor-core items would run before the id-GEMV launch instead of beside it; measured on
+// the Mixtral-like m = 4 layer). A launch uses the path only when some bucket can reach t
 // and the caller's workspace holds the activation images.
-int tc_min_setting() {
+int tc_min_env() {
     static int v = [] {
         const char* s = getenv("Q4K_TC_MIN");
-        return s ? atoi(s) : 4;
+        return s ? atoi(s) : -1;
     }();
     return v;
 }
+
+int tc_min_for(int routed_pairs, int num_experts) {
+    if (tc_min_env() >= 0) return tc_min_env();
+    return ((int64_t)routed_pairs >= 2 * (int64_t)num_experts || num_experts >= 64) ? 2 : 4;
+}
+
+// Workspace sizes do not depend on the expert count: size for the smallest threshold.
+int tc_min_sizing() { return tc_min_env() >= 0 ? tc_min_env() : 2; }
 
 // Worth it only with enough work to spread over the SMs: at least ~64 items of 128 weight
 // rows x a chunk of <= 32 tokens (a single shared expert with a few row tiles stays on the
 // id-GEMV kernel). Chunks: at least ceil(pairs / 32), and up to one per expert that can
 // reach t pairs when the buckets are spread (min(experts, pairs / t)).
-bool tc_wanted(int n_pairs, int num_experts, int n_rows) {
-    const int t = tc_min_setting();
+bool tc_wanted(int n_pairs, int num_experts, int n_rows, int t) {
     if (t <= 0 || n_pairs < t || (int64_t)n_pairs * 4 < (int64_t)t * num_experts) return false;
     const int64_t chunks = std::max<int64_t>((n_pairs + 31) / 32, std::min<int64_t>(num_experts, n_pairs / t));
     const int64_t items = chunks * ((n_rows + 127) / 128);
@@ -74,7 +84,7 @@ bool tc_wanted(int n_pairs, int num_experts, int n_rows) {
 }
 
 size_t tc_scratch(int n_pairs, int k) {
-    const int t = tc_min_setting();
+    const int t = tc_min_sizing();
     return t > 0 ? align_up(tc_image_bytes(n_pairs, k, t)) : 0;
 }
 
@@ -130,8 +140,9 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
     }
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
-    if (tc_ws && (tc_wanted(m * top_k, num_experts, inter) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter)))) {
-        tc = tc_min_setting();
+    const int t = tc_min_for(m * top_k, num_experts);
+    if (tc_ws && (tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t)))) {
+        tc = t;
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, hidden);
     }
@@ -154,8 +165,9 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
     }
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
-    if (tc_ws && (tc_wanted(m * top_k, num_experts, hidden) || (shared_inter > 0 && tc_wanted(m, 1, hidden)))) {
-        tc = tc_min_setting();
+    const int t = tc_min_for(m * top_k, num_experts);
+    if (tc_ws && (tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t)))) {
+        tc = t;
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, inter);
     }
@@ -222,8 +234,9 @@ size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidde
 
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     if (m <= 0 || top_k < 1 || num_experts < 1) return 0;
-    const bool tc_gu = tc_wanted(m * top_k, num_experts, inter) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter));
-    const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden) || (shared_inter > 0 && tc_wanted(m, 1, hidden));
+    const int t = tc_min_for(m * top_k, num_experts);
+    const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t));
+    const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t));
     return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0);
 }
 
@@ -267,8 +280,8 @@ int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_exp
     uint8_t* img[1] = {static_cast<uint8_t*>(d_workspace)};
     const size_t need = tc_scratch(m * top_k, k);
     if (d_workspace && need > 0 && ws_bytes >= need && (reinterpret_cast<uintptr_t>(d_workspace) & 255) == 0 &&
-        tc_wanted(m * top_k, num_experts, n))
-        tc = tc_min_setting();
+        tc_wanted(m * top_k, num_experts, n, tc_min_for(m * top_k, num_experts)))
+        tc = tc_min_for(m * top_k, num_experts);
     return cuda_status(launch_idgemv(&g, 1, false, false, d_err_flag, stream, tc, img), "id-gemv launch");
 }
 

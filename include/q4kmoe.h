@@ -112,9 +112,10 @@ int q4k_moe_bucket(const int32_t* d_ids, int n_pairs, int num_experts, int32_t* 
  *   d_a: 16-byte aligned; strides multiples of 4 floats
  *   d_out: [m*top_k, n] fp32
  * d_workspace is optional here: when it holds at least q4k_moe_workspace_size(m, top_k,
- * num_experts, n, k) bytes (256-byte aligned), experts whose bucket holds at least
- * Q4K_TC_MIN pairs (environment variable, default 4, 0 disables) run on the tcgen05
- * tensor-core grouped GEMM; all others on the id-GEMV kernel.
+ * num_experts, n, k) bytes (256-byte aligned), experts whose bucket holds at least t pairs
+ * run on the tcgen05 tensor-core grouped GEMM; all others on the id-GEMV kernel. t is the
+ * environment variable Q4K_TC_MIN when set (0 disables the path), else 2 when
+ * m*top_k >= 2*num_experts or num_experts >= 64, else 4.
  * Limits: num_experts <= 4096, k <= 65536.
  */
 int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_experts,

@@ -1,7 +1,8 @@
 """GPU parity of the tensor-core grouped GEMM (tcgen05) path against the CPU oracle.
 
-Buckets of at least 4 pairs (the default Q4K_TC_MIN) run on the tensor-core path when the
-caller provides the workspace; without it the same calls run on the id-GEMV kernel. Both
+Buckets of at least 2 pairs (the threshold these batches get: at least two pairs per expert)
+run on the tensor-core path when the caller provides the workspace; without it the same
+calls run on the id-GEMV kernel. Both
 must meet the per-row acceptance; their results differ in rounding (fp16 activations in the
 tensor-core products vs 16-bit fixed point), which shows the tensor-core path did run.
 """
