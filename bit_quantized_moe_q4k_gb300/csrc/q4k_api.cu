@@ -146,7 +146,9 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, hidden);
     }
-    return cuda_status(launch_idgemv(g, ng, true, false, err_flag, stream, tc, img, nullptr, zero, n_zero),
+    // a programmatic dependent launch that waits before reading anything: only the launch of its
+    // CTAs overlaps the previous kernel's tail
+    return cuda_status(launch_idgemv(g, ng, true, true, err_flag, stream, tc, img, nullptr, zero, n_zero, true),
                        "gate|up launch");
 }
 

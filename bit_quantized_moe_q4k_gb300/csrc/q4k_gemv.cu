@@ -59,6 +59,7 @@ struct GemvParams {
     unsigned* zero;         // CTA 0 zeroes zero[0..n_zero) first
     int n_zero;
     int fast;               // every group has at most 32 pairs: bucket with one warp per group
+    int wait_first;         // wait for the previous kernel before reading anything (first launch of a layer)
 };
 
 // Stage the activation rows of the item's pairs (token t at xs + t*tok_bytes, meta + t*(k/32)).
@@ -117,6 +118,9 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     __shared__ int s_staged_group, s_staged_nt, s_restage;
     __shared__ int s_pairs_key[3];  // (group, expert, chunk) whose pairs are in s_pairs
 
+    // the next launch (down, which reads the ids before its own wait) may start only once the
+    // ids are complete: with wait_first, trigger it after the wait
+    if (P.wait_first) pdl_wait();
     pdl_launch_dependents();
     if (threadIdx.x == 0) { s_staged_group = -1; s_staged_nt = 0; }
     if (P.zero && blockIdx.x == 0)
@@ -421,14 +425,14 @@ int idgemv_tile_rows(int k) {
 
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
-                          unsigned* zero, int n_zero) {
+                          unsigned* zero, int n_zero, bool pdl_wait_first) {
     if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
     if (tc_min > 0) {
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
         if (e != cudaSuccess) return e;
         pdl = false;  // the tensor-core kernels precede this launch in the stream
     }
-    if (stream_setting()) {
+    if (stream_setting() && !pdl_wait_first) {
         const cudaError_t se = launch_idgemv_stream(groups, n_groups, fused_swiglu, pdl, err_flag, stream, tc_min,
                                                     combine, zero, n_zero);
         if (se != cudaErrorNotSupported) return se;
@@ -439,6 +443,7 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     P.tc_min = tc_min;
     P.zero = zero;
     P.n_zero = zero ? n_zero : 0;
+    P.wait_first = (pdl && pdl_wait_first) ? 1 : 0;
     if (combine) {
         P.has_combine = 1;
         P.cb = *combine;

@@ -51,7 +51,9 @@ struct GemvGroup {
 // Launch the bucketed Q4_K id-GEMV over up to two groups in one grid (the routed experts
 // and the shared expert of a layer). fused_swiglu: out = silu(w . x) * (w2 . x).
 // pdl: the launch may start while the previous kernel of the stream drains (programmatic
-// dependent launch); the kernel waits for it before reading activations.
+// dependent launch); the kernel waits for it before reading activations, or, with
+// pdl_wait_first, before reading anything (for the first launch of a layer, whose ids and
+// activations the previous kernel may have written).
 // The combine fused into a down launch (group 0 = routed experts, group 1 = shared expert):
 // the last CTA to finish a row tile forms, for those rows of every token,
 //   y = h_mid + sum_s weights[t*top_k+s] * out0[t*top_k+s] + g_t * out1[t]
@@ -74,7 +76,8 @@ struct CombineSpec {
 // following down launch uses).
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr,
-                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0);
+                          const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0,
+                          bool pdl_wait_first = false);
 // rows per id-GEMV work item for a given k (bucketed kernel)
 int idgemv_tile_rows(int k);
 // The bulk-copy id-GEMV for small batches (q4k_stream.cu): cudaErrorNotSupported, before

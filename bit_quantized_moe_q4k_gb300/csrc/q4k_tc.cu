@@ -133,6 +133,8 @@ tc_prep_kernel(const __grid_constant__ TcParams P) {
     const TcGroup& G = P.g[gi];
     int* cnt = reinterpret_cast<int*>(smem);
     int* start = cnt + G.num_experts;
+    // the ids and activations may be the previous kernel's output
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int total = tc_chunks(G, P.tc_min, cnt, start, s_warp, &s_bad);
     const int q = blockIdx.x;
     if (q >= total) return;
@@ -145,8 +147,6 @@ tc_prep_kernel(const __grid_constant__ TcParams P) {
     __syncthreads();
     const int e = s_info[0], chunk = s_info[1], nt = s_info[2];
     if (threadIdx.x < 32) tc_gather(G, e, chunk, nt, s_pairs);
-    // the activations may be the previous kernel's output
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c4 = lane >> 3, ip = lane & 7;
