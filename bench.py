@@ -158,6 +158,15 @@ def oracle_sample_layers(W: Workload, n_layers: int, seed_base: int):
     return out
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def time_oracle(W: Workload, target_s: float) -> dict:
     """Time the oracle's whole layer on host cores; returns pairs/s and the sample."""
     import oracle
@@ -345,9 +354,7 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     layer_b = float(np.mean([p["layer"] for p in per]))
 
     if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
 
     # end to end through the host-buffer C-ABI call: per step H2D inputs, the layer, D2H output
     e2e = None
@@ -378,9 +385,7 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
         wall_ms = (time.perf_counter() - t0) * 1e3
         e2e_ms = max(e0.elapsed_time(e1), wall_ms)
         if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+            e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": P * K * world / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(m * H * 4 * 2 + P * 4 * 2 + m * 4),
                "d2h_bytes_per_step": int(m * H * 4),
@@ -428,7 +433,8 @@ def main():
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
 
     config = {"workload": W.name, "hidden": W.hidden, "inter": W.inter, "num_experts": W.num_experts,
