@@ -112,6 +112,18 @@ def test_id_gemv_matches_oracle(mode, E, n, k, m, T, kernel_path):
 
 
 @pytest.mark.parametrize("mode", ["gate_up", "down"])
+@pytest.mark.parametrize("E,n,k,m,T", [(64, 36, 256, 2, 16),    # top_k at its limit, one block per row
+                                       (64, 36, 256, 5, 16),    # 80 pairs: bucketed path, top_k 16
+                                       (4096, 8, 256, 3, 4),    # the expert-count limit
+                                       (1, 4, 256, 7, 1)])      # one expert, the smallest n
+def test_id_gemv_limits(mode, E, n, k, m, T, kernel_path):
+    w, ids, a, outer, inner = _gemv_case(300 + E + m, E, n, k, m, T, mode)
+    ref, _ = oracle.moe_id_gemv(w, E, a, outer, inner, ids, m, T, n, k)
+    got = _run_gemv(w, E, a, outer, inner, ids, m, T, n, k)
+    rows_close(got, ref, what=f"id-gemv limits {mode} E={E} T={T}")
+
+
+@pytest.mark.parametrize("mode", ["gate_up", "down"])
 def test_pages_tiny_case(mode, kernel_path):
     """The ferrum-kernels tiny case: its ids and input recipes, against the oracle, and
     batched == per-token calls on the GPU bit for bit."""
@@ -263,6 +275,17 @@ def test_layer_full_size_qwen3_like(name, kernel_path):
                                 W.m, W.top_k, W.hidden, W.inter)
     got = _run_layer_device(W, *args)
     rows_close(got, ref, what=name)
+
+
+def test_layer_top_k_16(kernel_path):
+    """The combine at the top_k limit (16 slots per token), with a sigmoid-gated shared expert."""
+    from bit_quantized_moe_q4k_gb300.workloads import Workload
+    W = Workload("topk16", 256, 256, 32, 16, 3, "uniform", 256, 1, 950)
+    args = _layer_inputs(W)
+    wg, wu, wd, shared, ids, x, hm, rw, gl = args
+    ref, _ = oracle.moe_layer(wg, wu, wd, W.num_experts, shared, W.shared_inter, W.shared_mode, x, hm, ids, rw, gl,
+                              W.m, W.top_k, W.hidden, W.inter)
+    rows_close(_run_layer_device(W, *args), ref, what="layer top_k 16")
 
 
 def test_layer_small_all_shared_modes_and_host_variant(kernel_path):
