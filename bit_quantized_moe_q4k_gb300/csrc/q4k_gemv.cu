@@ -456,6 +456,9 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         const bool to_tc = tc_min > 0 && pairs >= (int64_t)tc_min * groups[gi].num_experts;
         if (!to_tc && pairs > groups[gi].num_experts) tb = kTB;
     }
+    // buckets of tc_min or more pairs went to the tensor-core path: with tc_min = 2 every
+    // bucket left here holds one pair
+    if (tc_min > 0 && tc_min <= 2) tb = 1;
     int ints = 0, kmax = 0;
     int64_t max_items = 0;
     for (int gi = 0; gi < n_groups; ++gi) {
