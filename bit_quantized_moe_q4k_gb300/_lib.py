@@ -187,7 +187,8 @@ def q4k_moe_layer_forward(w_gate, w_up, w_down, num_experts, ws_gate, ws_up, ws_
 def q4k_moe_layer_forward_host(w_gate, w_up, w_down, num_experts, ws_gate, ws_up, ws_down, shared_inter, shared_mode,
                                h_post, h_mid, ids, weights, shared_gate, m, top_k, hidden, inter, y, workspace,
                                ws_bytes, err_flag=None, stream=None):
-    """h_post, h_mid, ids, weights, shared_gate and y are HOST tensors (pinned for asynchronous copies)."""
+    """h_post, h_mid, ids, weights, shared_gate and y are HOST tensors. Page-locked (pinned) ones are
+    read and written by the kernels directly; pageable ones are copied, one transfer per buffer."""
     _cuda(w_gate, w_up, w_down, ws_gate, ws_up, ws_down, workspace, err_flag)
     _check(load().q4k_moe_layer_forward_host(_ptr(w_gate), _ptr(w_up), _ptr(w_down), num_experts, _ptr(ws_gate),
                                              _ptr(ws_up), _ptr(ws_down), shared_inter, shared_mode, _ptr(h_post),

@@ -115,6 +115,19 @@ LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_i
     return s;
 }
 
+// The device's address of page-locked host memory (cudaHostAlloc / cudaHostRegister), usable by
+// kernels on the current device; false for any other host memory (pageable, unknown).
+bool host_device_view(const void* p, const void** out) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of the query
+        return false;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return false;
+    *out = a.devicePointer;
+    return true;
+}
+
 int check_workspace(void* ws, size_t ws_bytes, size_t need) {
     if (need == 0) return Q4K_OK;
     if (!ws) return fail(Q4K_ERR_WORKSPACE, "workspace is NULL but %zu bytes are needed", need);
@@ -435,17 +448,38 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
     int32_t* dids = reinterpret_cast<int32_t*>(stage + 3 * align_up(mh));
     float* dw = reinterpret_cast<float*>(stage + 3 * align_up(mh) + align_up(mt));
     float* dgate = reinterpret_cast<float*>(stage + 3 * align_up(mh) + 2 * align_up(mt));
-    cudaError_t e = cudaMemcpyAsync(dh_post, h_post, mh, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dh_mid, h_mid, mh, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dids, ids, mt, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dw, weights, mt, cudaMemcpyHostToDevice, stream);
-    if (e == cudaSuccess && shared_gate)
-        e = cudaMemcpyAsync(dgate, shared_gate, (size_t)m * 4, cudaMemcpyHostToDevice, stream);
+    // Page-locked host buffers have a device view: the inputs are then gathered by one kernel
+    // reading host memory, and the combine writes y into host memory. Any other host memory
+    // goes through the copy engine (one transfer per buffer).
+    const void* src[5] = {h_post, h_mid, ids, weights, shared_gate};
+    void* dst[5] = {dh_post, dh_mid, dids, dw, dgate};
+    const size_t bytes[5] = {mh, mh, mt, mt, shared_gate ? (size_t)m * 4 : 0};
+    const void* view[5] = {};
+    bool mapped = true;
+    for (int i = 0; i < 5 && mapped; ++i) mapped = bytes[i] == 0 || host_device_view(src[i], &view[i]);
+    cudaError_t e = cudaSuccess;
+    if (mapped && mh <= 0xFFFFFFFFu) {
+        GatherSpec g{};
+        for (int i = 0; i < 5; ++i)
+            if (bytes[i]) {
+                g.src[g.n] = view[i];
+                g.dst[g.n] = dst[i];
+                g.bytes[g.n] = (uint32_t)bytes[i];
+                ++g.n;
+            }
+        e = launch_gather(g, stream);
+    } else {
+        for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+            if (bytes[i]) e = cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyHostToDevice, stream);
+    }
     if (e != cudaSuccess) return cuda_status(e, "host-to-device copy");
+    const void* y_view = nullptr;
+    const bool y_mapped = host_device_view(y, &y_view);
+    float* y_dev = y_mapped ? static_cast<float*>(const_cast<void*>(y_view)) : dy;
     st = q4k_moe_layer_forward(d_w_gate, d_w_up, d_w_down, num_experts, d_ws_gate, d_ws_up, d_ws_down, sh,
                                shared_mode, dh_post, dh_mid, dids, dw, shared_gate ? dgate : nullptr, m, top_k,
-                               hidden, inter, dy, d_workspace, layer_bytes, d_err_flag, stream);
-    if (st) return st;
+                               hidden, inter, y_dev, d_workspace, layer_bytes, d_err_flag, stream);
+    if (st || y_mapped) return st;
     return cuda_status(cudaMemcpyAsync(y, dy, mh, cudaMemcpyDeviceToHost, stream), "device-to-host copy");
 }
 

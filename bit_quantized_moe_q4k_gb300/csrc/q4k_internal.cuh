@@ -35,6 +35,15 @@ cudaError_t launch_combine(const float* h_mid, const float* expert_out, const fl
                            int top_k, int hidden, float* y, bool pdl, cudaStream_t stream);
 cudaError_t launch_quantize(const float* x, int64_t rows, int k, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_stream_ceiling(const void* src, uint64_t bytes, uint32_t* sink, cudaStream_t stream);
+// Up to 5 small copies (sizes multiples of 4 bytes) in one launch; sources may be host memory
+// the device can address (page-locked, its device view).
+struct GatherSpec {
+    const void* src[5];
+    void* dst[5];
+    uint32_t bytes[5];
+    int n;
+};
+cudaError_t launch_gather(const GatherSpec& g, cudaStream_t stream);
 int stream_ceiling_grid();
 
 // One projection group of an id-GEMV launch: a stacked slab and how its pairs read rows.

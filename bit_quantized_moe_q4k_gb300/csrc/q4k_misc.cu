@@ -276,4 +276,27 @@ cudaError_t launch_stream_ceiling(const void* src, uint64_t bytes, uint32_t* sin
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------------
+// Gather of a few small buffers into device memory in one launch (the host-buffer layer call
+// uses it to read its page-locked inputs straight from host memory: one launch instead of one
+// copy-engine transfer per buffer). Sizes are multiples of 4 bytes; 4-byte words.
+__global__ void __launch_bounds__(256) gather_kernel(const GatherSpec G) {
+    for (int i = 0; i < G.n; ++i) {
+        const uint32_t words = G.bytes[i] / 4;
+        const uint32_t* src = static_cast<const uint32_t*>(G.src[i]);
+        uint32_t* dst = static_cast<uint32_t*>(G.dst[i]);
+        for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < words; w += gridDim.x * blockDim.x)
+            dst[w] = src[w];
+    }
+}
+
+cudaError_t launch_gather(const GatherSpec& g, cudaStream_t stream) {
+    uint32_t words = 0;
+    for (int i = 0; i < g.n; ++i) words = g.bytes[i] / 4 > words ? g.bytes[i] / 4 : words;
+    if (words == 0) return cudaSuccess;
+    const uint32_t grid = (words + 255) / 256 < 64 ? (words + 255) / 256 : 64;
+    gather_kernel<<<grid, 256, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
 }  // namespace q4k

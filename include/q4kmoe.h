@@ -223,11 +223,15 @@ int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, in
 
 /* ---------------------------------------------------------------------------------
  * q4k_moe_layer_forward_host -- the same layer with the per-step inputs and the
- * output in HOST memory (pinned memory gives asynchronous copies). Weights and the
- * workspace stay in device memory. Copies h_post, h_mid, ids, weights and
- * shared_gate into the staging area at the front of the workspace, runs the
- * layer, copies y back, all on `stream`; the call returns once these are
- * enqueued, so the caller synchronises `stream` before reading y.
+ * output in HOST memory. Weights and the workspace stay in device memory. The inputs
+ * h_post, h_mid, ids, weights and shared_gate land in the staging area behind the
+ * layer's workspace, the layer runs, y lands in host memory, all on `stream`; the
+ * call returns once this is enqueued, so the caller synchronises `stream` before
+ * reading y. Page-locked host buffers (cudaHostAlloc / cudaHostRegister, as
+ * reported by cudaPointerGetAttributes) are read and written by the kernels
+ * through their device view: one gather launch for all inputs, and the fused
+ * combine stores y into host memory. Other host memory goes through
+ * cudaMemcpyAsync, one transfer per buffer.
  * Workspace: q4k_moe_layer_workspace_size(...) + q4k_moe_layer_host_staging_size(...).
  */
 size_t q4k_moe_layer_host_staging_size(int m, int top_k, int hidden);

@@ -311,3 +311,11 @@ def test_layer_small_all_shared_modes_and_host_variant(kernel_path):
                                        ws_bytes)
         torch.cuda.synchronize()
         assert np.array_equal(y.numpy(), got)
+        # pageable host buffers take the copy-engine route: the same bytes
+        pg = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+        y2 = torch.empty((W.m, W.hidden), dtype=torch.float32)
+        q4k.q4k_moe_layer_forward_host(dev(wg), dev(wu), dev(wd), W.num_experts, sg, su, sd, sh, mode, pg(x),
+                                       pg(hm), pg(ids), pg(rw), pg(gl), W.m, W.top_k, W.hidden, W.inter, y2, ws,
+                                       ws_bytes)
+        torch.cuda.synchronize()
+        assert np.array_equal(y2.numpy(), got)
