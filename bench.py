@@ -297,8 +297,10 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
 
     K, Wm = args.steps, args.warmup
 
-    # the timed graph: K whole-layer steps; the kernel graph: the dominant kernel (fused
-    # gate|up, launched as in the step) over the same K layers back to back, for its duration
+    # the timed graph: K whole-layer steps; the kernel graph (two-launch layers): the dominant
+    # kernel (fused gate|up, launched as in the step) over the same K layers back to back.
+    # A single-launch layer's one kernel is the step: its duration comes from the timed graph.
+    single = q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is) == 1
     g_warm, g_timed, g_kernel = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g_warm, stream=stream, capture_error_mode="thread_local"):
@@ -307,9 +309,10 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
         with torch.cuda.graph(g_timed, stream=stream, capture_error_mode="thread_local"):
             for i in range(K):
                 step(layers[(Wm + i) % n_layers], Wm + i)
-        with torch.cuda.graph(g_kernel, stream=stream, capture_error_mode="thread_local"):
-            for i in range(K):
-                gate_up(layers[(Wm + i) % n_layers], Wm + i)
+        if not single:
+            with torch.cuda.graph(g_kernel, stream=stream, capture_error_mode="thread_local"):
+                for i in range(K):
+                    gate_up(layers[(Wm + i) % n_layers], Wm + i)
     stream.synchronize()
 
     dist = None
@@ -337,15 +340,17 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     clk = clocks.stop()
     total_ms = ev0.elapsed_time(ev1)
     # dominant kernel alone, same layers, right after the timed region
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g_kernel.replay()  # warm
-    k0.record(stream)
-    with torch.cuda.stream(stream):
-        g_kernel.replay()
-    k1.record(stream)
-    k1.synchronize()
-    gu_ms = [k0.elapsed_time(k1) / K]
+    gu_ms = [total_ms / K]
+    if not single:
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g_kernel.replay()  # warm
+        k0.record(stream)
+        with torch.cuda.stream(stream):
+            g_kernel.replay()
+        k1.record(stream)
+        k1.synchronize()
+        gu_ms = [k0.elapsed_time(k1) / K]
     assert int(flag.item()) == 0, "device error flag raised"
 
     # algorithmic bytes per step (touched experts differ per layer)
@@ -415,7 +420,7 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
 
     # kernels per step: gate|up and down (+ prep and GEMM of the tensor-core path when a half uses it)
     launches_per_step = q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is)
-    return {"launches_per_step": launches_per_step, "total_ms": total_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes, "layer_bytes": layer_b, "clocks": clk,
+    return {"single": single, "launches_per_step": launches_per_step, "total_ms": total_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes, "layer_bytes": layer_b, "clocks": clk,
             "n_layers": n_layers, "e2e": e2e, "per_layer_touched": per_layer_touched,
             "experts_touched": float(np.mean([p["experts_touched"] for p in per]))}
 
@@ -430,6 +435,20 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = {  # the files whose text a kernel's counters depend on
+    "idgemv_kernel<true>": ("q4k_gemv.cu", "q4k_gemv_common.cuh"),
+    "layer_kernel": ("q4k_layer.cu", "q4k_gemv_common.cuh"),
+}
+
+
+def source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "bit_quantized_moe_q4k_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(kernel: str, workload_name: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on the current source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -438,8 +457,7 @@ def kernel_traffic(kernel: str, workload_name: str):
             entries = json.load(f)
     except (OSError, ValueError):
         return None
-    src = os.path.join(ROOT, "bit_quantized_moe_q4k_gb300", "csrc", "q4k_gemv.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = source_sha(kernel)
     for e in entries:
         if e.get("kernel") == kernel and e.get("workload") == workload_name and e.get("source_sha") == sha:
             return e.get("traffic_bytes_per_launch")
@@ -484,7 +502,18 @@ def main():
     value = W.pairs * K * max(1, world) / (r["total_ms"] / 1e3)
     peak, peak_kind = measured_peaks()
     gu_ms = float(np.mean(r["gu_ms"]))
-    achieved = r["gu_bytes"] / (gu_ms * 1e-3) / 1e9
+    if r["single"]:
+        # one kernel per step: the whole layer's bytes over its launch duration
+        kernel, kbytes = "layer_kernel", r["layer_bytes"]
+        kdesc = "layer_kernel (gate|up+SwiGLU, down, combine; routed + shared) in one persistent launch"
+        ktiming = ("CUDA events around the timed graph: K back-to-back launches of this kernel, one per step, "
+                   "on the launching stream")
+    else:
+        kernel, kbytes = "idgemv_kernel<true>", r["gu_bytes"]
+        kdesc = "idgemv_kernel<fused gate|up+SwiGLU> (routed + shared)"
+        ktiming = ("CUDA events around a graph of K back-to-back launches of this kernel over the same rotating "
+                   "layers, right after the timed region")
+    achieved = kbytes / (gu_ms * 1e-3) / 1e9
     layer_gbs = r["layer_bytes"] / (step_ms * 1e-3) / 1e9
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -502,12 +531,10 @@ def main():
                     "h_mid/ids/routing weights as slices of stacked tensors"),
         "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / peak,
         "experts_touched_per_step": r["experts_touched"],
-        "roofline": {"kernel": "idgemv_kernel<fused gate|up+SwiGLU> (routed + shared)", "bound": "hbm",
+        "roofline": {"kernel": kdesc, "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "bytes_per_launch": r["gu_bytes"], "avg_launch_us": gu_ms * 1e3,
-                     "timing": "CUDA events around a graph of K back-to-back launches of this kernel over the "
-                               "same rotating layers, right after the timed region",
-                     "traffic": kernel_traffic("idgemv_kernel<true>", W.name)},
+                     "frac": achieved / peak, "bytes_per_launch": kbytes, "avg_launch_us": gu_ms * 1e3,
+                     "timing": ktiming, "traffic": kernel_traffic(kernel, W.name)},
         "cpu_baseline": cpu,
         "e2e": r["e2e"],
         "clocks": r["clocks"],

@@ -69,6 +69,13 @@ int tc_min_for(int routed_pairs, int num_experts) {
     return ((int64_t)routed_pairs >= 2 * (int64_t)num_experts || num_experts >= 64) ? 2 : 4;
 }
 
+// Switch (environment, read at every call): Q4K_SINGLE_LAUNCH=1 runs small layers as one
+// persistent launch where it applies (default 0: two launches, faster on GB300 at m = 1 so far).
+int single_launch_setting() {
+    const char* s = getenv("Q4K_SINGLE_LAUNCH");
+    return s ? (atoi(s) != 0 ? 1 : 0) : 0;
+}
+
 // Workspace sizes do not depend on the expert count: size for the smallest threshold.
 int tc_min_sizing() { return tc_min_env() >= 0 ? tc_min_env() : 2; }
 
@@ -83,6 +90,20 @@ bool tc_wanted(int n_pairs, int num_experts, int n_rows, int t) {
     return items >= 64;
 }
 
+// Would the two-launch layer send some bucket of either half to the tensor-core path?
+bool layer_wants_tc(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
+    const int t = tc_min_for(m * top_k, num_experts);
+    const bool sh = shared_inter > 0;
+    return tc_wanted(m * top_k, num_experts, inter, t) || (sh && tc_wanted(m, 1, shared_inter, t)) ||
+           tc_wanted(m * top_k, num_experts, hidden, t) || (sh && tc_wanted(m, 1, hidden, t));
+}
+
+// The layer runs as one persistent launch (q4k_layer.cu): a few pairs, no tensor-core bucket.
+bool layer_single_launch(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
+    return single_launch_setting() && layer_sync_words(m, top_k, hidden, inter, shared_inter) > 0 &&
+           !layer_wants_tc(m, top_k, num_experts, hidden, inter, shared_inter);
+}
+
 size_t tc_scratch(int n_pairs, int k) {
     const int t = tc_min_sizing();
     return t > 0 ? align_up(tc_image_bytes(n_pairs, k, t)) : 0;
@@ -95,13 +116,18 @@ size_t ffn_scratch(int m, int top_k, int hidden, int inter) {
 }
 
 struct LayerScratch {
-    size_t act, act_shared, eout, shared_out, tc_gu, tc_dn, counters, total;
+    size_t sync, act, act_shared, eout, shared_out, tc_gu, tc_dn, counters, total;
+    size_t n_sync_words;  // 0: these shapes always take the two-launch layer
     int n_counters;
 };
 
 LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_inter) {
     LayerScratch s{};
     size_t off = 0;
+    // the single-launch layer's generation word, start tags and item flags come first, so the
+    // generation word stays at offset 0 whatever the shapes of later calls
+    s.n_sync_words = layer_sync_words(m, top_k, hidden, inter, shared_inter);
+    s.sync = off;       off += align_up(s.n_sync_words * sizeof(uint64_t));
     s.act = off;        off += align_up((size_t)m * top_k * inter * sizeof(float));
     s.act_shared = off; off += align_up((size_t)m * shared_inter * sizeof(float));
     s.eout = off;       off += align_up((size_t)m * top_k * hidden * sizeof(float));
@@ -136,6 +162,30 @@ int check_workspace(void* ws, size_t ws_bytes, size_t need) {
     return Q4K_OK;
 }
 
+// The groups of the two halves of a layer: routed experts, then (shared_inter > 0) the
+// shared expert. Returns the group count.
+int gate_up_groups(const void* w_gate, const void* w_up, int num_experts, const float* h_post, const int32_t* ids,
+                   int m, int top_k, int hidden, int inter, float* act, const void* ws_gate, const void* ws_up,
+                   int shared_inter, float* act_shared, GemvGroup* g) {
+    g[0] = GemvGroup{static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), ids, h_post,
+                     hidden, 0, act, num_experts, m, top_k, inter, hidden};
+    if (shared_inter <= 0) return 1;
+    g[1] = GemvGroup{static_cast<const uint8_t*>(ws_gate), static_cast<const uint8_t*>(ws_up), nullptr, h_post,
+                     hidden, 0, act_shared, 1, m, 1, shared_inter, hidden};
+    return 2;
+}
+
+int down_groups(const void* w_down, int num_experts, const float* act, const int32_t* ids, int m, int top_k,
+                int hidden, int inter, float* expert_out, const void* ws_down, int shared_inter,
+                const float* act_shared, float* shared_out, GemvGroup* g) {
+    g[0] = GemvGroup{static_cast<const uint8_t*>(w_down), nullptr, ids, act, (int64_t)top_k * inter, inter,
+                     expert_out, num_experts, m, top_k, hidden, inter};
+    if (shared_inter <= 0) return 1;
+    g[1] = GemvGroup{static_cast<const uint8_t*>(ws_down), nullptr, nullptr, act_shared, shared_inter, 0,
+                     shared_out, 1, m, 1, hidden, shared_inter};
+    return 2;
+}
+
 // Gate|up + SwiGLU of the routed experts and (when shared_inter > 0) the shared expert, in
 // one launch; then the down projections of both, in one launch.
 int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const float* h_post, const int32_t* ids,
@@ -143,14 +193,8 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
                 int shared_inter, float* act_shared, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr,
                 unsigned* zero = nullptr, int n_zero = 0) {
     GemvGroup g[2] = {};
-    int ng = 1;
-    g[0] = GemvGroup{static_cast<const uint8_t*>(w_gate), static_cast<const uint8_t*>(w_up), ids, h_post,
-                     hidden, 0, act, num_experts, m, top_k, inter, hidden};
-    if (shared_inter > 0) {
-        g[1] = GemvGroup{static_cast<const uint8_t*>(ws_gate), static_cast<const uint8_t*>(ws_up), nullptr, h_post,
-                         hidden, 0, act_shared, 1, m, 1, shared_inter, hidden};
-        ng = 2;
-    }
+    const int ng = gate_up_groups(w_gate, w_up, num_experts, h_post, ids, m, top_k, hidden, inter, act, ws_gate,
+                                  ws_up, shared_inter, act_shared, g);
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
     const int t = tc_min_for(m * top_k, num_experts);
@@ -170,14 +214,8 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
              float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr,
              const CombineSpec* combine = nullptr) {
     GemvGroup g[2] = {};
-    int ng = 1;
-    g[0] = GemvGroup{static_cast<const uint8_t*>(w_down), nullptr, ids, act, (int64_t)top_k * inter, inter,
-                     expert_out, num_experts, m, top_k, hidden, inter};
-    if (shared_inter > 0) {
-        g[1] = GemvGroup{static_cast<const uint8_t*>(ws_down), nullptr, nullptr, act_shared, shared_inter, 0,
-                         shared_out, 1, m, 1, hidden, shared_inter};
-        ng = 2;
-    }
+    const int ng = down_groups(w_down, num_experts, act, ids, m, top_k, hidden, inter, expert_out, ws_down,
+                               shared_inter, act_shared, shared_out, g);
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
     const int t = tc_min_for(m * top_k, num_experts);
@@ -249,6 +287,7 @@ size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidde
 
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     if (m <= 0 || top_k < 1 || num_experts < 1) return 0;
+    if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) return 1;
     const int t = tc_min_for(m * top_k, num_experts);
     const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t));
     const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t));
@@ -376,6 +415,18 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
     float* act_shared = reinterpret_cast<float*>(ws + ls.act_shared);
     float* eout = reinterpret_cast<float*>(ws + ls.eout);
     float* sout = reinterpret_cast<float*>(ws + ls.shared_out);
+    // a few pairs and no tensor-core bucket: the whole layer in one persistent launch
+    if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) {
+        GemvGroup gu[2] = {}, dn[2] = {};
+        const int ng = gate_up_groups(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act,
+                                      d_ws_gate, d_ws_up, shared_inter, act_shared, gu);
+        down_groups(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,
+                    act_shared, sout, dn);
+        const CombineSpec cb1{d_y, d_h_mid, d_weights, d_shared_gate, shared_mode, nullptr, 0};
+        const cudaError_t e = launch_layer_persistent(gu, dn, ng, cb1, reinterpret_cast<uint64_t*>(ws + ls.sync),
+                                                      ls.n_sync_words, d_err_flag, stream);
+        if (e != cudaErrorNotSupported) return cuda_status(e, "layer launch");
+    }
     // two launches: gate|up + SwiGLU (routed and shared; it also zeroes the combine counters),
     // then down (routed and shared) with the combine fused into its last CTA per row tile
     unsigned* counters = reinterpret_cast<unsigned*>(ws + ls.counters);

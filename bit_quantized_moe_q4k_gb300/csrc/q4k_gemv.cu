@@ -31,19 +31,6 @@
 
 namespace q4k {
 
-struct GroupDev {
-    const uint8_t* w;
-    const uint8_t* w2;
-    const int32_t* ids;
-    const float* a;
-    float* out;
-    int64_t outer, inner;
-    int64_t nb01;  // bytes per row
-    int64_t nb02;  // bytes per expert
-    int num_experts, n_pairs, top_k, n, k, tiles;
-    int lg_split;  // log2 of the lanes splitting one row's blocks (rows per warp = 8 >> lg_split)
-};
-
 struct GemvParams {
     GroupDev g[kMaxGroups];
     int n_groups;
@@ -62,34 +49,6 @@ struct GemvParams {
     int wait_first;         // wait for the previous kernel before reading anything (first launch of a layer)
 };
 
-// Stage the activation rows of the item's pairs (token t at xs + t*tok_bytes, meta + t*(k/32)).
-// Thread f handles float4 f of the row; all loads of a pass are issued before any is used.
-__device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs, int nt, uint8_t* xs,
-                                           float2* meta) {
-    const int tid = threadIdx.x;
-    const int nf = G.k / 4;
-    const int nsb = G.k / 32;
-    const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
-    for (int t = 0; t < nt; ++t) {
-        const int p = s_pairs[t];
-        const float* row = G.a + (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
-        for (int f0 = 0; f0 < nf; f0 += kThreads * kStageUnroll) {
-            float4 v[kStageUnroll];
-#pragma unroll
-            for (int u = 0; u < kStageUnroll; ++u) {
-                const int f = f0 + u * kThreads + tid;
-                v[u] = f < nf ? __ldg(reinterpret_cast<const float4*>(row) + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < kStageUnroll; ++u) {
-                const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
-                if (f0 + u * kThreads >= nf) break;
-                stage_quad(v[u], f, f < nf, xs + t * tok_bytes, meta + t * nsb);
-            }
-        }
-    }
-}
-
 // Combine of rows [r0, r1) of every token, run by the last CTA of a row tile.
 __device__ void combine_rows(const GemvParams& P, int r0, int r1) {
     const GroupDev& R = P.g[0];
@@ -98,12 +57,6 @@ __device__ void combine_rows(const GemvParams& P, int r0, int r1) {
                  threadIdx.x, blockDim.x);
 }
 
-// Lane layout: lane = c | s << 2 | r << (2 + lg_split). c (0..3) picks the 64-weight group of
-// a block (code bytes 32c..32c+31 = sub-blocks 2c, 2c+1); s picks which blocks of the row the
-// lane streams (b = s, s + S, ...; S = 1 << lg_split lanes share a row's blocks); r is the row
-// within the warp (8 / S rows per warp). Splitting the row's blocks over more lanes keeps
-// each lane's share within the kDepth-deep register ring, so all of an item's weight loads
-// are in flight at once, and spreads the work over more warps.
 template <bool FUSED, int TB>
 __global__ void __launch_bounds__(kThreads, FUSED ? 3 : 4)
 idgemv_kernel(const __grid_constant__ GemvParams P) {
@@ -162,7 +115,6 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
     uint8_t* xs = smem + P.x_off;
     float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int c = lane & 3;
 
     // each CTA takes a contiguous range of items: consecutive row tiles of one expert and
     // chunk, so the staged activation rows and the bucket's pair list carry over
@@ -174,29 +126,15 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         // ---- locate the item: group, expert (search over the item offsets), tile, chunk
         if (P.fast) {
             if (warp == 0) {
-                int gi = 0;
-                while (gi + 1 < P.n_groups && item >= s_items[gi + 1]) ++gi;
-                const FastGroup& F = s_fast[gi];
-                const int local = item - s_items[gi];
-                const bool mine = lane < F.U && F.start[lane] <= local && local < F.start[lane + 1];
-                const unsigned hit = __ballot_sync(0xffffffffu, mine);
-                const int r = __ffs(hit) - 1;
-                const unsigned mask = F.mask[r];
-                const int cnt = __popc(mask);
-                const int in_e = local - F.start[r];
-                const int tiles = P.g[gi].tiles;
-                const int chunk = in_e / tiles;  // tiles of one chunk run together (no restaging)
-                const int nt = min(TB, cnt - chunk * TB);
-                // pair `lane` is a member: its place in the bucket is the members below it
-                const int q = __popc(mask & ((1u << lane) - 1u)) - chunk * TB;
-                if (((mask >> lane) & 1u) && q >= 0 && q < nt) s_pairs[q] = lane;
+                const FastLoc L = fast_locate(s_fast, s_items, P.g, P.n_groups, TB, item, s_pairs);
+                const int gi = L.gi, nt = L.nt;
                 if (lane == 0) {
                     s_item_info[0] = gi;
-                    s_item_info[1] = F.e[r];
-                    s_item_info[2] = in_e % tiles;
+                    s_item_info[1] = L.e;
+                    s_item_info[2] = L.tile;
                     s_item_info[3] = nt;
-                    s_item_info[4] = chunk;
-                    s_pairs_key[0] = gi; s_pairs_key[1] = F.e[r]; s_pairs_key[2] = chunk;
+                    s_item_info[4] = L.chunk;
+                    s_pairs_key[0] = gi; s_pairs_key[1] = L.e; s_pairs_key[2] = L.chunk;
                 }
                 __syncwarp();
                 // the same activation rows as the staged ones need no restaging
@@ -235,32 +173,9 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         const int chunk = s_item_info[4];
         const GroupDev& G = P.g[gi];
 
-        const int lgS = G.lg_split, S = 1 << lgS;
-        const int rows_per_warp = 8 >> lgS;
-
         // ---- start the weight stream before staging (independent of the activations)
-        const int sl = (lane >> 2) & (S - 1);
-        const int row = (tile * kWarps + warp) * rows_per_warp + (lane >> (2 + lgS));
-        const bool row_ok = row < G.n;
-        const int nb = G.k / kQK;
-        const int nbl = sl < nb ? (nb - sl + S - 1) / S : 0;  // blocks b = sl + S*i of this lane
-        const int nsb = G.k / 32;
-        const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
-        const uint8_t* wr = G.w + (int64_t)e * G.nb02 + (int64_t)(row_ok ? row : 0) * G.nb01;
-        const uint8_t* wr2 = FUSED ? G.w2 + (int64_t)e * G.nb02 + (int64_t)(row_ok ? row : 0) * G.nb01 : nullptr;
-        uint4 H[kDepth], Q0[kDepth], Q1[kDepth], H2[kDepth], R0[kDepth], R1[kDepth];
-#pragma unroll
-        for (int i = 0; i < kDepth; ++i) {
-            H[i] = Q0[i] = Q1[i] = H2[i] = R0[i] = R1[i] = make_uint4(0, 0, 0, 0);
-            if (row_ok && i < nbl) {
-                const uint8_t* p = wr + (int64_t)(sl + S * i) * kBlockBytes;
-                H[i] = ldg16(p); Q0[i] = ldg16(p + 16 + 32 * c); Q1[i] = ldg16(p + 32 + 32 * c);
-                if (FUSED) {
-                    const uint8_t* p2 = wr2 + (int64_t)(sl + S * i) * kBlockBytes;
-                    H2[i] = ldg16(p2); R0[i] = ldg16(p2 + 16 + 32 * c); R1[i] = ldg16(p2 + 32 + 32 * c);
-                }
-            }
-        }
+        ItemLane<FUSED ? kFused : kOne> L;
+        item_issue<FUSED ? kFused : kOne>(G, e, tile, lane, warp, L);
 
         if (!P.fast && warp == 0) {
             const bool have = s_pairs_key[0] == gi && s_pairs_key[1] == e && s_pairs_key[2] == chunk;
@@ -298,61 +213,8 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         }
         __syncthreads();
 
-        // ---- main loop over this lane's blocks, kDepth of them in flight
-        float acc[TB], acc2[TB];
-#pragma unroll
-        for (int t = 0; t < TB; ++t) { acc[t] = 0.0f; acc2[t] = 0.0f; }
-        for (int i0 = 0; i0 < nbl; i0 += kDepth) {
-#pragma unroll
-            for (int j = 0; j < kDepth; ++j) {
-                const int i = i0 + j;
-                if (i < nbl) {
-                    const int b = sl + S * i;
-                    float sa, ma, sb, mb, sa2 = 0.f, ma2 = 0.f, sb2 = 0.f, mb2 = 0.f;
-                    block_scales(H[j], c, sa, ma, sb, mb);
-                    if (FUSED) block_scales(H2[j], c, sa2, ma2, sb2, mb2);
-#pragma unroll
-                    for (int t = 0; t < TB; ++t) {
-                        if (t < nt) {
-                            const uint4* xp = reinterpret_cast<const uint4*>(xs + t * tok_bytes + (4 * b + c) * kPairBytes);
-                            const float4 mt = *reinterpret_cast<const float4*>(meta + t * nsb + 8 * b + 2 * c);
-                            int Sa, Sb;
-                            dot64(Q0[j], Q1[j], xp, Sa, Sb);
-                            acc[t] += mt.x * (sa * (float)Sa - ma * mt.y) + mt.z * (sb * (float)Sb - mb * mt.w);
-                            if (FUSED) {
-                                dot64(R0[j], R1[j], xp, Sa, Sb);
-                                acc2[t] += mt.x * (sa2 * (float)Sa - ma2 * mt.y) + mt.z * (sb2 * (float)Sb - mb2 * mt.w);
-                            }
-                        }
-                    }
-                    if (row_ok && i + kDepth < nbl) {  // refill this slot with block b + S*kDepth
-                        const uint8_t* p = wr + (int64_t)(b + S * kDepth) * kBlockBytes;
-                        H[j] = ldg16(p); Q0[j] = ldg16(p + 16 + 32 * c); Q1[j] = ldg16(p + 32 + 32 * c);
-                        if (FUSED) {
-                            const uint8_t* p2 = wr2 + (int64_t)(b + S * kDepth) * kBlockBytes;
-                            H2[j] = ldg16(p2); R0[j] = ldg16(p2 + 16 + 32 * c); R1[j] = ldg16(p2 + 32 + 32 * c);
-                        }
-                    }
-                }
-            }
-        }
-        // ---- reduce over the 4*S lanes of the row (c bits, then s bits) and write
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            for (int off = 1; off < (4 << lgS); off <<= 1) {
-                acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
-                if (FUSED) acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], off);
-            }
-        }
-        if (row_ok && (lane & ((4 << lgS) - 1)) == 0) {
-#pragma unroll
-            for (int t = 0; t < TB; ++t) {
-                if (t < nt) {
-                    const float v = FUSED ? silu(acc[t]) * acc2[t] : acc[t];
-                    G.out[(int64_t)s_pairs[t] * G.n + row] = v;
-                }
-            }
-        }
+        // ---- main loop over this lane's blocks, kDepth of them in flight; reduce; write
+        item_compute<FUSED ? kFused : kOne, TB>(G, L, s_pairs, nt, xs, meta, lane);
         __syncthreads();  // s_pairs / staged rows are rewritten by the next item
         if (P.has_combine) {
             // every item of this row tile, from either group, counts once; the last one combines
@@ -417,11 +279,7 @@ int num_sms() {
     return g_num_sms;
 }
 
-int idgemv_tile_rows(int k) {
-    const int nb = k / kQK;
-    const int lg = nb >= 4 * kDepth ? 2 : (nb >= 2 * kDepth ? 1 : 0);
-    return kWarps * (8 >> lg);
-}
+int idgemv_tile_rows(int k) { return kWarps * (8 >> lg_split_for(k)); }
 
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
@@ -463,21 +321,9 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     int64_t max_items = 0;
     for (int gi = 0; gi < n_groups; ++gi) {
         const GemvGroup& S = groups[gi];
-        GroupDev& G = P.g[gi];
-        G.w = S.w; G.w2 = S.w2; G.ids = S.ids; G.a = S.a; G.out = S.out;
-        G.outer = S.outer; G.inner = S.inner;
-        G.nb01 = (int64_t)(S.k / kQK) * kBlockBytes;
-        G.nb02 = (int64_t)S.n * G.nb01;
-        G.num_experts = S.num_experts; G.n_pairs = S.m * S.top_k; G.top_k = S.top_k;
-        G.n = S.n; G.k = S.k;
-        // split a row's blocks over up to 4 lanes so that a lane's share fits the kDepth-deep
-        // ring where possible (k = 2048: 2 lanes x 4 blocks; k = 4096: 4 x 4; k = 768: 1 x 3)
-        const int nb = S.k / kQK;
-        G.lg_split = nb >= 4 * kDepth ? 2 : (nb >= 2 * kDepth ? 1 : 0);
         // with the combine fused, every group uses group 0's row tiles (one counter per tile)
-        if (combine && gi > 0) G.lg_split = P.g[0].lg_split;
-        const int tile_rows = kWarps * (8 >> G.lg_split);
-        G.tiles = (S.n + tile_rows - 1) / tile_rows;
+        P.g[gi] = group_dev(S, (combine && gi > 0) ? P.g[0].lg_split : lg_split_for(S.k));
+        const GroupDev& G = P.g[gi];
         P.hist_off[gi] = ints;
         ints += 2 * S.num_experts;
         kmax = S.k > kmax ? S.k : kmax;

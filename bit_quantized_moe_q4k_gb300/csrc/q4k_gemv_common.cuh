@@ -199,11 +199,250 @@ __device__ __forceinline__ void fast_bucket(const int32_t* ids, int n_pairs, int
 }
 
 
+// One projection group of a launch as the kernels see it.
+struct GroupDev {
+    const uint8_t* w;
+    const uint8_t* w2;
+    const int32_t* ids;
+    const float* a;
+    float* out;
+    int64_t outer, inner;
+    int64_t nb01;  // bytes per row
+    int64_t nb02;  // bytes per expert
+    int num_experts, n_pairs, top_k, n, k, tiles;
+    int lg_split;  // log2 of the lanes splitting one row's blocks (rows per warp = 8 >> lg_split)
+};
+
+// What a lane streams for one work item: one row of one slab (kOne), the same row of two
+// slabs (kFused: gate and up, out = silu(g) * u), or two rows of one slab half a tile apart
+// (kPair: a tile of twice the rows for the same registers).
+constexpr int kOne = 0, kFused = 1, kPair = 2;
+
+// Rows of a work item's tile for a split lg and kind.
+__host__ __device__ __forceinline__ int item_tile_rows(int lg_split, int kind) {
+    return kWarps * (8 >> lg_split) * (kind == kPair ? 2 : 1);
+}
+
+// Host: log2 of the lanes that split one row's blocks for a given k, so that a lane's share
+// fits the kDepth-deep ring where possible (k = 2048: 2 lanes x 4 blocks; k = 4096: 4 x 4;
+// k = 768: 1 x 3).
+inline int lg_split_for(int k) {
+    const int nb = k / kQK;
+    return nb >= 4 * kDepth ? 2 : (nb >= 2 * kDepth ? 1 : 0);
+}
+
+// Host: the kernels' view of a group with the given split and item kind (row tiles of
+// item_tile_rows(lg_split, kind) rows).
+inline GroupDev group_dev(const GemvGroup& S, int lg_split, int kind = kOne) {
+    GroupDev G{};
+    G.w = S.w; G.w2 = S.w2; G.ids = S.ids; G.a = S.a; G.out = S.out;
+    G.outer = S.outer; G.inner = S.inner;
+    G.nb01 = (int64_t)(S.k / kQK) * kBlockBytes;
+    G.nb02 = (int64_t)S.n * G.nb01;
+    G.num_experts = S.num_experts; G.n_pairs = S.m * S.top_k; G.top_k = S.top_k;
+    G.n = S.n; G.k = S.k;
+    G.lg_split = lg_split;
+    const int tile_rows = item_tile_rows(lg_split, kind);
+    G.tiles = (S.n + tile_rows - 1) / tile_rows;
+    return G;
+}
+
+// Stage the activation rows of the item's pairs (token t at xs + t*tok_bytes, meta + t*(k/32)).
+// Thread f handles float4 f of the row; all loads of a pass are issued before any is used.
+// COHERENT: the rows were written by other CTAs of the same launch (read them from L2).
+template <bool COHERENT = false>
+__device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs, int nt, uint8_t* xs,
+                                           float2* meta) {
+    const int tid = threadIdx.x;
+    const int nf = G.k / 4;
+    const int nsb = G.k / 32;
+    const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
+    for (int t = 0; t < nt; ++t) {
+        const int p = s_pairs[t];
+        const float* row = G.a + (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+        for (int f0 = 0; f0 < nf; f0 += kThreads * kStageUnroll) {
+            float4 v[kStageUnroll];
+#pragma unroll
+            for (int u = 0; u < kStageUnroll; ++u) {
+                const int f = f0 + u * kThreads + tid;
+                const float4* src = reinterpret_cast<const float4*>(row) + f;
+                v[u] = f < nf ? (COHERENT ? __ldcg(src) : __ldg(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kStageUnroll; ++u) {
+                const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
+                if (f0 + u * kThreads >= nf) break;
+                stage_quad(v[u], f, f < nf, xs + t * tok_bytes, meta + t * nsb);
+            }
+        }
+    }
+}
+
+// A lane's share of one work item (a row tile of one expert's slab) and its kDepth-deep ring
+// of weight loads: H the block header, Q0/Q1 the lane's 32 code bytes of the first stream;
+// H2/R0/R1 the same of the second (kFused: the up slab's row; kPair: the row half a tile on).
+// Lane layout: lane = c | s << 2 | r << (2 + lg_split). c (0..3) picks the 64-weight group of
+// a block (code bytes 32c..32c+31 = sub-blocks 2c, 2c+1); s picks which blocks of the row the
+// lane streams (b = s, s + S, ...; S = 1 << lg_split lanes share a row's blocks); r is the row
+// within the warp (8 / S rows per warp). Splitting the row's blocks over more lanes keeps
+// each lane's share within the ring, so all of an item's weight loads are in flight at once.
+template <int KIND>
+struct ItemLane {
+    const uint8_t* wr;
+    const uint8_t* wr2;
+    int c, S, sl, row, row2, nbl;
+    bool row_ok, row2_ok;
+    uint4 H[kDepth], Q0[kDepth], Q1[kDepth], H2[kDepth], R0[kDepth], R1[kDepth];
+};
+
+// Start the item's weight stream: the first kDepth blocks of the lane's share.
+template <int KIND>
+__device__ __forceinline__ void item_issue(const GroupDev& G, int e, int tile, int lane, int warp,
+                                           ItemLane<KIND>& L) {
+    const int lgS = G.lg_split;
+    const int rpw = 8 >> lgS;  // rows per warp
+    L.c = lane & 3;
+    L.S = 1 << lgS;
+    L.sl = (lane >> 2) & (L.S - 1);
+    L.row = tile * item_tile_rows(lgS, KIND) + warp * rpw + (lane >> (2 + lgS));
+    L.row_ok = L.row < G.n;
+    L.row2 = L.row + kWarps * rpw;
+    L.row2_ok = KIND == kFused ? L.row_ok : (KIND == kPair && L.row2 < G.n);
+    const int nb = G.k / kQK;
+    L.nbl = L.sl < nb ? (nb - L.sl + L.S - 1) / L.S : 0;  // blocks b = sl + S*i of this lane
+    const uint8_t* slab = G.w + (int64_t)e * G.nb02;
+    L.wr = slab + (int64_t)(L.row_ok ? L.row : 0) * G.nb01;
+    L.wr2 = KIND == kFused ? G.w2 + (int64_t)e * G.nb02 + (int64_t)(L.row_ok ? L.row : 0) * G.nb01
+                           : (KIND == kPair ? slab + (int64_t)(L.row2_ok ? L.row2 : 0) * G.nb01 : nullptr);
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i) {
+        L.H[i] = L.Q0[i] = L.Q1[i] = L.H2[i] = L.R0[i] = L.R1[i] = make_uint4(0, 0, 0, 0);
+        if (i < L.nbl) {
+            if (L.row_ok) {
+                const uint8_t* p = L.wr + (int64_t)(L.sl + L.S * i) * kBlockBytes;
+                L.H[i] = ldg16(p); L.Q0[i] = ldg16(p + 16 + 32 * L.c); L.Q1[i] = ldg16(p + 32 + 32 * L.c);
+            }
+            if (KIND != kOne && L.row2_ok) {
+                const uint8_t* p2 = L.wr2 + (int64_t)(L.sl + L.S * i) * kBlockBytes;
+                L.H2[i] = ldg16(p2); L.R0[i] = ldg16(p2 + 16 + 32 * L.c); L.R1[i] = ldg16(p2 + 32 + 32 * L.c);
+            }
+        }
+    }
+}
+
+// The item's dot products against the nt staged tokens (pairs s_pairs[0..nt)), the reduction
+// over the lanes of a row, and the write of out[pair, row] (kFused: silu(g) * u; kPair: both
+// rows).
+template <int KIND, int TB>
+__device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND>& L, const int* s_pairs, int nt,
+                                             const uint8_t* xs, const float2* meta, int lane) {
+    constexpr bool TWO = KIND != kOne;
+    const int S = L.S, c = L.c;
+    const int nsb = G.k / 32;
+    const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
+    float acc[TB], acc2[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) { acc[t] = 0.0f; acc2[t] = 0.0f; }
+    for (int i0 = 0; i0 < L.nbl; i0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; ++j) {
+            const int i = i0 + j;
+            if (i < L.nbl) {
+                const int b = L.sl + S * i;
+                float sa, ma, sb, mb, sa2 = 0.f, ma2 = 0.f, sb2 = 0.f, mb2 = 0.f;
+                block_scales(L.H[j], c, sa, ma, sb, mb);
+                if (TWO) block_scales(L.H2[j], c, sa2, ma2, sb2, mb2);
+#pragma unroll
+                for (int t = 0; t < TB; ++t) {
+                    if (t < nt) {
+                        const uint4* xp = reinterpret_cast<const uint4*>(xs + t * tok_bytes + (4 * b + c) * kPairBytes);
+                        const float4 mt = *reinterpret_cast<const float4*>(meta + t * nsb + 8 * b + 2 * c);
+                        int Sa, Sb;
+                        dot64(L.Q0[j], L.Q1[j], xp, Sa, Sb);
+                        acc[t] += mt.x * (sa * (float)Sa - ma * mt.y) + mt.z * (sb * (float)Sb - mb * mt.w);
+                        if (TWO) {
+                            dot64(L.R0[j], L.R1[j], xp, Sa, Sb);
+                            acc2[t] += mt.x * (sa2 * (float)Sa - ma2 * mt.y) + mt.z * (sb2 * (float)Sb - mb2 * mt.w);
+                        }
+                    }
+                }
+                if (i + kDepth < L.nbl) {  // refill this slot with block b + S*kDepth
+                    if (L.row_ok) {
+                        const uint8_t* p = L.wr + (int64_t)(b + S * kDepth) * kBlockBytes;
+                        L.H[j] = ldg16(p); L.Q0[j] = ldg16(p + 16 + 32 * c); L.Q1[j] = ldg16(p + 32 + 32 * c);
+                    }
+                    if (TWO && L.row2_ok) {
+                        const uint8_t* p2 = L.wr2 + (int64_t)(b + S * kDepth) * kBlockBytes;
+                        L.H2[j] = ldg16(p2); L.R0[j] = ldg16(p2 + 16 + 32 * c); L.R1[j] = ldg16(p2 + 32 + 32 * c);
+                    }
+                }
+            }
+        }
+    }
+    // reduce over the 4*S lanes of the row (c bits, then s bits) and write
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+        for (int off = 1; off < 4 * S; off <<= 1) {
+            acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+            if (TWO) acc2[t] += __shfl_xor_sync(0xffffffffu, acc2[t], off);
+        }
+    }
+    if ((lane & (4 * S - 1)) == 0) {
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            if (t < nt) {
+                float* o = G.out + (int64_t)s_pairs[t] * G.n;
+                if (KIND == kFused) {
+                    if (L.row_ok) o[L.row] = silu(acc[t]) * acc2[t];
+                } else {
+                    if (L.row_ok) o[L.row] = acc[t];
+                    if (KIND == kPair && L.row2_ok) o[L.row2] = acc2[t];
+                }
+            }
+        }
+    }
+}
+
+// A work item of a launch whose groups were bucketed by fast_bucket: group gi, bucket rank r
+// (expert e), row tile, chunk of the bucket and its nt <= TB_ tokens.
+struct FastLoc {
+    int gi, r, e, tile, nt, chunk;
+};
+
+// Warp-wide (all 32 lanes; the result is the same in every lane). items[gi]: first item of
+// group gi. pairs != null: the chunk's pairs, in increasing order, go to pairs[0..nt).
+__device__ __forceinline__ FastLoc fast_locate(const FastGroup* F, const int* items, const GroupDev* g, int n_groups,
+                                               int TB_, int item, int* pairs) {
+    const int lane = threadIdx.x & 31;
+    int gi = 0;
+    while (gi + 1 < n_groups && item >= items[gi + 1]) ++gi;
+    const FastGroup& Fg = F[gi];
+    const int local = item - items[gi];
+    const bool mine = lane < Fg.U && Fg.start[lane] <= local && local < Fg.start[lane + 1];
+    const int r = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    const unsigned mask = Fg.mask[r];
+    const int in_e = local - Fg.start[r];
+    const int tiles = g[gi].tiles;
+    FastLoc L;
+    L.gi = gi;
+    L.r = r;
+    L.e = Fg.e[r];
+    L.chunk = in_e / tiles;  // tiles of one chunk run together (no restaging)
+    L.tile = in_e % tiles;
+    L.nt = min(TB_, __popc(mask) - L.chunk * TB_);
+    if (pairs) {  // pair `lane` is a member: its place in the bucket is the members below it
+        const int q = __popc(mask & ((1u << lane) - 1u)) - L.chunk * TB_;
+        if (((mask >> lane) & 1u) && q >= 0 && q < L.nt) pairs[q] = lane;
+    }
+    return L;
+}
+
 // Combine of rows [r0, r1) of every token (moeflux expert_forward.rs, the batched combine):
 //   y = h_mid + sum_s w[t*T+s] * out0[t*T+s] + g_t * out1[t],
 // g_t = sigmoid(shared_gate[t]) or 1 (out1 null: no shared term), slots in order. Expert
 // rows were written by other CTAs: read them from L2. A pair whose id is out of range
-// contributes nothing (its row is zero by definition). Thread tid of nthr.
+// contributes nothing (its row is zero by definition). Thread tid of nthr. All of an
+// element's loads are issued before the sums (one round trip), which run in slot order.
 __device__ __forceinline__ void combine_span(const CombineSpec& cb, const float* out0, const int32_t* ids,
                                              int num_experts, int n_pairs, int T, int H, const float* out1, int r0,
                                              int r1, int tid, int nthr) {
@@ -212,14 +451,23 @@ __device__ __forceinline__ void combine_span(const CombineSpec& cb, const float*
     for (int idx = tid; idx < m * span; idx += nthr) {
         const int t = idx / span, r = r0 + idx % span;
         const int64_t o = (int64_t)t * H + r;
-        float acc = cb.h_mid[o];
-        for (int s = 0; s < T; ++s) {
+        float v[Q4K_MAX_TOP_K], w[Q4K_MAX_TOP_K];
+        bool ok[Q4K_MAX_TOP_K];
+#pragma unroll
+        for (int s = 0; s < Q4K_MAX_TOP_K; ++s) {  // independent loads (rows of bad ids unused)
             const int p = t * T + s;
-            if (id_valid(ids ? ids[p] : 0, num_experts)) acc = fmaf(cb.weights[p], __ldcg(out0 + (int64_t)p * H + r), acc);
+            ok[s] = s < T && id_valid(ids ? ids[p] : 0, num_experts);
+            w[s] = s < T ? cb.weights[p] : 0.0f;
+            v[s] = s < T ? __ldcg(out0 + (int64_t)p * H + r) : 0.0f;
         }
+        const float sh = out1 ? __ldcg(out1 + o) : 0.0f;
+        float acc = cb.h_mid[o];
+#pragma unroll
+        for (int s = 0; s < Q4K_MAX_TOP_K; ++s)
+            if (ok[s]) acc = fmaf(w[s], v[s], acc);
         if (out1) {
             const float g = cb.shared_mode == Q4K_SHARED_SIGMOID ? 1.0f / (1.0f + expf(-cb.shared_gate[t])) : 1.0f;
-            acc = fmaf(g, __ldcg(out1 + o), acc);
+            acc = fmaf(g, sh, acc);
         }
         cb.y[o] = acc;
     }

@@ -99,6 +99,15 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);
 bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel's shared memory plan fits
 
+// The small-batch layer in one persistent launch (q4k_layer.cu): gu / dn the groups of the
+// gate|up and down halves (routed, then shared), cb the combine (counters unused). sync:
+// sync_words words of the layer workspace (layer_sync_words), any contents. Returns
+// cudaErrorNotSupported, before launching anything, where it does not apply (more than 32
+// pairs in a group, a sync area too small, rows too long for its shared memory).
+size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
+cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
+                                    uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream);
+
 int num_sms();
 
 // Record the calling thread's last error text (read back by q4k_last_error_string).

@@ -1,0 +1,369 @@
+// q4k_layer.cu -- a small-batch MoE layer in ONE persistent launch: gate|up + SwiGLU of the
+// routed experts and the shared expert, their down projections, and the combine.
+//
+// What it computes (moeflux expert_forward.rs: gate, up, SwiGLU, down, then the batched
+// combine y = h_mid + sum_s w_s * expert_out_s + g * shared_out; ferrum-kernels
+// q4_k_moe_id_gemv_batched.rs for each projection): exactly what the two-launch layer of
+// q4k_gemv.cu computes, bit for bit -- the same work items, activation staging, integer dot
+// products, lane reductions and combine order.
+//
+// Why one launch: with a few tokens the layer moves ~24 MB of weights in ~3.5 us of HBM time
+// but takes several times that in latency. A second launch re-reads and re-buckets the ids,
+// and can only start its weight stream once the first launch's CTAs leave the SMs. Here every
+// CTA buckets the pairs of both halves once, issues its down item's weight loads as soon as
+// its gate|up items are done, and starts that item's arithmetic as soon as the gate|up items of
+// its bucket chunk have landed. The combine of a row tile runs as soon as that tile's down items have.
+//
+// Hand-off between CTAs without zero-initialised state: every item, when its rows are
+// written, stores a 64-bit tag into its own flag word; a consumer waits until the flags it
+// needs hold the tag. The tag of a launch is mix(generation word), the generation word is
+// advanced to the tag at the end of the launch (by CTA 0, once every CTA has recorded that
+// it read the old value), so stale flags of earlier launches never match and nothing needs
+// clearing -- also not on the first call on fresh memory. Every wait is bounded in time;
+// one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid resident
+// at once: the grid is capped at what the SMs hold, and CTAs never wait on a CTA that is
+// itself waiting (gate|up items never wait; down items wait only on gate|up items; the
+// combine waits only on down items).
+#include <algorithm>
+#include <cstdlib>
+
+#include "q4k_gemv_common.cuh"
+#include "q4k_sm100.cuh"
+
+namespace q4k {
+
+constexpr int kLayerMaxCtas = 1024;   // start-tag words in the sync area
+constexpr int kLayerMaxPairs = 32;    // per group: one warp buckets a group
+constexpr uint32_t kLayerMaxPolls = 1u << 26;
+
+struct LayerParams {
+    GroupDev a[kMaxGroups];  // gate|up + SwiGLU: routed experts, shared expert
+    GroupDev b[kMaxGroups];  // down, same groups (the shared one on the routed row tiles)
+    int n_groups;
+    int x_off, meta_off;      // dynamic shared memory: staged rows of the larger k
+    CombineSpec cb;           // y, h_mid, weights, shared_gate, shared_mode (no counters)
+    uint64_t* gen;            // generation word
+    uint64_t* cta_tag;        // [kLayerMaxCtas] tag each CTA read
+    uint64_t* flag_a;         // [cap_a] one per gate|up item
+    uint64_t* flag_b;         // [cap_b] one per down item
+    int cap_a, cap_b;
+    int* err_flag;
+};
+
+// splitmix64's output function (Steele, Lea, Flood 2014): a bijective 64-bit mixer.
+__device__ __forceinline__ uint64_t mix64(uint64_t z) {
+    z += 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Block-wide: wait until flags[index(j)] == tag for all j < n. Each thread owns j = tid,
+// tid + kThreads, ...; it re-reads only those it has not yet seen set (up to 8 loads in flight
+// per round). True when all are set (with acquire order for what follows); false once the
+// wait has run for kWaitNs or kLayerMaxPolls rounds. Uniform over the block.
+template <class Index>
+__device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t tag, Index index) {
+    int j = threadIdx.x;
+    const uint64_t t0 = sm100::global_timer_ns();
+    for (uint32_t round = 0;; ++round) {
+        uint64_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int jj = j + u * kThreads;
+            v[u] = jj < n ? ld_relaxed_u64(flags + index(jj)) : tag;
+        }
+        int seen = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (v[u] != tag) break;
+            ++seen;
+        }
+        j += seen * kThreads;
+        if (__syncthreads_and(j >= n)) {
+            fence_acq_rel_gpu();
+            return true;
+        }
+        const bool late = round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > sm100::kWaitNs;
+        if (__syncthreads_or(late)) return false;
+        __nanosleep(32);
+    }
+}
+
+// Publish an item: its rows were written by this block's threads (the caller synchronised
+// the block); one thread stores the tag with release order at GPU scope, which makes those
+// rows visible first. It is a thread of the last warp: warp 0 locates the next item.
+__device__ __forceinline__ void publish(uint64_t* flag, uint64_t tag) {
+    if (threadIdx.x == kThreads - 32) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(tag) : "memory");
+}
+
+// TB: tokens per item; KB: kind of the down items (kOne, or kPair when one-row items would
+// outnumber the resident CTAs: a CTA then streams a tile of twice the rows with the registers
+// the fused gate|up items use).
+template <int TB, int KB>
+__global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constant__ LayerParams P) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ FastGroup s_fast[2][kMaxGroups];  // [half][group]: buckets with item offsets
+    __shared__ int s_items[2][kMaxGroups + 1];
+    __shared__ int s_bad[2][kMaxGroups];
+    __shared__ int s_pairs[kTB];
+    __shared__ int s_info[6];                    // group, rank, expert, tile, tokens, chunk
+    __shared__ int s_chunk_b[2 * kLayerMaxPairs]; // first down item of every (group, bucket, chunk)
+    __shared__ int s_n_chunks;
+    __shared__ uint64_t s_tag;
+
+    // ids, activations and the generation word may come from earlier kernels of the stream
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the generation word's load overlaps the bucketing (its value is used after it)
+    const uint64_t gen = threadIdx.x == 0 ? ld_relaxed_u64(P.gen) : 0;
+    {   // bucketing: warp w takes half w >> 1 (gate|up, down), group w & 1
+        const int half = warp >> 1, gi = warp & 1;
+        if (gi < P.n_groups) {
+            const GroupDev& G = half ? P.b[gi] : P.a[gi];
+            fast_bucket(G.ids, G.n_pairs, G.num_experts, G.tiles, TB, 0, s_fast[half][gi], &s_bad[half][gi]);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        const int half = threadIdx.x;
+        s_items[half][0] = 0;
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const FastGroup& F = s_fast[half][gi];
+            s_items[half][gi + 1] = s_items[half][gi] + F.start[F.U];
+        }
+        if (half == 0) {
+            const uint64_t tag = mix64(gen);
+            s_tag = tag;
+            st_relaxed_u64(P.cta_tag + blockIdx.x, tag);  // this CTA has read the generation
+        }
+    }
+    __syncthreads();
+    const uint64_t tag = s_tag;
+    const int na = s_items[0][P.n_groups], nb = s_items[1][P.n_groups];
+    // the caps bound any bucketing (chunks <= pairs); checked all the same
+    const bool fits = na <= P.cap_a && nb <= P.cap_b;
+    bool ok = fits;
+    const int64_t grid = gridDim.x, cta = blockIdx.x;
+    const int a0 = (int)(cta * na / grid), a1 = (int)((cta + 1) * na / grid);
+    const int b0 = (int)(cta * nb / grid), b1 = (int)((cta + 1) * nb / grid);
+    uint8_t* xs = smem + P.x_off;
+    float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
+
+    int staged = -1;  // (half, group, rank, chunk) of the staged activation rows
+    // ---- gate|up + SwiGLU items
+    for (int item = a0; ok && item < a1; ++item) {
+        if (warp == 0) {
+            const FastLoc L = fast_locate(s_fast[0], s_items[0], P.a, P.n_groups, TB, item, s_pairs);
+            if (lane == 0) { s_info[0] = L.gi; s_info[1] = L.r; s_info[2] = L.e; s_info[3] = L.tile; s_info[4] = L.nt; s_info[5] = L.chunk; }
+        }
+        __syncthreads();
+        const int gi = s_info[0], r = s_info[1], e = s_info[2], tile = s_info[3], nt = s_info[4], chunk = s_info[5];
+        const GroupDev& G = P.a[gi];
+        ItemLane<kFused> IL;
+        item_issue<kFused>(G, e, tile, lane, warp, IL);
+        const int key = ((gi * 32 + r) * 32 + chunk) * 2;
+        if (key != staged) {
+            stage_rows<false>(G, s_pairs, nt, xs, meta);
+            staged = key;
+        }
+        __syncthreads();
+        item_compute<kFused, TB>(G, IL, s_pairs, nt, xs, meta, lane);
+        __syncthreads();
+        publish(P.flag_a + item, tag);
+    }
+
+    // ---- down items: each waits for the gate|up items of its chunk (all their row tiles)
+    for (int item = b0; ok && item < b1; ++item) {
+        if (warp == 0) {
+            const FastLoc L = fast_locate(s_fast[1], s_items[1], P.b, P.n_groups, TB, item, s_pairs);
+            if (lane == 0) { s_info[0] = L.gi; s_info[1] = L.r; s_info[2] = L.e; s_info[3] = L.tile; s_info[4] = L.nt; s_info[5] = L.chunk; }
+        }
+        __syncthreads();
+        const int gi = s_info[0], r = s_info[1], e = s_info[2], tile = s_info[3], nt = s_info[4], chunk = s_info[5];
+        const GroupDev& G = P.b[gi];
+        ItemLane<KB> IL;
+        item_issue<KB>(G, e, tile, lane, warp, IL);  // weights do not depend on gate|up
+        const int key = ((gi * 32 + r) * 32 + chunk) * 2 + 1;
+        if (key != staged) {
+            const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
+            ok = wait_tags(P.flag_a, P.a[gi].tiles, tag, [first](int j) { return first + j; });
+            if (!ok) break;
+            stage_rows<true>(G, s_pairs, nt, xs, meta);
+            staged = key;
+        }
+        __syncthreads();
+        item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane);
+        __syncthreads();
+        publish(P.flag_b + item, tag);
+    }
+
+    // ---- combine: row tiles of the routed down group, each after its down items
+    if (threadIdx.x == 0) {  // down items of tile 0 of every chunk (the combine's wait list)
+        int nc = 0;
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const FastGroup& F = s_fast[1][gi];
+            for (int r = 0; r < F.U; ++r) {
+                const int chunks = (F.start[r + 1] - F.start[r]) / P.b[gi].tiles;
+                for (int c = 0; c < chunks && nc < 2 * kLayerMaxPairs; ++c)
+                    s_chunk_b[nc++] = s_items[1][gi] + F.start[r] + c * P.b[gi].tiles;
+            }
+        }
+        s_n_chunks = nc;
+    }
+    __syncthreads();
+    const int n_tiles = P.b[0].tiles;
+    const int t0 = (int)(cta * n_tiles / grid), t1 = (int)((cta + 1) * n_tiles / grid);
+    const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
+    const int tr = item_tile_rows(P.b[0].lg_split, KB);
+    for (int t = t0; ok && t < t1; ++t) {
+        ok = wait_tags(P.flag_b, s_n_chunks, tag, [t](int j) { return s_chunk_b[j] + t; });
+        if (!ok) break;
+        const GroupDev& R = P.b[0];
+        combine_span(P.cb, R.out, R.ids, R.num_experts, R.n_pairs, R.top_k, R.n, shared ? P.b[1].out : nullptr, t * tr,
+                     min(R.n, (t + 1) * tr), threadIdx.x, kThreads);
+    }
+
+    if (threadIdx.x == 0) {
+        if (!fits) raise_flag(P.err_flag, Q4K_ERR_LIMIT);
+        else if (!ok) raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+        if (blockIdx.x == 0)
+            for (int half = 0; half < 2; ++half)
+                for (int gi = 0; gi < P.n_groups; ++gi)
+                    if (s_bad[half][gi]) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
+    }
+    // ---- advance the generation once every CTA has read it
+    if (blockIdx.x == 0) {
+        const bool all = wait_tags(P.cta_tag, (int)gridDim.x, tag, [](int j) { return j; });
+        if (threadIdx.x == 0) {
+            if (all) st_relaxed_u64(P.gen, tag);
+            else raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+namespace {
+
+struct LayerPlan {
+    int lg_a[kMaxGroups], lg_b[kMaxGroups];
+    int64_t cap_a, cap_b;
+};
+
+// Row splits and the item caps for down items of kind kb (chunks <= pairs per bucket, so
+// items <= pairs x tiles).
+LayerPlan plan_of(const GemvGroup* gu, const GemvGroup* dn, int n_groups, int kb) {
+    LayerPlan L{};
+    for (int gi = 0; gi < n_groups; ++gi) {
+        L.lg_a[gi] = lg_split_for(gu[gi].k);
+        L.lg_b[gi] = gi == 0 ? lg_split_for(dn[0].k) : L.lg_b[0];
+        const int ta = item_tile_rows(L.lg_a[gi], kFused), tb = item_tile_rows(L.lg_b[gi], kb);
+        L.cap_a += (int64_t)gu[gi].m * gu[gi].top_k * ((gu[gi].n + ta - 1) / ta);
+        L.cap_b += (int64_t)dn[gi].m * dn[gi].top_k * ((dn[gi].n + tb - 1) / tb);
+    }
+    return L;
+}
+
+bool g_layer_attr_set[4][64] = {};
+
+}  // namespace
+
+size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter) {
+    if (m < 1 || (int64_t)m * top_k > kLayerMaxPairs || (shared_inter > 0 && m > kLayerMaxPairs)) return 0;
+    GemvGroup gu[2] = {}, dn[2] = {};
+    gu[0] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, top_k, inter, hidden};
+    dn[0] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, top_k, hidden, inter};
+    int ng = 1;
+    if (shared_inter > 0) {
+        gu[1] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, 1, shared_inter, hidden};
+        dn[1] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, 1, hidden, shared_inter};
+        ng = 2;
+    }
+    const LayerPlan L = plan_of(gu, dn, ng, kOne);  // one-row down items: the larger cap
+    if (L.cap_a + L.cap_b > (1 << 26)) return 0;
+    return 1 + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b;
+}
+
+cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
+                                    uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream) {
+    if (n_groups < 1 || n_groups > kMaxGroups) return cudaErrorNotSupported;
+    int64_t max_pairs = 0;
+    for (int gi = 0; gi < n_groups; ++gi) max_pairs = std::max<int64_t>(max_pairs, (int64_t)gu[gi].m * gu[gi].top_k);
+    if (max_pairs > kLayerMaxPairs) return cudaErrorNotSupported;
+    // paired down items when one-row items would outnumber the CTAs the SMs hold
+    const int64_t resident = (int64_t)num_sms() * 3;
+    const int kb = plan_of(gu, dn, n_groups, kOne).cap_b > resident ? kPair : kOne;
+    const LayerPlan L = plan_of(gu, dn, n_groups, kb);
+    if (sync == nullptr || sync_words < 1 + kLayerMaxCtas + (size_t)(L.cap_a + L.cap_b)) return cudaErrorNotSupported;
+    LayerParams P{};
+    P.n_groups = n_groups;
+    int kmax = 0, tb = 1;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        P.a[gi] = group_dev(gu[gi], L.lg_a[gi], kFused);
+        P.b[gi] = group_dev(dn[gi], L.lg_b[gi], kb);
+        kmax = std::max(kmax, std::max(gu[gi].k, dn[gi].k));
+        // tokens per item: 1 when every bucket holds about one pair (decode with distinct
+        // experts), else up to kTB -- as in the two-launch layer, so both compute alike
+        if ((int64_t)gu[gi].m * gu[gi].top_k > gu[gi].num_experts) tb = kTB;
+    }
+    const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
+    while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;
+    if (tb != 1 && tb != kTB) tb = 1;
+    P.x_off = 0;
+    P.meta_off = (int)(((int64_t)(kmax / 64) * kPairBytes * tb + 15) & ~int64_t(15));
+    const size_t smem = (size_t)P.meta_off + (size_t)(kmax / 32) * 8 * tb;
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
+    P.cb = cb;
+    P.gen = sync;
+    P.cta_tag = sync + 1;
+    P.flag_a = sync + 1 + kLayerMaxCtas;
+    P.flag_b = P.flag_a + L.cap_a;
+    P.cap_a = (int)L.cap_a;
+    P.cap_b = (int)L.cap_b;
+    P.err_flag = err_flag;
+
+    void (*kern)(LayerParams) = tb == 1 ? (kb == kPair ? layer_kernel<1, kPair> : layer_kernel<1, kOne>)
+                                        : (kb == kPair ? layer_kernel<kTB, kPair> : layer_kernel<kTB, kOne>);
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int kind = (tb == 1 ? 0 : 1) + (kb == kPair ? 2 : 0);
+    if (!g_layer_attr_set[kind][dev]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (err != cudaSuccess) return err;
+        g_layer_attr_set[kind][dev] = true;
+    }
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorNotSupported;
+    // every CTA must be resident at once (the waits): at most what the SMs hold
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    grid = std::min<int64_t>(grid, kLayerMaxCtas);
+    grid = std::min<int64_t>(grid, std::max<int64_t>(std::max(L.cap_a, L.cap_b), 1));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+}  // namespace q4k

@@ -113,3 +113,27 @@ def test_binding_raises_with_status_name():
     with pytest.raises(q4k.Q4KError) as ei:
         _lib._check(2)
     assert "Q4K_ERR_SHAPE" in str(ei.value)
+
+
+def test_layer_launch_count_single_launch_rule(monkeypatch):
+    """With Q4K_SINGLE_LAUNCH=1, layers with at most 32 routed pairs and no tensor-core bucket
+    run as one persistent launch; the rest (and every layer by default) as gate|up + down
+    (+ tensor-core kernels). The single launch's flag words widen the workspace only where it
+    can apply, whatever the switch."""
+    lib = q4k.load()
+    monkeypatch.delenv("Q4K_SINGLE_LAUNCH", raising=False)
+    assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) == 2   # default: two launches
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
+    assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) == 1   # Qwen3-like decode
+    assert lib.q4k_moe_layer_launch_count(4, 8, 128, 2048, 768, 768) == 1   # 32 pairs
+    assert lib.q4k_moe_layer_launch_count(5, 8, 128, 2048, 768, 768) == 2   # 40 pairs
+    assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 1     # Mixtral-like decode
+    assert lib.q4k_moe_layer_launch_count(16, 2, 8, 4096, 14336, 0) == 6    # tensor-core buckets
+    assert lib.q4k_moe_layer_launch_count(33, 1, 4, 256, 256, 256) == 2     # a 33-pair shared expert
+    with_flags = lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768)
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
+    assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) == 2
+    # the size does not depend on the switch (a workspace stays valid for both paths)
+    assert lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768) == with_flags
+    # the activations and expert outputs, plus the generation word and 1024 start tags
+    assert with_flags >= (8 * 768 + 768 + 8 * 2048 + 2048) * 4 + 8 * (1 + 1024)

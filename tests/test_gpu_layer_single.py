@@ -1,0 +1,205 @@
+"""GPU: the single-launch layer (one persistent kernel for gate|up + SwiGLU, down and the
+combine, routed and shared experts) against the two-launch layer and the oracle.
+
+The single launch runs the same work items with the same arithmetic as the two-launch
+layer, so the two agree bit for bit; against the oracle the per-row acceptance of
+helpers.rows_close applies. Its CTAs hand work to each other through tagged flag words at
+the start of the workspace, so the tests also run it on a workspace full of garbage, on one
+workspace call after call (and replayed from a CUDA graph), and with m changing between
+calls on one workspace.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import bit_quantized_moe_q4k_gb300 as q4k
+from bit_quantized_moe_q4k_gb300 import inputs
+from bit_quantized_moe_q4k_gb300.workloads import WORKLOADS, Workload
+
+from helpers import dev, err_flag, host, oracle_slab, rows_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+Q4K_ERR_EXPERT_ID = 6
+
+
+def _inputs(W, ids=None):
+    seed = W.seed
+    if ids is None:
+        ids = inputs.make_ids(seed, W.ids, W.m, W.top_k, W.num_experts)
+    used = sorted({int(e) for e in ids.tolist() if 0 <= e < W.num_experts})
+    wg = oracle_slab(seed, "gate", W.num_experts, W.inter, W.hidden, used)
+    wu = oracle_slab(seed, "up", W.num_experts, W.inter, W.hidden, used)
+    wd = oracle_slab(seed, "down", W.num_experts, W.hidden, W.inter, used)
+    shared = None
+    if W.shared_inter:
+        shared = (oracle_slab(seed, "sgate", 1, W.shared_inter, W.hidden),
+                  oracle_slab(seed, "sup", 1, W.shared_inter, W.hidden),
+                  oracle_slab(seed, "sdown", 1, W.hidden, W.shared_inter))
+    x = inputs.normal(seed, "h_post", (W.m, W.hidden))
+    hm = inputs.normal(seed, "h_mid", (W.m, W.hidden))
+    rw = inputs.routing_weights(seed, W.m, W.top_k)
+    gl = inputs.normal(seed, "shared_gate", (W.m,))
+    return dict(wg=wg, wu=wu, wd=wd, shared=shared, ids=np.asarray(ids, np.int32), x=x, hm=hm, rw=rw, gl=gl)
+
+
+class Layer:
+    """Device copies of one layer's inputs and a call of q4k_moe_layer_forward on them."""
+
+    def __init__(self, W, a):
+        self.W, self.a = W, a
+        self.d = {k: dev(a[k]) for k in ("wg", "wu", "wd", "ids", "x", "hm", "rw", "gl")}
+        self.sh = W.shared_inter if a["shared"] is not None else 0
+        self.s = tuple(dev(s) for s in a["shared"]) if a["shared"] is not None else (None, None, None)
+        self.y = torch.empty((W.m, W.hidden), dtype=torch.float32, device="cuda")
+
+    def ws_bytes(self):
+        W = self.W
+        return q4k.q4k_moe_layer_workspace_size(W.m, W.top_k, W.num_experts, W.hidden, W.inter, self.sh)
+
+    def run(self, ws, flag, stream=None):
+        W, d = self.W, self.d
+        q4k.q4k_moe_layer_forward(d["wg"], d["wu"], d["wd"], W.num_experts, *self.s, self.sh, W.shared_mode, d["x"],
+                                  d["hm"], d["ids"], d["rw"], d["gl"], W.m, W.top_k, W.hidden, W.inter, self.y, ws,
+                                  ws.numel(), flag, stream)
+
+    def oracle(self):
+        W, a = self.W, self.a
+        return oracle.moe_layer(a["wg"], a["wu"], a["wd"], W.num_experts, a["shared"], W.shared_inter, W.shared_mode,
+                                a["x"], a["hm"], a["ids"], a["rw"], a["gl"], W.m, W.top_k, W.hidden, W.inter)
+
+
+@pytest.fixture(autouse=True)
+def _single_launch_on(monkeypatch):
+    """The single launch is opt-in: every test here turns it on (and off for the references)."""
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
+    monkeypatch.setenv("Q4K_STREAM", "0")
+
+
+def _two_launch(layer, monkeypatch):
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
+    ws = torch.empty(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    layer.run(ws, f)
+    y = host(layer.y).copy()
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
+    return y, int(host(f)[0])
+
+
+CASES = [
+    # (hidden, inter, experts, top_k, m, ids, shared_inter, shared_mode)
+    (2048, 768, 128, 8, 1, "uniform", 768, 1),   # the Qwen3-MoE-like decode layer, full size
+    (1024, 512, 128, 8, 4, "uniform", 512, 2),   # 32 pairs: the single launch's limit
+    (512, 256, 4, 2, 3, "uniform", 256, 1),      # more pairs than experts: 4-token items
+    (256, 512, 32, 16, 2, "uniform", 256, 1),    # top_k at its limit
+    (768, 256, 4, 1, 32, "uniform", 512, 2),     # 32 tokens: a 32-pair shared expert
+    (1024, 1280, 16, 4, 2, "zipf", 0, 0),        # no shared expert; ragged row tiles
+    (4096, 1792, 8, 2, 1, "uniform", 0, 0),      # Mixtral-like shape at reduced inter
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "h{}_i{}_e{}_t{}_m{}_{}_s{}".format(*c[:7]))
+def test_single_launch_matches_two_launch_and_oracle(case, monkeypatch):
+    H, I, E, T, m, ids_kind, Is, mode = case
+    W = Workload("single", H, I, E, T, m, ids_kind, Is, mode, 1200 + sum(case[:5]))
+    assert q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is) == 1
+    layer = Layer(W, _inputs(W))
+    ref2, f2 = _two_launch(layer, monkeypatch)
+    assert f2 == 0
+    ws = torch.empty(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    layer.run(ws, f)
+    got = host(layer.y)
+    assert int(host(f)[0]) == 0
+    assert np.array_equal(got, ref2), "single launch differs from the two-launch layer"
+    ref, _ = layer.oracle()
+    rows_close(got, ref, what=f"single-launch layer {case}")
+
+
+def test_single_launch_duplicate_and_out_of_range_ids(monkeypatch):
+    """Repeated experts inside a token (buckets of several pairs) and ids outside [0, E):
+    the flag is raised and those pairs contribute nothing, as in the two-launch layer."""
+    W = Workload("dup", 512, 512, 16, 4, 3, "uniform", 256, 1, 1301)
+    ids = np.array([[3, 3, 7, -1], [7, 3, 16, 0], [5, 5, 5, 5]], np.int32).reshape(-1)
+    layer = Layer(W, _inputs(W, ids))
+    ref2, f2 = _two_launch(layer, monkeypatch)
+    assert f2 == Q4K_ERR_EXPERT_ID
+    ws = torch.empty(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    layer.run(ws, f)
+    got = host(layer.y)
+    assert int(host(f)[0]) == Q4K_ERR_EXPERT_ID
+    assert np.array_equal(got, ref2)
+    ref, bad = layer.oracle()
+    assert bad == 2
+    rows_close(got, ref, what="duplicate / out-of-range ids")
+
+
+@pytest.mark.parametrize("fill", ["random", "ones", "zeros"])
+def test_single_launch_any_workspace_contents(fill, monkeypatch):
+    """The workspace needs no initialisation: whatever it holds, the first call is right."""
+    W = Workload("garbage", 1024, 768, 32, 8, 2, "uniform", 768, 1, 1401)
+    layer = Layer(W, _inputs(W))
+    ref2, _ = _two_launch(layer, monkeypatch)
+    nbytes = layer.ws_bytes()
+    if fill == "random":
+        g = torch.Generator(device="cuda")
+        g.manual_seed(77)
+        ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=g)
+    else:
+        ws = torch.full((nbytes,), 255 if fill == "ones" else 0, dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    layer.run(ws, f)
+    assert int(host(f)[0]) == 0
+    assert np.array_equal(host(layer.y), ref2)
+
+
+def test_single_launch_chained_calls_and_graph_replays(monkeypatch):
+    """One workspace for a sequence of different layers (each call's flags must not be taken
+    for the next call's), then the sequence captured once and replayed three times."""
+    layers = []
+    for i in range(3):
+        W = Workload(f"chain{i}", 1024, 512, 64, 8, 1 + i, "uniform", 512, 1 + (i % 2), 1500 + i)
+        layers.append(Layer(W, _inputs(W)))
+    refs = [_two_launch(L, monkeypatch)[0] for L in layers]
+    nbytes = max(L.ws_bytes() for L in layers)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    for rep in range(2):
+        for L, ref in zip(layers, refs):
+            L.y.zero_()
+            L.run(ws, f)
+            assert np.array_equal(host(L.y), ref), f"eager pass {rep}"
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for L in layers:
+                L.run(ws, f, stream)
+    stream.synchronize()
+    for rep in range(3):
+        for L in layers:
+            L.y.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        for L, ref in zip(layers, refs):
+            assert np.array_equal(host(L.y), ref), f"graph replay {rep}"
+    assert int(host(f)[0]) == 0
+
+
+def test_single_launch_m_changes_on_one_workspace(monkeypatch):
+    """Calls with different token counts share one workspace (sized for the largest)."""
+    base = WORKLOADS["qwen3moe_h2048_i768_e128_t8_m1"]
+    seq = [base.with_m(1), base.with_m(4), base.with_m(2), base.with_m(1)]
+    layers = [Layer(W, _inputs(W)) for W in seq]
+    refs = [_two_launch(L, monkeypatch)[0] for L in layers]
+    ws = torch.empty(max(L.ws_bytes() for L in layers), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    for L, ref in zip(layers, refs):
+        L.run(ws, f)
+        assert np.array_equal(host(L.y), ref), f"m = {L.W.m}"
+    assert int(host(f)[0]) == 0
