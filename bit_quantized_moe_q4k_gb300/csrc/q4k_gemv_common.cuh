@@ -27,6 +27,17 @@ __device__ __forceinline__ uint4 ldg16(const uint8_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+// 16 bytes of a weight row: from global memory, or (SMEM) from a copy in shared memory.
+template <bool SMEM>
+__device__ __forceinline__ uint4 ldw16(const uint8_t* p) {
+    if (!SMEM) return ldg16(p);
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -247,35 +258,50 @@ inline GroupDev group_dev(const GemvGroup& S, int lg_split, int kind = kOne) {
     return G;
 }
 
+// Quantize one activation row of k floats into its planes (xs_row) and (delta, sum X) pairs
+// (meta_row). Thread f handles float4 f of the row; all loads of a pass are issued before any
+// is used. SRC: 0 global (read-only path), 1 global written by other CTAs of this launch (read
+// from L2), 2 shared memory.
+template <int SRC>
+__device__ __forceinline__ void stage_row(const float* row, int k, uint8_t* xs_row, float2* meta_row) {
+    const int tid = threadIdx.x;
+    const int nf = k / 4;
+    for (int f0 = 0; f0 < nf; f0 += kThreads * kStageUnroll) {
+        float4 v[kStageUnroll];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int f = f0 + u * kThreads + tid;
+            const float4* src = reinterpret_cast<const float4*>(row) + f;
+            v[u] = f < nf ? (SRC == 0 ? __ldg(src) : (SRC == 1 ? __ldcg(src) : *src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
+            if (f0 + u * kThreads >= nf) break;
+            stage_quad(v[u], f, f < nf, xs_row, meta_row);
+        }
+    }
+}
+
+// The activation row of pair p.
+__device__ __forceinline__ const float* act_row(const GroupDev& G, int p) {
+    return G.a + (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
+}
+
 // Stage the activation rows of the item's pairs (token t at xs + t*tok_bytes, meta + t*(k/32)).
-// Thread f handles float4 f of the row; all loads of a pass are issued before any is used.
 // COHERENT: the rows were written by other CTAs of the same launch (read them from L2).
 template <bool COHERENT = false>
 __device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs, int nt, uint8_t* xs,
                                            float2* meta) {
-    const int tid = threadIdx.x;
-    const int nf = G.k / 4;
-    const int nsb = G.k / 32;
     const int64_t tok_bytes = (int64_t)(G.k / 64) * kPairBytes;
-    for (int t = 0; t < nt; ++t) {
-        const int p = s_pairs[t];
-        const float* row = G.a + (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
-        for (int f0 = 0; f0 < nf; f0 += kThreads * kStageUnroll) {
-            float4 v[kStageUnroll];
-#pragma unroll
-            for (int u = 0; u < kStageUnroll; ++u) {
-                const int f = f0 + u * kThreads + tid;
-                const float4* src = reinterpret_cast<const float4*>(row) + f;
-                v[u] = f < nf ? (COHERENT ? __ldcg(src) : __ldg(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < kStageUnroll; ++u) {
-                const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
-                if (f0 + u * kThreads >= nf) break;
-                stage_quad(v[u], f, f < nf, xs + t * tok_bytes, meta + t * nsb);
-            }
-        }
-    }
+    for (int t = 0; t < nt; ++t)
+        stage_row<COHERENT ? 1 : 0>(act_row(G, s_pairs[t]), G.k, xs + t * tok_bytes, meta + t * (G.k / 32));
+}
+
+// The same from rows already copied into shared memory (token t at raw + t*k).
+__device__ __forceinline__ void stage_rows_smem(const float* raw, int nt, int k, uint8_t* xs, float2* meta) {
+    const int64_t tok_bytes = (int64_t)(k / 64) * kPairBytes;
+    for (int t = 0; t < nt; ++t) stage_row<2>(raw + (int64_t)t * k, k, xs + t * tok_bytes, meta + t * (k / 32));
 }
 
 // A lane's share of one work item (a row tile of one expert's slab) and its kDepth-deep ring
@@ -286,7 +312,7 @@ __device__ __forceinline__ void stage_rows(const GroupDev& G, const int* s_pairs
 // lane streams (b = s, s + S, ...; S = 1 << lg_split lanes share a row's blocks); r is the row
 // within the warp (8 / S rows per warp). Splitting the row's blocks over more lanes keeps
 // each lane's share within the ring, so all of an item's weight loads are in flight at once.
-template <int KIND>
+template <int KIND, bool SMEM = false>
 struct ItemLane {
     const uint8_t* wr;
     const uint8_t* wr2;
@@ -295,10 +321,13 @@ struct ItemLane {
     uint4 H[kDepth], Q0[kDepth], Q1[kDepth], H2[kDepth], R0[kDepth], R1[kDepth];
 };
 
-// Start the item's weight stream: the first kDepth blocks of the lane's share.
-template <int KIND>
+// Start the item's weight stream: the first kDepth blocks of the lane's share. SMEM: the
+// tile's rows (from its first row, consecutive, nb01 bytes each) are in shared memory at
+// smem_tile (kFused: the up slab's at smem_tile2).
+template <int KIND, bool SMEM = false>
 __device__ __forceinline__ void item_issue(const GroupDev& G, int e, int tile, int lane, int warp,
-                                           ItemLane<KIND>& L) {
+                                           ItemLane<KIND, SMEM>& L, const uint8_t* smem_tile = nullptr,
+                                           const uint8_t* smem_tile2 = nullptr) {
     const int lgS = G.lg_split;
     const int rpw = 8 >> lgS;  // rows per warp
     L.c = lane & 3;
@@ -310,9 +339,11 @@ __device__ __forceinline__ void item_issue(const GroupDev& G, int e, int tile, i
     L.row2_ok = KIND == kFused ? L.row_ok : (KIND == kPair && L.row2 < G.n);
     const int nb = G.k / kQK;
     L.nbl = L.sl < nb ? (nb - L.sl + L.S - 1) / L.S : 0;  // blocks b = sl + S*i of this lane
-    const uint8_t* slab = G.w + (int64_t)e * G.nb02;
+    const int64_t tile_off = (int64_t)tile * item_tile_rows(lgS, KIND) * G.nb01;
+    const uint8_t* slab = SMEM ? smem_tile - tile_off : G.w + (int64_t)e * G.nb02;
+    const uint8_t* slab2 = KIND != kFused ? nullptr : (SMEM ? smem_tile2 - tile_off : G.w2 + (int64_t)e * G.nb02);
     L.wr = slab + (int64_t)(L.row_ok ? L.row : 0) * G.nb01;
-    L.wr2 = KIND == kFused ? G.w2 + (int64_t)e * G.nb02 + (int64_t)(L.row_ok ? L.row : 0) * G.nb01
+    L.wr2 = KIND == kFused ? slab2 + (int64_t)(L.row_ok ? L.row : 0) * G.nb01
                            : (KIND == kPair ? slab + (int64_t)(L.row2_ok ? L.row2 : 0) * G.nb01 : nullptr);
 #pragma unroll
     for (int i = 0; i < kDepth; ++i) {
@@ -320,11 +351,13 @@ __device__ __forceinline__ void item_issue(const GroupDev& G, int e, int tile, i
         if (i < L.nbl) {
             if (L.row_ok) {
                 const uint8_t* p = L.wr + (int64_t)(L.sl + L.S * i) * kBlockBytes;
-                L.H[i] = ldg16(p); L.Q0[i] = ldg16(p + 16 + 32 * L.c); L.Q1[i] = ldg16(p + 32 + 32 * L.c);
+                L.H[i] = ldw16<SMEM>(p); L.Q0[i] = ldw16<SMEM>(p + 16 + 32 * L.c);
+                L.Q1[i] = ldw16<SMEM>(p + 32 + 32 * L.c);
             }
             if (KIND != kOne && L.row2_ok) {
                 const uint8_t* p2 = L.wr2 + (int64_t)(L.sl + L.S * i) * kBlockBytes;
-                L.H2[i] = ldg16(p2); L.R0[i] = ldg16(p2 + 16 + 32 * L.c); L.R1[i] = ldg16(p2 + 32 + 32 * L.c);
+                L.H2[i] = ldw16<SMEM>(p2); L.R0[i] = ldw16<SMEM>(p2 + 16 + 32 * L.c);
+                L.R1[i] = ldw16<SMEM>(p2 + 32 + 32 * L.c);
             }
         }
     }
@@ -333,8 +366,8 @@ __device__ __forceinline__ void item_issue(const GroupDev& G, int e, int tile, i
 // The item's dot products against the nt staged tokens (pairs s_pairs[0..nt)), the reduction
 // over the lanes of a row, and the write of out[pair, row] (kFused: silu(g) * u; kPair: both
 // rows).
-template <int KIND, int TB>
-__device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND>& L, const int* s_pairs, int nt,
+template <int KIND, int TB, bool SMEM = false>
+__device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND, SMEM>& L, const int* s_pairs, int nt,
                                              const uint8_t* xs, const float2* meta, int lane) {
     constexpr bool TWO = KIND != kOne;
     const int S = L.S, c = L.c;
@@ -369,11 +402,13 @@ __device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND>& 
                 if (i + kDepth < L.nbl) {  // refill this slot with block b + S*kDepth
                     if (L.row_ok) {
                         const uint8_t* p = L.wr + (int64_t)(b + S * kDepth) * kBlockBytes;
-                        L.H[j] = ldg16(p); L.Q0[j] = ldg16(p + 16 + 32 * c); L.Q1[j] = ldg16(p + 32 + 32 * c);
+                        L.H[j] = ldw16<SMEM>(p); L.Q0[j] = ldw16<SMEM>(p + 16 + 32 * c);
+                        L.Q1[j] = ldw16<SMEM>(p + 32 + 32 * c);
                     }
                     if (TWO && L.row2_ok) {
                         const uint8_t* p2 = L.wr2 + (int64_t)(b + S * kDepth) * kBlockBytes;
-                        L.H2[j] = ldg16(p2); L.R0[j] = ldg16(p2 + 16 + 32 * c); L.R1[j] = ldg16(p2 + 32 + 32 * c);
+                        L.H2[j] = ldw16<SMEM>(p2); L.R0[j] = ldw16<SMEM>(p2 + 16 + 32 * c);
+                        L.R1[j] = ldw16<SMEM>(p2 + 32 + 32 * c);
                     }
                 }
             }

@@ -26,6 +26,7 @@
 // combine waits only on down items).
 #include <algorithm>
 #include <cstdlib>
+#include <type_traits>
 
 #include "q4k_gemv_common.cuh"
 #include "q4k_sm100.cuh"
@@ -41,6 +42,13 @@ struct LayerParams {
     GroupDev b[kMaxGroups];  // down, same groups (the shared one on the routed row tiles)
     int n_groups;
     int x_off, meta_off;      // dynamic shared memory: staged rows of the larger k
+    int slot_off;             // ... and the copy of the CTA's first down tile (use_slot)
+    int use_slot;
+    int raw_off;              // ... and the gate|up items' raw activation rows (use_xcopy; when
+    int use_xcopy;            //     use_slot too they share the slot's space: slot_shares_raw)
+    int slot_shares_raw;
+    int atile_off, atile_bytes;  // ... and a gate|up item's weight tiles, gate then up (use_atile)
+    int use_atile;
     CombineSpec cb;           // y, h_mid, weights, shared_gate, shared_mode (no counters)
     uint64_t* gen;            // generation word
     uint64_t* cta_tag;        // [kLayerMaxCtas] tag each CTA read
@@ -121,6 +129,10 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     __shared__ int s_chunk_b[2 * kLayerMaxPairs]; // first down item of every (group, bucket, chunk)
     __shared__ int s_n_chunks;
     __shared__ uint64_t s_tag;
+    __shared__ __align__(8) uint64_t s_bar;  // the down tile's copy into shared memory
+    __shared__ __align__(8) uint64_t s_xbar; // a gate|up item's activation rows' copy
+    __shared__ __align__(8) uint64_t s_abar; // a gate|up item's weight tiles' copy
+    __shared__ int s_never;                  // (bounded waits take an abort word; never set)
 
     // ids, activations and the generation word may come from earlier kernels of the stream
     pdl_wait();
@@ -144,6 +156,11 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             s_items[half][gi + 1] = s_items[half][gi] + F.start[F.U];
         }
         if (half == 0) {
+            s_never = 0;
+            sm100::mbar_init(&s_bar, 1);
+            sm100::mbar_init(&s_xbar, 1);
+            sm100::mbar_init(&s_abar, 1);
+            sm100::fence_mbar_init();
             const uint64_t tag = mix64(gen);
             s_tag = tag;
             st_relaxed_u64(P.cta_tag + blockIdx.x, tag);  // this CTA has read the generation
@@ -160,9 +177,68 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     const int b0 = (int)(cta * nb / grid), b1 = (int)((cta + 1) * nb / grid);
     uint8_t* xs = smem + P.x_off;
     float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
+    uint8_t* slot = smem + P.slot_off;                          // the first down tile's copy
+    float* raw = reinterpret_cast<float*>(smem + P.raw_off);    // gate|up activation rows
+    uint8_t* atile = smem + P.atile_off;                        // gate|up weight tiles: gate, up
+
+    // ---- the CTA's first down tile (its rows are consecutive in the slab) is copied into
+    // shared memory with one bulk copy. When the raw activation rows share its space the copy
+    // starts after the last gate|up staging, else right away.
+    const bool slot_item = ok && P.use_slot && b0 < b1;
+    bool slot_issued = false, slot_waited = false;
+    auto issue_slot = [&]() {  // all threads
+        if (warp == 0) {
+            const FastLoc L = fast_locate(s_fast[1], s_items[1], P.b, P.n_groups, TB, b0, nullptr);
+            if (lane == 0) {
+                const GroupDev& G = P.b[L.gi];
+                const int tr = item_tile_rows(G.lg_split, KB);
+                const int r0 = L.tile * tr, rows = min(tr, G.n - r0);
+                const uint32_t bytes = (uint32_t)((int64_t)rows * G.nb01);
+                sm100::fence_proxy_async_smem();  // reads of a shared raw area come first
+                sm100::mbar_arrive_expect_tx(&s_bar, bytes);
+                sm100::bulk_g2s(slot, G.w + (int64_t)L.e * G.nb02 + (int64_t)r0 * G.nb01, bytes, &s_bar);
+            }
+        }
+        slot_issued = true;
+    };
+    if (slot_item && (a0 == a1 || !P.slot_shares_raw)) issue_slot();
+    uint32_t xphase = 0, aphase = 0;
+    bool x_pending = false, a_pending = false;  // a copy whose wait gave up
 
     int staged = -1;  // (half, group, rank, chunk) of the staged activation rows
-    // ---- gate|up + SwiGLU items
+    // ---- gate|up + SwiGLU items: activation rows and (use_atile) the weight tiles of both slabs
+    // arrive by bulk copy, which keeps them out of the SM's load queue
+    auto gate_up_item = [&](auto from_smem, int item, const GroupDev& G, int e, int tile, int nt, int key) -> bool {
+        constexpr bool SM = decltype(from_smem)::value;
+        ItemLane<kFused, SM> IL;
+        if constexpr (!SM) item_issue<kFused>(G, e, tile, lane, warp, IL);
+        if (key != staged) {
+            if (P.use_xcopy) {
+                const bool got = __syncthreads_and(sm100::mbar_wait(&s_xbar, xphase, &s_never));
+                xphase ^= 1u;
+                if (!got) { x_pending = true; return false; }
+                stage_rows_smem(raw, nt, G.k, xs, meta);
+            } else {
+                stage_rows<false>(G, s_pairs, nt, xs, meta);
+            }
+            staged = key;
+        }
+        if (slot_item && !slot_issued && item == a1 - 1) {
+            __syncthreads();  // the last reads of the raw rows
+            issue_slot();
+        }
+        if constexpr (SM) {
+            const bool got = __syncthreads_and(sm100::mbar_wait(&s_abar, aphase, &s_never));
+            aphase ^= 1u;
+            if (!got) { a_pending = true; return false; }
+            item_issue<kFused, true>(G, e, tile, lane, warp, IL, atile, atile + P.atile_bytes);
+        }
+        __syncthreads();
+        item_compute<kFused, TB>(G, IL, s_pairs, nt, xs, meta, lane);
+        __syncthreads();
+        publish(P.flag_a + item, tag);
+        return true;
+    };
     for (int item = a0; ok && item < a1; ++item) {
         if (warp == 0) {
             const FastLoc L = fast_locate(s_fast[0], s_items[0], P.a, P.n_groups, TB, item, s_pairs);
@@ -171,20 +247,45 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         __syncthreads();
         const int gi = s_info[0], r = s_info[1], e = s_info[2], tile = s_info[3], nt = s_info[4], chunk = s_info[5];
         const GroupDev& G = P.a[gi];
-        ItemLane<kFused> IL;
-        item_issue<kFused>(G, e, tile, lane, warp, IL);
         const int key = ((gi * 32 + r) * 32 + chunk) * 2;
-        if (key != staged) {
-            stage_rows<false>(G, s_pairs, nt, xs, meta);
-            staged = key;
+        if (threadIdx.x == 0) {
+            const bool xc = key != staged && P.use_xcopy;
+            if (xc || P.use_atile) sm100::fence_proxy_async_smem();  // earlier reads of these areas first
+            if (xc) {
+                sm100::mbar_arrive_expect_tx(&s_xbar, (uint32_t)(nt * G.k * 4));
+                for (int t = 0; t < nt; ++t)
+                    sm100::bulk_g2s(raw + t * G.k, act_row(G, s_pairs[t]), (uint32_t)(G.k * 4), &s_xbar);
+            }
+            if (P.use_atile) {
+                const int tra = item_tile_rows(G.lg_split, kFused);
+                const int r0 = tile * tra, rows = min(tra, G.n - r0);
+                const uint32_t bytes = (uint32_t)((int64_t)rows * G.nb01);
+                const int64_t src = (int64_t)e * G.nb02 + (int64_t)r0 * G.nb01;
+                sm100::mbar_arrive_expect_tx(&s_abar, 2 * bytes);
+                sm100::bulk_g2s(atile, G.w + src, bytes, &s_abar);
+                sm100::bulk_g2s(atile + P.atile_bytes, G.w2 + src, bytes, &s_abar);
+            }
         }
-        __syncthreads();
-        item_compute<kFused, TB>(G, IL, s_pairs, nt, xs, meta, lane);
-        __syncthreads();
-        publish(P.flag_a + item, tag);
+        ok = P.use_atile ? gate_up_item(std::true_type{}, item, G, e, tile, nt, key)
+                         : gate_up_item(std::false_type{}, item, G, e, tile, nt, key);
     }
 
     // ---- down items: each waits for the gate|up items of its chunk (all their row tiles)
+    // (the first from its shared-memory copy when there is one)
+    auto down_item = [&](auto& IL, int item, const GroupDev& G, int gi, int r, int nt, int chunk) -> bool {
+        const int key = ((gi * 32 + r) * 32 + chunk) * 2 + 1;
+        if (key != staged) {
+            const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
+            if (!wait_tags(P.flag_a, P.a[gi].tiles, tag, [first](int j) { return first + j; })) return false;
+            stage_rows<true>(G, s_pairs, nt, xs, meta);
+            staged = key;
+        }
+        __syncthreads();
+        item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane);
+        __syncthreads();
+        publish(P.flag_b + item, tag);
+        return true;
+    };
     for (int item = b0; ok && item < b1; ++item) {
         if (warp == 0) {
             const FastLoc L = fast_locate(s_fast[1], s_items[1], P.b, P.n_groups, TB, item, s_pairs);
@@ -193,21 +294,23 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         __syncthreads();
         const int gi = s_info[0], r = s_info[1], e = s_info[2], tile = s_info[3], nt = s_info[4], chunk = s_info[5];
         const GroupDev& G = P.b[gi];
-        ItemLane<KB> IL;
-        item_issue<KB>(G, e, tile, lane, warp, IL);  // weights do not depend on gate|up
-        const int key = ((gi * 32 + r) * 32 + chunk) * 2 + 1;
-        if (key != staged) {
-            const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
-            ok = wait_tags(P.flag_a, P.a[gi].tiles, tag, [first](int j) { return first + j; });
+        if (slot_issued && item == b0) {
+            ok = __syncthreads_and(sm100::mbar_wait(&s_bar, 0, &s_never));
+            slot_waited = true;
             if (!ok) break;
-            stage_rows<true>(G, s_pairs, nt, xs, meta);
-            staged = key;
+            ItemLane<KB, true> IL;
+            item_issue<KB, true>(G, e, tile, lane, warp, IL, slot);
+            ok = down_item(IL, item, G, gi, r, nt, chunk);
+        } else {
+            ItemLane<KB> IL;
+            item_issue<KB>(G, e, tile, lane, warp, IL);  // weights do not depend on gate|up
+            ok = down_item(IL, item, G, gi, r, nt, chunk);
         }
-        __syncthreads();
-        item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane);
-        __syncthreads();
-        publish(P.flag_b + item, tag);
     }
+    // a copy still in flight must land before the CTA leaves (after an abort)
+    if (slot_issued && !slot_waited) sm100::mbar_wait(&s_bar, 0, &s_never);
+    if (x_pending) sm100::mbar_wait(&s_xbar, xphase ^ 1u, &s_never);
+    if (a_pending) sm100::mbar_wait(&s_abar, aphase ^ 1u, &s_never);
 
     // ---- combine: row tiles of the routed down group, each after its down items
     if (threadIdx.x == 0) {  // down items of tile 0 of every chunk (the combine's wait list)
@@ -322,8 +425,35 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     if (tb != 1 && tb != kTB) tb = 1;
     P.x_off = 0;
     P.meta_off = (int)(((int64_t)(kmax / 64) * kPairBytes * tb + 15) & ~int64_t(15));
-    const size_t smem = (size_t)P.meta_off + (size_t)(kmax / 32) * 8 * tb;
-    if (smem > 200 * 1024) return cudaErrorNotSupported;
+    const size_t base_smem = (size_t)P.meta_off + (size_t)(kmax / 32) * 8 * tb;
+    // Shared memory beyond the staged planes, each part used where it fits:
+    //  - the gate|up item's weight tiles (gate, up) when both fit 48 KB (use_atile);
+    //  - the first down tile of the CTA when it fits 48 KB (use_slot);
+    //  - the gate|up activation rows when they fit 32 KB (use_xcopy), in the down tile's space
+    //    when there is one (its copy then starts after the last gate|up staging).
+    int64_t slot_bytes = 0, atile_bytes = 0;
+    int ka = 0;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        slot_bytes = std::max<int64_t>(slot_bytes, (int64_t)item_tile_rows(L.lg_b[gi], kb) * P.b[gi].nb01);
+        atile_bytes = std::max<int64_t>(atile_bytes, (int64_t)item_tile_rows(L.lg_a[gi], kFused) * P.a[gi].nb01);
+        ka = std::max(ka, gu[gi].k);
+    }
+    const int64_t raw_bytes = (int64_t)ka * 4 * tb;
+    P.use_slot = slot_bytes <= 48 * 1024 ? 1 : 0;
+    P.use_xcopy = raw_bytes <= 32 * 1024 ? 1 : 0;
+    P.slot_shares_raw = P.use_slot && P.use_xcopy ? 1 : 0;
+    P.atile_bytes = (int)atile_bytes;
+    auto layout = [&](bool atile) {
+        size_t off = (base_smem + 127) & ~size_t(127);
+        P.use_atile = atile ? 1 : 0;
+        P.atile_off = (int)off;
+        if (atile) off += (size_t)(2 * atile_bytes);
+        off = (off + 127) & ~size_t(127);
+        P.slot_off = P.raw_off = (int)off;
+        const int64_t region = std::max<int64_t>(P.use_slot ? slot_bytes : 0, P.use_xcopy ? raw_bytes : 0);
+        return off + (size_t)region;
+    };
+    size_t smem = layout(2 * atile_bytes <= 48 * 1024);
     P.cb = cb;
     P.gen = sync;
     P.cta_tag = sync + 1;
@@ -343,11 +473,19 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     if (!g_layer_attr_set[kind][dev]) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
         g_layer_attr_set[kind][dev] = true;
     }
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
     if (err != cudaSuccess) return err;
+    if (P.use_atile && per_sm < 3) {  // the weight tiles must not cost residency
+        smem = layout(false);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        if (err != cudaSuccess) return err;
+    }
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
     if (per_sm < 1) return cudaErrorNotSupported;
     // every CTA must be resident at once (the waits): at most what the SMs hold
     int64_t grid = (int64_t)num_sms() * per_sm;
