@@ -69,11 +69,12 @@ int tc_min_for(int routed_pairs, int num_experts) {
     return ((int64_t)routed_pairs >= 2 * (int64_t)num_experts || num_experts >= 64) ? 2 : 4;
 }
 
-// Switch (environment, read at every call): Q4K_SINGLE_LAUNCH=1 runs small layers as one
-// persistent launch where it applies (default 0: two launches, faster on GB300 at m = 1 so far).
+// Switch (environment, read at every call): Q4K_SINGLE_LAUNCH=1 runs every layer the single
+// launch can take that way, 0 none; unset (-1): the layers each of whose halves fits one round
+// of resident CTAs (there the saved launch is worth most; larger layers stream better as two).
 int single_launch_setting() {
     const char* s = getenv("Q4K_SINGLE_LAUNCH");
-    return s ? (atoi(s) != 0 ? 1 : 0) : 0;
+    return s ? (atoi(s) != 0 ? 1 : 0) : -1;
 }
 
 // Workspace sizes do not depend on the expert count: size for the smallest threshold.
@@ -100,8 +101,11 @@ bool layer_wants_tc(int m, int top_k, int num_experts, int hidden, int inter, in
 
 // The layer runs as one persistent launch (q4k_layer.cu): a few pairs, no tensor-core bucket.
 bool layer_single_launch(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
-    return single_launch_setting() && layer_sync_words(m, top_k, hidden, inter, shared_inter) > 0 &&
-           !layer_wants_tc(m, top_k, num_experts, hidden, inter, shared_inter);
+    const int setting = single_launch_setting();
+    if (setting == 0 || layer_sync_words(m, top_k, hidden, inter, shared_inter) == 0 ||
+        layer_wants_tc(m, top_k, num_experts, hidden, inter, shared_inter))
+        return false;
+    return setting == 1 || layer_one_round(m, top_k, hidden, inter, shared_inter);
 }
 
 size_t tc_scratch(int n_pairs, int k) {

@@ -105,6 +105,8 @@ bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel'
 // cudaErrorNotSupported, before launching anything, where it does not apply (more than 32
 // pairs in a group, a sync area too small, rows too long for its shared memory).
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
+// Both halves' work items fit one round of the CTAs the device's SMs hold at once.
+bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter);
 cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
                                     uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream);
 

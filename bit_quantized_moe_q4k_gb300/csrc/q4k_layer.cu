@@ -51,6 +51,9 @@ struct LayerParams {
     int use_atile;
     CombineSpec cb;           // y, h_mid, weights, shared_gate, shared_mode (no counters)
     uint64_t* gen;            // generation word
+    uint64_t* cnt_hdr;        // [2] tag for which counter set s is zero (set by the previous launch)
+    unsigned* cnt;            // [2][nt_max] per combine tile: down items done
+    int nt_max;
     uint64_t* cta_tag;        // [kLayerMaxCtas] tag each CTA read
     uint64_t* flag_a;         // [cap_a] one per gate|up item
     uint64_t* flag_b;         // [cap_b] one per down item
@@ -65,6 +68,18 @@ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return z ^ (z >> 31);
 }
+
+__device__ __forceinline__ uint64_t next_tag(uint64_t g) { return (mix64(g) & ~1ull) | ((g & 1ull) ^ 1ull); }
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// The tag of the launch after the one whose generation word is g: a hash of g whose lowest
+// bit flips at every launch (consecutive launches use different counter sets).
+__device__ __forceinline__ uint64_t next_tag(uint64_t g);
 
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     uint64_t v;
@@ -129,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     __shared__ int s_chunk_b[2 * kLayerMaxPairs]; // first down item of every (group, bucket, chunk)
     __shared__ int s_n_chunks;
     __shared__ uint64_t s_tag;
+    __shared__ int s_set, s_cnt_ok, s_per_tile, s_last;  // counter set, it is valid, items per tile
     __shared__ __align__(8) uint64_t s_bar;  // the down tile's copy into shared memory
     __shared__ __align__(8) uint64_t s_xbar; // a gate|up item's activation rows' copy
     __shared__ __align__(8) uint64_t s_abar; // a gate|up item's weight tiles' copy
@@ -140,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // the generation word's load overlaps the bucketing (its value is used after it)
     const uint64_t gen = threadIdx.x == 0 ? ld_relaxed_u64(P.gen) : 0;
+    const uint64_t hdr0 = threadIdx.x == 0 ? ld_relaxed_u64(P.cnt_hdr) : 0;
+    const uint64_t hdr1 = threadIdx.x == 0 ? ld_relaxed_u64(P.cnt_hdr + 1) : 0;
     {   // bucketing: warp w takes half w >> 1 (gate|up, down), group w & 1
         const int half = warp >> 1, gi = warp & 1;
         if (gi < P.n_groups) {
@@ -161,12 +179,21 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             sm100::mbar_init(&s_xbar, 1);
             sm100::mbar_init(&s_abar, 1);
             sm100::fence_mbar_init();
-            const uint64_t tag = mix64(gen);
+            const uint64_t tag = next_tag(gen);
             s_tag = tag;
+            // the previous launch zeroed this launch's counter set and stamped it with this tag
+            // (else: the first call on this memory, or a call of another shape) -> poll instead
+            s_set = (int)(tag & 1ull);
+            s_cnt_ok = ((tag & 1ull) ? hdr1 : hdr0) == tag && P.b[0].tiles <= P.nt_max;
             st_relaxed_u64(P.cta_tag + blockIdx.x, tag);  // this CTA has read the generation
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0) {  // down items per combine tile: every chunk has one on each tile
+        int per_tile = 0;
+        for (int gi = 0; gi < P.n_groups; ++gi) per_tile += (s_items[1][gi + 1] - s_items[1][gi]) / P.b[gi].tiles;
+        s_per_tile = per_tile;  // read after the barriers of the items below
+    }
     const uint64_t tag = s_tag;
     const int na = s_items[0][P.n_groups], nb = s_items[1][P.n_groups];
     // the caps bound any bucketing (chunks <= pairs); checked all the same
@@ -272,7 +299,14 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
 
     // ---- down items: each waits for the gate|up items of its chunk (all their row tiles)
     // (the first from its shared-memory copy when there is one)
-    auto down_item = [&](auto& IL, int item, const GroupDev& G, int gi, int r, int nt, int chunk) -> bool {
+    const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
+    const int tr = item_tile_rows(P.b[0].lg_split, KB);
+    auto combine_tile = [&](int t) {
+        const GroupDev& R = P.b[0];
+        combine_span(P.cb, R.out, R.ids, R.num_experts, R.n_pairs, R.top_k, R.n, shared ? P.b[1].out : nullptr, t * tr,
+                     min(R.n, (t + 1) * tr), threadIdx.x, kThreads);
+    };
+    auto down_item = [&](auto& IL, int item, const GroupDev& G, int gi, int r, int nt, int chunk, int tile) -> bool {
         const int key = ((gi * 32 + r) * 32 + chunk) * 2 + 1;
         if (key != staged) {
             const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
@@ -284,6 +318,15 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane);
         __syncthreads();
         publish(P.flag_b + item, tag);
+        if (s_cnt_ok) {  // the last down item of the tile combines it
+            if (threadIdx.x == kThreads - 32)
+                s_last = atom_add_acq_rel(P.cnt + s_set * P.nt_max + tile, 1u) + 1u == (unsigned)s_per_tile;
+            __syncthreads();
+            if (s_last) {
+                fence_acq_rel_gpu();
+                combine_tile(tile);
+            }
+        }
         return true;
     };
     for (int item = b0; ok && item < b1; ++item) {
@@ -300,11 +343,11 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             if (!ok) break;
             ItemLane<KB, true> IL;
             item_issue<KB, true>(G, e, tile, lane, warp, IL, slot);
-            ok = down_item(IL, item, G, gi, r, nt, chunk);
+            ok = down_item(IL, item, G, gi, r, nt, chunk, tile);
         } else {
             ItemLane<KB> IL;
             item_issue<KB>(G, e, tile, lane, warp, IL);  // weights do not depend on gate|up
-            ok = down_item(IL, item, G, gi, r, nt, chunk);
+            ok = down_item(IL, item, G, gi, r, nt, chunk, tile);
         }
     }
     // a copy still in flight must land before the CTA leaves (after an abort)
@@ -312,8 +355,9 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     if (x_pending) sm100::mbar_wait(&s_xbar, xphase ^ 1u, &s_never);
     if (a_pending) sm100::mbar_wait(&s_abar, aphase ^ 1u, &s_never);
 
-    // ---- combine: row tiles of the routed down group, each after its down items
-    if (threadIdx.x == 0) {  // down items of tile 0 of every chunk (the combine's wait list)
+    // ---- combine (without valid counters): row tiles of the routed down group, each by a
+    // designated CTA after its down items' flags
+    if (threadIdx.x == 0 && !s_cnt_ok) {  // down items of tile 0 of every chunk (the combine's wait list)
         int nc = 0;
         for (int gi = 0; gi < P.n_groups; ++gi) {
             const FastGroup& F = s_fast[1][gi];
@@ -328,14 +372,10 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     __syncthreads();
     const int n_tiles = P.b[0].tiles;
     const int t0 = (int)(cta * n_tiles / grid), t1 = (int)((cta + 1) * n_tiles / grid);
-    const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
-    const int tr = item_tile_rows(P.b[0].lg_split, KB);
-    for (int t = t0; ok && t < t1; ++t) {
+    for (int t = t0; ok && !s_cnt_ok && t < t1; ++t) {
         ok = wait_tags(P.flag_b, s_n_chunks, tag, [t](int j) { return s_chunk_b[j] + t; });
         if (!ok) break;
-        const GroupDev& R = P.b[0];
-        combine_span(P.cb, R.out, R.ids, R.num_experts, R.n_pairs, R.top_k, R.n, shared ? P.b[1].out : nullptr, t * tr,
-                     min(R.n, (t + 1) * tr), threadIdx.x, kThreads);
+        combine_tile(t);
     }
 
     if (threadIdx.x == 0) {
@@ -346,12 +386,23 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
                 for (int gi = 0; gi < P.n_groups; ++gi)
                     if (s_bad[half][gi]) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
     }
-    // ---- advance the generation once every CTA has read it
+    // ---- advance the generation once every CTA has read it, and prepare the next launch's
+    // counter set (the one this launch does not use): zero it, then stamp it with its tag
     if (blockIdx.x == 0) {
         const bool all = wait_tags(P.cta_tag, (int)gridDim.x, tag, [](int j) { return j; });
+        if (all) {
+            unsigned* next = P.cnt + (s_set ^ 1) * P.nt_max;
+            for (int i = threadIdx.x; i < P.nt_max; i += kThreads) next[i] = 0u;
+            __syncthreads();
+        }
         if (threadIdx.x == 0) {
-            if (all) st_relaxed_u64(P.gen, tag);
-            else raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+            if (all) {
+                __threadfence();
+                st_relaxed_u64(P.cnt_hdr + (s_set ^ 1), next_tag(tag));
+                st_relaxed_u64(P.gen, tag);
+            } else {
+                raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+            }
         }
     }
 }
@@ -380,6 +431,13 @@ LayerPlan plan_of(const GemvGroup* gu, const GemvGroup* dn, int n_groups, int kb
 
 bool g_layer_attr_set[4][64] = {};
 
+// Combine tiles of the smallest row tile (8 rows), whatever the down items' kind.
+int combine_tiles_max(int hidden) { return (hidden + 7) / 8; }
+
+// Words before the start tags: the generation word, two counter-set headers and two sets of
+// u32 counters. They depend on hidden only, so they stay in place when m changes.
+size_t sync_head_words(int hidden) { return 3 + (size_t)(combine_tiles_max(hidden) + 1) / 2 * 2; }
+
 }  // namespace
 
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter) {
@@ -395,7 +453,23 @@ size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inte
     }
     const LayerPlan L = plan_of(gu, dn, ng, kOne);  // one-row down items: the larger cap
     if (L.cap_a + L.cap_b > (1 << 26)) return 0;
-    return 1 + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b;
+    return sync_head_words(hidden) + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b;
+}
+
+bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter) {
+    if (m < 1 || top_k < 1) return false;
+    GemvGroup gu[2] = {}, dn[2] = {};
+    gu[0] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, top_k, inter, hidden};
+    dn[0] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, top_k, hidden, inter};
+    int ng = 1;
+    if (shared_inter > 0) {
+        gu[1] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, 1, shared_inter, hidden};
+        dn[1] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, 1, hidden, shared_inter};
+        ng = 2;
+    }
+    const int64_t resident = (int64_t)num_sms() * 3;
+    const LayerPlan L = plan_of(gu, dn, ng, kPair);
+    return L.cap_a <= resident && L.cap_b <= resident;
 }
 
 cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
@@ -408,7 +482,8 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     const int64_t resident = (int64_t)num_sms() * 3;
     const int kb = plan_of(gu, dn, n_groups, kOne).cap_b > resident ? kPair : kOne;
     const LayerPlan L = plan_of(gu, dn, n_groups, kb);
-    if (sync == nullptr || sync_words < 1 + kLayerMaxCtas + (size_t)(L.cap_a + L.cap_b)) return cudaErrorNotSupported;
+    const size_t head = sync_head_words(dn[0].n);
+    if (sync == nullptr || sync_words < head + kLayerMaxCtas + (size_t)(L.cap_a + L.cap_b)) return cudaErrorNotSupported;
     LayerParams P{};
     P.n_groups = n_groups;
     int kmax = 0, tb = 1;
@@ -456,8 +531,11 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     size_t smem = layout(2 * atile_bytes <= 48 * 1024);
     P.cb = cb;
     P.gen = sync;
-    P.cta_tag = sync + 1;
-    P.flag_a = sync + 1 + kLayerMaxCtas;
+    P.cnt_hdr = sync + 1;
+    P.cnt = reinterpret_cast<unsigned*>(sync + 3);
+    P.nt_max = combine_tiles_max(dn[0].n);
+    P.cta_tag = sync + head;
+    P.flag_a = P.cta_tag + kLayerMaxCtas;
     P.flag_b = P.flag_a + L.cap_a;
     P.cap_a = (int)L.cap_a;
     P.cap_b = (int)L.cap_b;

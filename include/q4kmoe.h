@@ -183,14 +183,18 @@ int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const 
  * Shared slabs (one expert, intermediate shared_inter) are NULL and shared_inter 0
  * when shared_mode is NONE. All device pointers; d_y [m, hidden] may alias d_h_mid.
  * Contains no host synchronisation, so it can be captured in a CUDA graph.
- * Launches: a gate|up launch and a down launch with the combine fused into it (+ the
- * tensor-core kernels of a half that uses them). With the environment variable
- * Q4K_SINGLE_LAUNCH=1, a layer with at most 32 routed pairs (m*top_k <= 32) and no
- * bucket large enough for the tensor-core path is instead ONE persistent launch whose
- * CTAs hand work to each other through tagged flag words at the start of the
- * workspace (same results bit for bit). The workspace needs no initialisation: the flag
- * words of a launch carry a tag derived from a generation word that the launch
- * advances, so leftovers of earlier calls (or of anything else) never match.
+ * Launches: a layer with at most 32 routed pairs (m*top_k <= 32), no bucket large
+ * enough for the tensor-core path, and halves whose work items each fit one round of the
+ * CTAs the device holds at once (a decode layer) is ONE persistent launch whose CTAs
+ * hand work to each other through tagged flag words and counters at the start of the
+ * workspace; any other layer is a gate|up launch and a down launch with the combine fused
+ * into it (+ the tensor-core kernels of a half that uses them). Both give the same
+ * results bit for bit. The environment variable Q4K_SINGLE_LAUNCH=1 takes every layer the
+ * single launch can run (the first condition alone) that way, =0 none. The workspace
+ * needs no initialisation: the flag words of a launch carry a tag derived from a
+ * generation word that the launch advances, so leftovers of earlier calls (or of
+ * anything else) never match; its counters are used only when the previous call on the
+ * workspace zeroed them and stamped them with this call's tag (else the call polls flags).
  * Concurrent calls on one workspace race, as with any scratch. After a device error
  * flag Q4K_ERR_TIMEOUT (a bounded wait gave up: the grid could not be resident at
  * once, e.g. under an SM partition) zero the workspace before its next use.
@@ -229,8 +233,8 @@ int q4k_moe_layer_down(const void* d_w_down, int num_experts, const void* d_ws_d
 size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int shared_inter, int k_shared);
 
 /* Number of kernels one q4k_moe_layer_forward call with its full workspace launches for these
- * sizes (1 for the single-launch layer; else 2, plus 2 per half that takes the tensor-core
- * path). 0 on invalid sizes. */
+ * sizes on the current device (1 for the single-launch layer; else 2, plus 2 per half that
+ * takes the tensor-core path). 0 on invalid sizes. */
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
 /* ---------------------------------------------------------------------------------

@@ -116,13 +116,12 @@ def test_binding_raises_with_status_name():
 
 
 def test_layer_launch_count_single_launch_rule(monkeypatch):
-    """With Q4K_SINGLE_LAUNCH=1, layers with at most 32 routed pairs and no tensor-core bucket
-    run as one persistent launch; the rest (and every layer by default) as gate|up + down
-    (+ tensor-core kernels). The single launch's flag words widen the workspace only where it
-    can apply, whatever the switch."""
+    """Q4K_SINGLE_LAUNCH=1: layers with at most 32 routed pairs and no tensor-core bucket run as
+    one persistent launch; =0: every layer as gate|up + down (+ tensor-core kernels). Unset: the
+    single launch for layers each of whose halves fits one round of resident CTAs (a property of
+    the device; a layer of thousands of row tiles never qualifies). The flag words widen the
+    workspace wherever the single launch can apply, whatever the switch."""
     lib = q4k.load()
-    monkeypatch.delenv("Q4K_SINGLE_LAUNCH", raising=False)
-    assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) == 2   # default: two launches
     monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
     assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) == 1   # Qwen3-like decode
     assert lib.q4k_moe_layer_launch_count(4, 8, 128, 2048, 768, 768) == 1   # 32 pairs
@@ -135,5 +134,8 @@ def test_layer_launch_count_single_launch_rule(monkeypatch):
     assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) == 2
     # the size does not depend on the switch (a workspace stays valid for both paths)
     assert lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768) == with_flags
+    monkeypatch.delenv("Q4K_SINGLE_LAUNCH", raising=False)
+    assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) in (1, 2)
+    assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 2     # 3584 gate|up row tiles
     # the activations and expert outputs, plus the generation word and 1024 start tags
     assert with_flags >= (8 * 768 + 768 + 8 * 2048 + 2048) * 4 + 8 * (1 + 1024)
