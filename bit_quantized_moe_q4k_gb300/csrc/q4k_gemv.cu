@@ -290,9 +290,9 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         if (e != cudaSuccess) return e;
         pdl = false;  // the tensor-core kernels precede this launch in the stream
     }
-    if (stream_setting() && !pdl_wait_first) {
+    if (stream_setting()) {
         const cudaError_t se = launch_idgemv_stream(groups, n_groups, fused_swiglu, pdl, err_flag, stream, tc_min,
-                                                    combine, zero, n_zero);
+                                                    combine, zero, n_zero, pdl_wait_first);
         if (se != cudaErrorNotSupported) return se;
     }
     GemvParams P{};

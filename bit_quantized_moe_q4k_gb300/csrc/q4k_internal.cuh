@@ -91,9 +91,10 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
 int idgemv_tile_rows(int k);
 // The bulk-copy id-GEMV for small batches (q4k_stream.cu): cudaErrorNotSupported, before
 // launching anything, when a group holds more than 32 pairs or its rows do not fit.
+// pdl_wait_first as for launch_idgemv.
 cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                                  cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
-                                 int n_zero);
+                                 int n_zero, bool pdl_wait_first = false);
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
                       int* err_flag, cudaStream_t stream);
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);

@@ -66,6 +66,7 @@ struct SParams {
     int n_zero;
     int stage_bytes;        // bytes per stage (both slabs)
     int xs_off, meta_off;   // staged activation planes and (delta, sumX) pairs
+    int wait_first;         // wait for the previous kernel before reading anything (first launch of a layer)
 };
 
 struct SItem {
@@ -139,6 +140,9 @@ idgemv_stream_kernel(const __grid_constant__ SParams P) {
     __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the ids and activations may come from the previous kernel: with wait_first, wait, then
+    // let the next launch (which reads the ids before its own wait) start
+    if (P.wait_first) pdl_wait();
     pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < kSStages; ++s) mbar_init(&bar_full[s], 1);
@@ -149,7 +153,8 @@ idgemv_stream_kernel(const __grid_constant__ SParams P) {
         for (int i = tid; i < P.n_zero; i += kSThreads) P.zero[i] = 0u;
     // the activation rows go towards L2 now, ahead of the weight copies in the memory queues
     // (only without a previous kernel still writing them)
-    if (!P.pdl && blockIdx.x < 4 && tid < P.n_groups && P.g[tid].a_bytes > 0) {
+    const bool acts_ready = !P.pdl || P.wait_first;
+    if (acts_ready && blockIdx.x < 4 && tid < P.n_groups && P.g[tid].a_bytes > 0) {
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(P.g[tid].a) & ~uintptr_t(15);
         const uintptr_t a1 = (reinterpret_cast<uintptr_t>(P.g[tid].a) + (uintptr_t)P.g[tid].a_bytes + 15) & ~uintptr_t(15);
         bulk_prefetch_l2(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
@@ -187,7 +192,7 @@ idgemv_stream_kernel(const __grid_constant__ SParams P) {
     // The first item's activation loads leave before the weight copies (responses come back
     // in about the order of the requests), unless the previous kernel may still write them.
     float4 xpre[kStageUnroll];
-    const bool have_pre = !P.pdl && ib < ie;
+    const bool have_pre = acts_ready && ib < ie;
     if (have_pre) {
         const SItem it0 = s_locate(s_fast, s_items, P.n_groups, ib);
         const SGroup& G0 = P.g[it0.gi];
@@ -398,13 +403,14 @@ int pow2_at_least(int v) {
 
 cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                                  cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
-                                 int n_zero) {
+                                 int n_zero, bool pdl_wait_first) {
     if (n_groups < 1 || n_groups > kMaxGroups) return cudaErrorNotSupported;
     SParams P{};
     P.n_groups = n_groups;
     P.err_flag = err_flag;
     P.tc_min = tc_min;
     P.pdl = pdl ? 1 : 0;
+    P.wait_first = (pdl && pdl_wait_first) ? 1 : 0;
     P.zero = zero;
     P.n_zero = zero ? n_zero : 0;
     if (combine) {

@@ -203,3 +203,19 @@ def test_single_launch_m_changes_on_one_workspace(monkeypatch):
         L.run(ws, f)
         assert np.array_equal(host(L.y), ref), f"m = {L.W.m}"
     assert int(host(f)[0]) == 0
+
+
+def test_two_launch_layer_with_bulk_copy_kernel_matches_oracle(monkeypatch):
+    """The two-launch layer on the opt-in bulk-copy id-GEMV (Q4K_STREAM=1), whose gate|up
+    launch waits for the previous kernel before reading the ids (the first launch of a layer)."""
+    W = Workload("stream", 1024, 512, 16, 4, 3, "uniform", 512, 1, 1601)
+    layer = Layer(W, _inputs(W))
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
+    monkeypatch.setenv("Q4K_STREAM", "1")
+    ws = torch.empty(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    layer.run(ws, f)
+    got = host(layer.y)
+    assert int(host(f)[0]) == 0
+    ref, _ = layer.oracle()
+    rows_close(got, ref, what="two-launch layer, bulk-copy kernel")
