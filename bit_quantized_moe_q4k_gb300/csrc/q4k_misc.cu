@@ -280,13 +280,27 @@ cudaError_t launch_stream_ceiling(const void* src, uint64_t bytes, uint32_t* sin
 // Gather of a few small buffers into device memory in one launch (the host-buffer layer call
 // uses it to read its page-locked inputs straight from host memory: one launch instead of one
 // copy-engine transfer per buffer). Sizes are multiples of 4 bytes; 4-byte words.
+// A thread loads its word of every buffer before storing any, so the reads of host memory
+// cost one round trip. The next kernel (the layer, launched as a programmatic dependent, which
+// waits for this kernel before reading its results) may start its prologue right away; this
+// launch itself is ordinary, since it overwrites buffers the previous kernel reads.
 __global__ void __launch_bounds__(256) gather_kernel(const GatherSpec G) {
-    for (int i = 0; i < G.n; ++i) {
-        const uint32_t words = G.bytes[i] / 4;
-        const uint32_t* src = static_cast<const uint32_t*>(G.src[i]);
-        uint32_t* dst = static_cast<uint32_t*>(G.dst[i]);
-        for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < words; w += gridDim.x * blockDim.x)
-            dst[w] = src[w];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x;; w += stride) {
+        uint32_t v[5];
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            if (i < G.n && w < G.bytes[i] / 4) {
+                v[i] = static_cast<const uint32_t*>(G.src[i])[w];
+                any = true;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 5; ++i)
+            if (i < G.n && w < G.bytes[i] / 4) static_cast<uint32_t*>(G.dst[i])[w] = v[i];
+        if (!any) break;
     }
 }
 
