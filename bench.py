@@ -441,11 +441,22 @@ KERNEL_SOURCES = {  # the files whose text a kernel's counters depend on
 }
 
 
-def source_sha(kernel: str) -> str:
+def code_text(text: str) -> str:
+    """The source without blank lines and whole-line comments (code lines, trailing comments
+    included, are kept): an edit of comments alone does not invalidate a capture."""
+    return "\n".join(ln for ln in text.splitlines() if ln.strip() and not ln.strip().startswith("//"))
+
+
+def source_sha(kernel: str, read=None) -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "bit_quantized_moe_q4k_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        path = os.path.join("bit_quantized_moe_q4k_gb300", "csrc", name)
+        if read is None:
+            with open(os.path.join(ROOT, path)) as f:
+                text = f.read()
+        else:
+            text = read(path)
+        h.update(code_text(text).encode())
     return h.hexdigest()[:16]
 
 

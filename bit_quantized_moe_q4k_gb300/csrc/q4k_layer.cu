@@ -9,20 +9,24 @@
 //
 // Why one launch: with a few tokens the layer moves ~24 MB of weights in ~3.5 us of HBM time
 // but takes several times that in latency. A second launch re-reads and re-buckets the ids,
-// and can only start its weight stream once the first launch's CTAs leave the SMs. Here every
-// CTA buckets the pairs of both halves once, issues its down item's weight loads as soon as
-// its gate|up items are done, and starts that item's arithmetic as soon as the gate|up items of
-// its bucket chunk have landed. The combine of a row tile runs as soon as that tile's down items have.
+// and can only start once the first launch's CTAs leave the SMs. Here every CTA buckets the
+// pairs of both halves once; moves its gate|up item's activation row and weight tiles, and
+// then its down tile, into shared memory with bulk copies (outside the SM's load queue);
+// starts its down item as soon as the gate|up items of that bucket chunk have landed; and the
+// last down item of a row tile combines that tile.
 //
 // Hand-off between CTAs without zero-initialised state: every item, when its rows are
 // written, stores a 64-bit tag into its own flag word; a consumer waits until the flags it
-// needs hold the tag. The tag of a launch is mix(generation word), the generation word is
-// advanced to the tag at the end of the launch (by CTA 0, once every CTA has recorded that
-// it read the old value), so stale flags of earlier launches never match and nothing needs
-// clearing -- also not on the first call on fresh memory. Every wait is bounded in time;
-// one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid resident
-// at once: the grid is capped at what the SMs hold, and CTAs never wait on a CTA that is
-// itself waiting (gate|up items never wait; down items wait only on gate|up items; the
+// needs hold the tag. The tag of a launch is next_tag(generation word); the generation word is
+// advanced to the tag at the end of the launch (by CTA 0, once every CTA has recorded that it
+// read the old value), so stale flags of earlier launches never match and nothing needs
+// clearing -- also not on the first call on fresh memory. The combine's per-tile counters come
+// in two sets used by alternate launches: a launch zeroes the set the next one uses and stamps
+// its header with that launch's tag; a launch whose set is not stamped so (the first on this
+// memory, a call of another shape) polls the down items' flags instead. Every wait is bounded
+// in time; one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid
+// resident at once: the grid is capped at what the SMs hold, and CTAs never wait on a CTA that
+// is itself waiting (gate|up items never wait; down items wait only on gate|up items; the
 // combine waits only on down items).
 #include <algorithm>
 #include <cstdlib>
