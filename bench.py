@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ceiling", action="store_true", help="skip the loads-only ceiling of the step's bytes")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--layers", type=int, default=0, help="size of the layer rotation (default: > 3x L2 touched)")
     ap.add_argument("--separate-inputs", action="store_true",
@@ -361,6 +362,38 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     if dist:
         total_ms = max_over_ranks(total_ms, dev)
 
+    # the loads-only ceiling of the same burst: the layer's algorithmic bytes streamed by a
+    # kernel that only loads them (q4k_stream_ceiling), from windows of a buffer larger than
+    # L2 taken in turn so every launch reads from HBM; K launches in a graph
+    ceiling = None
+    if not args.no_ceiling:
+        burst = int(layer_b) // 4096 * 4096
+        # (a burst of twice the L2 or more streams from HBM on its own)
+        n_win = 1 if burst >= 2 * L2_BYTES else max(4, -(-3 * L2_BYTES // burst))
+        big = torch.empty(burst * n_win, dtype=torch.uint8, device=dev)
+        big.fill_(1)
+        sink = torch.empty(q4k.q4k_stream_ceiling_sink_words(), dtype=torch.int32, device=dev)
+        g_ceil = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                q4k.q4k_stream_ceiling(big[(i % n_win) * burst:], burst, sink, stream)
+            with torch.cuda.graph(g_ceil, stream=stream, capture_error_mode="thread_local"):
+                for i in range(K):
+                    q4k.q4k_stream_ceiling(big[(i % n_win) * burst:], burst, sink, stream)
+            g_ceil.replay()
+        stream.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        with torch.cuda.stream(stream):
+            g_ceil.replay()
+        c1.record(stream)
+        c1.synchronize()
+        ceil_us = c0.elapsed_time(c1) / K * 1e3
+        ceiling = {"kernel": "stream_ceiling_kernel (loads only, same bytes as one layer step)",
+                   "bytes_per_launch": burst, "avg_launch_us": ceil_us,
+                   "gbs": burst / (ceil_us * 1e-6) / 1e9}
+        del big
+
     # end to end through the host-buffer C-ABI call: per step H2D inputs, the layer, D2H output
     e2e = None
     if not args.no_e2e:
@@ -420,7 +453,7 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
 
     # kernels per step: gate|up and down (+ prep and GEMM of the tensor-core path when a half uses it)
     launches_per_step = q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is)
-    return {"single": single, "launches_per_step": launches_per_step, "total_ms": total_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes, "layer_bytes": layer_b, "clocks": clk,
+    return {"ceiling": ceiling, "single": single, "launches_per_step": launches_per_step, "total_ms": total_ms, "gu_ms": gu_ms, "gu_bytes": gu_bytes, "layer_bytes": layer_b, "clocks": clk,
             "n_layers": n_layers, "e2e": e2e, "per_layer_touched": per_layer_touched,
             "experts_touched": float(np.mean([p["experts_touched"] for p in per]))}
 
@@ -542,6 +575,7 @@ def main():
                     "h_mid/ids/routing weights as slices of stacked tensors"),
         "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / peak,
         "experts_touched_per_step": r["experts_touched"],
+        "ceiling": r["ceiling"],
         "roofline": {"kernel": kdesc, "bound": "hbm",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "bytes_per_launch": kbytes, "avg_launch_us": gu_ms * 1e3,
