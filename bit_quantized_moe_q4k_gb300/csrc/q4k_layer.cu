@@ -75,6 +75,13 @@ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
 
 __device__ __forceinline__ uint64_t next_tag(uint64_t g) { return (mix64(g) & ~1ull) | ((g & 1ull) ^ 1ull); }
 
+// A counter set's header: the tag of the launch it was prepared for, bound to the sets' size
+// (which moves with hidden), so a call of another shape never takes words laid out for
+// another as its zeroed counters.
+__device__ __forceinline__ uint64_t set_stamp(uint64_t tag, int nt_max) {
+    return tag ^ ((uint64_t)(unsigned)nt_max * 0x9E3779B97F4A7C15ull);
+}
+
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
     unsigned old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             // the previous launch zeroed this launch's counter set and stamped it with this tag
             // (else: the first call on this memory, or a call of another shape) -> poll instead
             s_set = (int)(tag & 1ull);
-            s_cnt_ok = ((tag & 1ull) ? hdr1 : hdr0) == tag && P.b[0].tiles <= P.nt_max;
+            s_cnt_ok = ((tag & 1ull) ? hdr1 : hdr0) == set_stamp(tag, P.nt_max) && P.b[0].tiles <= P.nt_max;
             st_relaxed_u64(P.cta_tag + blockIdx.x, tag);  // this CTA has read the generation
         }
     }
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         if (threadIdx.x == 0) {
             if (all) {
                 __threadfence();
-                st_relaxed_u64(P.cnt_hdr + (s_set ^ 1), next_tag(tag));
+                st_relaxed_u64(P.cnt_hdr + (s_set ^ 1), set_stamp(next_tag(tag), P.nt_max));
                 st_relaxed_u64(P.gen, tag);
             } else {
                 raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);

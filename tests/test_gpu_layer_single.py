@@ -219,3 +219,20 @@ def test_two_launch_layer_with_bulk_copy_kernel_matches_oracle(monkeypatch):
     assert int(host(f)[0]) == 0
     ref, _ = layer.oracle()
     rows_close(got, ref, what="two-launch layer, bulk-copy kernel")
+
+
+def test_single_launch_hidden_changes_on_one_workspace(monkeypatch):
+    """Layers of different hidden sizes share one workspace: the sync area's layout moves with
+    hidden, so a call finds the previous call's counters and flags at other offsets (it falls
+    back to polling, then prepares its counters for the next call of its own shape)."""
+    seq = [Workload("h1", 1024, 512, 64, 8, 1, "uniform", 512, 1, 1701),
+           Workload("h2", 2048, 512, 64, 8, 1, "uniform", 512, 2, 1702)]
+    layers = [Layer(W, _inputs(W)) for W in seq]
+    refs = [_two_launch(L, monkeypatch)[0] for L in layers]
+    ws = torch.empty(max(L.ws_bytes() for L in layers), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    for L, ref in [(layers[i % 2], refs[i % 2]) for i in range(5)]:
+        L.y.zero_()
+        L.run(ws, f)
+        assert np.array_equal(host(L.y), ref), L.W.name
+    assert int(host(f)[0]) == 0
