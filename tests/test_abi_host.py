@@ -139,3 +139,16 @@ def test_layer_launch_count_single_launch_rule(monkeypatch):
     assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 2     # 3584 gate|up row tiles
     # the activations and expert outputs, plus the generation word and 1024 start tags
     assert with_flags >= (8 * 768 + 768 + 8 * 2048 + 2048) * 4 + 8 * (1 + 1024)
+
+
+def test_bench_traffic_record_keys_on_code_lines():
+    """The committed DRAM traffic of a kernel is matched to its source by a hash of the code
+    lines: whole-line comments and blank lines do not change it, code does."""
+    import bench
+    src = "int a = 1;  // keep\n\n// a comment\n    // another\nint b = 2;\n"
+    assert bench.code_text(src) == bench.code_text("// new header\n" + src + "\n\n")
+    assert bench.code_text(src) != bench.code_text(src.replace("int b = 2;", "int b = 3;"))
+    assert bench.code_text(src) != bench.code_text(src.replace("// keep", "// changed"))  # code line
+    sha = bench.source_sha("layer_kernel")
+    assert len(sha) == 16 and sha == bench.source_sha("layer_kernel", read=lambda p: open(
+        os.path.join(ROOT, p)).read())

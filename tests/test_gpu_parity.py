@@ -24,8 +24,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(params=["bulk_copy", "bucketed"])
 def kernel_path(request, monkeypatch):
-    """Small batches run on the bulk-copy kernel by default; Q4K_STREAM=0 sends them to the
-    bucketed kernel, so both are compared with the oracle."""
+    """Small batches run on the bucketed kernel by default; Q4K_STREAM=1 sends them to the
+    opt-in bulk-copy kernel, so both are compared with the oracle."""
     monkeypatch.setenv("Q4K_STREAM", "1" if request.param == "bulk_copy" else "0")
     return request.param
 
