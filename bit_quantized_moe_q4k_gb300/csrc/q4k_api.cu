@@ -119,8 +119,12 @@ size_t ffn_scratch(int m, int top_k, int hidden, int inter) {
            tc_scratch(m * top_k, inter);
 }
 
+// Down rows at least this long are quantized once before the down launch (launch_prestage)
+// rather than in every CTA that takes one of their items.
+constexpr int kPrestageMinK = 4096;
+
 struct LayerScratch {
-    size_t sync, act, act_shared, eout, shared_out, tc_gu, tc_dn, counters, total;
+    size_t sync, act, act_shared, eout, shared_out, tc_gu, tc_dn, counters, pre, pre_shared, total;
     size_t n_sync_words;  // 0: these shapes always take the two-launch layer
     int n_counters;
 };
@@ -141,6 +145,9 @@ LayerScratch layer_scratch(int m, int top_k, int hidden, int inter, int shared_i
     // combine counters of the down launch: one per row tile of hidden, for any tiling
     s.n_counters = hidden;
     s.counters = off;   off += align_up((size_t)s.n_counters * sizeof(unsigned));
+    // staged down rows (routed pairs, then the shared expert's tokens) where they are long
+    s.pre = off;        off += inter >= kPrestageMinK ? align_up((size_t)prestage_bytes(m * top_k, inter)) : 0;
+    s.pre_shared = off; off += shared_inter >= kPrestageMinK ? align_up((size_t)prestage_bytes(m, shared_inter)) : 0;
     s.total = off;
     return s;
 }
@@ -216,10 +223,26 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
 int run_down(const void* w_down, int num_experts, const float* act, const int32_t* ids, int m, int top_k,
              int hidden, int inter, float* expert_out, const void* ws_down, int shared_inter, const float* act_shared,
              float* shared_out, int* err_flag, cudaStream_t stream, uint8_t* tc_ws = nullptr,
-             const CombineSpec* combine = nullptr) {
+             const CombineSpec* combine = nullptr, uint8_t* pre_ws = nullptr, uint8_t* pre_shared_ws = nullptr) {
     GemvGroup g[2] = {};
     const int ng = down_groups(w_down, num_experts, act, ids, m, top_k, hidden, inter, expert_out, ws_down,
                                shared_inter, act_shared, shared_out, g);
+    // long rows: quantize each once (a launch between gate|up and down) for the down items to copy
+    PreStaged pre{};
+    uint8_t* pre_ws_g[2] = {inter >= kPrestageMinK ? pre_ws : nullptr,
+                            shared_inter >= kPrestageMinK ? pre_shared_ws : nullptr};
+    bool any_pre = false;
+    for (int gi = 0; gi < ng; ++gi) {
+        if (!pre_ws_g[gi]) continue;
+        const int rows = g[gi].m * g[gi].top_k;
+        pre.planes[gi] = pre_ws_g[gi];
+        pre.meta[gi] = reinterpret_cast<const float2*>(pre_ws_g[gi] + (int64_t)rows * (g[gi].k / 64) * 144);
+        any_pre = true;
+    }
+    if (any_pre) {
+        const int st = cuda_status(launch_prestage(g, ng, pre, stream), "prestage launch");
+        if (st) return st;
+    }
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
     const int t = tc_min_for(m * top_k, num_experts);
@@ -228,7 +251,9 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
         img[0] = tc_ws;
         img[1] = tc_ws + tc_scratch(m * top_k, inter);
     }
-    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream, tc, img, combine), "down launch");
+    return cuda_status(launch_idgemv(g, ng, false, true, err_flag, stream, tc, img, combine, nullptr, 0, false,
+                                     any_pre ? &pre : nullptr),
+                       "down launch");
 }
 
 int run_ffn(const void* w_gate, const void* w_up, const void* w_down, int num_experts, const float* h_post,
@@ -439,7 +464,7 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
     if (st) return st;
     CombineSpec cb{d_y, d_h_mid, d_weights, d_shared_gate, shared_mode, counters, ls.n_counters};
     return run_down(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,
-                    act_shared, sout, d_err_flag, stream, ws + ls.tc_dn, &cb);
+                    act_shared, sout, d_err_flag, stream, ws + ls.tc_dn, &cb, ws + ls.pre, ws + ls.pre_shared);
 }
 
 int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,

@@ -47,7 +47,34 @@ struct GemvParams {
     int n_zero;
     int fast;               // every group has at most 32 pairs: bucket with one warp per group
     int wait_first;         // wait for the previous kernel before reading anything (first launch of a layer)
+    const uint8_t* pre_planes[kMaxGroups];  // group's rows already staged by prestage_kernel (or null)
+    const float2* pre_meta[kMaxGroups];
 };
+
+// Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from global into shared memory
+// with the block's threads by asynchronous copies: no registers held while the item's weight
+// ring is live. The caller waits (cp.async.wait_group) and synchronises the block.
+__device__ __forceinline__ void copy_block16(const uint8_t* src, uint8_t* dst, int64_t bytes) {
+    const int64_t n = bytes / 16;
+    for (int64_t i = threadIdx.x; i < n; i += kThreads)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst + 16 * i)), "l"(src + 16 * i)
+                     : "memory");
+}
+
+// The item's rows as prestage_kernel left them (pair p's planes at planes + p * (k/64) * 144,
+// its (delta, sum X) pairs at meta + p * (k/32)): copied, not quantized again.
+__device__ __forceinline__ void copy_staged(const uint8_t* planes, const float2* metas, int k, const int* pairs,
+                                            int nt, uint8_t* xs, float2* meta) {
+    const int64_t pb = (int64_t)(k / 64) * kPairBytes;
+    const int nsb = k / 32;
+    for (int t = 0; t < nt; ++t) {
+        const int p = pairs[t];
+        copy_block16(planes + (int64_t)p * pb, xs + t * pb, pb);
+        copy_block16(reinterpret_cast<const uint8_t*>(metas + (int64_t)p * nsb),
+                     reinterpret_cast<uint8_t*>(meta + (int64_t)t * nsb), (int64_t)nsb * 8);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 
 // Combine of rows [r0, r1) of every token, run by the last CTA of a row tile.
 __device__ void combine_rows(const GemvParams& P, int r0, int r1) {
@@ -209,7 +236,14 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
                 s_rows[lane] = (int64_t)(p / G.top_k) * G.outer + (int64_t)(p % G.top_k) * G.inner;
             }
             if (threadIdx.x == 0) { s_staged_group = gi; s_staged_nt = nt; }
-            stage_rows(G, s_pairs, nt, xs, meta);
+            bool copied = false;
+            if constexpr (!FUSED) {  // (down launches only)
+                if (P.pre_planes[gi]) {
+                    copy_staged(P.pre_planes[gi], P.pre_meta[gi], G.k, s_pairs, nt, xs, meta);
+                    copied = true;
+                }
+            }
+            if (!copied) stage_rows(G, s_pairs, nt, xs, meta);
         }
         __syncthreads();
 
@@ -283,7 +317,7 @@ int idgemv_tile_rows(int k) { return kWarps * (8 >> lg_split_for(k)); }
 
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
-                          unsigned* zero, int n_zero, bool pdl_wait_first) {
+                          unsigned* zero, int n_zero, bool pdl_wait_first, const PreStaged* pre) {
     if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
     if (tc_min > 0) {
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
@@ -302,6 +336,10 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     P.zero = zero;
     P.n_zero = zero ? n_zero : 0;
     P.wait_first = (pdl && pdl_wait_first) ? 1 : 0;
+    for (int gi = 0; pre && gi < n_groups; ++gi) {
+        P.pre_planes[gi] = pre->planes[gi];
+        P.pre_meta[gi] = pre->meta[gi];
+    }
     if (combine) {
         P.has_combine = 1;
         P.cb = *combine;
@@ -387,6 +425,67 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+// ------------------------------------------------------------------------------------------
+// Activation rows of a down launch quantized once into the staged format, for the down
+// items to copy instead of quantizing them again in every CTA that takes an item of the row
+// (long rows: ~600 CTAs share the 2 rows of a Mixtral-like m = 1 down launch). The same
+// arithmetic as the in-kernel staging (stage_row), sub-block by sub-block, so the planes are
+// identical. Grid (rows, slices of kPreSlice elements, groups); a programmatic dependent of
+// the gate|up launch that waits for it before reading.
+constexpr int kPreSlice = 2048;
+
+struct PreStageParams {
+    const float* a[kMaxGroups];
+    int64_t outer[kMaxGroups], inner[kMaxGroups];
+    int top_k[kMaxGroups], rows[kMaxGroups], k[kMaxGroups];
+    uint8_t* planes[kMaxGroups];
+    float2* meta[kMaxGroups];
+    int n_groups;
+};
+
+__global__ void __launch_bounds__(kThreads) prestage_kernel(const __grid_constant__ PreStageParams P) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int g = blockIdx.z, r = blockIdx.x, s0 = blockIdx.y * kPreSlice;
+    if (g >= P.n_groups || P.planes[g] == nullptr || r >= P.rows[g] || s0 >= P.k[g]) return;
+    const int k = P.k[g], len = min(kPreSlice, k - s0);
+    const float* row = P.a[g] + (int64_t)(r / P.top_k[g]) * P.outer[g] + (int64_t)(r % P.top_k[g]) * P.inner[g];
+    const int64_t pb = (int64_t)(k / 64) * kPairBytes;
+    stage_row<0>(row + s0, len, P.planes[g] + (int64_t)r * pb + (s0 / 64) * kPairBytes,
+                 P.meta[g] + (int64_t)r * (k / 32) + s0 / 32);
+}
+
+int64_t prestage_bytes(int rows, int k) {
+    return (int64_t)rows * ((int64_t)(k / 64) * kPairBytes + (int64_t)(k / 32) * 8);
+}
+
+cudaError_t launch_prestage(const GemvGroup* groups, int n_groups, const PreStaged& pre, cudaStream_t stream) {
+    PreStageParams P{};
+    P.n_groups = n_groups;
+    int rows = 0, slices = 0;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        const GemvGroup& S = groups[gi];
+        P.a[gi] = S.a; P.outer[gi] = S.outer; P.inner[gi] = S.inner; P.top_k[gi] = S.top_k;
+        P.rows[gi] = S.m * S.top_k; P.k[gi] = S.k;
+        P.planes[gi] = const_cast<uint8_t*>(pre.planes[gi]);
+        P.meta[gi] = const_cast<float2*>(pre.meta[gi]);
+        if (!P.planes[gi]) continue;
+        rows = std::max(rows, P.rows[gi]);
+        slices = std::max(slices, (S.k + kPreSlice - 1) / kPreSlice);
+    }
+    if (rows == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows, (unsigned)slices, (unsigned)n_groups);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prestage_kernel, P);
 }
 
 }  // namespace q4k

@@ -83,10 +83,22 @@ struct CombineSpec {
 // the id-GEMV kernel. combine: fuse the combine into this (down) launch. zero / n_zero: CTA 0
 // zeroes these words before anything else (the gate|up launch prepares the counters the
 // following down launch uses).
+// Rows of a one-slab launch quantized once by launch_prestage (per group, or null): pair p's
+// staged planes at planes[g] + p * (k/64) * 144 bytes, its (delta, sum X) at meta[g] + p * (k/32).
+struct PreStaged {
+    const uint8_t* planes[2];
+    const float2* meta[2];
+};
+// Bytes of `rows` staged rows of length k (planes and (delta, sum X) pairs).
+int64_t prestage_bytes(int rows, int k);
+// Quantize the activation rows of the groups with planes into PreStaged (a programmatic
+// dependent launch that waits for the previous kernel before reading).
+cudaError_t launch_prestage(const GemvGroup* groups, int n_groups, const PreStaged& pre, cudaStream_t stream);
+
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min = 0, uint8_t* const* tc_img = nullptr,
                           const CombineSpec* combine = nullptr, unsigned* zero = nullptr, int n_zero = 0,
-                          bool pdl_wait_first = false);
+                          bool pdl_wait_first = false, const PreStaged* pre = nullptr);
 // rows per id-GEMV work item for a given k (bucketed kernel)
 int idgemv_tile_rows(int k);
 // The bulk-copy id-GEMV for small batches (q4k_stream.cu): cudaErrorNotSupported, before
