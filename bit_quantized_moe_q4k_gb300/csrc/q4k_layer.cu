@@ -240,8 +240,10 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         slot_issued = true;
     };
     if (slot_item && (a0 == a1 || !P.slot_shares_raw)) issue_slot();
-    uint32_t xphase = 0, aphase = 0;
-    bool x_pending = false, a_pending = false;  // a copy whose wait gave up
+    // the bulk copies of the gate|up items: bit 0 / 1 = a copy on s_xbar / s_abar not yet waited
+    // for (drained before the CTA leaves, also after a wait gave up), bit 2 / 3 = the parity of
+    // the phase that barrier completes next
+    uint32_t cps = 0;
 
     int staged = -1;  // (half, group, rank, chunk) of the staged activation rows
     // ---- gate|up + SwiGLU items: activation rows and (use_atile) the weight tiles of both slabs
@@ -252,9 +254,8 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         if constexpr (!SM) item_issue<kFused>(G, e, tile, lane, warp, IL);
         if (key != staged) {
             if (P.use_xcopy) {
-                const bool got = __syncthreads_and(sm100::mbar_wait(&s_xbar, xphase, &s_never));
-                xphase ^= 1u;
-                if (!got) { x_pending = true; return false; }
+                if (!__syncthreads_and(sm100::mbar_wait(&s_xbar, (cps >> 2) & 1u, &s_never))) return false;
+                cps = (cps ^ 4u) & ~1u;
                 stage_rows_smem(raw, nt, G.k, xs, meta);
             } else {
                 stage_rows<false>(G, s_pairs, nt, xs, meta);
@@ -266,9 +267,8 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             issue_slot();
         }
         if constexpr (SM) {
-            const bool got = __syncthreads_and(sm100::mbar_wait(&s_abar, aphase, &s_never));
-            aphase ^= 1u;
-            if (!got) { a_pending = true; return false; }
+            if (!__syncthreads_and(sm100::mbar_wait(&s_abar, (cps >> 3) & 1u, &s_never))) return false;
+            cps = (cps ^ 8u) & ~2u;
             item_issue<kFused, true>(G, e, tile, lane, warp, IL, atile, atile + P.atile_bytes);
         }
         __syncthreads();
@@ -286,8 +286,9 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         const int gi = s_info[0], r = s_info[1], e = s_info[2], tile = s_info[3], nt = s_info[4], chunk = s_info[5];
         const GroupDev& G = P.a[gi];
         const int key = ((gi * 32 + r) * 32 + chunk) * 2;
+        const bool xc = key != staged && P.use_xcopy;  // (uniform) this item's copies
+        cps |= (xc ? 1u : 0u) | (P.use_atile ? 2u : 0u);
         if (threadIdx.x == 0) {
-            const bool xc = key != staged && P.use_xcopy;
             if (xc || P.use_atile) sm100::fence_proxy_async_smem();  // earlier reads of these areas first
             if (xc) {
                 sm100::mbar_arrive_expect_tx(&s_xbar, (uint32_t)(nt * G.k * 4));
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         const GroupDev& G = P.b[gi];
         if (slot_issued && item == b0) {
             ok = __syncthreads_and(sm100::mbar_wait(&s_bar, 0, &s_never));
-            slot_waited = true;
+            slot_waited = ok;
             if (!ok) break;
             ItemLane<KB, true> IL;
             item_issue<KB, true>(G, e, tile, lane, warp, IL, slot);
@@ -363,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     }
     // a copy still in flight must land before the CTA leaves (after an abort)
     if (slot_issued && !slot_waited) sm100::mbar_wait(&s_bar, 0, &s_never);
-    if (x_pending) sm100::mbar_wait(&s_xbar, xphase ^ 1u, &s_never);
-    if (a_pending) sm100::mbar_wait(&s_abar, aphase ^ 1u, &s_never);
+    if (cps & 1u) sm100::mbar_wait(&s_xbar, (cps >> 2) & 1u, &s_never);
+    if (cps & 2u) sm100::mbar_wait(&s_abar, (cps >> 3) & 1u, &s_never);
 
     // ---- combine (without valid counters): row tiles of the routed down group, each by a
     // designated CTA after its down items' flags
