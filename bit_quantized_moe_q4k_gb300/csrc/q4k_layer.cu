@@ -329,15 +329,16 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         __syncthreads();
         item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane);
         __syncthreads();
-        publish(P.flag_b + item, tag);
         if (s_cnt_ok) {  // the last down item of the tile combines it
+            // the counter's release makes this item's rows visible (no flag: only the combine
+            // without counters reads the down flags); its acquire, passed on to the block by the
+            // barrier, orders the reads of the other items' rows (from L2) after their releases
             if (threadIdx.x == kThreads - 32)
                 s_last = atom_add_acq_rel(P.cnt + s_set * P.nt_max + tile, 1u) + 1u == (unsigned)s_per_tile;
             __syncthreads();
-            if (s_last) {
-                fence_acq_rel_gpu();
-                combine_tile(tile);
-            }
+            if (s_last) combine_tile(tile);
+        } else {
+            publish(P.flag_b + item, tag);
         }
         return true;
     };
