@@ -97,15 +97,21 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // Block-wide: wait until flags[index(j)] == tag for all j < n. Each thread owns j = tid,
-// tid + kThreads, ...; it re-reads only those it has not yet seen set (up to 8 loads in flight
-// per round). True when all are set (with acquire order for what follows); false once the
-// wait has run for kWaitNs or kLayerMaxPolls rounds. Uniform over the block.
+// tid + kThreads, ...; it re-reads only those it has not yet seen set (up to 8 loads per
+// round). The reads are acquire loads, so every flag was acquired before the barrier that
+// ends the wait, and what any thread of the block does after it is ordered after the
+// flags' releases. True when all are set; false once the wait has run for kWaitNs or
+// kLayerMaxPolls rounds. Uniform over the block.
 template <class Index>
 __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t tag, Index index) {
     int j = threadIdx.x;
@@ -115,7 +121,7 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int jj = j + u * kThreads;
-            v[u] = jj < n ? ld_relaxed_u64(flags + index(jj)) : tag;
+            v[u] = jj < n ? ld_acquire_u64(flags + index(jj)) : tag;
         }
         int seen = 0;
 #pragma unroll
@@ -124,10 +130,7 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
             ++seen;
         }
         j += seen * kThreads;
-        if (__syncthreads_and(j >= n)) {
-            fence_acq_rel_gpu();
-            return true;
-        }
+        if (__syncthreads_and(j >= n)) return true;
         const bool late = round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > sm100::kWaitNs;
         if (__syncthreads_or(late)) return false;
         __nanosleep(32);
