@@ -84,6 +84,9 @@ def layer_bytes(W: Workload, ids: np.ndarray) -> dict:
 # ---------------------------------------------------------------------------------------------
 # clocks sampled during the timed region
 
+CLOCK_SOAK_S = 0.8
+
+
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -328,7 +331,19 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     clocks.start()
-    time.sleep(0.3)
+    # The timed region lasts milliseconds, less than the sampler's 100 ms period, so the same
+    # graph is replayed (untimed) for CLOCK_SOAK_S seconds right before it: the clock samples
+    # are taken under this load, and the sampler keeps running through the timed region.
+    soak, t_soak = 0, time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t_soak < CLOCK_SOAK_S and soak < 100000:
+            g_timed.replay()
+            stream.synchronize()
+            soak += 1
+    soak_s = time.perf_counter() - t_soak
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
     ev0.record(stream)
     with torch.cuda.stream(stream):
         g_timed.replay()
@@ -337,8 +352,9 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    time.sleep(0.2)
     clk = clocks.stop()
+    clk["window"] = (f"nvidia-smi every 100 ms over {soak} untimed replays of the timed graph "
+                     f"({soak_s:.2f} s) and then the timed region")
     total_ms = ev0.elapsed_time(ev1)
     # dominant kernel alone, same layers, right after the timed region
     gu_ms = [total_ms / K]
