@@ -72,7 +72,8 @@ class Layer:
 
 @pytest.fixture(autouse=True)
 def _single_launch_on(monkeypatch):
-    """The single launch is opt-in: every test here turns it on (and off for the references)."""
+    """By default the layer call takes the single launch only where each half fits one round of
+    resident CTAs; every test here forces it on (and off for the two-launch references)."""
     monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
     monkeypatch.setenv("Q4K_STREAM", "0")
 
