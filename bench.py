@@ -185,9 +185,22 @@ def time_oracle(W: Workload, target_s: float) -> dict:
         t_total += time.perf_counter() - t0
         done += 1
         pairs += W.pairs
+    # the same on one core, a shorter sample
+    oracle.set_threads(1)
+    done1, t1 = 0, 0.0
+    while t1 < min(3.0, target_s / 4) and done1 < 1000:
+        wg, wu, wd, E, shared, ids, x, hm, rw, gl = layers[done1 % len(layers)]
+        t0 = time.perf_counter()
+        oracle.moe_layer(wg, wu, wd, E, shared, W.shared_inter, W.shared_mode, x, hm, ids, rw, gl, W.m, W.top_k,
+                         W.hidden, W.inter)
+        t1 += time.perf_counter() - t0
+        done1 += 1
+    oracle.set_threads(threads)
     return {"value": pairs / t_total, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{done} layer forwards of {W.name} (2 distinct layers' weights, touched experts only), "
-                      f"{t_total:.1f} s of oracle time, OpenMP over output rows"}
+                      f"{t_total:.1f} s of oracle time, OpenMP over output rows",
+            "single_thread": {"value": done1 * W.pairs / t1, "unit": UNIT, "cores": 1,
+                              "sample": f"{done1} layer forwards of the same layers, {t1:.1f} s on one thread"}}
 
 
 # ---------------------------------------------------------------------------------------------
