@@ -11,7 +11,9 @@
  *        bound and `BadK`, the sigmoid-gated / unscaled shared expert in
  *        `combine_kernel_name`, the batched combine
  *        `encode_moe_combine_residual_n_tokens`, and the expert bucketing of
- *        `encode_moe_batched_permute_fuse` / `encode_moe_gather_id_fuse`).
+ *        `encode_moe_batched_permute_fuse` / `encode_moe_gather_id_fuse`);
+ *   [P3] cortiq-engine 0.7.7, examples/mv_lab.rs (4-bit matvec kernel variants and
+ *        the loads-only `ld` kernel that gives the access pattern's ceiling).
  *
  * Data formats
  *   Q4_K block: 256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes of
@@ -261,7 +263,9 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
 
 /* ---------------------------------------------------------------------------------
  * q4k_quantize_rows -- fp32 [rows, k] -> Q4_K bytes [rows, k/256*144] on the device
- * (weight preparation; not part of the layer). Per 32-weight sub-block:
+ * (weight preparation; not part of the layer: the [P1] tests make their slabs by
+ * quantizing fp32 weights with candle's Q4K, whose steps the page does not show, so
+ * this is a min/max quantizer of the Q4_K format). Per 32-weight sub-block:
  * lo = min(0, min x), hi = max x, scale = (hi-lo)/15, mn = -lo; d = fp16(max scale/63),
  * dmin = fp16(max mn/63); sc = min(63, rint(scale/d)), m = min(63, rint(mn/dmin));
  * q = clamp(rint((x + dmin*m)/(d*sc)), 0, 15); every step one IEEE binary32
@@ -271,7 +275,7 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
 int q4k_quantize_rows(const float* d_x, int64_t rows, int k, void* d_out, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
- * q4k_stream_ceiling -- loads-only kernel over `bytes` of device memory (16-byte
+ * q4k_stream_ceiling -- loads-only kernel [P3 `ld`] over `bytes` of device memory (16-byte
  * aligned, bytes % 16 == 0): the same coalesced 16-byte loads as the GEMV's weight
  * stream, reduced to one XOR word per CTA in d_sink (grid-sized, caller-provided,
  * at least q4k_stream_ceiling_sink_words() ints). A measurement tool: its
