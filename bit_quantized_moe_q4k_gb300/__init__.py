@@ -7,6 +7,9 @@ the seeded synthetic-input generators (``inputs``) and the workload table
 first call does, and raises if it cannot.
 """
 from ._lib import (  # noqa: F401
+    PATH_PERSISTENT,
+    PATH_RESIDENT,
+    PATH_TWO_LAUNCH,
     Q4KError,
     SHARED_NONE,
     SHARED_SIGMOID,
@@ -25,6 +28,7 @@ from ._lib import (  # noqa: F401
     q4k_moe_layer_gate_up,
     q4k_moe_layer_half_workspace_size,
     q4k_moe_layer_launch_count,
+    q4k_moe_layer_path,
     q4k_moe_layer_host_staging_size,
     q4k_moe_layer_workspace_size,
     q4k_moe_workspace_size,

@@ -23,6 +23,7 @@ STATUS_NAMES = {
     10: "Q4K_ERR_TIMEOUT",
 }
 SHARED_NONE, SHARED_SIGMOID, SHARED_UNSCALED = 0, 1, 2
+PATH_TWO_LAUNCH, PATH_PERSISTENT, PATH_RESIDENT = 0, 1, 2
 
 # Exported C symbols and their signatures (restype, argtypes).
 _P, _I, _I64, _U64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
@@ -46,6 +47,7 @@ SIGNATURES = {
     "q4k_moe_layer_down": (_I, [_P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
     "q4k_moe_layer_half_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "q4k_moe_layer_launch_count": (_I, [_I, _I, _I, _I, _I, _I]),
+    "q4k_moe_layer_path": (_I, [_I, _I, _I, _I, _I, _I]),
     "q4k_quantize_rows": (_I, [_P, _I64, _I, _P, _P]),
     "q4k_stream_ceiling_sink_words": (_I, []),
     "q4k_stream_ceiling": (_I, [_P, _U64, _P, _P]),
@@ -199,6 +201,11 @@ def q4k_moe_layer_forward_host(w_gate, w_up, w_down, num_experts, ws_gate, ws_up
 
 def q4k_moe_layer_launch_count(m, top_k, num_experts, hidden, inter, shared_inter) -> int:
     return int(load().q4k_moe_layer_launch_count(m, top_k, num_experts, hidden, inter, shared_inter))
+
+
+def q4k_moe_layer_path(m, top_k, num_experts, hidden, inter, shared_inter) -> int:
+    """PATH_RESIDENT, PATH_PERSISTENT or PATH_TWO_LAUNCH: the kernels one layer call runs."""
+    return int(load().q4k_moe_layer_path(m, top_k, num_experts, hidden, inter, shared_inter))
 
 
 def q4k_moe_layer_half_workspace_size(m, top_k, k_routed, shared_inter, k_shared) -> int:

@@ -295,13 +295,6 @@ static int g_num_sms = 0;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 200 * 1024;
 static bool g_smem_attr_set[4][kMaxDevices] = {};
-// Switch (environment, read at every launch): Q4K_STREAM=1 sends small batches to the
-// bulk-copy kernel (q4k_stream.cu) instead of this one (default off: slower on GB300 at m = 1).
-static int env_flag(const char* name, int dflt) {
-    const char* s = getenv(name);
-    return s ? (atoi(s) != 0 ? 1 : 0) : dflt;
-}
-int stream_setting() { return env_flag("Q4K_STREAM", 0); }
 
 int num_sms() {
     if (g_num_sms == 0) {
@@ -323,11 +316,6 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
         if (e != cudaSuccess) return e;
         pdl = false;  // the tensor-core kernels precede this launch in the stream
-    }
-    if (stream_setting()) {
-        const cudaError_t se = launch_idgemv_stream(groups, n_groups, fused_swiglu, pdl, err_flag, stream, tc_min,
-                                                    combine, zero, n_zero, pdl_wait_first);
-        if (se != cudaErrorNotSupported) return se;
     }
     GemvParams P{};
     P.n_groups = n_groups;

@@ -120,6 +120,17 @@ __device__ __forceinline__ void dot64(const uint4& q0, const uint4& q1, const ui
     dot64_regs(q0, q1, x, Sa, Sb);
 }
 
+// One lane's contribution of sub-blocks a and b of a block to a row's sum for one token:
+//   acc + delta_a * (d*sc_a * S_a - dmin*m_a * sum X_a) + delta_b * (d*sc_b * S_b - dmin*m_b * sum X_b)
+// (mt = (delta_a, sum X_a, delta_b, sum X_b)). Every rounding is spelled out, so each kernel
+// that computes a row with the same lanes gets the same bits (no contraction choices).
+__device__ __forceinline__ float acc_sub_pair(float acc, const float4& mt, float sa, float ma, float sb, float mb,
+                                              int Sa, int Sb) {
+    const float ua = __fmaf_rn(sa, (float)Sa, -__fmul_rn(ma, mt.y));
+    const float ub = __fmaf_rn(sb, (float)Sb, -__fmul_rn(mb, mt.w));
+    return __fmaf_rn(mt.z, ub, __fmaf_rn(mt.x, ua, acc));
+}
+
 // Quantize one float4 (elements 4*fi .. 4*fi+3 of a row) as part of its 32-element sub-block:
 // the 8 consecutive lanes holding fi = 8j .. 8j+7 reduce max|x| and sum(X) with shuffles.
 // All 32 lanes of the warp must call it together (v = 0 where a lane has nothing); lanes with
@@ -261,23 +272,23 @@ inline GroupDev group_dev(const GemvGroup& S, int lg_split, int kind = kOne) {
 // Quantize one activation row of k floats into its planes (xs_row) and (delta, sum X) pairs
 // (meta_row). Thread f handles float4 f of the row; all loads of a pass are issued before any
 // is used. SRC: 0 global (read-only path), 1 global written by other CTAs of this launch (read
-// from L2), 2 shared memory.
-template <int SRC>
-__device__ __forceinline__ void stage_row(const float* row, int k, uint8_t* xs_row, float2* meta_row) {
-    const int tid = threadIdx.x;
+// from L2), 2 shared memory. NTHR threads (whole warps) take part, tid = 0 .. NTHR-1.
+template <int SRC, int NTHR = kThreads>
+__device__ __forceinline__ void stage_row(const float* row, int k, uint8_t* xs_row, float2* meta_row,
+                                          int tid = threadIdx.x) {
     const int nf = k / 4;
-    for (int f0 = 0; f0 < nf; f0 += kThreads * kStageUnroll) {
+    for (int f0 = 0; f0 < nf; f0 += NTHR * kStageUnroll) {
         float4 v[kStageUnroll];
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
-            const int f = f0 + u * kThreads + tid;
+            const int f = f0 + u * NTHR + tid;
             const float4* src = reinterpret_cast<const float4*>(row) + f;
             v[u] = f < nf ? (SRC == 0 ? __ldg(src) : (SRC == 1 ? __ldcg(src) : *src)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
-            const int f = f0 + u * kThreads + tid;  // groups of 8 threads are all in or all out
-            if (f0 + u * kThreads >= nf) break;
+            const int f = f0 + u * NTHR + tid;  // groups of 8 threads are all in or all out
+            if (f0 + u * NTHR >= nf) break;
             stage_quad(v[u], f, f < nf, xs_row, meta_row);
         }
     }
@@ -392,10 +403,10 @@ __device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND, S
                         const float4 mt = *reinterpret_cast<const float4*>(meta + t * nsb + 8 * b + 2 * c);
                         int Sa, Sb;
                         dot64(L.Q0[j], L.Q1[j], xp, Sa, Sb);
-                        acc[t] += mt.x * (sa * (float)Sa - ma * mt.y) + mt.z * (sb * (float)Sb - mb * mt.w);
+                        acc[t] = acc_sub_pair(acc[t], mt, sa, ma, sb, mb, Sa, Sb);
                         if (TWO) {
                             dot64(L.R0[j], L.R1[j], xp, Sa, Sb);
-                            acc2[t] += mt.x * (sa2 * (float)Sa - ma2 * mt.y) + mt.z * (sb2 * (float)Sb - mb2 * mt.w);
+                            acc2[t] = acc_sub_pair(acc2[t], mt, sa2, ma2, sb2, mb2, Sa, Sb);
                         }
                     }
                 }

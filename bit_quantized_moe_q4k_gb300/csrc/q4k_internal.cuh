@@ -101,12 +101,6 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
                           bool pdl_wait_first = false, const PreStaged* pre = nullptr);
 // rows per id-GEMV work item for a given k (bucketed kernel)
 int idgemv_tile_rows(int k);
-// The bulk-copy id-GEMV for small batches (q4k_stream.cu): cudaErrorNotSupported, before
-// launching anything, when a group holds more than 32 pairs or its rows do not fit.
-// pdl_wait_first as for launch_idgemv.
-cudaError_t launch_idgemv_stream(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
-                                 cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
-                                 int n_zero, bool pdl_wait_first = false);
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
                       int* err_flag, cudaStream_t stream);
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);
@@ -120,10 +114,28 @@ bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel'
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
 // Both halves' work items fit one round of the CTAs the device's SMs hold at once.
 bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter);
+// Words at the start of the sync area that hold the generation word and the counter sets.
+size_t layer_sync_head_words(int hidden);
+
+// The decode layer in one launch with all touched weights resident in shared memory at once
+// (q4k_decode.cu). Applies where the shared-memory plan for the most buckets the ids can make
+// fits one CTA per SM (a few tokens); cudaErrorNotSupported otherwise, before launching
+// anything. stage[g]: workspace for the staged down inputs of group g (routed pairs, shared
+// tokens), 2.5 bytes per element. sync as for launch_layer_persistent (the head is left alone).
+bool layer_decode_fits(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
+size_t layer_decode_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
+cudaError_t launch_layer_decode(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
+                                uint64_t* sync, size_t sync_words, uint8_t* const* stage, int* err_flag,
+                                cudaStream_t stream);
 cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
                                     uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream);
 
 int num_sms();
+
+// Limit of every bounded wait inside the single-launch layer kernels, in nanoseconds: the
+// environment variable Q4K_WAIT_NS when set to a positive number (read at every launch), else
+// 2 s. A wait that runs out raises Q4K_ERR_TIMEOUT in the device error flag.
+uint64_t wait_limit_ns();
 
 // Record the calling thread's last error text (read back by q4k_last_error_string).
 void set_last_error(int status, const char* message);

@@ -34,6 +34,7 @@
 
 #include "q4k_gemv_common.cuh"
 #include "q4k_sm100.cuh"
+#include "q4k_sync.cuh"
 
 namespace q4k {
 
@@ -63,17 +64,8 @@ struct LayerParams {
     uint64_t* flag_b;         // [cap_b] one per down item
     int cap_a, cap_b;
     int* err_flag;
+    uint64_t wait_ns;         // limit of every wait
 };
-
-// splitmix64's output function (Steele, Lea, Flood 2014): a bijective 64-bit mixer.
-__device__ __forceinline__ uint64_t mix64(uint64_t z) {
-    z += 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return z ^ (z >> 31);
-}
-
-__device__ __forceinline__ uint64_t next_tag(uint64_t g) { return (mix64(g) & ~1ull) | ((g & 1ull) ^ 1ull); }
 
 // A counter set's header: the tag of the launch it was prepared for, bound to the sets' size
 // (which moves with hidden), so a call of another shape never takes words laid out for
@@ -88,32 +80,14 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
     return old;
 }
 
-// The tag of the launch after the one whose generation word is g: a hash of g whose lowest
-// bit flips at every launch (consecutive launches use different counter sets).
-__device__ __forceinline__ uint64_t next_tag(uint64_t g);
-
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 // Block-wide: wait until flags[index(j)] == tag for all j < n. Each thread owns j = tid,
 // tid + kThreads, ...; it re-reads only those it has not yet seen set (up to 8 loads per
 // round). The reads are acquire loads, so every flag was acquired before the barrier that
 // ends the wait, and what any thread of the block does after it is ordered after the
-// flags' releases. True when all are set; false once the wait has run for kWaitNs or
+// flags' releases. True when all are set; false once the wait has run for limit_ns or
 // kLayerMaxPolls rounds. Uniform over the block.
 template <class Index>
-__device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t tag, Index index) {
+__device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t tag, uint64_t limit_ns, Index index) {
     int j = threadIdx.x;
     const uint64_t t0 = sm100::global_timer_ns();
     for (uint32_t round = 0;; ++round) {
@@ -131,7 +105,7 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
         }
         j += seen * kThreads;
         if (__syncthreads_and(j >= n)) return true;
-        const bool late = round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > sm100::kWaitNs;
+        const bool late = round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > limit_ns;
         if (__syncthreads_or(late)) return false;
         __nanosleep(32);
     }
@@ -257,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         if constexpr (!SM) item_issue<kFused>(G, e, tile, lane, warp, IL);
         if (key != staged) {
             if (P.use_xcopy) {
-                if (!__syncthreads_and(sm100::mbar_wait(&s_xbar, (cps >> 2) & 1u, &s_never))) return false;
+                if (!__syncthreads_and(mbar_wait_for(&s_xbar, (cps >> 2) & 1u, &s_never, P.wait_ns))) return false;
                 cps = (cps ^ 4u) & ~1u;
                 stage_rows_smem(raw, nt, G.k, xs, meta);
             } else {
@@ -270,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             issue_slot();
         }
         if constexpr (SM) {
-            if (!__syncthreads_and(sm100::mbar_wait(&s_abar, (cps >> 3) & 1u, &s_never))) return false;
+            if (!__syncthreads_and(mbar_wait_for(&s_abar, (cps >> 3) & 1u, &s_never, P.wait_ns))) return false;
             cps = (cps ^ 8u) & ~2u;
             item_issue<kFused, true>(G, e, tile, lane, warp, IL, atile, atile + P.atile_bytes);
         }
@@ -325,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         const int key = ((gi * 32 + r) * 32 + chunk) * 2 + 1;
         if (key != staged) {
             const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
-            if (!wait_tags(P.flag_a, P.a[gi].tiles, tag, [first](int j) { return first + j; })) return false;
+            if (!wait_tags(P.flag_a, P.a[gi].tiles, tag, P.wait_ns, [first](int j) { return first + j; })) return false;
             stage_rows<true>(G, s_pairs, nt, xs, meta);
             staged = key;
         }
@@ -354,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         const int gi = s_info[0], r = s_info[1], e = s_info[2], tile = s_info[3], nt = s_info[4], chunk = s_info[5];
         const GroupDev& G = P.b[gi];
         if (slot_issued && item == b0) {
-            ok = __syncthreads_and(sm100::mbar_wait(&s_bar, 0, &s_never));
+            ok = __syncthreads_and(mbar_wait_for(&s_bar, 0, &s_never, P.wait_ns));
             slot_waited = ok;
             if (!ok) break;
             ItemLane<KB, true> IL;
@@ -389,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     const int n_tiles = P.b[0].tiles;
     const int t0 = (int)(cta * n_tiles / grid), t1 = (int)((cta + 1) * n_tiles / grid);
     for (int t = t0; ok && !s_cnt_ok && t < t1; ++t) {
-        ok = wait_tags(P.flag_b, s_n_chunks, tag, [t](int j) { return s_chunk_b[j] + t; });
+        ok = wait_tags(P.flag_b, s_n_chunks, tag, P.wait_ns, [t](int j) { return s_chunk_b[j] + t; });
         if (!ok) break;
         combine_tile(t);
     }
@@ -405,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     // ---- advance the generation once every CTA has read it, and prepare the next launch's
     // counter set (the one this launch does not use): zero it, then stamp it with its tag
     if (blockIdx.x == 0) {
-        const bool all = wait_tags(P.cta_tag, (int)gridDim.x, tag, [](int j) { return j; });
+        const bool all = wait_tags(P.cta_tag, (int)gridDim.x, tag, P.wait_ns, [](int j) { return j; });
         if (all) {
             unsigned* next = P.cnt + (s_set ^ 1) * P.nt_max;
             for (int i = threadIdx.x; i < P.nt_max; i += kThreads) next[i] = 0u;
@@ -424,6 +398,15 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
 }
 
 // ------------------------------------------------------------------------------------------
+uint64_t wait_limit_ns() {
+    const char* s = getenv("Q4K_WAIT_NS");
+    if (s) {
+        const long long v = atoll(s);
+        if (v > 0) return (uint64_t)v;
+    }
+    return sm100::kWaitNs;
+}
+
 namespace {
 
 struct LayerPlan {
@@ -456,6 +439,8 @@ size_t sync_head_words(int hidden) { return 3 + (size_t)(combine_tiles_max(hidde
 
 }  // namespace
 
+size_t layer_sync_head_words(int hidden) { return sync_head_words(hidden); }
+
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter) {
     if (m < 1 || (int64_t)m * top_k > kLayerMaxPairs || (shared_inter > 0 && m > kLayerMaxPairs)) return 0;
     GemvGroup gu[2] = {}, dn[2] = {};
@@ -469,7 +454,8 @@ size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inte
     }
     const LayerPlan L = plan_of(gu, dn, ng, kOne);  // one-row down items: the larger cap
     if (L.cap_a + L.cap_b > (1 << 26)) return 0;
-    return sync_head_words(hidden) + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b;
+    return std::max(sync_head_words(hidden) + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b,
+                    layer_decode_sync_words(m, top_k, hidden, inter, shared_inter));
 }
 
 bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter) {
@@ -556,6 +542,7 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     P.cap_a = (int)L.cap_a;
     P.cap_b = (int)L.cap_b;
     P.err_flag = err_flag;
+    P.wait_ns = wait_limit_ns();
 
     void (*kern)(LayerParams) = tb == 1 ? (kb == kPair ? layer_kernel<1, kPair> : layer_kernel<1, kOne>)
                                         : (kb == kPair ? layer_kernel<kTB, kPair> : layer_kernel<kTB, kOne>);

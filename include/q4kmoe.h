@@ -239,6 +239,21 @@ size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int sha
  * takes the tensor-core path). 0 on invalid sizes. */
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
+/* Which kernels one q4k_moe_layer_forward call runs for these sizes on the current device
+ * (the environment switches included):
+ *   Q4K_PATH_RESIDENT   one launch with every weight byte the layer touches resident in
+ *                       shared memory at once (a decode layer whose touched rows fit the
+ *                       SMs' shared memory; each CTA also forms the combine of its rows);
+ *   Q4K_PATH_PERSISTENT one persistent launch that streams work items through registers;
+ *   Q4K_PATH_TWO_LAUNCH a gate|up launch and a down launch with the combine fused (plus the
+ *                       tensor-core kernels of a half that uses them).
+ * All three give the same results bit for bit. -1 on invalid sizes. The environment variable
+ * Q4K_DECODE=0 turns the resident path off. */
+#define Q4K_PATH_TWO_LAUNCH 0
+#define Q4K_PATH_PERSISTENT 1
+#define Q4K_PATH_RESIDENT 2
+int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
+
 /* ---------------------------------------------------------------------------------
  * q4k_moe_layer_forward_host -- the same layer with the per-step inputs and the
  * output in HOST memory. Weights and the workspace stay in device memory. The inputs

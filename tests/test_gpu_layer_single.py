@@ -1,12 +1,15 @@
-"""GPU: the single-launch layer (one persistent kernel for gate|up + SwiGLU, down and the
-combine, routed and shared experts) against the two-launch layer and the oracle.
+"""GPU: the single-launch layers against the two-launch layer and the oracle.
 
-The single launch runs the same work items with the same arithmetic as the two-launch
-layer, so the two agree bit for bit; against the oracle the per-row acceptance of
-helpers.rows_close applies. Its CTAs hand work to each other through tagged flag words at
-the start of the workspace, so the tests also run it on a workspace full of garbage, on one
-workspace call after call (and replayed from a CUDA graph), and with m changing between
-calls on one workspace.
+Two kernels run a layer in one launch: the resident-weights decode kernel (every weight byte
+the layer touches in shared memory at once; each CTA combines its own rows of hidden) where
+its shared-memory plan fits, else the persistent kernel (work items streamed through
+registers, last-arriver combine). Both reduce every output row with the same lanes in the
+same order as the two-launch layer, so all three agree bit for bit; against the oracle the
+per-row acceptance of helpers.rows_close applies. Their CTAs hand work to each other through
+tagged flag words at the start of the workspace, so the tests also run them on a workspace
+full of garbage, on one workspace call after call (and replayed from a CUDA graph), with m
+changing between calls on one workspace, and with a wait limit so short that the waits give
+up (the error flag reports it, and the next call on a cleared workspace is right).
 """
 import numpy as np
 import pytest
@@ -22,6 +25,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 Q4K_ERR_EXPERT_ID = 6
+Q4K_ERR_TIMEOUT = 10
 
 
 def _inputs(W, ids=None):
@@ -75,7 +79,6 @@ def _single_launch_on(monkeypatch):
     """By default the layer call takes the single launch only where each half fits one round of
     resident CTAs; every test here forces it on (and off for the two-launch references)."""
     monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
-    monkeypatch.setenv("Q4K_STREAM", "0")
 
 
 def _two_launch(layer, monkeypatch):
@@ -89,22 +92,26 @@ def _two_launch(layer, monkeypatch):
 
 
 CASES = [
-    # (hidden, inter, experts, top_k, m, ids, shared_inter, shared_mode)
-    (2048, 768, 128, 8, 1, "uniform", 768, 1),   # the Qwen3-MoE-like decode layer, full size
-    (1024, 512, 128, 8, 4, "uniform", 512, 2),   # 32 pairs: the single launch's limit
-    (512, 256, 4, 2, 3, "uniform", 256, 1),      # more pairs than experts: 4-token items
-    (256, 512, 32, 16, 2, "uniform", 256, 1),    # top_k at its limit
-    (768, 256, 4, 1, 32, "uniform", 512, 2),     # 32 tokens: a 32-pair shared expert
-    (1024, 1280, 16, 4, 2, "zipf", 0, 0),        # no shared expert; ragged row tiles
-    (4096, 1792, 8, 2, 1, "uniform", 0, 0),      # Mixtral-like shape at reduced inter
+    # (hidden, inter, experts, top_k, m, ids, shared_inter, shared_mode, resident on GB300)
+    (2048, 768, 128, 8, 1, "uniform", 768, 1, True),   # the Qwen3-MoE-like decode layer, full size
+    (1024, 512, 128, 8, 4, "uniform", 512, 2, False),  # 32 pairs: the single launch's limit
+    (512, 256, 4, 2, 3, "uniform", 256, 1, True),      # more pairs than experts: shared buckets
+    (256, 512, 32, 16, 2, "uniform", 256, 1, True),    # top_k at its limit
+    (768, 256, 4, 1, 32, "uniform", 512, 2, False),    # 32 tokens: a 32-pair shared expert
+    (1024, 1280, 16, 4, 2, "zipf", 0, 0, True),        # no shared expert; ragged row tiles
+    (4096, 1792, 8, 2, 1, "uniform", 0, 0, True),      # Mixtral-like shape at reduced inter
 ]
 
 
+@pytest.mark.parametrize("decode", ["1", "0"], ids=["resident_if_fits", "persistent"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "h{}_i{}_e{}_t{}_m{}_{}_s{}".format(*c[:7]))
-def test_single_launch_matches_two_launch_and_oracle(case, monkeypatch):
-    H, I, E, T, m, ids_kind, Is, mode = case
+def test_single_launch_matches_two_launch_and_oracle(case, decode, monkeypatch):
+    H, I, E, T, m, ids_kind, Is, mode, resident = case
+    monkeypatch.setenv("Q4K_DECODE", decode)
     W = Workload("single", H, I, E, T, m, ids_kind, Is, mode, 1200 + sum(case[:5]))
     assert q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is) == 1
+    want = q4k.PATH_RESIDENT if (decode == "1" and resident) else q4k.PATH_PERSISTENT
+    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) == want
     layer = Layer(W, _inputs(W))
     ref2, f2 = _two_launch(layer, monkeypatch)
     assert f2 == 0
@@ -206,22 +213,6 @@ def test_single_launch_m_changes_on_one_workspace(monkeypatch):
     assert int(host(f)[0]) == 0
 
 
-def test_two_launch_layer_with_bulk_copy_kernel_matches_oracle(monkeypatch):
-    """The two-launch layer on the opt-in bulk-copy id-GEMV (Q4K_STREAM=1), whose gate|up
-    launch waits for the previous kernel before reading the ids (the first launch of a layer)."""
-    W = Workload("stream", 1024, 512, 16, 4, 3, "uniform", 512, 1, 1601)
-    layer = Layer(W, _inputs(W))
-    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
-    monkeypatch.setenv("Q4K_STREAM", "1")
-    ws = torch.empty(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
-    f = err_flag()
-    layer.run(ws, f)
-    got = host(layer.y)
-    assert int(host(f)[0]) == 0
-    ref, _ = layer.oracle()
-    rows_close(got, ref, what="two-launch layer, bulk-copy kernel")
-
-
 def test_single_launch_hidden_changes_on_one_workspace(monkeypatch):
     """Layers of different hidden sizes share one workspace: the sync area's layout moves with
     hidden, so a call finds the previous call's counters and flags at other offsets (it falls
@@ -237,3 +228,29 @@ def test_single_launch_hidden_changes_on_one_workspace(monkeypatch):
         L.run(ws, f)
         assert np.array_equal(host(L.y), ref), L.W.name
     assert int(host(f)[0]) == 0
+
+
+@pytest.mark.parametrize("decode", ["1", "0"], ids=["resident", "persistent"])
+def test_single_launch_wait_limit_runs_out(decode, monkeypatch):
+    """A wait limit of 1 ns (Q4K_WAIT_NS) makes the hand-off waits give up: the kernel returns
+    with Q4K_ERR_TIMEOUT in the device flag after its bulk copies have landed (no fault, no
+    hang, the context stays usable), and the next call on a cleared workspace with the default
+    limit is right."""
+    monkeypatch.setenv("Q4K_DECODE", decode)
+    W = WORKLOADS["qwen3moe_h2048_i768_e128_t8_m1"]
+    layer = Layer(W, _inputs(W))
+    ref2, _ = _two_launch(layer, monkeypatch)
+    path = q4k.q4k_moe_layer_path(W.m, W.top_k, W.num_experts, W.hidden, W.inter, W.shared_inter)
+    assert path == (q4k.PATH_RESIDENT if decode == "1" else q4k.PATH_PERSISTENT)
+    ws = torch.zeros(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
+    f = err_flag()
+    monkeypatch.setenv("Q4K_WAIT_NS", "1")
+    layer.run(ws, f)
+    assert int(host(f)[0]) == Q4K_ERR_TIMEOUT
+    monkeypatch.delenv("Q4K_WAIT_NS")
+    ws.zero_()
+    f.zero_()
+    layer.y.zero_()
+    layer.run(ws, f)
+    assert int(host(f)[0]) == 0
+    assert np.array_equal(host(layer.y), ref2)

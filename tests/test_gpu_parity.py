@@ -22,13 +22,6 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["bulk_copy", "bucketed"])
-def kernel_path(request, monkeypatch):
-    """Small batches run on the bucketed kernel by default; Q4K_STREAM=1 sends them to the
-    opt-in bulk-copy kernel, so both are compared with the oracle."""
-    monkeypatch.setenv("Q4K_STREAM", "1" if request.param == "bulk_copy" else "0")
-    return request.param
-
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -104,7 +97,7 @@ def _run_gemv(w, E, a, outer, inner, ids, m, T, n, k, flag=None):
                                        (2, 24, 4096, 2, 2),     # 64 threads per row: cross-warp sums
                                        (1, 40, 7168, 2, 1),     # 112 of 128 threads per row, ragged tile
                                        (2, 20, 10240, 1, 2)])   # two 64-weight groups per thread
-def test_id_gemv_matches_oracle(mode, E, n, k, m, T, kernel_path):
+def test_id_gemv_matches_oracle(mode, E, n, k, m, T):
     w, ids, a, outer, inner = _gemv_case(100 + n, E, n, k, m, T, mode)
     ref, _ = oracle.moe_id_gemv(w, E, a, outer, inner, ids, m, T, n, k)
     got = _run_gemv(w, E, a, outer, inner, ids, m, T, n, k)
@@ -116,7 +109,7 @@ def test_id_gemv_matches_oracle(mode, E, n, k, m, T, kernel_path):
                                        (64, 36, 256, 5, 16),    # 80 pairs: bucketed path, top_k 16
                                        (4096, 8, 256, 3, 4),    # the expert-count limit
                                        (1, 4, 256, 7, 1)])      # one expert, the smallest n
-def test_id_gemv_limits(mode, E, n, k, m, T, kernel_path):
+def test_id_gemv_limits(mode, E, n, k, m, T):
     w, ids, a, outer, inner = _gemv_case(300 + E + m, E, n, k, m, T, mode)
     ref, _ = oracle.moe_id_gemv(w, E, a, outer, inner, ids, m, T, n, k)
     got = _run_gemv(w, E, a, outer, inner, ids, m, T, n, k)
@@ -124,7 +117,7 @@ def test_id_gemv_limits(mode, E, n, k, m, T, kernel_path):
 
 
 @pytest.mark.parametrize("mode", ["gate_up", "down"])
-def test_pages_tiny_case(mode, kernel_path):
+def test_pages_tiny_case(mode):
     """The ferrum-kernels tiny case: its ids and input recipes, against the oracle, and
     batched == per-token calls on the GPU bit for bit."""
     with open(os.path.join(GOLDEN, "ferrum_tiny_case.json")) as f:
@@ -152,7 +145,7 @@ def test_pages_tiny_case(mode, kernel_path):
     assert np.array_equal(batched, np.concatenate(per_token))
 
 
-def test_id_gemv_weight_byte_offset_and_duplicates(kernel_path):
+def test_id_gemv_weight_byte_offset_and_duplicates():
     E, n, k, m, T = 5, 64, 512, 4, 3
     w, _, a, outer, inner = _gemv_case(7, E, n, k, m, T, "gate_up")
     ids = np.array([1, 1, 4, 0, 0, 0, 2, 1, 2, 3, 3, 3], np.int32)  # same expert twice in one token
@@ -165,7 +158,7 @@ def test_id_gemv_weight_byte_offset_and_duplicates(kernel_path):
     rows_close(host(out), ref, what="offset+duplicates")
 
 
-def test_id_gemv_out_of_range_ids_flag_and_zero_rows(kernel_path):
+def test_id_gemv_out_of_range_ids_flag_and_zero_rows():
     E, n, k, m, T = 4, 64, 256, 3, 2
     w, _, a, outer, inner = _gemv_case(9, E, n, k, m, T, "gate_up")
     ids = np.array([0, 9, -1, 2, 3, 1], np.int32)
@@ -177,14 +170,14 @@ def test_id_gemv_out_of_range_ids_flag_and_zero_rows(kernel_path):
     rows_close(got, ref, what="invalid ids")
 
 
-def test_id_gemv_empty_batch(kernel_path):
+def test_id_gemv_empty_batch():
     w, ids, a, outer, inner = _gemv_case(10, 4, 64, 256, 1, 2, "gate_up")
     out = torch.full((2, 64), 7.0, device="cuda")
     q4k.q4k_moe_id_gemv(dev(w), 0, 4, dev(a), outer, inner, dev(ids), 0, 2, 64, 256, out)
     assert np.all(host(out) == 7.0)
 
 
-def test_id_gemv_skewed_bucket_many_chunks(kernel_path):
+def test_id_gemv_skewed_bucket_many_chunks():
     """One expert takes every pair (a Zipf head): 20 pairs -> 5 chunks over the same tiles."""
     E, n, k, m, T = 16, 96, 1024, 20, 1
     w, _, a, outer, inner = _gemv_case(11, E, n, k, m, T, "gate_up")
@@ -205,7 +198,7 @@ def _ffn_case(seed, E, H, I, m, T):
 
 
 @pytest.mark.parametrize("E,H,I,m,T", [(8, 512, 256, 5, 2), (16, 1024, 768, 3, 4), (4, 256, 512, 9, 2)])
-def test_expert_ffn_matches_oracle(E, H, I, m, T, kernel_path):
+def test_expert_ffn_matches_oracle(E, H, I, m, T):
     wg, wu, wd, ids, x = _ffn_case(40 + E, E, H, I, m, T)
     ref, _ = oracle.expert_ffn(wg, wu, wd, E, x, ids, m, T, H, I)
     ws_bytes = q4k.q4k_moe_workspace_size(m, T, E, max(H, I), max(H, I))
@@ -216,7 +209,7 @@ def test_expert_ffn_matches_oracle(E, H, I, m, T, kernel_path):
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
-def test_combine_matches_oracle(mode, kernel_path):
+def test_combine_matches_oracle(mode):
     m, T, H = 5, 3, 520
     rng = np.random.default_rng(mode)
     eo = rng.standard_normal((m * T, H)).astype(np.float32)
@@ -264,7 +257,7 @@ def _run_layer_device(W, wg, wu, wd, shared, ids, x, hm, rw, gl):
 
 
 @pytest.mark.parametrize("name", ["qwen3moe_h2048_i768_e128_t8_m1", "qwen3moe_h2048_i768_e128_t8_m16_zipf"])
-def test_layer_full_size_qwen3_like(name, kernel_path):
+def test_layer_full_size_qwen3_like(name):
     """The Qwen3-MoE-like layer at its full size (m=1 and m=16 Zipf), in the launch
     configuration the benchmark times, against the oracle's whole layer."""
     from bit_quantized_moe_q4k_gb300.workloads import WORKLOADS
@@ -277,7 +270,7 @@ def test_layer_full_size_qwen3_like(name, kernel_path):
     rows_close(got, ref, what=name)
 
 
-def test_layer_top_k_16(kernel_path):
+def test_layer_top_k_16():
     """The combine at the top_k limit (16 slots per token), with a sigmoid-gated shared expert."""
     from bit_quantized_moe_q4k_gb300.workloads import Workload
     W = Workload("topk16", 256, 256, 32, 16, 3, "uniform", 256, 1, 950)
@@ -288,7 +281,7 @@ def test_layer_top_k_16(kernel_path):
     rows_close(_run_layer_device(W, *args), ref, what="layer top_k 16")
 
 
-def test_layer_small_all_shared_modes_and_host_variant(kernel_path):
+def test_layer_small_all_shared_modes_and_host_variant():
     from bit_quantized_moe_q4k_gb300.workloads import Workload
     for mode in (0, 1, 2):
         W = Workload("small", 512, 256, 12, 3, 6, "uniform", 0 if mode == 0 else 512, mode, 900 + mode)
