@@ -4,10 +4,10 @@
 // What it computes (moeflux expert_forward.rs: gate, up, SwiGLU, down, then the batched
 // combine y = h_mid + sum_s w_s * expert_out_s + g * shared_out; ferrum-kernels
 // q4_k_moe_id_gemv_batched.rs for each projection): the same as the two-launch layer of
-// q4k_gemv.cu, bit for bit. Every output row is reduced by the same lanes in the same order
-// (acc_sub_pair, then the lane shuffles), the down input is staged with the same arithmetic
-// (per 32-element sub-block: max|x|, X = rint(x * 32767 / max), sum X), and the combine adds
-// the slots in order.
+// q4k_gemv.cu, bit for bit. Every output row is summed in the order all kernels use (each
+// lane's block terms folded left to right, then the xor shuffles over its lanes; see
+// block_term), the down input is staged with the same arithmetic (per 32-element sub-block:
+// max|x|, X = rint(x * 32767 / max), sum X), and the combine adds the slots in order.
 //
 // How (GB300 design). One CTA per SM, 16 warps, up to ~220 KB of shared memory each, so a
 // decode layer's touched weights (Qwen3-MoE-like m = 1: 24 MB) fit in the grid's shared
@@ -18,13 +18,16 @@
 //     mbarrier each), then its down rows (one contiguous range of hidden rows of every expert
 //     of the batch and of the shared expert). Before waiting for the previous kernel it
 //     already starts its share of the shared expert's slabs into L2.
-//  2. Gate|up: warps take slices as they land (gate rows and up rows as separate tasks); the
-//     warp that completes an item forms silu(g) * u for its 32 rows -- one 32-element
-//     sub-block of the down input -- quantizes that sub-block to the staged 16-bit form,
-//     stores it to the workspace and publishes the item's flag.
+//  2. Gate|up: rows stream through the warps as their slices land. A lane owns one 64-weight
+//     group of one block of every row it sees and keeps that block's activations in
+//     registers, so shared memory only delivers the weights (the activation planes are 2.2x
+//     the bytes of the weights they meet, and re-reading them per row left the kernel bound
+//     by shared-memory bandwidth). The warp that completes an item forms silu(g) * u for its
+//     32 rows -- one 32-element sub-block of the down input -- quantizes that sub-block to the
+//     staged 16-bit form, stores it to the workspace and publishes the item's flag.
 //  3. Down: each CTA waits for every item's flag (the one hand-off between CTAs), copies the
-//     staged down inputs of all pairs from L2, and computes its hidden rows of every expert
-//     from shared memory.
+//     staged down inputs of all pairs from L2, and streams its hidden rows of every expert
+//     through the warps the same way.
 //  4. Combine: the CTA holds those rows of every expert, so it forms y for them itself: no
 //     second hand-off, no counters, no atomics.
 // CTA 0 advances the generation word of the tagged flags (q4k_sync.cuh) while it waits for
@@ -49,7 +52,6 @@ constexpr int kDecMaxItems = 8;                         // gate|up items per CTA
 constexpr int kDecMaxTokens = 4;                        // m
 constexpr int kDecMaxPairs = 32;                        // routed pairs (one warp buckets them)
 constexpr int kDecRowTile = 8;                          // hidden rows per down tile
-constexpr int kDecTok = 4;                              // tokens per pass of a task
 constexpr int kDecBarB = kDecMaxItems * kDecSlices;     // the down rows' mbarrier
 constexpr int kDecMaxCtas = 1024;                       // start-tag words
 
@@ -88,45 +90,68 @@ __device__ __forceinline__ uint4 lds16(const uint8_t* p) {
     return v;
 }
 
-// One lane's share of a row: blocks b = sl, sl + S, ... of the row at wrow (shared memory)
-// against up to kDecTok staged rows (xs[t], ms[t]; t < nt). The same sequence of acc_sub_pair
-// updates as item_compute performs for the lane with these (c, sl, S), so after the lane
-// reduction the row's sum is the same float.
-__device__ __forceinline__ void lane_dots(const uint8_t* wrow, bool row_ok, int nb, int S, int sl, int c,
-                                          const uint8_t* const (&xs)[kDecTok], const float2* const (&ms)[kDecTok],
-                                          int nt, float (&acc)[kDecTok]) {
-#pragma unroll
-    for (int t = 0; t < kDecTok; ++t) acc[t] = 0.0f;
-    const int nbl = sl < nb ? (nb - sl + S - 1) / S : 0;
-    for (int i = 0; i < nbl; ++i) {
-        const int b = sl + S * i;
-        uint4 H = make_uint4(0, 0, 0, 0), Q0 = H, Q1 = H;
-        if (row_ok) {
-            const uint8_t* p = wrow + b * kBlockBytes;
-            H = lds16(p);
-            Q0 = lds16(p + 16 + 32 * c);
-            Q1 = lds16(p + 32 + 32 * c);
-        }
-        float sa, ma, sb, mb;
-        block_scales(H, c, sa, ma, sb, mb);
-#pragma unroll
-        for (int t = 0; t < kDecTok; ++t) {
-            if (t < nt) {
-                const uint4* xp = reinterpret_cast<const uint4*>(xs[t] + (4 * b + c) * kPairBytes);
-                const float4 mt = *reinterpret_cast<const float4*>(ms[t] + 8 * b + 2 * c);
-                int Sa, Sb;
-                dot64(Q0, Q1, xp, Sa, Sb);
-                acc[t] = acc_sub_pair(acc[t], mt, sa, ma, sb, mb, Sa, Sb);
-            }
-        }
-    }
+// Lanes of a row stream. A row of k weights has nb = k/256 blocks, which item_compute splits
+// over S = 1 << lg lanes (block b to lane sl = b % S, i = b / S) times 4 (the 64-weight group
+// c). Here they are laid out side by side: a slot of L = 4*S*NI lanes, NI = ceil(nb / S), in
+// which lane c | sl << 2 | i << (2 + lg) owns group c of block b = sl + S*i of every row that
+// passes (lanes with b >= nb hold nothing), with that block's staged activations in
+// registers. A row's sum is then formed in the fixed order of block_term: the fold over i by
+// NI - 1 shuffles up the slot, then the xor shuffles over c and sl.
+struct RowLanes {
+    int S, nb, NI, L, NS, slot, c, sl, i, b;
+    bool live;  // the lane belongs to a slot
+};
+
+__host__ __device__ __forceinline__ int row_slot_lanes(int k, int lg) {
+    const int S = 1 << lg, nb = k / kQK;
+    return 4 * S * ((nb + S - 1) / S);
 }
 
-// Reduce over the 4*S lanes of a row (c bits, then s bits), as item_compute does.
-__device__ __forceinline__ void lane_reduce(float (&acc)[kDecTok], int S) {
+__device__ __forceinline__ RowLanes row_lanes_of(int k, int lg, int lane) {
+    RowLanes R;
+    R.S = 1 << lg;
+    R.nb = k / kQK;
+    R.NI = (R.nb + R.S - 1) / R.S;
+    R.L = 4 * R.S * R.NI;
+    R.NS = 32 / R.L;
+    R.slot = lane / R.L;
+    const int w = lane - R.slot * R.L;
+    R.c = w & 3;
+    R.sl = (w >> 2) & (R.S - 1);
+    R.i = w >> (2 + lg);
+    R.b = R.sl + R.S * R.i;
+    R.live = R.slot < R.NS;
+    return R;
+}
+
+// The lane's block of a staged token row (planes and (delta, sum X) pairs in shared memory).
+__device__ __forceinline__ void load_x(const uint8_t* xrow, const float2* xmeta, const RowLanes& R, uint32_t (&x)[32],
+                                       float4& mt) {
+    const uint8_t* xp = xrow + (4 * R.b + R.c) * kPairBytes;
 #pragma unroll
-    for (int t = 0; t < kDecTok; ++t)
-        for (int off = 1; off < 4 * S; off <<= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+    for (int u = 0; u < 8; ++u) {
+        const uint4 v = lds16(xp + 16 * u);
+        x[4 * u] = v.x; x[4 * u + 1] = v.y; x[4 * u + 2] = v.z; x[4 * u + 3] = v.w;
+    }
+    const uint4 m4 = lds16(reinterpret_cast<const uint8_t*>(xmeta + 8 * R.b + 2 * R.c));
+    mt = make_float4(__uint_as_float(m4.x), __uint_as_float(m4.y), __uint_as_float(m4.z), __uint_as_float(m4.w));
+}
+
+// The row's sum from every lane's term T: valid in the slot's lanes of the last stage
+// (i == NI - 1); lanes outside every slot pass junk that no slot reads.
+__device__ __forceinline__ float row_sum(float T, const RowLanes& R) {
+    float F = T;
+    for (int d = 1; d < R.NI; ++d) {
+        const float prev = __shfl_up_sync(0xffffffffu, F, 4 * R.S);
+        if (R.i == d) F = R.b < R.nb ? __fadd_rn(prev, T) : prev;
+    }
+    for (int off = 1; off < 4 * R.S; off <<= 1) F += __shfl_xor_sync(0xffffffffu, F, off);
+    return F;
+}
+
+// Lane (c = 0, sl = 0) of the last stage of a live slot: the one that holds the row's sum.
+__device__ __forceinline__ bool row_owner(const RowLanes& R) {
+    return R.live && R.i == R.NI - 1 && R.c == 0 && R.sl == 0;
 }
 
 // Block-wide: wait until f1[j] == tag for j < n1 and f2[j] == tag for j < n2 (acquire loads;
@@ -203,7 +228,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const __gr
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ DecBuckets s_b;
     __shared__ __align__(8) uint64_t s_bar[kDecBarB + 1];
-    __shared__ int s_done[kDecMaxItems];   // tasks of each gate|up item finished
+    __shared__ int s_done[kDecMaxItems];   // rows of each gate|up item finished (per pair)
+    __shared__ int s_icnt[kDecMaxItems];   // pairs of each gate|up item of the CTA
+    __shared__ uint8_t s_itok[kDecMaxItems][kDecMaxPairs];  // token of each pair slot
+    __shared__ int s_pmax;
     __shared__ float s_w[kDecMaxPairs];    // routing weights
     __shared__ float s_g[kDecMaxTokens];   // shared-expert gate factor per token
     __shared__ uint64_t s_tag;
@@ -287,6 +315,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const __gr
         }
     };
     const int units_b = U + (P.has_shared ? 1 : 0);
+    // the CTA's items: pairs, and the token of each pair slot
+    if (warp == 1 && fits) {
+        int pm = 0;
+        for (int j = 0; j < nitems; ++j) {
+            int g, r, e, tile;
+            locate(a0 + j, g, r, e, tile);
+            const int cnt = g == 0 ? s_b.cnt[r] : m;
+            if (lane < cnt) s_itok[j][lane] = (uint8_t)(g == 0 ? s_b.plist[r][lane] / T : lane);
+            if (lane == 0) s_icnt[j] = cnt;
+            pm = max(pm, cnt);
+        }
+        if (lane == 0) s_pmax = pm;
+    }
     int64_t boff_sh = 0;  // byte offset of the shared expert's down rows in region B
     if (tid == 0 && fits) {
         // every weight byte of the CTA, in the order it is needed
@@ -322,87 +363,105 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const __gr
         }
     }
     boff_sh = (int64_t)U * rows_c * B0.nb01;
+    __syncthreads();  // the item tables (and the issue, which runs before any wait in its warp)
 
-    // ---- gate|up tasks: (item, slice, gate or up, group of rows of a warp), slices in order
+    // ---- gate|up rows, streamed through the warps' slots: stream sigma takes the rows
+    // rho = sigma, sigma + ns, ... of the CTA's items in (item, slice, gate|up, row) order, so all
+    // streams move through the slices in the order they land; each row once per pair slot
+    // pi < pmax (slots beyond the item's pairs do nothing)
     {
-        const int lgA = A0.lg_split, S = 1 << lgA, rpw = 8 >> lgA;
-        const int rgs = kDecSliceRows / rpw;          // row groups per slice
-        const int tpi = kDecSlices * rgs * 2;         // tasks per item
-        const int c = lane & 3, sl = (lane >> 2) & (S - 1), lrow = lane >> (2 + lgA);
-        const int nb = ka / kQK;
+        const RowLanes R = row_lanes_of(ka, A0.lg_split, lane);
+        const int ns = kDecWarps * R.NS;
+        const int sigma = warp * R.NS + R.slot;
+        const int NR = fits ? nitems * 2 * kDecItemRows : 0;
+        const int nrho = (R.live && sigma < NR) ? (NR - sigma + ns - 1) / ns : 0;
+        const int nrho_max = __reduce_max_sync(0xffffffffu, nrho);
+        const int pmax = s_pmax;
         float* gu = reinterpret_cast<float*>(smem + P.off_gu);
-        for (int task = warp; fits && task < nitems * tpi; task += kDecWarps) {
-            if (__shfl_sync(0xffffffffu, s_abort, 0)) break;  // (the same decision in every lane)
-            const int j = task / tpi, q = task % tpi;
-            const int s = q / (2 * rgs), rem = q % (2 * rgs), slab = rem & 1, rg = rem >> 1;
-            int g, r, e, tile;
-            locate(a0 + j, g, r, e, tile);
-            const GroupDev& A = P.a[g];
-            if (!__all_sync(0xffffffffu, mbar_wait_for(&s_bar[j * kDecSlices + s], 0, &s_abort, P.wait_ns))) {
+        uint32_t x[32];
+        float4 mt = make_float4(0.f, 0.f, 0.f, 0.f);
+        int xkey = -1, last_bar = -1;
+        for (int t = 0; t < nrho_max; ++t) {
+            const int rho = sigma + t * ns;
+            const bool rvalid = t < nrho;
+            const int j = rho >> 6, s = (rho >> 4) & 3, slab = (rho >> 3) & 1, rin = (rho & 7) + 8 * s;
+            bool landed = true;
+            if (rvalid && j * kDecSlices + s != last_bar) {
+                last_bar = j * kDecSlices + s;
+                landed = mbar_wait_for(&s_bar[last_bar], 0, &s_abort, P.wait_ns);
+            }
+            if (!__all_sync(0xffffffffu, landed)) {
                 s_abort = 1;
                 break;
             }
-            const int rin = s * kDecSliceRows + rg * rpw + lrow;  // row within the item (always < 32)
-            const uint8_t* wrow = smem + P.off_a + (int64_t)j * P.item_bytes + (int64_t)(slab * kDecItemRows + rin) * A.nb01;
-            const int cnt = g == 0 ? s_b.cnt[r] : m;
-            for (int p0 = 0; p0 < cnt; p0 += kDecTok) {
-                const int nt = min(kDecTok, cnt - p0);
-                const uint8_t* xs[kDecTok];
-                const float2* ms[kDecTok];
-#pragma unroll
-                for (int t = 0; t < kDecTok; ++t) {
-                    const int pi = min(p0 + t, cnt - 1);
-                    const int tok = g == 0 ? s_b.plist[r][pi] / T : pi;
-                    xs[t] = xs0 + tok * xrow;
-                    ms[t] = xm0 + tok * (ka / 32);
+            const int cnt = rvalid ? s_icnt[j] : 0;
+            uint4 H = make_uint4(0, 0, 0, 0), Q0 = H, Q1 = H;
+            if (rvalid && R.b < R.nb) {
+                const uint8_t* p = smem + P.off_a + (int64_t)j * P.item_bytes +
+                                   (int64_t)(slab * kDecItemRows + rin) * A0.nb01 + R.b * kBlockBytes;
+                H = lds16(p);
+                Q0 = lds16(p + 16 + 32 * R.c);
+                Q1 = lds16(p + 32 + 32 * R.c);
+            }
+            float sa, ma, sb, mb;
+            block_scales(H, R.c, sa, ma, sb, mb);
+            int trig = -1;
+            for (int pi = 0; pi < pmax; ++pi) {
+                const bool work = pi < cnt;
+                float T = 0.0f;
+                if (work && R.b < R.nb) {
+                    const int tok = s_itok[j][pi];
+                    if (tok != xkey) {
+                        load_x(xs0 + tok * xrow, xm0 + tok * (ka / 32), R, x, mt);
+                        xkey = tok;
+                    }
+                    int Sa, Sb;
+                    dot64_regs(Q0, Q1, x, Sa, Sb);
+                    T = block_term(mt, sa, ma, sb, mb, Sa, Sb);
                 }
-                float acc[kDecTok];
-                lane_dots(wrow, true, nb, S, sl, c, xs, ms, nt, acc);
-                lane_reduce(acc, S);
-                if ((lane & (4 * S - 1)) == 0) {
-#pragma unroll
-                    for (int t = 0; t < kDecTok; ++t)
-                        if (t < nt) gu[((j * P.gu_pairs + p0 + t) * 2 + slab) * kDecItemRows + rin] = acc[t];
+                const float v = row_sum(T, R);
+                if (work && row_owner(R)) {
+                    gu[((j * P.gu_pairs + pi) * 2 + slab) * kDecItemRows + rin] = v;
+                    __threadfence_block();
+                    if (atomicAdd(&s_done[j], 1) == 2 * kDecItemRows * cnt - 1) trig = j;
                 }
             }
-            // the warp that completes the item stages its 32 rows of the down input
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) {
+            // an item whose rows are all done: the warp stages its 32 rows of the down input
+            for (unsigned tm = __ballot_sync(0xffffffffu, trig >= 0); tm; tm &= tm - 1u) {
+                const int jj = __shfl_sync(0xffffffffu, trig, __ffs(tm) - 1);
+                __syncwarp();
                 __threadfence_block();
-                last = atomicAdd(&s_done[j], 1) == tpi - 1;
-                __threadfence_block();
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            __syncwarp();
-            if (!last) continue;
-            const GroupDev& B = P.b[g];
-            const int kb = B.k;
-            const int64_t pb = (int64_t)(kb / 64) * kPairBytes;
-            for (int pi = 0; pi < cnt; ++pi) {
-                const int p = g == 0 ? s_b.plist[r][pi] : pi;
-                const float gv = gu[((j * P.gu_pairs + pi) * 2 + 0) * kDecItemRows + lane];
-                const float uv = gu[((j * P.gu_pairs + pi) * 2 + 1) * kDecItemRows + lane];
-                const float v = silu(gv) * uv;
-                float mx = fabsf(v);
+                int gg, rr, ee, tt;
+                locate(a0 + jj, gg, rr, ee, tt);
+                const int cc = s_icnt[jj];
+                const GroupDev& B = P.b[gg];
+                const int kb = B.k;
+                const int64_t pb = (int64_t)(kb / 64) * kPairBytes;
+                for (int pp = 0; pp < cc; ++pp) {
+                    const int p = gg == 0 ? s_b.plist[rr][pp] : pp;
+                    const float gv = gu[((jj * P.gu_pairs + pp) * 2 + 0) * kDecItemRows + lane];
+                    const float uv = gu[((jj * P.gu_pairs + pp) * 2 + 1) * kDecItemRows + lane];
+                    const float a = silu(gv) * uv;
+                    float mx = fabsf(a);
 #pragma unroll
-                for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                int X = 0;
-                if (mx > 0.0f) {
-                    const float inv = 32767.0f / mx;
-                    X = max(-32767, min(32767, __float2int_rn(v * inv)));
+                    for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    int X = 0;
+                    if (mx > 0.0f) {
+                        const float inv = 32767.0f / mx;
+                        X = max(-32767, min(32767, __float2int_rn(a * inv)));
+                    }
+                    int sx = X;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, off);
+                    uint8_t* planes = P.stg_planes[gg] + (int64_t)p * pb + (tt >> 1) * kPairBytes + (tt & 1) * 64;
+                    planes[lane] = (uint8_t)(X & 0xFF);
+                    planes[32 + lane] = (uint8_t)((X >> 8) & 0xFF);
+                    if (lane == 0) P.stg_meta[gg][(int64_t)p * (kb / 32) + tt] = make_float2(mx / 32767.0f, (float)sx);
                 }
-                int sx = X;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) sx += __shfl_xor_sync(0xffffffffu, sx, off);
-                uint8_t* planes = P.stg_planes[g] + (int64_t)p * pb + (tile >> 1) * kPairBytes + (tile & 1) * 64;
-                planes[lane] = (uint8_t)(X & 0xFF);
-                planes[32 + lane] = (uint8_t)((X >> 8) & 0xFF);
-                if (lane == 0) P.stg_meta[g][(int64_t)p * (kb / 32) + tile] = make_float2(mx / 32767.0f, (float)sx);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_u64(P.flags + a0 + jj, tag);
             }
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_u64(P.flags + a0 + j, tag);
         }
     }
     __syncthreads();  // the gate|up tiles' space is free for the staged down inputs
@@ -413,74 +472,89 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const __gr
     if (ok) ok = dec_wait_tags(P.flags, na, P.cta_tag, cta == 0 ? G : 0, tag, P.wait_ns);
     if (ok && cta == 0 && tid == 0) st_relaxed_u64(P.gen, tag);
     if (ok) {
-        // staged down inputs of every pair (routed, then the shared expert's tokens), from L2
-        for (int g = 0; g < P.n_groups; ++g) {
-            const int rows = g == 0 ? n_pairs : m;
-            const int kb = P.b[g].k;
-            const int64_t n16 = (int64_t)rows * ((kb / 64) * kPairBytes + (kb / 32) * 8) / 16;
-            const int64_t np16 = (int64_t)rows * (kb / 64) * kPairBytes / 16;
-            const uint4* sp = reinterpret_cast<const uint4*>(P.stg_planes[g]);
-            const uint4* sm = reinterpret_cast<const uint4*>(P.stg_meta[g]);
-            uint4* dp = reinterpret_cast<uint4*>(smem + P.off_act[g]);
-            uint4* dm = reinterpret_cast<uint4*>(smem + P.off_actmeta[g]);
-            for (int64_t i0 = 0; i0 < n16; i0 += 4 * kDecThreads) {
-                uint4 v[4];
+        // staged down inputs of every pair (routed, then the shared expert's tokens), from L2:
+        // both groups' rows (planes, then (delta, sum X) pairs, contiguous per group in the
+        // workspace and in shared memory) in one pass of loads
+        const int64_t n0 = (int64_t)n_pairs * ((B0.k / 64) * kPairBytes + (B0.k / 32) * 8) / 16;
+        const int64_t n1 = P.has_shared ? (int64_t)m * ((P.b[1].k / 64) * kPairBytes + (P.b[1].k / 32) * 8) / 16 : 0;
+        const uint4* s0 = reinterpret_cast<const uint4*>(P.stg_planes[0]);
+        const uint4* s1 = reinterpret_cast<const uint4*>(P.stg_planes[1]);
+        uint4* d0 = reinterpret_cast<uint4*>(smem + P.off_act[0]);
+        uint4* d1 = reinterpret_cast<uint4*>(smem + P.off_act[1]);
+        for (int64_t i0 = 0; i0 < n0 + n1; i0 += 8 * kDecThreads) {
+            uint4 v[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t i = i0 + u * kDecThreads + tid;
-                    if (i < n16) v[u] = __ldcg(i < np16 ? sp + i : sm + (i - np16));
-                }
+            for (int u = 0; u < 8; ++u) {
+                const int64_t i = i0 + u * kDecThreads + tid;
+                if (i < n0 + n1) v[u] = __ldcg(i < n0 ? s0 + i : s1 + (i - n0));
+            }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t i = i0 + u * kDecThreads + tid;
-                    if (i < n16) {
-                        if (i < np16) dp[i] = v[u]; else dm[i - np16] = v[u];
-                    }
-                }
+            for (int u = 0; u < 8; ++u) {
+                const int64_t i = i0 + u * kDecThreads + tid;
+                if (i < n0) d0[i] = v[u];
+                else if (i < n0 + n1) d1[i - n0] = v[u];
             }
         }
         ok = __syncthreads_and(rows_c == 0 || mbar_wait_for(&s_bar[kDecBarB], 0, &s_abort, P.wait_ns));
     }
 
-    // ---- down rows of every expert (and the shared expert) for the CTA's rows of hidden
+    // ---- down rows of every expert (and the shared expert) for the CTA's rows of hidden,
+    // streamed through the warps' slots: a pass over the routed units (and the shared expert
+    // when its rows have the same length), then one over the shared expert otherwise. Stream
+    // sigma takes a contiguous range of the pass's (unit, pair slot, row) items, so its lanes
+    // reload their activations only when the pair changes.
     float* eout = reinterpret_cast<float*>(smem + P.off_eout);
     if (ok && rows_c > 0) {
-        const int lgB = B0.lg_split, S = 1 << lgB, rpw = 8 >> lgB;
-        const int spu = (rows_c + rpw - 1) / rpw;
-        const int c = lane & 3, sl = (lane >> 2) & (S - 1), lrow = lane >> (2 + lgB);
-        for (int task = warp; task < units_b * spu; task += kDecWarps) {
-            const int u = task / spu, q = task % spu;
-            const int g = u < U ? 0 : 1;
-            const GroupDev& B = P.b[g];
-            const int kb = B.k, nb = kb / kQK;
-            const int rl = q * rpw + lrow;
-            const bool row_ok = rl < rows_c;
-            const int64_t boff = g == 0 ? (int64_t)u * rows_c * B.nb01 : boff_sh;
-            const uint8_t* wrow = smem + P.off_b + boff + (int64_t)(row_ok ? rl : 0) * B.nb01;
-            const int cnt = g == 0 ? s_b.cnt[u] : m;
-            const int64_t pb = (int64_t)(kb / 64) * kPairBytes;
-            const uint8_t* xa = smem + P.off_act[g];
-            const float2* xm = reinterpret_cast<const float2*>(smem + P.off_actmeta[g]);
-            for (int p0 = 0; p0 < cnt; p0 += kDecTok) {
-                const int nt = min(kDecTok, cnt - p0);
-                const uint8_t* xs[kDecTok];
-                const float2* ms[kDecTok];
-                int rowid[kDecTok];
-#pragma unroll
-                for (int t = 0; t < kDecTok; ++t) {
-                    const int pi = min(p0 + t, cnt - 1);
-                    const int p = g == 0 ? s_b.plist[u][pi] : pi;
-                    xs[t] = xa + p * pb;
-                    ms[t] = xm + p * (kb / 32);
-                    rowid[t] = g == 0 ? p : n_pairs + p;
+        const bool same_k = !P.has_shared || P.b[1].k == B0.k;
+        for (int pass = 0; pass < (same_k ? 1 : 2); ++pass) {
+            const int u_lo = pass == 0 ? 0 : U;
+            const int u_hi = pass == 0 ? (same_k ? units_b : U) : units_b;
+            const int kb = pass == 0 ? B0.k : P.b[1].k;
+            const RowLanes R = row_lanes_of(kb, B0.lg_split, lane);
+            const int ns = kDecWarps * R.NS;
+            const int sigma = warp * R.NS + R.slot;
+            int pmax = 1;
+            for (int u = u_lo; u < u_hi; ++u) pmax = max(pmax, u < U ? s_b.cnt[u] : m);
+            const int NQ = (u_hi - u_lo) * pmax * rows_c;
+            const int q0 = R.live ? (int)((int64_t)sigma * NQ / ns) : 0;
+            const int nq = R.live ? (int)((int64_t)(sigma + 1) * NQ / ns) - q0 : 0;
+            const int nq_max = __reduce_max_sync(0xffffffffu, nq);
+            uint32_t x[32];
+            float4 mt = make_float4(0.f, 0.f, 0.f, 0.f);
+            int xkey = -1;
+            // the lane's item: unit, pair slot, row (advanced one by one)
+            int rl = q0 % rows_c, pi = (q0 / rows_c) % pmax, u = u_lo + q0 / rows_c / pmax;
+            for (int t = 0; t < nq_max; ++t) {
+                const bool valid = t < nq;
+                const int g = u < U ? 0 : 1;
+                const int cnt = g == 0 ? s_b.cnt[u] : m;
+                const bool work = valid && pi < cnt;
+                const int p = work ? (g == 0 ? s_b.plist[u][pi] : pi) : 0;
+                float T = 0.0f;
+                if (work && R.b < R.nb) {
+                    const int key = u * kDecMaxPairs + pi;
+                    if (key != xkey) {
+                        load_x(smem + P.off_act[g] + (int64_t)p * (kb / 64) * kPairBytes,
+                               reinterpret_cast<const float2*>(smem + P.off_actmeta[g]) + (int64_t)p * (kb / 32), R, x, mt);
+                        xkey = key;
+                    }
+                    const GroupDev& B = P.b[g];
+                    const int64_t boff = g == 0 ? (int64_t)u * rows_c * B.nb01 : boff_sh;
+                    const uint8_t* w = smem + P.off_b + boff + (int64_t)rl * B.nb01 + R.b * kBlockBytes;
+                    const uint4 H = lds16(w), Q0 = lds16(w + 16 + 32 * R.c), Q1 = lds16(w + 32 + 32 * R.c);
+                    float sa, ma, sb, mb;
+                    block_scales(H, R.c, sa, ma, sb, mb);
+                    int Sa, Sb;
+                    dot64_regs(Q0, Q1, x, Sa, Sb);
+                    T = block_term(mt, sa, ma, sb, mb, Sa, Sb);
                 }
-                float acc[kDecTok];
-                lane_dots(wrow, row_ok, nb, S, sl, c, xs, ms, nt, acc);
-                lane_reduce(acc, S);
-                if ((lane & (4 * S - 1)) == 0 && row_ok) {
-#pragma unroll
-                    for (int t = 0; t < kDecTok; ++t)
-                        if (t < nt) eout[rowid[t] * P.rows_max + rl] = acc[t];
+                const float v = row_sum(T, R);
+                if (work && row_owner(R)) eout[(g == 0 ? p : n_pairs + p) * P.rows_max + rl] = v;
+                if (valid) {
+                    if (++rl == rows_c) {
+                        rl = 0;
+                        if (++pi == pmax) { pi = 0; ++u; }
+                    }
                 }
             }
         }
@@ -532,6 +606,11 @@ DecPlan dec_plan(int m, int top_k, int num_experts, int hidden, int inter, int s
     const int P = m * top_k;
     if (m < 1 || m > kDecMaxTokens || P > kDecMaxPairs || grid < 1 || grid > kDecMaxCtas) return D;
     if (hidden % kQK || inter % kQK || shared_inter % kQK) return D;
+    // every row must fit one warp's slot of lanes (the row streams)
+    const int lg_b = lg_split_for(inter);
+    if (row_slot_lanes(hidden, lg_split_for(hidden)) > 32 || row_slot_lanes(inter, lg_b) > 32 ||
+        (shared_inter > 0 && row_slot_lanes(shared_inter, lg_b) > 32))
+        return D;
     const int umax = std::min(P, num_experts);
     const bool sh = shared_inter > 0;
     D.na_max = umax * (inter / kDecItemRows) + (sh ? shared_inter / kDecItemRows : 0);

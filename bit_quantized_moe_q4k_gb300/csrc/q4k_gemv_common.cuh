@@ -120,15 +120,26 @@ __device__ __forceinline__ void dot64(const uint4& q0, const uint4& q1, const ui
     dot64_regs(q0, q1, x, Sa, Sb);
 }
 
-// One lane's contribution of sub-blocks a and b of a block to a row's sum for one token:
-//   acc + delta_a * (d*sc_a * S_a - dmin*m_a * sum X_a) + delta_b * (d*sc_b * S_b - dmin*m_b * sum X_b)
-// (mt = (delta_a, sum X_a, delta_b, sum X_b)). Every rounding is spelled out, so each kernel
-// that computes a row with the same lanes gets the same bits (no contraction choices).
-__device__ __forceinline__ float acc_sub_pair(float acc, const float4& mt, float sa, float ma, float sb, float mb,
-                                              int Sa, int Sb) {
+// One lane's term of a block for one token, its sub-blocks a and b:
+//   delta_a * (d*sc_a * S_a - dmin*m_a * sum X_a) + delta_b * (d*sc_b * S_b - dmin*m_b * sum X_b)
+// (mt = (delta_a, sum X_a, delta_b, sum X_b)). Every rounding is spelled out (no contraction
+// choices left to the compiler).
+//
+// The order in which a row's terms are summed is fixed for every kernel, whatever lanes it
+// gives the row: with the row's blocks split over S lanes (block b to lane sl = b % S, in the
+// order i = b / S), each (c, sl) first folds its terms left to right, T_0 + T_1 + T_2 + ...,
+// then the partial sums of the 4*S lanes (c, sl) are added by xor shuffles over c (1, 2) and
+// then over sl (4, 8, ...). So every kernel gets the same bits for a row (fold_term and the
+// lane shuffles of item_compute; the row streams of q4k_decode.cu).
+__device__ __forceinline__ float block_term(const float4& mt, float sa, float ma, float sb, float mb, int Sa, int Sb) {
     const float ua = __fmaf_rn(sa, (float)Sa, -__fmul_rn(ma, mt.y));
     const float ub = __fmaf_rn(sb, (float)Sb, -__fmul_rn(mb, mt.w));
-    return __fmaf_rn(mt.z, ub, __fmaf_rn(mt.x, ua, acc));
+    return __fmaf_rn(mt.z, ub, __fmul_rn(mt.x, ua));
+}
+
+// The fold of a lane's terms: the first term as it is, every later one added on.
+__device__ __forceinline__ float fold_term(float acc, float term, bool first) {
+    return first ? term : __fadd_rn(acc, term);
 }
 
 // Quantize one float4 (elements 4*fi .. 4*fi+3 of a row) as part of its 32-element sub-block:
@@ -403,10 +414,10 @@ __device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND, S
                         const float4 mt = *reinterpret_cast<const float4*>(meta + t * nsb + 8 * b + 2 * c);
                         int Sa, Sb;
                         dot64(L.Q0[j], L.Q1[j], xp, Sa, Sb);
-                        acc[t] = acc_sub_pair(acc[t], mt, sa, ma, sb, mb, Sa, Sb);
+                        acc[t] = fold_term(acc[t], block_term(mt, sa, ma, sb, mb, Sa, Sb), i == 0);
                         if (TWO) {
                             dot64(L.R0[j], L.R1[j], xp, Sa, Sb);
-                            acc2[t] = acc_sub_pair(acc2[t], mt, sa2, ma2, sb2, mb2, Sa, Sb);
+                            acc2[t] = fold_term(acc2[t], block_term(mt, sa2, ma2, sb2, mb2, Sa, Sb), i == 0);
                         }
                     }
                 }

@@ -45,15 +45,18 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
 }
 
 // Wait for the mbarrier phase with the given parity. Gives up (false) after limit_ns of wall
-// time or once *abort is set.
+// time or once *abort is set. Below a millisecond the waits poll without suspending the
+// thread (try_wait may suspend it for longer than such a limit), so a short limit holds.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort,
                                               uint64_t limit_ns) {
-    if (sm100::mbar_try_wait(bar, parity)) return true;
+    const bool short_limit = limit_ns < 1000000ull;
+    auto try_once = [&]() { return short_limit ? sm100::mbar_test_wait(bar, parity) : sm100::mbar_try_wait(bar, parity); };
+    if (try_once()) return true;
     const uint64_t t0 = sm100::global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (sm100::mbar_try_wait(bar, parity)) return true;
+        if (try_once()) return true;
         if (*abort) return false;
-        if ((i & 15) == 0 && sm100::global_timer_ns() - t0 > limit_ns) return false;
+        if (((i & 15) == 0 || short_limit) && sm100::global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -99,7 +99,7 @@ CASES = [
     (256, 512, 32, 16, 2, "uniform", 256, 1, True),    # top_k at its limit
     (768, 256, 4, 1, 32, "uniform", 512, 2, False),    # 32 tokens: a 32-pair shared expert
     (1024, 1280, 16, 4, 2, "zipf", 0, 0, True),        # no shared expert; ragged row tiles
-    (4096, 1792, 8, 2, 1, "uniform", 0, 0, True),      # Mixtral-like shape at reduced inter
+    (4096, 1792, 8, 2, 1, "uniform", 0, 0, False),     # Mixtral-like shape at reduced inter
 ]
 
 
