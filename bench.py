@@ -508,9 +508,7 @@ def measured_peaks():
 KERNEL_SOURCES = {  # the files whose text a kernel's counters depend on
     "idgemv_kernel<true>": ("q4k_gemv.cu", "q4k_gemv_common.cuh"),
     "layer_kernel": ("q4k_layer.cu", "q4k_gemv_common.cuh", "q4k_sync.cuh"),
-    "decode_layer_kernel": ("q4k_decode.cu", "q4k_gemv_common.cuh", "q4k_sync.cuh"),
 }
-PATH_RESIDENT = 2
 
 
 def code_text(text: str) -> str:
@@ -585,13 +583,7 @@ def main():
     value = W.pairs * K * max(1, world) / (r["total_ms"] / 1e3)
     peak, peak_kind = measured_peaks()
     gu_ms = float(np.mean(r["gu_ms"]))
-    if r["single"] and r["path"] == PATH_RESIDENT:
-        kernel, kbytes = "decode_layer_kernel", r["layer_bytes"]
-        kdesc = ("decode_layer_kernel (gate|up+SwiGLU, down, combine; routed + shared) in one launch, every "
-                 "touched weight byte resident in shared memory")
-        ktiming = ("CUDA events around the timed graph: K back-to-back launches of this kernel, one per step, "
-                   "on the launching stream")
-    elif r["single"]:
+    if r["single"]:
         # one kernel per step: the whole layer's bytes over its launch duration
         kernel, kbytes = "layer_kernel", r["layer_bytes"]
         kdesc = "layer_kernel (gate|up+SwiGLU, down, combine; routed + shared) in one persistent launch"

@@ -8,7 +8,6 @@ first call does, and raises if it cannot.
 """
 from ._lib import (  # noqa: F401
     PATH_PERSISTENT,
-    PATH_RESIDENT,
     PATH_TWO_LAUNCH,
     Q4KError,
     SHARED_NONE,

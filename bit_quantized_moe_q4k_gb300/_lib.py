@@ -23,7 +23,7 @@ STATUS_NAMES = {
     10: "Q4K_ERR_TIMEOUT",
 }
 SHARED_NONE, SHARED_SIGMOID, SHARED_UNSCALED = 0, 1, 2
-PATH_TWO_LAUNCH, PATH_PERSISTENT, PATH_RESIDENT = 0, 1, 2
+PATH_TWO_LAUNCH, PATH_PERSISTENT = 0, 1
 
 # Exported C symbols and their signatures (restype, argtypes).
 _P, _I, _I64, _U64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
@@ -204,7 +204,7 @@ def q4k_moe_layer_launch_count(m, top_k, num_experts, hidden, inter, shared_inte
 
 
 def q4k_moe_layer_path(m, top_k, num_experts, hidden, inter, shared_inter) -> int:
-    """PATH_RESIDENT, PATH_PERSISTENT or PATH_TWO_LAUNCH: the kernels one layer call runs."""
+    """PATH_PERSISTENT or PATH_TWO_LAUNCH: the kernels one layer call runs."""
     return int(load().q4k_moe_layer_path(m, top_k, num_experts, hidden, inter, shared_inter))
 
 

@@ -99,22 +99,6 @@ bool layer_wants_tc(int m, int top_k, int num_experts, int hidden, int inter, in
            tc_wanted(m * top_k, num_experts, hidden, t) || (sh && tc_wanted(m, 1, hidden, t));
 }
 
-// Switch (environment, read at every call): Q4K_DECODE=0 keeps decode layers off the
-// resident-weights kernel (q4k_decode.cu), so they take the persistent layer kernel instead.
-bool decode_setting() {
-    const char* s = getenv("Q4K_DECODE");
-    return s == nullptr || atoi(s) != 0;
-}
-
-// The layer runs as one launch of the resident-weights decode kernel (q4k_decode.cu): a few
-// tokens whose touched weights fit the grid's shared memory, no tensor-core bucket.
-bool layer_decode(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
-    if (single_launch_setting() == 0 || !decode_setting() || layer_sync_words(m, top_k, hidden, inter, shared_inter) == 0 ||
-        layer_wants_tc(m, top_k, num_experts, hidden, inter, shared_inter))
-        return false;
-    return layer_decode_fits(m, top_k, num_experts, hidden, inter, shared_inter);
-}
-
 // The layer runs as one persistent launch (q4k_layer.cu): a few pairs, no tensor-core bucket.
 bool layer_single_launch(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     const int setting = single_launch_setting();
@@ -332,9 +316,7 @@ size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidde
 
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     if (m <= 0 || top_k < 1 || num_experts < 1) return 0;
-    if (layer_decode(m, top_k, num_experts, hidden, inter, shared_inter) ||
-        layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter))
-        return 1;
+    if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) return 1;
     const int t = tc_min_for(m * top_k, num_experts);
     const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t));
     const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t));
@@ -345,7 +327,6 @@ int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter,
     if (m <= 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || num_experts < 1 || hidden < 1 || inter < 1 ||
         shared_inter < 0)
         return -1;
-    if (layer_decode(m, top_k, num_experts, hidden, inter, shared_inter)) return Q4K_PATH_RESIDENT;
     if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) return Q4K_PATH_PERSISTENT;
     return Q4K_PATH_TWO_LAUNCH;
 }
@@ -471,24 +452,16 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
     float* act_shared = reinterpret_cast<float*>(ws + ls.act_shared);
     float* eout = reinterpret_cast<float*>(ws + ls.eout);
     float* sout = reinterpret_cast<float*>(ws + ls.shared_out);
-    // a few pairs and no tensor-core bucket: the whole layer in one launch -- the resident-weights
-    // decode kernel where its shared-memory plan fits, else the persistent layer kernel
-    const bool dec = layer_decode(m, top_k, num_experts, hidden, inter, shared_inter);
-    if (dec || layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) {
+    // a few pairs and no tensor-core bucket: the whole layer in one persistent launch
+    if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) {
         GemvGroup gu[2] = {}, dn[2] = {};
         const int ng = gate_up_groups(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act,
                                       d_ws_gate, d_ws_up, shared_inter, act_shared, gu);
         down_groups(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,
                     act_shared, sout, dn);
         const CombineSpec cb1{d_y, d_h_mid, d_weights, d_shared_gate, shared_mode, nullptr, 0};
-        uint64_t* sync = reinterpret_cast<uint64_t*>(ws + ls.sync);
-        cudaError_t e = cudaErrorNotSupported;
-        if (dec) {
-            uint8_t* stage[2] = {reinterpret_cast<uint8_t*>(act), reinterpret_cast<uint8_t*>(act_shared)};
-            e = launch_layer_decode(gu, dn, ng, cb1, sync, ls.n_sync_words, stage, d_err_flag, stream);
-        }
-        if (e == cudaErrorNotSupported && layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter))
-            e = launch_layer_persistent(gu, dn, ng, cb1, sync, ls.n_sync_words, d_err_flag, stream);
+        const cudaError_t e = launch_layer_persistent(gu, dn, ng, cb1, reinterpret_cast<uint64_t*>(ws + ls.sync),
+                                                      ls.n_sync_words, d_err_flag, stream);
         if (e != cudaErrorNotSupported) return cuda_status(e, "layer launch");
     }
     // two launches: gate|up + SwiGLU (routed and shared; it also zeroes the combine counters),

@@ -117,16 +117,6 @@ bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter);
 // Words at the start of the sync area that hold the generation word and the counter sets.
 size_t layer_sync_head_words(int hidden);
 
-// The decode layer in one launch with all touched weights resident in shared memory at once
-// (q4k_decode.cu). Applies where the shared-memory plan for the most buckets the ids can make
-// fits one CTA per SM (a few tokens); cudaErrorNotSupported otherwise, before launching
-// anything. stage[g]: workspace for the staged down inputs of group g (routed pairs, shared
-// tokens), 2.5 bytes per element. sync as for launch_layer_persistent (the head is left alone).
-bool layer_decode_fits(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
-size_t layer_decode_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
-cudaError_t launch_layer_decode(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
-                                uint64_t* sync, size_t sync_words, uint8_t* const* stage, int* err_flag,
-                                cudaStream_t stream);
 cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
                                     uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream);
 

@@ -454,8 +454,7 @@ size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inte
     }
     const LayerPlan L = plan_of(gu, dn, ng, kOne);  // one-row down items: the larger cap
     if (L.cap_a + L.cap_b > (1 << 26)) return 0;
-    return std::max(sync_head_words(hidden) + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b,
-                    layer_decode_sync_words(m, top_k, hidden, inter, shared_inter));
+    return sync_head_words(hidden) + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b;
 }
 
 bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter) {

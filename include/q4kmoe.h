@@ -241,17 +241,12 @@ int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, in
 
 /* Which kernels one q4k_moe_layer_forward call runs for these sizes on the current device
  * (the environment switches included):
- *   Q4K_PATH_RESIDENT   one launch with every weight byte the layer touches resident in
- *                       shared memory at once (a decode layer whose touched rows fit the
- *                       SMs' shared memory; each CTA also forms the combine of its rows);
- *   Q4K_PATH_PERSISTENT one persistent launch that streams work items through registers;
+ *   Q4K_PATH_PERSISTENT one persistent launch for the whole layer (a decode layer);
  *   Q4K_PATH_TWO_LAUNCH a gate|up launch and a down launch with the combine fused (plus the
  *                       tensor-core kernels of a half that uses them).
- * All three give the same results bit for bit. -1 on invalid sizes. The environment variable
- * Q4K_DECODE=0 turns the resident path off. */
+ * Both give the same results bit for bit. -1 on invalid sizes. */
 #define Q4K_PATH_TWO_LAUNCH 0
 #define Q4K_PATH_PERSISTENT 1
-#define Q4K_PATH_RESIDENT 2
 int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
 /* ---------------------------------------------------------------------------------

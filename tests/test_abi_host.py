@@ -141,6 +141,19 @@ def test_layer_launch_count_single_launch_rule(monkeypatch):
     assert with_flags >= (8 * 768 + 768 + 8 * 2048 + 2048) * 4 + 8 * (1 + 1024)
 
 
+def test_layer_path_query(monkeypatch):
+    """q4k_moe_layer_path names the kernels a layer call runs: the persistent single launch for a
+    decode layer, two launches otherwise or when switched off; -1 for invalid sizes."""
+    lib = q4k.load()
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
+    assert lib.q4k_moe_layer_path(1, 8, 128, 2048, 768, 768) == q4k.PATH_PERSISTENT
+    assert lib.q4k_moe_layer_path(5, 8, 128, 2048, 768, 768) == q4k.PATH_TWO_LAUNCH  # 40 pairs
+    monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
+    assert lib.q4k_moe_layer_path(1, 8, 128, 2048, 768, 768) == q4k.PATH_TWO_LAUNCH
+    assert lib.q4k_moe_layer_path(0, 8, 128, 2048, 768, 768) == -1
+    assert lib.q4k_moe_layer_path(1, 17, 128, 2048, 768, 768) == -1
+
+
 def test_bench_traffic_record_keys_on_code_lines():
     """The committed DRAM traffic of a kernel is matched to its source by a hash of the code
     lines: whole-line comments and blank lines do not change it, code does."""

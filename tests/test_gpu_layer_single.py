@@ -1,15 +1,14 @@
-"""GPU: the single-launch layers against the two-launch layer and the oracle.
+"""GPU: the single-launch layer (one persistent kernel for gate|up + SwiGLU, down and the
+combine, routed and shared experts) against the two-launch layer and the oracle.
 
-Two kernels run a layer in one launch: the resident-weights decode kernel (every weight byte
-the layer touches in shared memory at once; each CTA combines its own rows of hidden) where
-its shared-memory plan fits, else the persistent kernel (work items streamed through
-registers, last-arriver combine). Both reduce every output row with the same lanes in the
-same order as the two-launch layer, so all three agree bit for bit; against the oracle the
-per-row acceptance of helpers.rows_close applies. Their CTAs hand work to each other through
-tagged flag words at the start of the workspace, so the tests also run them on a workspace
-full of garbage, on one workspace call after call (and replayed from a CUDA graph), with m
-changing between calls on one workspace, and with a wait limit so short that the waits give
-up (the error flag reports it, and the next call on a cleared workspace is right).
+The single launch sums every output row in the same order as the two-launch layer (the order
+all kernels share: each lane's block terms folded left to right, then the lane shuffles), so
+the two agree bit for bit; against the oracle the per-row acceptance of helpers.rows_close
+applies. Its CTAs hand work to each other through tagged flag words at the start of the
+workspace, so the tests also run it on a workspace full of garbage, on one workspace call
+after call (and replayed from a CUDA graph), with m changing between calls on one workspace,
+and with a wait limit so short that the waits give up (the error flag reports it, and the
+next call on a cleared workspace is right).
 """
 import numpy as np
 import pytest
@@ -92,26 +91,23 @@ def _two_launch(layer, monkeypatch):
 
 
 CASES = [
-    # (hidden, inter, experts, top_k, m, ids, shared_inter, shared_mode, resident on GB300)
-    (2048, 768, 128, 8, 1, "uniform", 768, 1, True),   # the Qwen3-MoE-like decode layer, full size
-    (1024, 512, 128, 8, 4, "uniform", 512, 2, False),  # 32 pairs: the single launch's limit
-    (512, 256, 4, 2, 3, "uniform", 256, 1, True),      # more pairs than experts: shared buckets
-    (256, 512, 32, 16, 2, "uniform", 256, 1, True),    # top_k at its limit
-    (768, 256, 4, 1, 32, "uniform", 512, 2, False),    # 32 tokens: a 32-pair shared expert
-    (1024, 1280, 16, 4, 2, "zipf", 0, 0, True),        # no shared expert; ragged row tiles
-    (4096, 1792, 8, 2, 1, "uniform", 0, 0, False),     # Mixtral-like shape at reduced inter
+    # (hidden, inter, experts, top_k, m, ids, shared_inter, shared_mode)
+    (2048, 768, 128, 8, 1, "uniform", 768, 1),   # the Qwen3-MoE-like decode layer, full size
+    (1024, 512, 128, 8, 4, "uniform", 512, 2),   # 32 pairs: the single launch's limit
+    (512, 256, 4, 2, 3, "uniform", 256, 1),      # more pairs than experts: 4-token items
+    (256, 512, 32, 16, 2, "uniform", 256, 1),    # top_k at its limit
+    (768, 256, 4, 1, 32, "uniform", 512, 2),     # 32 tokens: a 32-pair shared expert
+    (1024, 1280, 16, 4, 2, "zipf", 0, 0),        # no shared expert; ragged row tiles
+    (4096, 1792, 8, 2, 1, "uniform", 0, 0),      # Mixtral-like shape at reduced inter
 ]
 
 
-@pytest.mark.parametrize("decode", ["1", "0"], ids=["resident_if_fits", "persistent"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "h{}_i{}_e{}_t{}_m{}_{}_s{}".format(*c[:7]))
-def test_single_launch_matches_two_launch_and_oracle(case, decode, monkeypatch):
-    H, I, E, T, m, ids_kind, Is, mode, resident = case
-    monkeypatch.setenv("Q4K_DECODE", decode)
+def test_single_launch_matches_two_launch_and_oracle(case, monkeypatch):
+    H, I, E, T, m, ids_kind, Is, mode = case
     W = Workload("single", H, I, E, T, m, ids_kind, Is, mode, 1200 + sum(case[:5]))
     assert q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is) == 1
-    want = q4k.PATH_RESIDENT if (decode == "1" and resident) else q4k.PATH_PERSISTENT
-    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) == want
+    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) == q4k.PATH_PERSISTENT
     layer = Layer(W, _inputs(W))
     ref2, f2 = _two_launch(layer, monkeypatch)
     assert f2 == 0
@@ -230,18 +226,17 @@ def test_single_launch_hidden_changes_on_one_workspace(monkeypatch):
     assert int(host(f)[0]) == 0
 
 
-@pytest.mark.parametrize("decode", ["1", "0"], ids=["resident", "persistent"])
-def test_single_launch_wait_limit_runs_out(decode, monkeypatch):
-    """A wait limit of 1 ns (Q4K_WAIT_NS) makes the hand-off waits give up: the kernel returns
-    with Q4K_ERR_TIMEOUT in the device flag after its bulk copies have landed (no fault, no
-    hang, the context stays usable), and the next call on a cleared workspace with the default
-    limit is right."""
-    monkeypatch.setenv("Q4K_DECODE", decode)
+def test_single_launch_wait_limit_runs_out(monkeypatch):
+    """A wait limit of 1 ns (Q4K_WAIT_NS) makes the waits give up: the kernel returns with
+    Q4K_ERR_TIMEOUT in the device flag after its bulk copies have landed (no fault, no hang, the
+    context stays usable), and the next call on a cleared workspace with the default limit is
+    right. (Below a millisecond the mbarrier waits poll without suspending, so the first copy
+    that has not landed yet makes its wait give up.)"""
     W = WORKLOADS["qwen3moe_h2048_i768_e128_t8_m1"]
     layer = Layer(W, _inputs(W))
     ref2, _ = _two_launch(layer, monkeypatch)
-    path = q4k.q4k_moe_layer_path(W.m, W.top_k, W.num_experts, W.hidden, W.inter, W.shared_inter)
-    assert path == (q4k.PATH_RESIDENT if decode == "1" else q4k.PATH_PERSISTENT)
+    assert q4k.q4k_moe_layer_path(W.m, W.top_k, W.num_experts, W.hidden, W.inter, W.shared_inter) == \
+        q4k.PATH_PERSISTENT
     ws = torch.zeros(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
     f = err_flag()
     monkeypatch.setenv("Q4K_WAIT_NS", "1")
