@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from bit_quantized_moe_q4k_gb300 import inputs  # noqa: E402
-from bit_quantized_moe_q4k_gb300.workloads import HEADLINE, WORKLOADS, Workload  # noqa: E402
+from bit_quantized_moe_q4k_gb300.workloads import HEADLINE, MIXTRAL_M_SWEEP, WORKLOADS, Workload  # noqa: E402
 
 METRIC = "Q4_K MoE id-GEMV: achieved HBM GB/s (% of peak) and (token,expert) pairs/sec"
 # What the kernels compute in: weights Q4_K as stored; activations fp32 in HBM, staged on chip
@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="size of the layer rotation (default: > 3x L2 touched)")
     ap.add_argument("--separate-inputs", action="store_true",
                     help="one allocation per layer for its activations, ids and weights instead of stacked tensors")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' records (per_config) after the headline")
+    ap.add_argument("--per-config-steps", type=int, default=10)
     return ap.parse_args()
 
 
@@ -495,6 +498,48 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
             "experts_touched": float(np.mean([p["experts_touched"] for p in per]))}
 
 
+# The other workloads of the layer, measured after the headline in the same run (one record each).
+PER_CONFIG = [("qwen3moe_h2048_i768_e128_t8_m16_zipf", 0), ("deepseekv3_h7168_i2048_e256_t8_m64", 0)] + \
+    [("mixtral_h4096_i14336_e8_t2", m) for m in MIXTRAL_M_SWEEP]
+
+
+def per_config_records(args, rank, world, local_rank, peak):
+    import argparse
+    import torch
+    global CLOCK_SOAK_S
+    out = []
+    soak = CLOCK_SOAK_S
+    CLOCK_SOAK_S = 0.3
+    try:
+        for name, m in PER_CONFIG:
+            W = WORKLOADS[name].with_m(m) if m else WORKLOADS[name]
+            sub = argparse.Namespace(**vars(args))
+            sub.steps, sub.warmup, sub.no_e2e, sub.no_ceiling, sub.layers = args.per_config_steps, 3, True, True, 0
+            r = run_ours(sub, W, rank, world, local_rank)
+            K = sub.steps
+            step_ms = r["total_ms"] / K
+            gu_ms = float(np.mean(r["gu_ms"]))
+            kbytes = r["layer_bytes"] if r["single"] else r["gu_bytes"]
+            out.append({
+                "workload": name if not m else f"{name}_m{m}", "m": W.m, "pairs": W.pairs,
+                "ms_per_step": step_ms, "pairs_per_s": W.pairs * K * max(1, world) / (r["total_ms"] / 1e3),
+                "layer_bytes": r["layer_bytes"], "layer_hbm_gbs": r["layer_bytes"] / (step_ms * 1e-3) / 1e9,
+                "layer_hbm_frac": r["layer_bytes"] / (step_ms * 1e-3) / 1e9 / peak,
+                "experts_touched_per_step": r["experts_touched"], "launches_per_step": r["launches_per_step"],
+                "roofline": {"kernel": "layer_kernel (one persistent launch)" if r["single"] else
+                             "idgemv_kernel<fused gate|up+SwiGLU> (routed + shared)",
+                             "bound": "hbm", "bytes_per_launch": kbytes, "avg_launch_us": gu_ms * 1e3,
+                             "achieved": kbytes / (gu_ms * 1e-3) / 1e9, "peak": peak,
+                             "frac": kbytes / (gu_ms * 1e-3) / 1e9 / peak, "unit": "GB/s"},
+                "clocks": r["clocks"], "l2": f"rotating {r['n_layers']} layers ({r['per_layer_touched'] / 1e6:.0f} MB "
+                                             f"touched per step)"})
+            del r
+            torch.cuda.empty_cache()
+    finally:
+        CLOCK_SOAK_S = soak
+    return out
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -596,6 +641,9 @@ def main():
                    "layers, right after the timed region")
     achieved = kbytes / (gu_ms * 1e-3) / 1e9
     layer_gbs = r["layer_bytes"] / (step_ms * 1e-3) / 1e9
+    per_config = None
+    if not args.no_per_config and not args.m and args.workload == HEADLINE:
+        per_config = per_config_records(args, rank, world, local_rank, peak)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = time_oracle(W, args.cpu_seconds)
@@ -621,6 +669,7 @@ def main():
         "e2e": r["e2e"],
         "clocks": r["clocks"],
         "gpu_launches": r["launches_per_step"] * K,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 

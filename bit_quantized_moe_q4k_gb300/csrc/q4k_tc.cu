@@ -37,6 +37,7 @@
 #include "q4k_bucket.cuh"
 #include "q4k_internal.cuh"
 #include "q4k_sm100.cuh"
+#include "q4k_sync.cuh"
 
 namespace q4k {
 using namespace sm100;
@@ -81,6 +82,7 @@ struct TcParams {
     int hist_off[2];  // int offsets of each group's tables in shared memory
     int tab_off;      // byte offset of the tables
     int* err_flag;
+    uint64_t wait_ns; // limit of the pipeline waits (the drains after an abort keep their own)
 };
 
 // Per-CTA bucketing for the tensor-core path: cnt[e] pairs per expert and start[e] = first
@@ -314,7 +316,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 const int slab = s / nb, b = s % nb;
                 int okl = 1;
                 if (lane == 0) {
-                    okl = mbar_wait(&bar_raw_empty[rst], rph ^ 1, &s_abort);
+                    okl = mbar_wait_for(&bar_raw_empty[rst], rph ^ 1, &s_abort, P.wait_ns);
                     if (okl) {
                         // one tensor load: 128 rows x 144 bytes of block b (rows past the slab read as zero)
                         mbar_arrive_expect_tx(&bar_raw_full[rst], kRawStage);
@@ -325,7 +327,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
                 raw_issued = gs + 1;
                 if (lane == 0) {
-                    okl = mbar_wait(&bar_b_empty[bst], bph ^ 1, &s_abort);
+                    okl = mbar_wait_for(&bar_b_empty[bst], bph ^ 1, &s_abort, P.wait_ns);
                     if (okl) {
                         mbar_arrive_expect_tx(&bar_b_full[bst], kImgBlock);
                         bulk_g2s(bimg + bst * kImgBlock, img + (int64_t)b * kImgBlock, kImgBlock, &bar_b_full[bst]);
@@ -357,8 +359,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     const uint32_t ph = (gs >> 1) & 1;
                     const int bst = gs % kNImg;
                     const uint32_t bph = (gs / kNImg) & 1;
-                    if (!mbar_wait(&bar_a_full[st], ph, &s_abort) || !mbar_wait(&bar_b_full[bst], bph, &s_abort) ||
-                        !mbar_wait(&bar_d_empty[st], ph ^ 1, &s_abort)) {
+                    if (!mbar_wait_for(&bar_a_full[st], ph, &s_abort, P.wait_ns) || !mbar_wait_for(&bar_b_full[bst], bph, &s_abort, P.wait_ns) ||
+                        !mbar_wait_for(&bar_d_empty[st], ph ^ 1, &s_abort, P.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -417,7 +419,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 if (s < steps) {
                     const int rst = g_cur % kNRaw;
                     const uint32_t rph = (g_cur / kNRaw) & 1;
-                    if (!mbar_wait(&bar_raw_full[rst], rph, &s_abort)) { ok = false; break; }
+                    if (!mbar_wait_for(&bar_raw_full[rst], rph, &s_abort, P.wait_ns)) { ok = false; break; }
                     // this half's code bytes: 64-weight groups 2*half, 2*half + 1 (bytes 64*half ..)
                     const uint4* rp = reinterpret_cast<const uint4*>(raw + rst * kRawStage + r * kBlockBytes);
                     const uint4 h = rp[0];
@@ -437,7 +439,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                         sc[j + 4] = (w & 15u) | ((y >> 6) << 4);
                         mn[j + 4] = (w >> 4) | ((z >> 6) << 4);
                     }
-                    if (!mbar_wait(&bar_a_empty[st], ph ^ 1, &s_abort)) { ok = false; break; }
+                    if (!mbar_wait_for(&bar_a_empty[st], ph ^ 1, &s_abort, P.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     // A columns: code word i -> columns 4i..4i+3 = low nibbles of bytes (0,2), (1,3),
                     // high nibbles of bytes (0,2), (1,3), each the exact fp16 pair sc_j * q
@@ -482,7 +484,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     const int pg = g_cur - 1;
                     const int ps = pg & 1;
                     const uint32_t pph = (pg >> 1) & 1;
-                    if (!mbar_wait(&bar_d_full[ps], pph, &s_abort)) { ok = false; break; }
+                    if (!mbar_wait_for(&bar_d_full[ps], pph, &s_abort, P.wait_ns)) { ok = false; break; }
                     tc_fence_after();
                     uint32_t d1[kHalfTok], d2[kHalfTok], d3[kHalfTok];
                     tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kHalfTok * half, d1);
@@ -583,6 +585,7 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
     P.n_groups = n_groups;
     P.tc_min = tc_min;
     P.err_flag = err_flag;
+    P.wait_ns = wait_limit_ns();
     int ints = 0;
     int64_t max_chunks = 0;
     int max_tiles = 0;

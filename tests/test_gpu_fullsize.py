@@ -4,10 +4,12 @@ times (the whole layer through q4k_moe_layer_forward with its workspace, so larg
 take the tensor-core path).
 
 Weights are fp32 N(0, 0.02) drawn per (projection, expert) by a seeded device generator and
-quantized on the GPU by q4k_quantize_rows. For a few sampled tokens, the experts they use are
-drawn again, copied to the host and quantized by the oracle: the bytes must be identical to
-the GPU's. The oracle then runs the whole layer for those tokens on its own bytes, and the
-GPU rows must meet the per-row acceptance.
+quantized on the GPU by q4k_quantize_rows. For sampled tokens (at least 8 per layer; for the
+Mixtral-like layers the first and last pair of every 32-pair chunk of every expert, so each
+tensor-core chunk is checked), the experts they use are drawn again, copied to the host and
+quantized by the oracle: the bytes must be identical to the GPU's. The oracle then runs the
+whole layer for those tokens on its own bytes, and the GPU rows (every row tile of hidden)
+must meet the per-row acceptance.
 """
 import numpy as np
 import pytest
@@ -88,11 +90,28 @@ def _run(W, sample):
     assert np.isfinite(got).all()
 
 
+def _chunk_sample(W, per_chunk=32, extra=8):
+    """Tokens that reach every 32-pair chunk of every expert's bucket (the tensor-core path
+    splits a bucket into chunks of 32 pairs, in pair order): the first and the last pair of each
+    chunk, plus `extra` evenly spaced tokens and the last token."""
+    ids = inputs.make_ids(W.seed, W.ids, W.m, W.top_k, W.num_experts)
+    toks = set(range(0, W.m, max(1, W.m // extra))) | {W.m - 1}
+    for e in range(W.num_experts):
+        pairs = np.flatnonzero(ids == e)
+        for c0 in range(0, len(pairs), per_chunk):
+            chunk = pairs[c0:c0 + per_chunk]
+            toks |= {int(chunk[0]) // W.top_k, int(chunk[-1]) // W.top_k}
+    return sorted(toks)
+
+
 def test_fullsize_deepseek_v3_like_m64():
-    _run(WORKLOADS["deepseekv3_h7168_i2048_e256_t8_m64"], sample=[0, 37, 63])
+    W = WORKLOADS["deepseekv3_h7168_i2048_e256_t8_m64"]
+    _run(W, sample=list(range(0, 64, 7)) + [63])  # 11 tokens
 
 
 @pytest.mark.parametrize("m", MIXTRAL_M_SWEEP)
 def test_fullsize_mixtral_like_sweep(m):
     W = WORKLOADS["mixtral_h4096_i14336_e8_t2"].with_m(m)
-    _run(W, sample=[0, m // 2, m - 1])
+    sample = _chunk_sample(W)
+    assert len(sample) >= min(8, m)
+    _run(W, sample=sample)

@@ -117,3 +117,29 @@ def test_tc_layer_shared_expert_takes_tensor_cores():
     got = host(y)
     assert int(host(f)[0]) == 0
     rows_close(got, ref, what="tc layer")
+
+
+def test_tc_wait_limit_runs_out(monkeypatch):
+    """A wait limit of 1 ns (Q4K_WAIT_NS) makes the tensor-core kernel's pipeline waits give up:
+    the roles leave together (abort word), the MMAs already issued and the copies in flight
+    finish before tensor memory is freed, Q4K_ERR_TIMEOUT is in the device flag, and the next
+    call with the default limit on the same workspace is right (the GPU context stays usable)."""
+    E, n, k, m, T = 4, 2148, 512, 64, 2
+    seed = 733
+    w = oracle_slab(seed, "tc", E, n, k)
+    ids = inputs.ids_uniform_distinct(seed, m, T, E)
+    a = inputs.normal(seed, "a", (m, k))
+    ref, _ = oracle.moe_id_gemv(w, E, a, k, 0, ids, m, T, n, k)
+    ws, nbytes = _ws(q4k.q4k_moe_workspace_size(m, T, E, n, k))
+    dw, da, dids = dev(w), dev(a), dev(ids)
+    out = torch.empty((m * T, n), dtype=torch.float32, device="cuda")
+    f = err_flag()
+    monkeypatch.setenv("Q4K_WAIT_NS", "1")
+    q4k.q4k_moe_id_gemv(dw, 0, E, da, k, 0, dids, m, T, n, k, out, ws, nbytes, f)
+    assert int(host(f)[0]) == 10  # Q4K_ERR_TIMEOUT
+    monkeypatch.delenv("Q4K_WAIT_NS")
+    f.zero_()
+    q4k.q4k_moe_id_gemv(dw, 0, E, da, k, 0, dids, m, T, n, k, out, ws, nbytes, f)
+    got = host(out)
+    assert int(host(f)[0]) == 0
+    rows_close(got, ref, what="tensor-core path after a timed-out call")

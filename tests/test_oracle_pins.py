@@ -190,6 +190,39 @@ def test_quantizer_header_follows_definition():
                 assert sc == min(63, int(np.rint(np.float32(scale[j]) / np.float32(d))))
 
 
+def test_quantizer_mins_and_codes_follow_definition():
+    """Every 6-bit min m_j and every 4-bit code q_i against the definition recomputed with
+    numpy float32 (one rounding per step, round-half-even):
+    m_j = min(63, rint(mn_j / dmin)) (0 when dmin = 0),
+    q_i = clamp(rint((x_i + dmin*m_j) / (d*sc_j)), 0, 15) (0 when d*sc_j = 0).
+    Rows include a sub-block of zeros and an all-positive row (dmin = 0)."""
+    x = inputs.normal(4, "pin_q3", (5, 768), 0.02)
+    x[1, 256:288] = 0.0                                       # one sub-block of zeros
+    x[2] = np.abs(x[2]) + np.float32(0.001)                   # nothing below zero: dmin = 0
+    q = oracle.quantize_rows(x).reshape(5, 3, 144)
+    f32 = np.float32
+    for r in range(5):
+        for b in range(3):
+            d, dmin, sm = _fields(q[r, b])
+            codes = np.empty(256, np.int64)
+            qs = q[r, b, 16:]
+            for c in range(4):
+                codes[64 * c: 64 * c + 32] = qs[32 * c: 32 * c + 32] & 0x0F
+                codes[64 * c + 32: 64 * c + 64] = qs[32 * c: 32 * c + 32] >> 4
+            for j, (sc, mn) in enumerate(sm):
+                xs = x[r, 256 * b + 32 * j: 256 * b + 32 * j + 32].astype(f32)
+                mn_j = f32(-min(f32(0), xs.min()))
+                m_exp = 0 if dmin == 0 else min(63, int(np.rint(f32(mn_j / f32(dmin)))))
+                assert mn == m_exp, (r, b, j, mn, m_exp)
+                ds = f32(f32(d) * f32(sc))
+                dm = f32(f32(dmin) * f32(mn))
+                if ds == 0:
+                    want = np.zeros(32, np.int64)
+                else:
+                    want = np.clip(np.rint(((xs + dm).astype(f32) / ds).astype(f32)), 0, 15).astype(np.int64)
+                assert np.array_equal(codes[32 * j: 32 * j + 32], want), (r, b, j)
+
+
 def test_quantizer_special_cases():
     z = np.zeros((1, 256), np.float32)
     assert not oracle.quantize_rows(z).any()  # all fields zero, all weights zero
