@@ -18,7 +18,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "q4k_oracle.c")
+_SRCS = [os.path.join(_HERE, f) for f in ("q4k_oracle.c", "q4o_route.c", "q4o_fmt4.c")]
 _HDR = os.path.join(_HERE, "q4k_oracle.h")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
@@ -32,14 +32,14 @@ def build(force: bool = False) -> str:
     """Compile liboracle.so with gcc (OpenMP when available). Returns its path."""
     with _lock:
         fresh = (os.path.exists(_LIB_PATH)
-                 and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+                 and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f) for f in _SRCS + [_HDR]))
         if fresh and not force:
             return _LIB_PATH
         base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
                 "-Wall", "-Wextra", "-Wno-unused-parameter"]
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         for extra in (["-fopenmp"], []):
-            cmd = base + extra + ["-o", tmp, _SRC, "-lm"]
+            cmd = base + extra + ["-o", tmp] + _SRCS + ["-lm"]
             res = subprocess.run(cmd, capture_output=True, text=True)
             if res.returncode == 0:
                 os.replace(tmp, _LIB_PATH)
@@ -72,6 +72,16 @@ def _load():
         "q4o_moe_combine": (None, [P, P, P, P, P, i32, i32, i32, i32, P]),
         "q4o_moe_layer": (i32, [P, P, P, i32, P, P, P, i32, i32, P, P, P, P, P, i32, i32, i32, i32, P]),
         "q4o_bucket": (i32, [P, i32, i32, P, P, P]),
+        "q4o_bf16_to_double": (ctypes.c_double, [ctypes.c_uint16]),
+        "q4o_router_logits": (None, [P, P, i32, i32, i32, P]),
+        "q4o_route_softmax": (i32, [P, i32, i32, i32, i32, P, P]),
+        "q4o_route_sigmoid_grouped": (i32, [P, P, i32, i32, i32, i32, i32, i32, ctypes.c_double, P, P]),
+        "q4o_rms_norm": (None, [P, P, i32, i32, ctypes.c_double, P]),
+        "q4o_affine4_dequant": (None, [P, ctypes.c_uint64, ctypes.c_uint64, i64, i64, i32, P]),
+        "q4o_q4tp_dequant": (None, [P, i64, i64, P]),
+        "q4o_fmt4_matrix_bytes": (ctypes.c_uint64, [i32, i64, i64, i32]),
+        "q4o_moe_id_gemv_fmt4": (i32, [i32, P, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, i32, i32, P,
+                                       i64, i64, P, i32, i32, i32, i32, P]),
         "q4o_set_threads": (i32, [i32]),
         "q4o_get_threads": (i32, []),
     }
@@ -228,6 +238,94 @@ def bucket(ids, num_experts):
     if bad < 0:
         raise MemoryError("oracle allocation failed")
     return counts, offsets, perm, bad
+
+
+# ---- router and chained norm ---------------------------------------------------------------
+
+FMT_AFFINE = 0
+FMT_Q4TP = 1
+
+
+def bf16_to_double(b: int) -> float:
+    return float(_load().q4o_bf16_to_double(int(b)))
+
+
+def router_logits(x, w_bf16, m, num_experts, hidden):
+    """fp64 logits[m, num_experts] = x . bf16(w)^T (w given as uint16 bits)."""
+    x = _c(x, np.float32)
+    w_bf16 = _c(w_bf16, np.uint16)
+    out = np.empty((m, num_experts), np.float64)
+    _load().q4o_router_logits(_ptr(x), _ptr(w_bf16), m, num_experts, hidden, _ptr(out))
+    return out
+
+
+def route_softmax(logits, top_k, normalize=True):
+    """(ids[m, top_k] int32, weights[m, top_k] fp64): softmax top-k routing."""
+    logits = _c(logits, np.float64)
+    m, E = logits.shape
+    ids = np.empty((m, top_k), np.int32)
+    w = np.empty((m, top_k), np.float64)
+    rc = _load().q4o_route_softmax(_ptr(logits), m, E, top_k, 1 if normalize else 0, _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("route_softmax: bad arguments")
+    return ids, w
+
+
+def route_sigmoid_grouped(logits, bias, top_k, n_group=1, topk_group=1, normalize=True, scale=1.0):
+    """(ids, weights): sigmoid scores, bias-corrected, group-limited top-k (noaux_tc)."""
+    logits = _c(logits, np.float64)
+    m, E = logits.shape
+    bias = None if bias is None else _c(bias, np.float32)
+    ids = np.empty((m, top_k), np.int32)
+    w = np.empty((m, top_k), np.float64)
+    rc = _load().q4o_route_sigmoid_grouped(_ptr(logits), _ptr(bias), m, E, top_k, n_group, topk_group,
+                                           1 if normalize else 0, float(scale), _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("route_sigmoid_grouped: bad arguments")
+    return ids, w
+
+
+def rms_norm(x, w_bf16, eps):
+    """fp64 x / sqrt(mean(x^2) + eps) * bf16(w), row by row."""
+    x = _c(x, np.float64)
+    m, H = x.shape
+    w_bf16 = _c(w_bf16, np.uint16)
+    out = np.empty((m, H), np.float64)
+    _load().q4o_rms_norm(_ptr(x), _ptr(w_bf16), m, H, float(eps), _ptr(out))
+    return out
+
+
+# ---- other 4-bit formats ---------------------------------------------------------------------
+
+def affine4_dequant(mat, s_off, b_off, n, k, gs):
+    mat = _c(mat, np.uint8)
+    out = np.empty((n, k), np.float64)
+    _load().q4o_affine4_dequant(_ptr(mat), int(s_off), int(b_off), n, k, gs, _ptr(out))
+    return out
+
+
+def q4tp_dequant(mat, n, k):
+    mat = _c(mat, np.uint8)
+    out = np.empty((n, k), np.float64)
+    _load().q4o_q4tp_dequant(_ptr(mat), n, k, _ptr(out))
+    return out
+
+
+def fmt4_matrix_bytes(fmt, n, k, gs=64):
+    return int(_load().q4o_fmt4_matrix_bytes(fmt, n, k, gs))
+
+
+def moe_id_gemv_fmt4(fmt, w, expert_stride, s_off, b_off, gs, num_experts, a, outer, inner, ids, m, top_k, n, k):
+    """fp64 out[m*top_k, n] and the count of out-of-range ids, for an affine or q4tp slab."""
+    w = _c(w, np.uint8)
+    a = _c(a, np.float32)
+    ids = _c(ids, np.int32)
+    out = np.empty((m * top_k, n), np.float64)
+    bad = _load().q4o_moe_id_gemv_fmt4(fmt, _ptr(w), int(expert_stride), int(s_off), int(b_off), gs, num_experts,
+                                       _ptr(a), outer, inner, _ptr(ids), m, top_k, n, k, _ptr(out))
+    if bad < 0:
+        raise MemoryError("oracle allocation failed")
+    return out, bad
 
 
 def set_threads(n: int) -> int:

@@ -124,6 +124,40 @@ int q4o_moe_layer(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* w_d
 int q4o_bucket(const int32_t* ids, int n_pairs, int num_experts, int32_t* counts,
                int32_t* offsets, int32_t* perm);
 
+/* ---- router and chained norm (q4o_route.c) [P2] -------------------------------------
+ * bf16 decode: the upper 16 bits of a binary32. */
+double q4o_bf16_to_double(uint16_t b);
+/* logits[t, e] = sum_h bf16(w[e, h]) * x[t, h]   (w [num_experts, hidden] bf16 bits). */
+void q4o_router_logits(const float* x, const uint16_t* w, int m, int num_experts, int hidden,
+                       double* logits);
+/* Softmax over all experts; the top_k largest logits are chosen, larger first, equal logits
+ * by lower id; weight = the expert's softmax probability, divided by the chosen experts' sum
+ * when normalize. ids/weights [m, top_k]. Returns 0, or -1 on bad arguments. */
+int q4o_route_softmax(const double* logits, int m, int num_experts, int top_k, int normalize,
+                      int32_t* ids, double* weights);
+/* noaux_tc: s = sigmoid(logit), choice on s + bias within the topk_group best of n_group
+ * groups (group score: sum of its max(1, top_k/topk_group) best s + bias), weight = s
+ * (normalised over the chosen when normalize) * scale. Returns 0, or -1 on bad arguments. */
+int q4o_route_sigmoid_grouped(const double* logits, const float* bias, int m, int num_experts,
+                              int top_k, int n_group, int topk_group, int normalize, double scale,
+                              int32_t* ids, double* weights);
+/* out[t, h] = x[t, h] / sqrt(mean_h x[t, h]^2 + eps) * bf16(w[h]). */
+void q4o_rms_norm(const double* x, const uint16_t* w, int m, int hidden, double eps, double* out);
+
+/* ---- other 4-bit formats (q4o_fmt4.c) [P2 MLX-affine blob, P3 q4tp] ----------------- */
+#define Q4O_FMT_AFFINE 0 /* w = scale*q + bias, bf16 scale/bias per gs weights of a row   */
+#define Q4O_FMT_Q4TP 1   /* w = (q - 8) * 2^(base + code*step), 5-bit code per 32 weights  */
+void q4o_affine4_dequant(const uint8_t* mat, uint64_t s_off, uint64_t b_off, int64_t n, int64_t k,
+                         int gs, double* out);
+void q4o_q4tp_dequant(const uint8_t* mat, int64_t n, int64_t k, double* out);
+uint64_t q4o_fmt4_matrix_bytes(int fmt, int64_t n, int64_t k, int gs);
+/* The q4o_moe_id_gemv walk over a slab of either format (expert e at w + e*expert_stride).
+ * Returns the number of out-of-range ids (zero rows), or -1 if allocation failed. */
+int q4o_moe_id_gemv_fmt4(int fmt, const uint8_t* w, uint64_t expert_stride, uint64_t s_off,
+                         uint64_t b_off, int gs, int num_experts, const float* a, int64_t outer,
+                         int64_t inner, const int32_t* ids, int m, int top_k, int n, int k,
+                         double* out);
+
 /* ---- threading ---------------------------------------------------------------- */
 /* Threads used by the parallel loops (0 = OpenMP default). Returns the count in effect. */
 int q4o_set_threads(int n);
