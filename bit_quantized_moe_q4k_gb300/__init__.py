@@ -10,6 +10,8 @@ from ._lib import (  # noqa: F401
     PATH_PERSISTENT,
     PATH_TWO_LAUNCH,
     Q4KError,
+    ROUTE_SIGMOID_GROUPED,
+    ROUTE_SOFTMAX,
     SHARED_NONE,
     SHARED_SIGMOID,
     SHARED_UNSCALED,
@@ -30,6 +32,8 @@ from ._lib import (  # noqa: F401
     q4k_moe_layer_path,
     q4k_moe_layer_host_staging_size,
     q4k_moe_layer_workspace_size,
+    q4k_moe_router,
+    q4k_rms_norm,
     q4k_moe_workspace_size,
     q4k_quantize_rows,
     q4k_stream_ceiling,

@@ -24,6 +24,7 @@ STATUS_NAMES = {
 }
 SHARED_NONE, SHARED_SIGMOID, SHARED_UNSCALED = 0, 1, 2
 PATH_TWO_LAUNCH, PATH_PERSISTENT = 0, 1
+ROUTE_SOFTMAX, ROUTE_SIGMOID_GROUPED = 0, 1
 
 # Exported C symbols and their signatures (restype, argtypes).
 _P, _I, _I64, _U64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
@@ -48,6 +49,8 @@ SIGNATURES = {
     "q4k_moe_layer_half_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "q4k_moe_layer_launch_count": (_I, [_I, _I, _I, _I, _I, _I]),
     "q4k_moe_layer_path": (_I, [_I, _I, _I, _I, _I, _I]),
+    "q4k_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P, _P, _P]),
+    "q4k_rms_norm": (_I, [_P, _P, _I, _I, ctypes.c_float, _P, _P]),
     "q4k_quantize_rows": (_I, [_P, _I64, _I, _P, _P]),
     "q4k_stream_ceiling_sink_words": (_I, []),
     "q4k_stream_ceiling": (_I, [_P, _U64, _P, _P]),
@@ -173,6 +176,22 @@ def moe_combine_residual(h_mid, expert_out, weights, shared_out, shared_gate, sh
     _check(load().moe_combine_residual(_ptr(h_mid), _ptr(expert_out), _ptr(weights), _ptr(shared_out),
                                        _ptr(shared_gate), shared_mode, m, top_k, hidden, _ptr(hidden_out),
                                        _stream(stream)))
+
+
+def q4k_moe_router(x, w_router, bias, w_shared_gate, m, num_experts, hidden, top_k, scoring, normalize, scale,
+                   n_group, topk_group, ids, weights, logits=None, shared_gate=None, stream=None):
+    """Gate logits, top-k choice and routing weights on the device (w_router / w_shared_gate: bf16 bits as
+    int16/uint16 tensors)."""
+    _cuda(x, w_router, bias, w_shared_gate, ids, weights, logits, shared_gate)
+    _check(load().q4k_moe_router(_ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_shared_gate), m, num_experts, hidden,
+                                 top_k, scoring, 1 if normalize else 0, float(scale), n_group, topk_group, _ptr(ids),
+                                 _ptr(weights), _ptr(logits), _ptr(shared_gate), _stream(stream)))
+
+
+def q4k_rms_norm(x, w, m, hidden, eps, out, stream=None):
+    """out = x / sqrt(mean(x^2) + eps) * bf16(w), row by row (w: bf16 bits)."""
+    _cuda(x, w, out)
+    _check(load().q4k_rms_norm(_ptr(x), _ptr(w), m, hidden, float(eps), _ptr(out), _stream(stream)))
 
 
 def q4k_moe_layer_forward(w_gate, w_up, w_down, num_experts, ws_gate, ws_up, ws_down, shared_inter, shared_mode,

@@ -571,6 +571,49 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
     return cuda_status(cudaMemcpyAsync(y, dy, mh, cudaMemcpyDeviceToHost, stream), "device-to-host copy");
 }
 
+int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_bias, const uint16_t* d_w_shared_gate,
+                   int m, int num_experts, int hidden, int top_k, int scoring, int normalize, float scale, int n_group,
+                   int topk_group, int32_t* d_ids, float* d_weights, float* d_logits, float* d_shared_gate,
+                   cudaStream_t stream) {
+    if (m < 0) return fail(Q4K_ERR_SHAPE, "m must be >= 0 (got %d)", m);
+    if (num_experts < 1) return fail(Q4K_ERR_SHAPE, "num_experts must be >= 1 (got %d)", num_experts);
+    if (num_experts > kMaxExperts) return fail(Q4K_ERR_LIMIT, "num_experts must be <= %d (got %d)", kMaxExperts, num_experts);
+    if (top_k < 1 || top_k > Q4K_MAX_TOP_K || top_k > num_experts)
+        return fail(Q4K_ERR_TOPK, "top_k must be in [1, min(16, num_experts)] (got %d)", top_k);
+    if (hidden < 8 || hidden % 8 != 0) return fail(Q4K_ERR_SHAPE, "hidden must be a positive multiple of 8 (got %d)", hidden);
+    if (hidden > router_max_hidden()) return fail(Q4K_ERR_LIMIT, "hidden must be <= %d (got %d)", router_max_hidden(), hidden);
+    if (scoring != Q4K_ROUTE_SOFTMAX && scoring != Q4K_ROUTE_SIGMOID_GROUPED)
+        return fail(Q4K_ERR_MODE, "scoring must be Q4K_ROUTE_SOFTMAX or Q4K_ROUTE_SIGMOID_GROUPED (got %d)", scoring);
+    if (scoring == Q4K_ROUTE_SIGMOID_GROUPED) {
+        if (n_group < 1 || n_group > 32 || num_experts % n_group != 0)
+            return fail(Q4K_ERR_SHAPE, "n_group must be in [1, 32] and divide num_experts (got %d)", n_group);
+        if (topk_group < 1 || topk_group > n_group)
+            return fail(Q4K_ERR_SHAPE, "topk_group must be in [1, n_group] (got %d)", topk_group);
+        const int gsize = num_experts / n_group, per = std::max(1, top_k / topk_group);
+        if (per > std::min(16, gsize) || top_k > topk_group * gsize)
+            return fail(Q4K_ERR_SHAPE, "top_k %d cannot be chosen from %d groups of %d", top_k, topk_group, gsize);
+    }
+    if (m == 0) return Q4K_OK;
+    if (!d_x || !d_w_router || !d_ids || !d_weights) return fail(Q4K_ERR_NULL, "x, w_router, ids and weights are required");
+    if (d_w_shared_gate && !d_shared_gate) return fail(Q4K_ERR_NULL, "w_shared_gate given without shared_gate");
+    if (!aligned16(d_x) || !aligned16(d_w_router) || (d_w_shared_gate && !aligned16(d_w_shared_gate)))
+        return fail(Q4K_ERR_ALIGN, "x, w_router and w_shared_gate must be 16-byte aligned");
+    return cuda_status(launch_router(d_x, d_w_router, d_bias, d_w_shared_gate, m, num_experts, hidden, top_k, scoring,
+                                     normalize ? 1 : 0, scale, n_group, topk_group, d_ids, d_weights, d_logits,
+                                     d_shared_gate, stream),
+                       "router launch");
+}
+
+int q4k_rms_norm(const float* d_x, const uint16_t* d_w, int m, int hidden, float eps, float* d_out, cudaStream_t stream) {
+    if (m < 0) return fail(Q4K_ERR_SHAPE, "m must be >= 0 (got %d)", m);
+    if (hidden < 4 || hidden % 4 != 0) return fail(Q4K_ERR_SHAPE, "hidden must be a positive multiple of 4 (got %d)", hidden);
+    if (m == 0) return Q4K_OK;
+    if (!d_x || !d_w || !d_out) return fail(Q4K_ERR_NULL, "x, w and out are required");
+    if (!aligned16(d_x) || !aligned16(d_out) || (reinterpret_cast<uintptr_t>(d_w) & 7u))
+        return fail(Q4K_ERR_ALIGN, "x and out must be 16-byte aligned, w 8-byte aligned");
+    return cuda_status(launch_rms_norm(d_x, d_w, m, hidden, eps, d_out, stream), "rms_norm launch");
+}
+
 int q4k_quantize_rows(const float* d_x, int64_t rows, int k, void* d_out, cudaStream_t stream) {
     if (rows < 0) return fail(Q4K_ERR_SHAPE, "rows must be >= 0");
     if (k < 1 || k % kQK != 0) return fail(Q4K_ERR_SHAPE, "k must be a positive multiple of 256 (got %d)", k);

@@ -33,6 +33,12 @@ cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int3
 cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
                            const float* shared_out, const float* shared_gate, int shared_mode, int m,
                            int top_k, int hidden, float* y, bool pdl, cudaStream_t stream);
+cudaError_t launch_router(const float* x, const uint16_t* w, const float* bias, const uint16_t* w_sg, int m, int E,
+                          int H, int top_k, int scoring, int normalize, float scale, int n_group, int topk_group,
+                          int32_t* ids, float* weights, float* logits, float* shared_gate, cudaStream_t stream);
+int router_max_hidden();
+cudaError_t launch_rms_norm(const float* x, const uint16_t* w, int m, int hidden, float eps, float* out,
+                            cudaStream_t stream);
 cudaError_t launch_quantize(const float* x, int64_t rows, int k, uint8_t* out, cudaStream_t stream);
 cudaError_t launch_stream_ceiling(const void* src, uint64_t bytes, uint32_t* sink, cudaStream_t stream);
 // Up to 5 small copies (sizes multiples of 4 bytes) in one launch; sources may be host memory

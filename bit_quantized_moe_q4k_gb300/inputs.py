@@ -13,7 +13,10 @@ seed and the input's name):
   * ids, "zipf": expert e has probability proportional to 1/(e+1)^s
     (rank = id); a token draws top_k distinct experts by weighted sampling
     without replacement (a repeated draw is redrawn);
-  * routing weights: softmax over the top_k slots of N(0, 1) logits.
+  * routing weights: softmax over the top_k slots of N(0, 1) logits;
+  * router weights: N(0, 1/hidden) stored as bf16 (round to nearest even), so the
+    gate logits of N(0, 1) activations are about N(0, 1); correction biases
+    uniform in [-0.05, 0.05]; norm weights 1 + N(0, 0.1) in bf16.
 """
 from __future__ import annotations
 
@@ -34,6 +37,21 @@ def normal(seed: int, name: str, shape, std: float = 1.0, *extra: int) -> np.nda
 def expert_weights(seed: int, proj: str, expert: int, n: int, k: int, std: float = 0.02) -> np.ndarray:
     """fp32 [n, k] N(0, std) weights of one expert's projection (proj in gate/up/down/...)."""
     return normal(seed, "w_" + proj, (n, k), std, expert)
+
+
+def to_bf16_bits(x) -> np.ndarray:
+    """uint16 bf16 bit patterns of float32 values, rounded to nearest even (data conversion)."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_normal(seed: int, name: str, shape, std: float = 1.0, mean: float = 0.0) -> np.ndarray:
+    """uint16 bf16 bits of mean + N(0, std) draws."""
+    return to_bf16_bits(normal(seed, name, shape, std) + np.float32(mean))
+
+
+def uniform(seed: int, name: str, shape, lo: float, hi: float) -> np.ndarray:
+    return _stream(seed, name).uniform(lo, hi, size=shape).astype(np.float32)
 
 
 def ids_uniform_distinct(seed: int, m: int, top_k: int, num_experts: int, name: str = "ids") -> np.ndarray:

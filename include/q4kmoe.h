@@ -26,8 +26,15 @@
  *
  * Conventions of every call
  *   - Pointers named d_* or documented as device memory are device pointers
- *     owned by the caller; the library allocates no device memory, holds no
- *     global device state and keeps no pointer past the call.
+ *     owned by the caller; the library allocates no device memory and keeps no
+ *     pointer past the call. The one global device state is the static scratch
+ *     array of q4k_expert_ffn_forward_noalloc (4 MiB per device, part of the
+ *     library image); after a cudaDeviceReset the process must not call that
+ *     entry point again (the address it keeps belongs to the old context).
+ *   - Waits inside a kernel for work of other CTAs of the same launch are bounded
+ *     in time: the environment variable Q4K_WAIT_NS (nanoseconds, read at every
+ *     call; default 2 s) sets the limit, after which the kernel stops waiting, sets
+ *     *err_flag to Q4K_ERR_TIMEOUT and returns.
  *   - Calls are asynchronous on `stream` (the last argument) and return a
  *     q4k_status. Host-side validation happens before anything is enqueued;
  *     on an error status nothing was enqueued.
@@ -270,6 +277,48 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
                                const float* weights, const float* shared_gate, int m, int top_k,
                                int hidden, int inter, float* y, void* d_workspace,
                                size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_moe_router -- the layer's router [P2: MoeBuffers::gate_logits, the `noaux_tc`
+ * routing, synth::expert_weights_seeded]: gate logits, top-k choice and routing weights,
+ * written where q4k_moe_layer_forward reads ids, weights and shared_gate.
+ *   logits[t, e] = sum_h bf16(w_router[e, h]) * x[t, h]   (fp32)
+ *   scoring Q4K_ROUTE_SOFTMAX: the top_k largest logits, weight = softmax over all experts
+ *     (normalize: divided by the chosen experts' sum).
+ *   scoring Q4K_ROUTE_SIGMOID_GROUPED (noaux_tc): s = sigmoid(logit), the choice on
+ *     s + bias (bias NULL: 0) among the experts of the topk_group best of n_group groups of
+ *     consecutive ids, a group scored by the sum of its max(1, top_k/topk_group) best
+ *     s + bias; weight = s (normalize: divided by the chosen s' sum) * scale.
+ *   Choice order: larger score first, equal scores by the lower id; ids [m, top_k] int32 in
+ *   that order, weights [m, top_k] fp32. d_logits [m, num_experts] (optional) receives the
+ *   logits. d_w_shared_gate (optional, bf16 [hidden]) adds the shared expert's gate logit
+ *   d_shared_gate[t] = sum_h bf16(w_shared_gate[h]) * x[t, h].
+ * Layouts: d_x [m, hidden] fp32; d_w_router [num_experts, hidden] bf16 bits (uint16),
+ * both 16-byte aligned. Limits: hidden % 8 == 0, hidden <= 16384; num_experts <= 4096;
+ * top_k <= min(16, num_experts); grouped: n_group <= 32 divides num_experts,
+ * 1 <= topk_group <= n_group, max(1, top_k/topk_group) <= min(16, num_experts/n_group),
+ * top_k <= topk_group * num_experts/n_group. One launch (thread-block clusters of 16 or 8
+ * CTAs), a programmatic dependent of the previous kernel in the stream, no workspace;
+ * the result is the same bits at every call.
+ */
+#define Q4K_ROUTE_SOFTMAX 0
+#define Q4K_ROUTE_SIGMOID_GROUPED 1
+int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_bias,
+                   const uint16_t* d_w_shared_gate, int m, int num_experts, int hidden, int top_k,
+                   int scoring, int normalize, float scale, int n_group, int topk_group,
+                   int32_t* d_ids, float* d_weights, float* d_logits, float* d_shared_gate,
+                   cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * q4k_rms_norm -- RMSNorm chained after the combine [P2: ChainToNormed, rms_norm_sum_sq +
+ * rms_norm_apply_bf16]: the next layer's normed input from this layer's output.
+ *   out[t, h] = x[t, h] / sqrt(sum_h x[t, h]^2 / hidden + eps) * bf16(w[h])   (fp32)
+ * d_x, d_out [m, hidden] fp32 (d_out may alias d_x), d_w bf16 [hidden]; 16-byte aligned
+ * rows (hidden % 4 == 0), d_w 8-byte aligned. One launch, a programmatic dependent of the
+ * previous kernel (its launch overlaps that kernel's tail).
+ */
+int q4k_rms_norm(const float* d_x, const uint16_t* d_w, int m, int hidden, float eps, float* d_out,
+                 cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * q4k_quantize_rows -- fp32 [rows, k] -> Q4_K bytes [rows, k/256*144] on the device

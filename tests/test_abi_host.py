@@ -109,6 +109,44 @@ def test_bucket_and_quantize_reject():
     assert lib.q4k_quantize_rows(A16, 0, 256, A16, None) == 0
 
 
+def router(**kw):
+    a = dict(x=A16, w=A16, bias=None, wsg=None, m=3, E=128, H=2048, k=8, scoring=0, norm=1, scale=1.0, ng=1, tg=1,
+             ids=A16, wt=A16, logits=None, sg=None)
+    a.update(kw)
+    return q4k.load().q4k_moe_router(a["x"], a["w"], a["bias"], a["wsg"], a["m"], a["E"], a["H"], a["k"], a["scoring"],
+                                     a["norm"], a["scale"], a["ng"], a["tg"], a["ids"], a["wt"], a["logits"], a["sg"],
+                                     None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(m=-1), 2), (dict(E=0), 2), (dict(E=4097), 9), (dict(k=0), 3), (dict(k=17), 3), (dict(E=4, k=5), 3),
+    (dict(H=12), 2), (dict(H=0), 2), (dict(H=16384 + 8), 9), (dict(scoring=2), 8),
+    (dict(scoring=1, ng=3), 2), (dict(scoring=1, ng=64, E=128), 2), (dict(scoring=1, ng=8, tg=9), 2),
+    (dict(scoring=1, ng=8, tg=0), 2), (dict(scoring=1, E=16, ng=8, tg=2, k=6), 2),
+    (dict(x=None), 1), (dict(w=None), 1), (dict(ids=None), 1), (dict(wt=None), 1), (dict(wsg=A16), 1),
+    (dict(x=MISALIGNED), 7), (dict(w=MISALIGNED), 7), (dict(wsg=MISALIGNED, sg=A16), 7),
+])
+def test_router_rejects(kw, status):
+    assert router(**kw) == status
+    assert q4k.load().q4k_last_error_string()
+
+
+def test_router_and_norm_empty_batch():
+    assert router(m=0) == 0
+    assert router(m=0, scoring=1, ng=8, tg=4, E=256, H=7168) == 0
+    lib = q4k.load()
+    assert lib.q4k_rms_norm(A16, A16, 0, 2048, 1e-6, A16, None) == 0
+
+
+def test_rms_norm_rejects():
+    lib = q4k.load()
+    assert lib.q4k_rms_norm(A16, A16, -1, 2048, 1e-6, A16, None) == 2
+    assert lib.q4k_rms_norm(A16, A16, 2, 2050, 1e-6, A16, None) == 2
+    assert lib.q4k_rms_norm(None, A16, 2, 2048, 1e-6, A16, None) == 1
+    assert lib.q4k_rms_norm(MISALIGNED, A16, 2, 2048, 1e-6, A16, None) == 7
+    assert lib.q4k_rms_norm(A16, A16 + 2, 2, 2048, 1e-6, A16, None) == 7
+
+
 def test_binding_raises_with_status_name():
     with pytest.raises(q4k.Q4KError) as ei:
         _lib._check(2)
