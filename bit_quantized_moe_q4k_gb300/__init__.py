@@ -7,6 +7,8 @@ the seeded synthetic-input generators (``inputs``) and the workload table
 first call does, and raises if it cannot.
 """
 from ._lib import (  # noqa: F401
+    FMT_AFFINE4,
+    FMT_Q4TP,
     PATH_PERSISTENT,
     PATH_TWO_LAUNCH,
     Q4KError,
@@ -23,6 +25,7 @@ from ._lib import (  # noqa: F401
     q4k_expert_ffn_noalloc_max_scratch_bytes,
     q4k_moe_bucket,
     q4k_moe_id_gemv,
+    q4k_moe_id_gemv_fmt,
     q4k_moe_layer_forward,
     q4k_moe_layer_down,
     q4k_moe_layer_forward_host,

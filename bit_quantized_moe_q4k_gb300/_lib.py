@@ -25,6 +25,7 @@ STATUS_NAMES = {
 SHARED_NONE, SHARED_SIGMOID, SHARED_UNSCALED = 0, 1, 2
 PATH_TWO_LAUNCH, PATH_PERSISTENT = 0, 1
 ROUTE_SOFTMAX, ROUTE_SIGMOID_GROUPED = 0, 1
+FMT_AFFINE4, FMT_Q4TP = 1, 2
 
 # Exported C symbols and their signatures (restype, argtypes).
 _P, _I, _I64, _U64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
@@ -49,6 +50,8 @@ SIGNATURES = {
     "q4k_moe_layer_half_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "q4k_moe_layer_launch_count": (_I, [_I, _I, _I, _I, _I, _I]),
     "q4k_moe_layer_path": (_I, [_I, _I, _I, _I, _I, _I]),
+    "q4k_moe_id_gemv_fmt": (_I, [_I, _P, _P, _U64, _U64, _U64, _U64, _I, _I, _P, _I64, _I64, _P, _I, _I, _I, _I, _P,
+                                 _P, _P]),
     "q4k_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P, _P, _P]),
     "q4k_rms_norm": (_I, [_P, _P, _I, _I, ctypes.c_float, _P, _P]),
     "q4k_quantize_rows": (_I, [_P, _I64, _I, _P, _P]),
@@ -176,6 +179,15 @@ def moe_combine_residual(h_mid, expert_out, weights, shared_out, shared_gate, sh
     _check(load().moe_combine_residual(_ptr(h_mid), _ptr(expert_out), _ptr(weights), _ptr(shared_out),
                                        _ptr(shared_gate), shared_mode, m, top_k, hidden, _ptr(hidden_out),
                                        _stream(stream)))
+
+
+def q4k_moe_id_gemv_fmt(fmt, w, w2, w_byte_offset, expert_stride, scales_offset, biases_offset, group_size,
+                        num_experts, a, outer, inner, ids, m, top_k, n, k, out, err_flag=None, stream=None):
+    """Batched id-GEMV over an MLX-affine (FMT_AFFINE4) or q4tp (FMT_Q4TP) slab; w2: fused gate|up."""
+    _cuda(w, w2, a, ids, out, err_flag)
+    _check(load().q4k_moe_id_gemv_fmt(fmt, _ptr(w), _ptr(w2), w_byte_offset, expert_stride, scales_offset,
+                                      biases_offset, group_size, num_experts, _ptr(a), outer, inner, _ptr(ids), m,
+                                      top_k, n, k, _ptr(out), _ptr(err_flag), _stream(stream)))
 
 
 def q4k_moe_router(x, w_router, bias, w_shared_gate, m, num_experts, hidden, top_k, scoring, normalize, scale,

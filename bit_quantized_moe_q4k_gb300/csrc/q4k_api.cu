@@ -571,6 +571,39 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
     return cuda_status(cudaMemcpyAsync(y, dy, mh, cudaMemcpyDeviceToHost, stream), "device-to-host copy");
 }
 
+int q4k_moe_id_gemv_fmt(int fmt, const void* d_w, const void* d_w2, uint64_t w_byte_offset, uint64_t expert_stride,
+                        uint64_t scales_offset, uint64_t biases_offset, int group_size, int num_experts,
+                        const float* d_a, int64_t src1_outer_stride, int64_t src1_inner_stride, const int32_t* d_ids,
+                        int m, int top_k, int n, int k, float* d_out, int* d_err_flag, cudaStream_t stream) {
+    if (fmt != Q4K_FMT_AFFINE4 && fmt != Q4K_FMT_Q4TP)
+        return fail(Q4K_ERR_MODE, "fmt must be Q4K_FMT_AFFINE4 or Q4K_FMT_Q4TP (got %d)", fmt);
+    int st = check_gemv_shape(num_experts, m, top_k, n, k);
+    if (st != Q4K_OK) return st;
+    if (fmt == Q4K_FMT_AFFINE4) {
+        if (group_size != 32 && group_size != 64 && group_size != 128)
+            return fail(Q4K_ERR_SHAPE, "group_size must be 32, 64 or 128 (got %d)", group_size);
+        if (scales_offset % 4 != 0 || biases_offset % 4 != 0)
+            return fail(Q4K_ERR_ALIGN, "scales and biases offsets must be multiples of 4");
+    }
+    const uint64_t mat = fmt == Q4K_FMT_AFFINE4
+                             ? (uint64_t)n * (k / 2)
+                             : (uint64_t)n * (k / 2) + 4ull * n + (uint64_t)n * ((k / 32) * 5 / 8);
+    if (expert_stride % 16 != 0 || (num_experts > 1 && expert_stride < mat))
+        return fail(Q4K_ERR_SHAPE, "expert_stride must be a multiple of 16 holding the codes (%llu bytes)",
+                    (unsigned long long)mat);
+    if (m == 0) return Q4K_OK;
+    if (!d_w || !d_a || !d_ids || !d_out) return fail(Q4K_ERR_NULL, "w, a, ids and out are required");
+    const uint8_t* w = static_cast<const uint8_t*>(d_w) + w_byte_offset;
+    const uint8_t* w2 = d_w2 ? static_cast<const uint8_t*>(d_w2) + w_byte_offset : nullptr;
+    if (!aligned16(w) || (w2 && !aligned16(w2))) return fail(Q4K_ERR_ALIGN, "slabs (+ offset) must be 16-byte aligned");
+    if (!aligned16(d_a) || src1_outer_stride % 4 != 0 || src1_inner_stride % 4 != 0)
+        return fail(Q4K_ERR_ALIGN, "activation rows must be 16-byte aligned");
+    return cuda_status(launch_fmt4(fmt, w, w2, expert_stride, scales_offset, biases_offset, group_size, num_experts,
+                                   d_a, src1_outer_stride, src1_inner_stride, d_ids, m, top_k, n, k, d_out,
+                                   d_err_flag, stream),
+                       "fmt4 id-GEMV launch");
+}
+
 int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_bias, const uint16_t* d_w_shared_gate,
                    int m, int num_experts, int hidden, int top_k, int scoring, int normalize, float scale, int n_group,
                    int topk_group, int32_t* d_ids, float* d_weights, float* d_logits, float* d_shared_gate,

@@ -279,6 +279,32 @@ int q4k_moe_layer_forward_host(const void* d_w_gate, const void* d_w_up, const v
                                size_t ws_bytes, int* d_err_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * q4k_moe_id_gemv_fmt -- the batched id-GEMV of q4k_moe_id_gemv over two other 4-bit
+ * weight formats (same pair walk, bucketing, outputs and id checks; d_w2 != NULL gives the
+ * fused gate|up form out = silu(W . a) * (W2 . a), W2 read with the same offsets):
+ *   Q4K_FMT_AFFINE4 [P2: the MLX-style affine expert blob, weights | scales | biases bound
+ *     at three offsets, GROUP_SIZE]: expert e's [n, k] matrix starts at
+ *     M = d_w + w_byte_offset + e*expert_stride: codes at M (row r: k/2 bytes from r*k/2;
+ *     weight c of the row in nibble c%2 of byte c/2, low nibble first), bf16 scales
+ *     [n, k/group_size] at M + scales_offset, bf16 biases [n, k/group_size] at
+ *     M + biases_offset; w = scale * q + bias. group_size 32, 64 or 128.
+ *   Q4K_FMT_Q4TP [P3: the q4tp matrix of mv_lab.rs' production kernel]: M as above holds
+ *     the codes (row r group g's 32 weights in the 16 bytes at (r*k/32 + g)*16, weight order
+ *     as above), then binary16 (base, step) per row at M + n*k/2 + 4r, then 5-bit group codes
+ *     at M + n*k/2 + 4n with k/32*5/8 bytes per row (group g in bits 5g..5g+4, LSB first);
+ *     w = (q - 8) * 2^(base + code*step). scales_offset, biases_offset, group_size unused.
+ * Alignment: d_w (+ offset) and expert_stride multiples of 16; affine offsets multiples of 4.
+ * Limits and the rest as q4k_moe_id_gemv (k % 256 == 0, n % 4 == 0, num_experts <= 4096).
+ */
+#define Q4K_FMT_AFFINE4 1
+#define Q4K_FMT_Q4TP 2
+int q4k_moe_id_gemv_fmt(int fmt, const void* d_w, const void* d_w2, uint64_t w_byte_offset,
+                        uint64_t expert_stride, uint64_t scales_offset, uint64_t biases_offset,
+                        int group_size, int num_experts, const float* d_a, int64_t src1_outer_stride,
+                        int64_t src1_inner_stride, const int32_t* d_ids, int m, int top_k, int n, int k,
+                        float* d_out, int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * q4k_moe_router -- the layer's router [P2: MoeBuffers::gate_logits, the `noaux_tc`
  * routing, synth::expert_weights_seeded]: gate logits, top-k choice and routing weights,
  * written where q4k_moe_layer_forward reads ids, weights and shared_gate.

@@ -58,3 +58,29 @@ def host(t):
 def err_flag():
     import torch
     return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def fmt4_slab(seed, fmt, E, n, k, gs=64, pad=0, name="w"):
+    """A seeded slab of E [n, k] matrices in an other 4-bit format (oracle numbering: fmt 0
+    MLX-affine, 1 q4tp), laid out as the header documents: random code bytes; affine bf16
+    scales U(0.005, 0.03) and biases U(-0.15, 0.05) per group of gs; q4tp binary16 base
+    U(-8, -5) and step U(0, 1/8) per row and random 5-bit group codes. Returns
+    (slab uint8, expert_stride, scales_offset, biases_offset)."""
+    mb = oracle.fmt4_matrix_bytes(fmt, n, k, gs)
+    stride = ((mb + 15) // 16) * 16 + pad
+    g = np.random.default_rng([seed, fmt, E, n, k, gs, pad, sum(name.encode())])
+    slab = g.integers(0, 256, E * stride, dtype=np.uint8)
+    s_off = n * k // 2
+    b_off = s_off + 2 * n * (k // gs)
+    for e in range(E):
+        base = e * stride
+        if fmt == 0:
+            ng = n * (k // gs)
+            sc = inputs.to_bf16_bits(g.uniform(0.005, 0.03, ng).astype(np.float32)).view(np.uint8)
+            bi = inputs.to_bf16_bits(g.uniform(-0.15, 0.05, ng).astype(np.float32)).view(np.uint8)
+            slab[base + s_off: base + s_off + 2 * ng] = sc
+            slab[base + b_off: base + b_off + 2 * ng] = bi
+        else:
+            prm = np.stack([g.uniform(-8, -5, n), g.uniform(0, 0.125, n)], 1).astype(np.float16).reshape(-1)
+            slab[base + s_off: base + s_off + 4 * n] = prm.view(np.uint8)
+    return slab, stride, s_off, b_off

@@ -109,6 +109,32 @@ def test_bucket_and_quantize_reject():
     assert lib.q4k_quantize_rows(A16, 0, 256, A16, None) == 0
 
 
+def fmt4(**kw):
+    a = dict(fmt=1, w=A16, w2=None, off=0, stride=1 << 20, so=0, bo=0, gs=64, E=4, a=A16, outer=256, inner=0, ids=A16,
+             m=3, T=2, n=64, k=256, out=A16, flag=None)
+    a.update(kw)
+    return q4k.load().q4k_moe_id_gemv_fmt(a["fmt"], a["w"], a["w2"], a["off"], a["stride"], a["so"], a["bo"], a["gs"],
+                                          a["E"], a["a"], a["outer"], a["inner"], a["ids"], a["m"], a["T"], a["n"],
+                                          a["k"], a["out"], a["flag"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=0), 8), (dict(fmt=3), 8), (dict(gs=48), 2), (dict(gs=256), 2), (dict(so=2), 7), (dict(bo=6), 7),
+    (dict(stride=1000), 2), (dict(stride=16), 2), (dict(fmt=2, stride=64 * 128 + 256 + 64 * 5 - 16), 2),
+    (dict(k=100), 2), (dict(n=6), 2), (dict(T=17), 3), (dict(E=5000), 9),
+    (dict(w=None), 1), (dict(a=None), 1), (dict(ids=None), 1), (dict(out=None), 1),
+    (dict(w=MISALIGNED), 7), (dict(off=8), 7), (dict(w2=MISALIGNED), 7), (dict(a=MISALIGNED), 7), (dict(outer=255), 7),
+])
+def test_fmt4_id_gemv_rejects(kw, status):
+    assert fmt4(**kw) == status
+    assert q4k.load().q4k_last_error_string()
+
+
+def test_fmt4_empty_batch():
+    assert fmt4(m=0) == 0
+    assert fmt4(m=0, fmt=2, stride=64 * 128 + 256 + 64 * 5 + 16 - (64 * 128 + 256 + 64 * 5) % 16) == 0
+
+
 def router(**kw):
     a = dict(x=A16, w=A16, bias=None, wsg=None, m=3, E=128, H=2048, k=8, scoring=0, norm=1, scale=1.0, ng=1, tg=1,
              ids=A16, wt=A16, logits=None, sg=None)
