@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the other workloads' records (per_config) after the headline")
     ap.add_argument("--per-config-steps", type=int, default=10)
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the router, routed-step and weight-format records after the headline")
     return ap.parse_args()
 
 
@@ -540,6 +542,248 @@ def per_config_records(args, rank, world, local_rank, peak):
     return out
 
 
+# ---------------------------------------------------------------------------------------------
+# The rows after the layer: router, the routed decode step, other 4-bit weight formats
+
+def time_graph(step, K, Wm, stream, local_rank, soak_s=0.3):
+    """Eager warm-up, W steps then K steps captured in CUDA graphs; clocks sampled over an
+    untimed soak of the K-step graph and the timed replay. Returns (ms per step, clocks)."""
+    import torch
+    for i in range(3):
+        with torch.cuda.stream(stream):
+            step(i)
+    stream.synchronize()
+    g_warm, g = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_warm, stream=stream, capture_error_mode="thread_local"):
+            for i in range(Wm):
+                step(i)
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(K):
+                step(Wm + i)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t0 < soak_s:
+            g.replay()
+            stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    return e0.elapsed_time(e1) / K, clk
+
+
+def rotation(bytes_per_step, cap_bytes, bytes_per_copy):
+    """Copies to rotate through so the bytes touched between two uses of one exceed 3x L2."""
+    n = max(4, -(-3 * L2_BYTES // max(1, bytes_per_step)))
+    return int(max(2, min(n, cap_bytes // max(1, bytes_per_copy))))
+
+
+ROUTER_CONFIGS = [
+    # (name, num_experts, hidden, top_k, scoring, n_group, topk_group, scale, m)
+    ("qwen3moe_router_e128_h2048_t8_softmax", 128, 2048, 8, 0, 1, 1, 1.0, 1),
+    ("qwen3moe_router_e128_h2048_t8_softmax", 128, 2048, 8, 0, 1, 1, 1.0, 16),
+    ("deepseekv3_router_e256_h7168_t8_noaux_g8k4", 256, 7168, 8, 1, 8, 4, 2.5, 1),
+    ("deepseekv3_router_e256_h7168_t8_noaux_g8k4", 256, 7168, 8, 1, 8, 4, 2.5, 64),
+]
+
+
+def router_records(args, local_rank, peak):
+    import torch
+    import bit_quantized_moe_q4k_gb300 as q4k
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    out = []
+    for name, E, H, k, scoring, ng, tg, scale, m in ROUTER_CONFIGS:
+        wbytes = E * H * 2
+        n = rotation(wbytes, 4 << 30, wbytes)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(E * 131 + H)
+        wr = (torch.randn(n, E, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16).view(torch.int16)
+        bias = (torch.rand(E, generator=gen, device=dev) - 0.5) * 0.1
+        xs = torch.randn(16, m, H, generator=gen, device=dev)
+        ids = torch.empty(m, k, dtype=torch.int32, device=dev)
+        wt = torch.empty(m, k, dtype=torch.float32, device=dev)
+        lg = torch.empty(m, E, dtype=torch.float32, device=dev)
+
+        def step(i):
+            q4k.q4k_moe_router(xs[i % 16], wr[i % n], bias if scoring else None, None, m, E, H, k, scoring, True,
+                               scale, ng, tg, ids, wt, lg, None, stream)
+
+        K = max(10, args.per_config_steps * 4)
+        ms, clk = time_graph(step, K, 3, stream, local_rank)
+        b = wbytes + m * H * 4 + m * k * 8
+        out.append({"workload": f"{name}_m{m}", "kernel": "router_logits_kernel + router_topk_kernel (two launches, "
+                                                            "programmatic dependent)",
+                    "bound": "hbm", "bytes_per_launch": b, "avg_launch_us": ms * 1e3,
+                    "achieved": b / (ms * 1e-3) / 1e9, "peak": peak, "frac": b / (ms * 1e-3) / 1e9 / peak,
+                    "unit": "GB/s", "clocks": clk, "l2": f"rotating {n} router weight copies"})
+        del wr, xs
+        torch.cuda.empty_cache()
+    return out
+
+
+def routed_step_record(args, W: Workload, local_rank, peak):
+    """One decode MoE block per step, chained as in a model: the router (softmax top-k, plus
+    the shared expert's gate logit) on h_post, the layer with the router's ids / weights /
+    gate, the next layer's input RMSNorm on the layer's output, which is the next step's
+    h_post."""
+    import torch
+    import bit_quantized_moe_q4k_gb300 as q4k
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    H, I, E, T, m, Is = W.hidden, W.inter, W.num_experts, W.top_k, W.m, W.shared_inter
+    ids0 = inputs.make_ids(W.seed, "uniform", m, T, E)
+    lb = layer_bytes(W, ids0)
+    per_layer = lb["layer"] + E * H * 2 + H * 2 * 2
+    slab_total = E * (2 * slab_bytes(I, H) + slab_bytes(H, I)) + (3 * slab_bytes(Is, H) if Is else 0)
+    n = rotation(per_layer, 40 << 30, slab_total)
+    gen = torch.Generator(device=dev)
+
+    def slab(seed, n_exp, rows, k):
+        buf = torch.empty(n_exp * rows * (k // 256) * 144, dtype=torch.uint8, device=dev)
+        gen.manual_seed(seed)
+        step_rows = max(1, (64 << 20) // (4 * k))
+        for r0 in range(0, n_exp * rows, step_rows):
+            r1 = min(n_exp * rows, r0 + step_rows)
+            x = torch.randn(r1 - r0, k, generator=gen, device=dev) * 0.02
+            q4k.q4k_quantize_rows(x, r1 - r0, k, buf[r0 * (k // 256) * 144:])
+        return buf
+
+    layers = []
+    for li in range(n):
+        s = 50000 + li * 8
+        L = {"wg": slab(s + 1, E, I, H), "wu": slab(s + 2, E, I, H), "wd": slab(s + 3, E, H, I)}
+        L.update({"sg": slab(s + 4, 1, Is, H), "su": slab(s + 5, 1, Is, H), "sd": slab(s + 6, 1, H, Is)} if Is else
+                 {"sg": None, "su": None, "sd": None})
+        gen.manual_seed(s + 7)
+        L["wr"] = (torch.randn(E, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16).view(torch.int16)
+        L["wsg"] = (torch.randn(H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16).view(torch.int16)
+        L["wn"] = (1 + 0.1 * torch.randn(H, generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+        L["hm"] = torch.randn(m, H, generator=gen, device=dev)
+        layers.append(L)
+    ids = torch.empty(m, T, dtype=torch.int32, device=dev)
+    wt = torch.empty(m, T, dtype=torch.float32, device=dev)
+    sgl = torch.empty(m, dtype=torch.float32, device=dev)
+    lgt = torch.empty(m, E, dtype=torch.float32, device=dev)
+    y = torch.empty(m, H, dtype=torch.float32, device=dev)
+    xy = [torch.randn(m, H, generator=gen, device=dev), torch.empty(m, H, dtype=torch.float32, device=dev)]
+    ws_bytes = q4k.q4k_moe_layer_workspace_size(m, T, E, H, I, Is)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(i):
+        L = layers[i % n]
+        x, xn = xy[i % 2], xy[(i + 1) % 2]
+        q4k.q4k_moe_router(x, L["wr"], None, L["wsg"] if Is else None, m, E, H, T, q4k.ROUTE_SOFTMAX, True, 1.0, 1, 1,
+                           ids, wt, lgt, sgl if Is else None, stream)
+        q4k.q4k_moe_layer_forward(L["wg"], L["wu"], L["wd"], E, L["sg"], L["su"], L["sd"], Is, W.shared_mode, x,
+                                  L["hm"], ids, wt, sgl if Is else None, m, T, H, I, y, ws, ws_bytes, flag, stream)
+        q4k.q4k_rms_norm(y, L["wn"], m, H, 1e-6, xn, stream)
+
+    K = max(10, args.per_config_steps * 4)
+    ms, clk = time_graph(step, K, 3, stream, local_rank)
+    assert int(flag.item()) == 0, "device error flag raised"
+    b = per_layer + m * H * 4 * 2
+    rec = {"workload": f"{W.name} + router + rms_norm", "ms_per_step": ms,
+           "launches_per_step": 3 + q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is),
+           "bytes_per_step": b, "hbm_gbs": b / (ms * 1e-3) / 1e9, "hbm_frac": b / (ms * 1e-3) / 1e9 / peak,
+           "chain": "router -> layer -> rms_norm on one stream, each a programmatic dependent of the one before; "
+                    "the norm's output is the next step's h_post", "clocks": clk,
+           "l2": f"rotating {n} layers"}
+    del layers
+    torch.cuda.empty_cache()
+    return rec
+
+
+FORMAT_CASES = [  # (format, affine group size); the Q4_K row is the same projection through the layer half
+    ("q4k", 0), ("mlx_affine4_gs64", 64), ("q4tp", 0)]
+
+
+def format_records(args, local_rank, peak):
+    """Fused gate|up + SwiGLU of the Qwen3-like routed experts (128 experts, hidden 2048, width 768,
+    top-8) in each 4-bit format, m = 1 and m = 16: the same walk, bucketing and staging, different
+    block decoders and bytes per weight."""
+    import torch
+    import bit_quantized_moe_q4k_gb300 as q4k
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    E, H, I, T = 128, 2048, 768, 8
+    out = []
+    for fmt, gs in FORMAT_CASES:
+        if fmt == "q4k":
+            mat = slab_bytes(I, H)
+            stride = mat
+        elif fmt == "q4tp":
+            mat = I * H // 2 + 4 * I + I * (H // 32) * 5 // 8
+            stride = -(-mat // 16) * 16
+        else:
+            mat = I * H // 2 + 4 * I * (H // gs)
+            stride = -(-mat // 16) * 16
+        for m in (1, 16):
+            ids_np = [inputs.ids_uniform_distinct(60000 + j, m, T, E) for j in range(8)]
+            U = np.mean([len(set(a.tolist())) for a in ids_np])
+            per_step = U * 2 * mat + m * H * 4 + m * T * I * 4
+            n = rotation(int(per_step), 24 << 30, 2 * E * stride)
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(70000 + m)
+            slabs = [torch.randint(0, 256, (2, E * stride), dtype=torch.uint8, device=dev, generator=gen)
+                     for _ in range(n)]
+            if fmt != "q4k":  # sane scales: affine bf16 scale/bias ~ 0.01, q4tp base -7, step 0.1
+                for sl in slabs:
+                    v = sl.view(2, E, stride)
+                    if fmt == "q4tp":
+                        prm = torch.tensor([-7.0, 0.1], dtype=torch.float16, device=dev).view(torch.uint8)
+                        v[:, :, I * H // 2: I * H // 2 + 4 * I] = prm.repeat(I)
+                    else:
+                        sc = torch.full((I * (H // gs),), 0.01, dtype=torch.bfloat16, device=dev).view(torch.uint8)
+                        v[:, :, I * H // 2: I * H // 2 + 2 * I * (H // gs)] = sc
+                        v[:, :, I * H // 2 + 2 * I * (H // gs): mat] = sc
+            else:
+                for sl in slabs:  # real Q4_K blocks
+                    for j in range(2):
+                        x = torch.randn(E * I, H, generator=gen, device=dev) * 0.02
+                        q4k.q4k_quantize_rows(x, E * I, H, sl[j])
+            ids = [torch.from_numpy(a).to(dev) for a in ids_np]
+            xs = torch.randn(8, m, H, generator=gen, device=dev)
+            act = torch.empty(m * T, I, dtype=torch.float32, device=dev)
+            flag = torch.zeros(1, dtype=torch.int32, device=dev)
+            ws_bytes = q4k.q4k_moe_layer_half_workspace_size(m, T, H, 0, H)
+            ws = torch.empty(max(256, ws_bytes), dtype=torch.uint8, device=dev)
+
+            def step(i):
+                sl = slabs[i % n]
+                if fmt == "q4k":
+                    q4k.q4k_moe_layer_gate_up(sl[0], sl[1], E, None, None, 0, xs[i % 8], ids[i % 8], m, T, H, I, act,
+                                              None, ws, ws_bytes, flag, stream)
+                else:
+                    q4k.q4k_moe_id_gemv_fmt(q4k.FMT_Q4TP if fmt == "q4tp" else q4k.FMT_AFFINE4, sl[0], sl[1], 0,
+                                            stride, I * H // 2, I * H // 2 + 2 * I * (H // max(gs, 1)), max(gs, 32),
+                                            E, xs[i % 8], H, 0, ids[i % 8], m, T, I, H, act, flag, stream)
+
+            K = max(10, args.per_config_steps * 4)
+            ms, clk = time_graph(step, K, 3, stream, local_rank)
+            assert int(flag.item()) == 0, "device error flag raised"
+            out.append({"workload": f"qwen3moe_gate_up_{fmt}_m{m}", "format": fmt,
+                        "bytes_per_weight": mat / (I * H), "kernel": "idgemv_kernel<fused>" if fmt == "q4k" else
+                        "fmt4_kernel<fused>", "bound": "hbm", "bytes_per_launch": per_step,
+                        "avg_launch_us": ms * 1e3, "achieved": per_step / (ms * 1e-3) / 1e9, "peak": peak,
+                        "frac": per_step / (ms * 1e-3) / 1e9 / peak, "unit": "GB/s", "clocks": clk,
+                        "l2": f"rotating {n} slab pairs"})
+            del slabs
+            torch.cuda.empty_cache()
+    return out
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -644,6 +888,11 @@ def main():
     per_config = None
     if not args.no_per_config and not args.m and args.workload == HEADLINE:
         per_config = per_config_records(args, rank, world, local_rank, peak)
+    next_rows = None
+    if not args.no_next_rows and not args.m and args.workload == HEADLINE:
+        next_rows = {"router": router_records(args, local_rank, peak),
+                     "routed_step": routed_step_record(args, W, local_rank, peak),
+                     "formats": format_records(args, local_rank, peak)}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = time_oracle(W, args.cpu_seconds)
@@ -670,6 +919,7 @@ def main():
         "clocks": r["clocks"],
         "gpu_launches": r["launches_per_step"] * K,
         "per_config": per_config,
+        "next_rows": next_rows,
     }
     print(json.dumps(line), flush=True)
 

@@ -191,7 +191,7 @@ def q4k_moe_id_gemv_fmt(fmt, w, w2, w_byte_offset, expert_stride, scales_offset,
 
 
 def q4k_moe_router(x, w_router, bias, w_shared_gate, m, num_experts, hidden, top_k, scoring, normalize, scale,
-                   n_group, topk_group, ids, weights, logits=None, shared_gate=None, stream=None):
+                   n_group, topk_group, ids, weights, logits, shared_gate=None, stream=None):
     """Gate logits, top-k choice and routing weights on the device (w_router / w_shared_gate: bf16 bits as
     int16/uint16 tensors)."""
     _cuda(x, w_router, bias, w_shared_gate, ids, weights, logits, shared_gate)

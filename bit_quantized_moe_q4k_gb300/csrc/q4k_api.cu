@@ -627,7 +627,8 @@ int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_
             return fail(Q4K_ERR_SHAPE, "top_k %d cannot be chosen from %d groups of %d", top_k, topk_group, gsize);
     }
     if (m == 0) return Q4K_OK;
-    if (!d_x || !d_w_router || !d_ids || !d_weights) return fail(Q4K_ERR_NULL, "x, w_router, ids and weights are required");
+    if (!d_x || !d_w_router || !d_ids || !d_weights || !d_logits)
+        return fail(Q4K_ERR_NULL, "x, w_router, ids, weights and logits are required");
     if (d_w_shared_gate && !d_shared_gate) return fail(Q4K_ERR_NULL, "w_shared_gate given without shared_gate");
     if (!aligned16(d_x) || !aligned16(d_w_router) || (d_w_shared_gate && !aligned16(d_w_shared_gate)))
         return fail(Q4K_ERR_ALIGN, "x, w_router and w_shared_gate must be 16-byte aligned");

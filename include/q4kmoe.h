@@ -316,16 +316,16 @@ int q4k_moe_id_gemv_fmt(int fmt, const void* d_w, const void* d_w2, uint64_t w_b
  *     consecutive ids, a group scored by the sum of its max(1, top_k/topk_group) best
  *     s + bias; weight = s (normalize: divided by the chosen s' sum) * scale.
  *   Choice order: larger score first, equal scores by the lower id; ids [m, top_k] int32 in
- *   that order, weights [m, top_k] fp32. d_logits [m, num_experts] (optional) receives the
- *   logits. d_w_shared_gate (optional, bf16 [hidden]) adds the shared expert's gate logit
- *   d_shared_gate[t] = sum_h bf16(w_shared_gate[h]) * x[t, h].
+ *   that order, weights [m, top_k] fp32. d_logits [m, num_experts] fp32 (required) receives
+ *   the logits, which the choice then reads. d_w_shared_gate (optional, bf16 [hidden]) adds
+ *   the shared expert's gate logit d_shared_gate[t] = sum_h bf16(w_shared_gate[h]) * x[t, h].
  * Layouts: d_x [m, hidden] fp32; d_w_router [num_experts, hidden] bf16 bits (uint16),
  * both 16-byte aligned. Limits: hidden % 8 == 0, hidden <= 16384; num_experts <= 4096;
  * top_k <= min(16, num_experts); grouped: n_group <= 32 divides num_experts,
  * 1 <= topk_group <= n_group, max(1, top_k/topk_group) <= min(16, num_experts/n_group),
- * top_k <= topk_group * num_experts/n_group. One launch (thread-block clusters of 16 or 8
- * CTAs), a programmatic dependent of the previous kernel in the stream, no workspace;
- * the result is the same bits at every call.
+ * top_k <= topk_group * num_experts/n_group. Two launches: the gate matvec over all SMs,
+ * then the choice (one warp per token), each a programmatic dependent of the kernel before
+ * it in the stream; the result is the same bits at every call and for any m.
  */
 #define Q4K_ROUTE_SOFTMAX 0
 #define Q4K_ROUTE_SIGMOID_GROUPED 1

@@ -137,7 +137,7 @@ def test_fmt4_empty_batch():
 
 def router(**kw):
     a = dict(x=A16, w=A16, bias=None, wsg=None, m=3, E=128, H=2048, k=8, scoring=0, norm=1, scale=1.0, ng=1, tg=1,
-             ids=A16, wt=A16, logits=None, sg=None)
+             ids=A16, wt=A16, logits=A16, sg=None)
     a.update(kw)
     return q4k.load().q4k_moe_router(a["x"], a["w"], a["bias"], a["wsg"], a["m"], a["E"], a["H"], a["k"], a["scoring"],
                                      a["norm"], a["scale"], a["ng"], a["tg"], a["ids"], a["wt"], a["logits"], a["sg"],
@@ -150,6 +150,7 @@ def router(**kw):
     (dict(scoring=1, ng=3), 2), (dict(scoring=1, ng=64, E=128), 2), (dict(scoring=1, ng=8, tg=9), 2),
     (dict(scoring=1, ng=8, tg=0), 2), (dict(scoring=1, E=16, ng=8, tg=2, k=6), 2),
     (dict(x=None), 1), (dict(w=None), 1), (dict(ids=None), 1), (dict(wt=None), 1), (dict(wsg=A16), 1),
+    (dict(logits=None), 1),
     (dict(x=MISALIGNED), 7), (dict(w=MISALIGNED), 7), (dict(wsg=MISALIGNED, sg=A16), 7),
 ])
 def test_router_rejects(kw, status):

@@ -237,9 +237,10 @@ def test_router_feeds_the_layer():
     ids = torch.empty((m, k), dtype=torch.int32, device="cuda")
     wt = torch.empty((m, k), dtype=torch.float32, device="cuda")
     sg = torch.empty((m,), dtype=torch.float32, device="cuda")
+    lg = torch.empty((m, E), dtype=torch.float32, device="cuda")
     xd = dev(x)
     q4k.q4k_moe_router(xd, dev(wr.view(np.int16)), None, dev(wsg.view(np.int16)), m, E, H, k, q4k.ROUTE_SOFTMAX,
-                       True, 1.0, 1, 1, ids, wt, None, sg)
+                       True, 1.0, 1, 1, ids, wt, lg, sg)
     y = torch.empty((m, H), dtype=torch.float32, device="cuda")
     nbytes = q4k.q4k_moe_layer_workspace_size(m, k, E, H, I, SI)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
