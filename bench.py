@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from bit_quantized_moe_q4k_gb300 import inputs  # noqa: E402
-from bit_quantized_moe_q4k_gb300.workloads import HEADLINE, MIXTRAL_M_SWEEP, WORKLOADS, Workload  # noqa: E402
+from bit_quantized_moe_q4k_gb300.workloads import HEADLINE, MIXTRAL_M_SWEEP, PREFILL, WORKLOADS, Workload  # noqa: E402
 
 METRIC = "Q4_K MoE id-GEMV: achieved HBM GB/s (% of peak) and (token,expert) pairs/sec"
 # What the kernels compute in: weights Q4_K as stored; activations fp32 in HBM, staged on chip
@@ -502,12 +502,13 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
 
 # The other workloads of the layer, measured after the headline in the same run (one record each).
 PER_CONFIG = [("qwen3moe_h2048_i768_e128_t8_m16_zipf", 0), ("deepseekv3_h7168_i2048_e256_t8_m64", 0)] + \
-    [("mixtral_h4096_i14336_e8_t2", m) for m in MIXTRAL_M_SWEEP]
+    [("mixtral_h4096_i14336_e8_t2", m) for m in MIXTRAL_M_SWEEP] + list(PREFILL)
 
 
 def per_config_records(args, rank, world, local_rank, peak):
     import argparse
     import torch
+    tensor_peak = measured_tensor_peak()
     global CLOCK_SOAK_S
     out = []
     soak = CLOCK_SOAK_S
@@ -522,8 +523,11 @@ def per_config_records(args, rank, world, local_rank, peak):
             step_ms = r["total_ms"] / K
             gu_ms = float(np.mean(r["gu_ms"]))
             kbytes = r["layer_bytes"] if r["single"] else r["gu_bytes"]
+            flops = 2.0 * 3 * W.hidden * (W.pairs * W.inter + W.m * W.shared_inter)  # the layer's multiply-adds x 2
             out.append({
-                "workload": name if not m else f"{name}_m{m}", "m": W.m, "pairs": W.pairs,
+                "workload": name if not m else f"{name.removesuffix('_m1')}_m{m}", "m": W.m, "pairs": W.pairs,
+                "layer_tflops": flops / (step_ms * 1e-3) / 1e12,
+                "layer_tensor_frac": flops / (step_ms * 1e-3) / 1e12 / tensor_peak,
                 "ms_per_step": step_ms, "pairs_per_s": W.pairs * K * max(1, world) / (r["total_ms"] / 1e3),
                 "layer_bytes": r["layer_bytes"], "layer_hbm_gbs": r["layer_bytes"] / (step_ms * 1e-3) / 1e9,
                 "layer_hbm_frac": r["layer_bytes"] / (step_ms * 1e-3) / 1e9 / peak,
@@ -782,6 +786,16 @@ def format_records(args, local_rank, peak):
             del slabs
             torch.cuda.empty_cache()
     return out
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s (cuBLAS, sustained when measured; the fp16 MMA rate is the same)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops_sustained") or d["bf16_tflops"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return 1700.0
 
 
 def measured_peaks():

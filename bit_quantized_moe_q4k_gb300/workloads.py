@@ -57,6 +57,9 @@ WORKLOADS = {
 }
 
 MIXTRAL_M_SWEEP = (1, 4, 16, 64, 256)
+# Prefill-size batches of the same layers (the tensor-core grouped GEMM carries them).
+PREFILL = (("mixtral_h4096_i14336_e8_t2", 512), ("mixtral_h4096_i14336_e8_t2", 2048),
+           ("qwen3moe_h2048_i768_e128_t8_m1", 512))
 
 # The headline decode layer: the Qwen3-MoE-like layer at m=1.
 HEADLINE = "qwen3moe_h2048_i768_e128_t8_m1"

@@ -17,7 +17,7 @@ import pytest
 import oracle
 import bit_quantized_moe_q4k_gb300 as q4k
 from bit_quantized_moe_q4k_gb300 import inputs
-from bit_quantized_moe_q4k_gb300.workloads import MIXTRAL_M_SWEEP, WORKLOADS
+from bit_quantized_moe_q4k_gb300.workloads import MIXTRAL_M_SWEEP, PREFILL, WORKLOADS
 
 from helpers import err_flag, host, rows_close
 
@@ -114,4 +114,26 @@ def test_fullsize_mixtral_like_sweep(m):
     W = WORKLOADS["mixtral_h4096_i14336_e8_t2"].with_m(m)
     sample = _chunk_sample(W)
     assert len(sample) >= min(8, m)
+    _run(W, sample=sample)
+
+
+def _bucket_ends_sample(W, extra=8):
+    """Tokens of the first and the last pair of every expert's bucket, plus `extra` evenly
+    spaced tokens and the last token (prefill sizes: the oracle on every chunk would take
+    minutes)."""
+    ids = inputs.make_ids(W.seed, W.ids, W.m, W.top_k, W.num_experts)
+    toks = set(range(0, W.m, max(1, W.m // extra))) | {W.m - 1}
+    for e in range(W.num_experts):
+        pairs = np.flatnonzero(ids == e)
+        if len(pairs):
+            toks |= {int(pairs[0]) // W.top_k, int(pairs[-1]) // W.top_k}
+    return sorted(toks)
+
+
+@pytest.mark.parametrize("name,m", PREFILL, ids=[f"{n.split('_')[0]}-m{m}" for n, m in PREFILL])
+def test_fullsize_prefill(name, m):
+    W = WORKLOADS[name].with_m(m)
+    sample = _bucket_ends_sample(W)
+    if W.num_experts > 16:  # keep the oracle's share to a few tens of tokens
+        sample = sorted(set(sample[::max(1, len(sample) // 24)]) | {m - 1})
     _run(W, sample=sample)
