@@ -130,7 +130,8 @@ __device__ __forceinline__ void dot64(const uint4& q0, const uint4& q1, const ui
 // order i = b / S), each (c, sl) first folds its terms left to right, T_0 + T_1 + T_2 + ...,
 // then the partial sums of the 4*S lanes (c, sl) are added by xor shuffles over c (1, 2) and
 // then over sl (4, 8, ...). So every kernel gets the same bits for a row (fold_term and the
-// lane shuffles of item_compute; the row streams of q4k_decode.cu).
+// lane shuffles of item_compute, used by the id-GEMV, the single-launch layer and the other
+// 4-bit formats' kernel).
 __device__ __forceinline__ float block_term(const float4& mt, float sa, float ma, float sb, float mb, int Sa, int Sb) {
     const float ua = __fmaf_rn(sa, (float)Sa, -__fmul_rn(ma, mt.y));
     const float ub = __fmaf_rn(sb, (float)Sb, -__fmul_rn(mb, mt.w));

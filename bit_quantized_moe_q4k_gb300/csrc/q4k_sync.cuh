@@ -1,5 +1,6 @@
 // q4k_sync.cuh -- hand-off between the CTAs of one launch without zero-initialised state,
-// shared by the single-launch layer kernels (q4k_layer.cu, q4k_decode.cu).
+// used by the single-launch layer kernel (q4k_layer.cu) and the tensor-core kernel's bounded
+// waits (q4k_tc.cu).
 //
 // A launch's tag is next_tag(generation word). A CTA that finishes a piece of work stores the
 // tag into that piece's flag word (release); a CTA that needs the piece waits until the word
