@@ -65,6 +65,10 @@ def parse():
     ap.add_argument("--per-config-steps", type=int, default=10)
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the router, routed-step and weight-format records after the headline")
+    ap.add_argument("--next-rows-only", action="store_true",
+                    help="run only the router, routed-step and weight-format records (a profiling aid)")
+    ap.add_argument("--mem-cap-gb", type=float, default=24.0,
+                    help="device memory the next-row records may fill with rotated weights")
     return ap.parse_args()
 
 
@@ -322,7 +326,7 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
         for i in range(max(1, min(args.warmup, n_layers))):
             step(layers[i % n_layers], i)
     stream.synchronize()
-    assert int(flag.item()) == 0, "device error flag raised"
+    assert int(flag.item()) == 0, f"device error flag raised: {int(flag.item())}"
 
     K, Wm = args.steps, args.warmup
 
@@ -394,7 +398,7 @@ def run_ours(args, W: Workload, rank: int, world: int, local_rank: int):
         k1.record(stream)
         k1.synchronize()
         gu_ms = [k0.elapsed_time(k1) / K]
-    assert int(flag.item()) == 0, "device error flag raised"
+    assert int(flag.item()) == 0, f"device error flag raised: {int(flag.item())}"
 
     # algorithmic bytes per step (touched experts differ per layer)
     per = [layer_bytes(W, layers[(Wm + i) % n_layers]["ids_np"]) for i in range(K)]
@@ -586,10 +590,11 @@ def time_graph(step, K, Wm, stream, local_rank, soak_s=0.3):
     return e0.elapsed_time(e1) / K, clk
 
 
-def rotation(bytes_per_step, cap_bytes, bytes_per_copy):
-    """Copies to rotate through so the bytes touched between two uses of one exceed 3x L2."""
+def rotation(bytes_per_step, cap, bytes_per_copy):
+    """Copies to rotate through so the bytes touched between two uses of one exceed 3x L2
+    (at most `cap` bytes of copies)."""
     n = max(4, -(-3 * L2_BYTES // max(1, bytes_per_step)))
-    return int(max(2, min(n, cap_bytes // max(1, bytes_per_copy))))
+    return int(max(2, min(n, cap // max(1, bytes_per_copy))))
 
 
 ROUTER_CONFIGS = [
@@ -601,6 +606,10 @@ ROUTER_CONFIGS = [
 ]
 
 
+def cap_bytes(args, default_gb):
+    return int(min(default_gb, args.mem_cap_gb) * (1 << 30))
+
+
 def router_records(args, local_rank, peak):
     import torch
     import bit_quantized_moe_q4k_gb300 as q4k
@@ -609,7 +618,7 @@ def router_records(args, local_rank, peak):
     out = []
     for name, E, H, k, scoring, ng, tg, scale, m in ROUTER_CONFIGS:
         wbytes = E * H * 2
-        n = rotation(wbytes, 4 << 30, wbytes)
+        n = rotation(wbytes, cap_bytes(args, 4), wbytes)
         gen = torch.Generator(device=dev)
         gen.manual_seed(E * 131 + H)
         wr = (torch.randn(n, E, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16).view(torch.int16)
@@ -636,11 +645,11 @@ def router_records(args, local_rank, peak):
     return out
 
 
-def routed_step_record(args, W: Workload, local_rank, peak):
+def routed_step_record(args, W: Workload, local_rank, peak, fused=True):
     """One decode MoE block per step, chained as in a model: the router (softmax top-k, plus
     the shared expert's gate logit) on h_post, the layer with the router's ids / weights /
     gate, the next layer's input RMSNorm on the layer's output, which is the next step's
-    h_post."""
+    h_post. fused: one q4k_moe_layer_forward_routed call per step; else the three calls."""
     import torch
     import bit_quantized_moe_q4k_gb300 as q4k
     dev = torch.device("cuda", local_rank)
@@ -650,7 +659,7 @@ def routed_step_record(args, W: Workload, local_rank, peak):
     lb = layer_bytes(W, ids0)
     per_layer = lb["layer"] + E * H * 2 + H * 2 * 2
     slab_total = E * (2 * slab_bytes(I, H) + slab_bytes(H, I)) + (3 * slab_bytes(Is, H) if Is else 0)
-    n = rotation(per_layer, 40 << 30, slab_total)
+    n = rotation(per_layer, cap_bytes(args, 40), slab_total)
     gen = torch.Generator(device=dev)
 
     def slab(seed, n_exp, rows, k):
@@ -681,13 +690,20 @@ def routed_step_record(args, W: Workload, local_rank, peak):
     lgt = torch.empty(m, E, dtype=torch.float32, device=dev)
     y = torch.empty(m, H, dtype=torch.float32, device=dev)
     xy = [torch.randn(m, H, generator=gen, device=dev), torch.empty(m, H, dtype=torch.float32, device=dev)]
-    ws_bytes = q4k.q4k_moe_layer_workspace_size(m, T, E, H, I, Is)
+    ws_bytes = (q4k.q4k_moe_layer_routed_workspace_size if fused else q4k.q4k_moe_layer_workspace_size)(
+        m, T, E, H, I, Is)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step(i):
         L = layers[i % n]
         x, xn = xy[i % 2], xy[(i + 1) % 2]
+        if fused:
+            q4k.q4k_moe_layer_forward_routed(L["wg"], L["wu"], L["wd"], E, L["sg"], L["su"], L["sd"], Is,
+                                             W.shared_mode, x, L["hm"], L["wr"], None, L["wsg"] if Is else None,
+                                             q4k.ROUTE_SOFTMAX, True, 1.0, 1, 1, m, T, H, I, y, L["wn"], 1e-6, xn,
+                                             None, None, ws, ws_bytes, flag, stream)
+            return
         q4k.q4k_moe_router(x, L["wr"], None, L["wsg"] if Is else None, m, E, H, T, q4k.ROUTE_SOFTMAX, True, 1.0, 1, 1,
                            ids, wt, lgt, sgl if Is else None, stream)
         q4k.q4k_moe_layer_forward(L["wg"], L["wu"], L["wd"], E, L["sg"], L["su"], L["sd"], Is, W.shared_mode, x,
@@ -696,13 +712,16 @@ def routed_step_record(args, W: Workload, local_rank, peak):
 
     K = max(10, args.per_config_steps * 4)
     ms, clk = time_graph(step, K, 3, stream, local_rank)
-    assert int(flag.item()) == 0, "device error flag raised"
+    assert int(flag.item()) == 0, f"device error flag raised: {int(flag.item())}"
     b = per_layer + m * H * 4 * 2
-    rec = {"workload": f"{W.name} + router + rms_norm", "ms_per_step": ms,
+    rec = {"workload": f"{W.name} + router + rms_norm" + (" (one call)" if fused else " (three calls)"),
+           "ms_per_step": ms,
            "launches_per_step": 3 + q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is),
            "bytes_per_step": b, "hbm_gbs": b / (ms * 1e-3) / 1e9, "hbm_frac": b / (ms * 1e-3) / 1e9 / peak,
-           "chain": "router -> layer -> rms_norm on one stream, each a programmatic dependent of the one before; "
-                    "the norm's output is the next step's h_post", "clocks": clk,
+           "chain": ("q4k_moe_layer_forward_routed: the router's two kernels, the layer, the norm kernel, "
+                     "in one call" if fused else
+                     "router -> layer -> rms_norm on one stream, each a programmatic dependent of the one before") +
+                    "; the norm's output is the next step's h_post", "clocks": clk,
            "l2": f"rotating {n} layers"}
     del layers
     torch.cuda.empty_cache()
@@ -737,7 +756,7 @@ def format_records(args, local_rank, peak):
             ids_np = [inputs.ids_uniform_distinct(60000 + j, m, T, E) for j in range(8)]
             U = np.mean([len(set(a.tolist())) for a in ids_np])
             per_step = U * 2 * mat + m * H * 4 + m * T * I * 4
-            n = rotation(int(per_step), 24 << 30, 2 * E * stride)
+            n = rotation(int(per_step), cap_bytes(args, 24), 2 * E * stride)
             gen = torch.Generator(device=dev)
             gen.manual_seed(70000 + m)
             slabs = [torch.randint(0, 256, (2, E * stride), dtype=torch.uint8, device=dev, generator=gen)
@@ -776,7 +795,7 @@ def format_records(args, local_rank, peak):
 
             K = max(10, args.per_config_steps * 4)
             ms, clk = time_graph(step, K, 3, stream, local_rank)
-            assert int(flag.item()) == 0, "device error flag raised"
+            assert int(flag.item()) == 0, f"device error flag raised: {int(flag.item())}"
             out.append({"workload": f"qwen3moe_gate_up_{fmt}_m{m}", "format": fmt,
                         "bytes_per_weight": mat / (I * H), "kernel": "idgemv_kernel<fused>" if fmt == "q4k" else
                         "fmt4_kernel<fused>", "bound": "hbm", "bytes_per_launch": per_step,
@@ -880,6 +899,13 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    if args.next_rows_only:
+        peak, _ = measured_peaks()
+        if rank == 0:
+            print(json.dumps({"next_rows": {"router": router_records(args, local_rank, peak),
+                                            "routed_step": routed_step_record(args, W, local_rank, peak),
+                                            "formats": format_records(args, local_rank, peak)}}), flush=True)
+        return
     r = run_ours(args, W, rank, world, local_rank)
     K = args.steps
     step_ms = r["total_ms"] / K

@@ -32,7 +32,9 @@ from ._lib import (  # noqa: F401
     q4k_moe_layer_gate_up,
     q4k_moe_layer_half_workspace_size,
     q4k_moe_layer_launch_count,
+    q4k_moe_layer_forward_routed,
     q4k_moe_layer_path,
+    q4k_moe_layer_routed_workspace_size,
     q4k_moe_layer_host_staging_size,
     q4k_moe_layer_workspace_size,
     q4k_moe_router,

@@ -52,6 +52,10 @@ SIGNATURES = {
     "q4k_moe_layer_path": (_I, [_I, _I, _I, _I, _I, _I]),
     "q4k_moe_id_gemv_fmt": (_I, [_I, _P, _P, _U64, _U64, _U64, _U64, _I, _I, _P, _I64, _I64, _P, _I, _I, _I, _I, _P,
                                  _P, _P]),
+    "q4k_moe_layer_routed_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "q4k_moe_layer_forward_routed": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I,
+                                          ctypes.c_float, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_float, _P, _P,
+                                          _P, _P, _SZ, _P, _P]),
     "q4k_moe_router": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P, _P, _P]),
     "q4k_rms_norm": (_I, [_P, _P, _I, _I, ctypes.c_float, _P, _P]),
     "q4k_quantize_rows": (_I, [_P, _I64, _I, _P, _P]),
@@ -188,6 +192,25 @@ def q4k_moe_id_gemv_fmt(fmt, w, w2, w_byte_offset, expert_stride, scales_offset,
     _check(load().q4k_moe_id_gemv_fmt(fmt, _ptr(w), _ptr(w2), w_byte_offset, expert_stride, scales_offset,
                                       biases_offset, group_size, num_experts, _ptr(a), outer, inner, _ptr(ids), m,
                                       top_k, n, k, _ptr(out), _ptr(err_flag), _stream(stream)))
+
+
+def q4k_moe_layer_routed_workspace_size(m, top_k, num_experts, hidden, inter, shared_inter) -> int:
+    return int(load().q4k_moe_layer_routed_workspace_size(m, top_k, num_experts, hidden, inter, shared_inter))
+
+
+def q4k_moe_layer_forward_routed(w_gate, w_up, w_down, num_experts, ws_gate, ws_up, ws_down, shared_inter,
+                                 shared_mode, h_post, h_mid, w_router, bias, w_shared_gate, scoring, normalize, scale,
+                                 n_group, topk_group, m, top_k, hidden, inter, y, w_norm, eps, normed, ids_out,
+                                 weights_out, workspace, ws_bytes, err_flag=None, stream=None):
+    """Router -> layer -> (optional) RMSNorm from the layer input; one launch for a decode layer."""
+    _cuda(w_gate, w_up, w_down, ws_gate, ws_up, ws_down, h_post, h_mid, w_router, bias, w_shared_gate, y, w_norm,
+          normed, ids_out, weights_out, workspace, err_flag)
+    _check(load().q4k_moe_layer_forward_routed(
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), num_experts, _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), shared_inter,
+        shared_mode, _ptr(h_post), _ptr(h_mid), _ptr(w_router), _ptr(bias), _ptr(w_shared_gate), scoring,
+        1 if normalize else 0, float(scale), n_group, topk_group, m, top_k, hidden, inter, _ptr(y), _ptr(w_norm),
+        float(eps), _ptr(normed), _ptr(ids_out), _ptr(weights_out), _ptr(workspace), ws_bytes, _ptr(err_flag),
+        _stream(stream)))
 
 
 def q4k_moe_router(x, w_router, bias, w_shared_gate, m, num_experts, hidden, top_k, scoring, normalize, scale,

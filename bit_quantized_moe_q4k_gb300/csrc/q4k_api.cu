@@ -123,6 +123,46 @@ size_t ffn_scratch(int m, int top_k, int hidden, int inter) {
 // rather than in every CTA that takes one of their items.
 constexpr int kPrestageMinK = 4096;
 
+// Shapes and rule of a router call (q4k_moe_router, q4k_moe_layer_forward_routed).
+int check_router_args(int m, int num_experts, int hidden, int top_k, int scoring, int n_group, int topk_group) {
+    if (m < 0) return fail(Q4K_ERR_SHAPE, "m must be >= 0 (got %d)", m);
+    if (num_experts < 1) return fail(Q4K_ERR_SHAPE, "num_experts must be >= 1 (got %d)", num_experts);
+    if (num_experts > kMaxExperts) return fail(Q4K_ERR_LIMIT, "num_experts must be <= %d (got %d)", kMaxExperts, num_experts);
+    if (top_k < 1 || top_k > Q4K_MAX_TOP_K || top_k > num_experts)
+        return fail(Q4K_ERR_TOPK, "top_k must be in [1, min(16, num_experts)] (got %d)", top_k);
+    if (hidden < 8 || hidden % 8 != 0) return fail(Q4K_ERR_SHAPE, "hidden must be a positive multiple of 8 (got %d)", hidden);
+    if (hidden > router_max_hidden()) return fail(Q4K_ERR_LIMIT, "hidden must be <= %d (got %d)", router_max_hidden(), hidden);
+    if (scoring != Q4K_ROUTE_SOFTMAX && scoring != Q4K_ROUTE_SIGMOID_GROUPED)
+        return fail(Q4K_ERR_MODE, "scoring must be Q4K_ROUTE_SOFTMAX or Q4K_ROUTE_SIGMOID_GROUPED (got %d)", scoring);
+    if (scoring == Q4K_ROUTE_SIGMOID_GROUPED) {
+        if (n_group < 1 || n_group > 32 || num_experts % n_group != 0)
+            return fail(Q4K_ERR_SHAPE, "n_group must be in [1, 32] and divide num_experts (got %d)", n_group);
+        if (topk_group < 1 || topk_group > n_group)
+            return fail(Q4K_ERR_SHAPE, "topk_group must be in [1, n_group] (got %d)", topk_group);
+        const int gsize = num_experts / n_group, per = std::max(1, top_k / topk_group);
+        if (per > std::min(16, gsize) || top_k > topk_group * gsize)
+            return fail(Q4K_ERR_SHAPE, "top_k %d cannot be chosen from %d groups of %d", top_k, topk_group, gsize);
+    }
+    return Q4K_OK;
+}
+
+// Scratch of the routed layer behind the layer's own workspace: the router's logits, the
+// shared gate logits, ids and weights.
+struct RouteScratch {
+    size_t logits, sg, ids, weights, total;
+};
+
+RouteScratch route_scratch(size_t base, int m, int top_k, int num_experts, int hidden) {
+    RouteScratch r{};
+    size_t off = base;
+    r.logits = off;  off += align_up((size_t)m * num_experts * sizeof(float));
+    r.sg = off;      off += align_up((size_t)m * sizeof(float));
+    r.ids = off;     off += align_up((size_t)m * top_k * sizeof(int32_t));
+    r.weights = off; off += align_up((size_t)m * top_k * sizeof(float));
+    r.total = off;
+    return r;
+}
+
 struct LayerScratch {
     size_t sync, act, act_shared, eout, shared_out, tc_gu, tc_dn, counters, pre, pre_shared, total;
     size_t n_sync_words;  // 0: these shapes always take the two-launch layer
@@ -475,6 +515,61 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
                     act_shared, sout, d_err_flag, stream, ws + ls.tc_dn, &cb, ws + ls.pre, ws + ls.pre_shared);
 }
 
+size_t q4k_moe_layer_routed_workspace_size(int m, int top_k, int num_experts, int hidden, int inter,
+                                           int shared_inter) {
+    const size_t base = q4k_moe_layer_workspace_size(m, top_k, num_experts, hidden, inter, shared_inter);
+    if (base == 0 || num_experts < 1 || num_experts > kMaxExperts || hidden < 1) return 0;
+    return route_scratch(align_up(base), m, top_k, num_experts, hidden).total;
+}
+
+int q4k_moe_layer_forward_routed(const void* d_w_gate, const void* d_w_up, const void* d_w_down, int num_experts,
+                                 const void* d_ws_gate, const void* d_ws_up, const void* d_ws_down, int shared_inter,
+                                 int shared_mode, const float* d_h_post, const float* d_h_mid,
+                                 const uint16_t* d_w_router, const float* d_bias, const uint16_t* d_w_shared_gate,
+                                 int scoring, int normalize, float scale, int n_group, int topk_group, int m,
+                                 int top_k, int hidden, int inter, float* d_y, const uint16_t* d_w_norm, float eps,
+                                 float* d_normed, int32_t* d_ids_out, float* d_weights_out, void* d_workspace,
+                                 size_t ws_bytes, int* d_err_flag, cudaStream_t stream) {
+    int st = check_router_args(m, num_experts, hidden, top_k, scoring, n_group, topk_group);
+    if (st) return st;
+    st = check_gemv_shape(num_experts, m, top_k, inter, hidden);
+    if (!st) st = check_gemv_shape(num_experts, m, top_k, hidden, inter);
+    if (st) return st;
+    if (shared_mode < 0 || shared_mode > 2) return fail(Q4K_ERR_MODE, "shared_mode must be 0, 1 or 2 (got %d)", shared_mode);
+    if (shared_mode == Q4K_SHARED_NONE) shared_inter = 0;
+    else if (shared_inter < 1) return fail(Q4K_ERR_SHAPE, "shared_inter must be >= 1 with a shared expert");
+    if (!d_w_router) return fail(Q4K_ERR_NULL, "w_router is NULL");
+    if (shared_mode == Q4K_SHARED_SIGMOID && !d_w_shared_gate)
+        return fail(Q4K_ERR_NULL, "a sigmoid-gated shared expert needs w_shared_gate");
+    if (d_w_norm && !d_normed) return fail(Q4K_ERR_NULL, "w_norm given without normed");
+    if ((d_ids_out == nullptr) != (d_weights_out == nullptr))
+        return fail(Q4K_ERR_NULL, "ids_out and weights_out are given together or not at all");
+    if (!aligned16(d_w_router) || (d_w_shared_gate && !aligned16(d_w_shared_gate)) ||
+        (d_normed && !aligned16(d_normed)) || (d_w_norm && (reinterpret_cast<uintptr_t>(d_w_norm) & 7u)))
+        return fail(Q4K_ERR_ALIGN, "w_router, w_shared_gate and normed must be 16-byte aligned, w_norm 8-byte");
+    const size_t base = align_up(q4k_moe_layer_workspace_size(m, top_k, num_experts, hidden, inter, shared_inter));
+    const RouteScratch rs = route_scratch(base, m, top_k, num_experts, hidden);
+    st = check_workspace(d_workspace, ws_bytes, rs.total);
+    if (st) return st;
+    if (m == 0) return Q4K_OK;
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    int32_t* ids = d_ids_out ? d_ids_out : reinterpret_cast<int32_t*>(ws + rs.ids);
+    float* wts = d_weights_out ? d_weights_out : reinterpret_cast<float*>(ws + rs.weights);
+    float* logits = reinterpret_cast<float*>(ws + rs.logits);
+    float* sg = reinterpret_cast<float*>(ws + rs.sg);
+    const uint16_t* wsg = shared_mode == Q4K_SHARED_NONE ? nullptr : d_w_shared_gate;
+    // the router's two launches, the layer, the norm: each a programmatic dependent of the one
+    // before where that is safe (measured faster than choosing in every CTA of the layer)
+    st = q4k_moe_router(d_h_post, d_w_router, d_bias, wsg, m, num_experts, hidden, top_k, scoring, normalize, scale,
+                        n_group, topk_group, ids, wts, logits, wsg ? sg : nullptr, stream);
+    if (st) return st;
+    st = q4k_moe_layer_forward(d_w_gate, d_w_up, d_w_down, num_experts, d_ws_gate, d_ws_up, d_ws_down, shared_inter,
+                               shared_mode, d_h_post, d_h_mid, ids, wts, wsg ? sg : nullptr, m, top_k, hidden, inter,
+                               d_y, d_workspace, base, d_err_flag, stream);
+    if (st || !d_w_norm) return st;
+    return q4k_rms_norm(d_y, d_w_norm, m, hidden, eps, d_normed, stream);
+}
+
 int q4k_moe_layer_gate_up(const void* d_w_gate, const void* d_w_up, int num_experts, const void* d_ws_gate,
                           const void* d_ws_up, int shared_inter, const float* d_h_post, const int32_t* d_ids, int m,
                           int top_k, int hidden, int inter, float* d_act, float* d_act_shared, void* d_workspace,
@@ -608,24 +703,8 @@ int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_
                    int m, int num_experts, int hidden, int top_k, int scoring, int normalize, float scale, int n_group,
                    int topk_group, int32_t* d_ids, float* d_weights, float* d_logits, float* d_shared_gate,
                    cudaStream_t stream) {
-    if (m < 0) return fail(Q4K_ERR_SHAPE, "m must be >= 0 (got %d)", m);
-    if (num_experts < 1) return fail(Q4K_ERR_SHAPE, "num_experts must be >= 1 (got %d)", num_experts);
-    if (num_experts > kMaxExperts) return fail(Q4K_ERR_LIMIT, "num_experts must be <= %d (got %d)", kMaxExperts, num_experts);
-    if (top_k < 1 || top_k > Q4K_MAX_TOP_K || top_k > num_experts)
-        return fail(Q4K_ERR_TOPK, "top_k must be in [1, min(16, num_experts)] (got %d)", top_k);
-    if (hidden < 8 || hidden % 8 != 0) return fail(Q4K_ERR_SHAPE, "hidden must be a positive multiple of 8 (got %d)", hidden);
-    if (hidden > router_max_hidden()) return fail(Q4K_ERR_LIMIT, "hidden must be <= %d (got %d)", router_max_hidden(), hidden);
-    if (scoring != Q4K_ROUTE_SOFTMAX && scoring != Q4K_ROUTE_SIGMOID_GROUPED)
-        return fail(Q4K_ERR_MODE, "scoring must be Q4K_ROUTE_SOFTMAX or Q4K_ROUTE_SIGMOID_GROUPED (got %d)", scoring);
-    if (scoring == Q4K_ROUTE_SIGMOID_GROUPED) {
-        if (n_group < 1 || n_group > 32 || num_experts % n_group != 0)
-            return fail(Q4K_ERR_SHAPE, "n_group must be in [1, 32] and divide num_experts (got %d)", n_group);
-        if (topk_group < 1 || topk_group > n_group)
-            return fail(Q4K_ERR_SHAPE, "topk_group must be in [1, n_group] (got %d)", topk_group);
-        const int gsize = num_experts / n_group, per = std::max(1, top_k / topk_group);
-        if (per > std::min(16, gsize) || top_k > topk_group * gsize)
-            return fail(Q4K_ERR_SHAPE, "top_k %d cannot be chosen from %d groups of %d", top_k, topk_group, gsize);
-    }
+    const int rst = check_router_args(m, num_experts, hidden, top_k, scoring, n_group, topk_group);
+    if (rst != Q4K_OK) return rst;
     if (m == 0) return Q4K_OK;
     if (!d_x || !d_w_router || !d_ids || !d_weights || !d_logits)
         return fail(Q4K_ERR_NULL, "x, w_router, ids, weights and logits are required");

@@ -25,7 +25,8 @@
 // its header with that launch's tag; a launch whose set is not stamped so (the first on this
 // memory, a call of another shape) polls the down items' flags instead. Every wait is bounded
 // in time; one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid
-// resident at once: the grid is capped at what the SMs hold, and CTAs never wait on a CTA that
+// resident at once: the grid is capped at what the SMs hold, it is an ordinary launch (it
+// starts on SMs the previous kernel has left), and CTAs never wait on a CTA that
 // is itself waiting (gate|up items never wait; down items wait only on gate|up items; the
 // combine waits only on down items).
 #include <algorithm>
@@ -138,7 +139,9 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     __shared__ __align__(8) uint64_t s_abar; // a gate|up item's weight tiles' copy
     __shared__ int s_never;                  // (bounded waits take an abort word; never set)
 
-    // ids, activations and the generation word may come from earlier kernels of the stream
+    // (launched as an ordinary launch, so earlier kernels of the stream are complete and the
+    // wait returns at once); the next kernel may launch early: it can only take space left
+    // over once every CTA of this grid has started, which the trigger implies
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -576,11 +579,9 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // an ordinary launch: it starts on idle SMs. As a programmatic dependent its CTAs could be
+    // placed beside the previous kernel's last CTAs on SMs configured for a smaller shared-memory
+    // share, which then hold fewer of them than the grid needs resident at once.
     return cudaLaunchKernelEx(&cfg, kern, P);
 }
 

@@ -26,6 +26,7 @@
 #include <algorithm>
 
 #include "q4k_internal.cuh"
+#include "q4k_route.cuh"
 
 namespace q4k {
 namespace {
@@ -54,71 +55,6 @@ struct RouterParams {
 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-
-// Ranking key: NaN below every number.
-__device__ __forceinline__ float rank_key(float v) { return v != v ? -INFINITY : v; }
-
-// (v, i) beats (u, j): a candidate (i >= 0) beats none; a larger key wins; equal keys go to
-// the lower index.
-__device__ __forceinline__ bool beats(float v, int i, float u, int j) {
-    if (i < 0) return false;
-    if (j < 0) return true;
-    return v > u || (v == u && i < j);
-}
-
-// Warp-wide best of the lanes' (v, i); every lane gets the winner.
-__device__ __forceinline__ void warp_best(float& v, int& i) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float u = __shfl_xor_sync(0xffffffffu, v, off);
-        const int j = __shfl_xor_sync(0xffffffffu, i, off);
-        if (beats(u, j, v, i)) { v = u; i = j; }
-    }
-}
-
-// Choose the top_k (<= N) best entries of key[0..E) (warp-wide; with gsize > 0 only experts
-// whose group g = e / gsize has bit g of `kept` set). Each lane keeps its own best N
-// candidates, sorted, in registers (one pass over e = lane, lane + 32, ...; visiting them in
-// increasing e keeps equal keys in id order); then top_k rounds of a warp-wide best over the
-// lanes' heads, the winner's lane dropping its head. Lane j < top_k gets the j-th choice.
-template <int N>
-__device__ __forceinline__ void choose(const float* key, int E, int top_k, uint32_t kept, int gsize, int lane,
-                                       int& my_i) {
-    float lv[N];
-    int li[N];
-#pragma unroll
-    for (int j = 0; j < N; ++j) { lv[j] = -INFINITY; li[j] = -1; }
-    for (int e = lane; e < E; e += 32) {
-        if (gsize > 0 && !((kept >> (e / gsize)) & 1u)) continue;
-        float v = rank_key(key[e]);
-        int i = e;
-#pragma unroll
-        for (int j = 0; j < N; ++j) {  // insertion into the sorted list
-            if (j < top_k && beats(v, i, lv[j], li[j])) {
-                const float tv = lv[j];
-                const int ti = li[j];
-                lv[j] = v; li[j] = i;
-                v = tv; i = ti;
-            }
-        }
-    }
-    my_i = -1;
-    for (int j = 0; j < top_k; ++j) {
-        float bv = lv[0];
-        int bi = li[0];
-        warp_best(bv, bi);
-        if (lane == j) my_i = bi;
-        if (bi >= 0 && li[0] == bi) {  // this lane's head was chosen: drop it
-#pragma unroll
-            for (int q = 0; q + 1 < N; ++q) { lv[q] = lv[q + 1]; li[q] = li[q + 1]; }
-            lv[N - 1] = -INFINITY;
-            li[N - 1] = -1;
-        }
-    }
-}
 
 // Gate logits of rows [blockIdx.x*rb, +rb) of the (expert rows, then the shared-expert gate
 // row) for the token tile blockIdx.y.
@@ -173,8 +109,8 @@ __global__ void __launch_bounds__(kRThreads, 1) router_logits_kernel(const Route
                 const uint32_t u[4] = {wv[b][c].x, wv[b][c].y, wv[b][c].z, wv[b][c].w};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    s = __fmaf_rn(bf16_lo(u[h]), xr[t][c][2 * h], s);
-                    s = __fmaf_rn(bf16_hi(u[h]), xr[t][c][2 * h + 1], s);
+                    s = __fmaf_rn(route_bf16_lo(u[h]), xr[t][c][2 * h], s);
+                    s = __fmaf_rn(route_bf16_hi(u[h]), xr[t][c][2 * h + 1], s);
                 }
             }
 #pragma unroll
@@ -194,32 +130,6 @@ __global__ void __launch_bounds__(kRThreads, 1) router_logits_kernel(const Route
             else P.shared_gate[t0 + t] = s;
         }
     }
-}
-
-// Sum, largest first, of the `per` (<= N) largest values of v[0..n) (rank keys).
-template <int N>
-__device__ __forceinline__ float top_sum(const float* v, int n, int per) {
-    float top[N];
-#pragma unroll
-    for (int j = 0; j < N; ++j) top[j] = -INFINITY;
-    for (int e0 = 0; e0 < n; e0 += 8) {
-        float x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = e0 + u < n ? rank_key(v[e0 + u]) : -INFINITY;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            float y = x[u];
-#pragma unroll
-            for (int j = 0; j < N; ++j) {  // insertion into a descending list
-                if (j < per && y > top[j]) { const float o = top[j]; top[j] = y; y = o; }
-            }
-        }
-    }
-    float s = top[0];
-#pragma unroll
-    for (int j = 1; j < N; ++j)
-        if (j < per) s = __fadd_rn(s, top[j]);
-    return rank_key(s);
 }
 
 // The choice for the tile's tokens (token blockIdx.x * tile + warp) from their logits.
@@ -260,56 +170,10 @@ __global__ void __launch_bounds__(kRThreads) router_topk_kernel(const RouterPara
     const int t = t_base + warp;
     float* lg = s_lg + (size_t)warp * E;
     float* cs = s_cs + (size_t)warp * E;
-    int my_i = -1;
-    float my_w = 0.0f;
-    if (!grouped) {
-        if (K <= 8) choose<8>(lg, E, K, 0u, 0, lane, my_i);
-        else choose<16>(lg, E, K, 0u, 0, lane, my_i);
-        const float lmax = __shfl_sync(0xffffffffu, my_i >= 0 ? lg[my_i] : 0.0f, 0);
-        const float p = (lane < K && my_i >= 0) ? expf(lg[my_i] - lmax) : 0.0f;
-        float z = 0.0f;
-        if (P.normalize) {  // over the chosen, in choice order
-            for (int j = 0; j < K; ++j) z = __fadd_rn(z, __shfl_sync(0xffffffffu, p, j));
-        } else {  // over all experts: each lane's in index order, then xor shuffles
-            for (int e = lane; e < E; e += 32) z = __fadd_rn(z, expf(lg[e] - lmax));
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) z = __fadd_rn(z, __shfl_xor_sync(0xffffffffu, z, off));
-        }
-        my_w = p / z;
-    } else {
-        const int gsize = E / P.n_group;
-        for (int e = lane; e < E; e += 32) cs[e] = __fadd_rn(1.0f / (1.0f + expf(-lg[e])), s_bias[e]);
-        __syncwarp();
-        uint32_t kept = 0xffffffffu;
-        if (P.n_group > 1) {
-            // lane g scores group g; the topk_group best groups are kept
-            float gs = -INFINITY;
-            int gi = -1;
-            if (lane < P.n_group) {
-                gs = P.per <= 4 ? top_sum<4>(cs + lane * gsize, gsize, P.per) : top_sum<16>(cs + lane * gsize, gsize, P.per);
-                gi = lane;
-            }
-            kept = 0u;
-            for (int j = 0; j < P.topk_group; ++j) {
-                float bv = gs;
-                int bi = gi;
-                warp_best(bv, bi);
-                if (bi >= 0) kept |= 1u << bi;
-                if (lane == bi) gi = -1;
-            }
-        }
-        const int gs_arg = P.n_group > 1 ? gsize : 0;
-        if (K <= 8) choose<8>(cs, E, K, kept, gs_arg, lane, my_i);
-        else choose<16>(cs, E, K, kept, gs_arg, lane, my_i);
-        const float s = (lane < K && my_i >= 0) ? 1.0f / (1.0f + expf(-lg[my_i])) : 0.0f;
-        if (P.normalize) {
-            float z = 0.0f;
-            for (int j = 0; j < K; ++j) z = __fadd_rn(z, __shfl_sync(0xffffffffu, s, j));
-            my_w = __fmul_rn(s / z, P.scale);
-        } else {
-            my_w = __fmul_rn(s, P.scale);
-        }
-    }
+    RouteRule R{E, K, P.scoring, P.normalize, P.n_group, P.topk_group, P.per, P.scale};
+    int my_i;
+    float my_w;
+    route_token(lg, cs, grouped ? s_bias : nullptr, R, lane, my_i, my_w);
     if (lane < K) {
         P.ids[(int64_t)t * K + lane] = my_i;
         P.weights[(int64_t)t * K + lane] = my_w;
@@ -366,6 +230,21 @@ cudaError_t dispatch_nch(const RouterParams& P, cudaStream_t stream) {
 
 int num_sms();
 
+// The router's first launch alone: logits [m, E] (+ the shared gate logits with w_sg).
+cudaError_t launch_router_logits(const float* x, const uint16_t* w, const uint16_t* w_sg, int m, int E, int H,
+                                 float* logits, float* shared_gate, cudaStream_t stream) {
+    if (m == 0) return cudaSuccess;
+    RouterParams P{};
+    P.x = x; P.w = w; P.w_sg = w_sg;
+    P.logits = logits; P.shared_gate = shared_gate;
+    P.m = m; P.E = E; P.H = H;
+    const int nch = (H / 8 + kRThreads - 1) / kRThreads;
+    return nch <= 1 ? dispatch_nch<1>(P, stream)
+         : nch <= 2 ? dispatch_nch<2>(P, stream)
+         : nch <= 4 ? dispatch_nch<4>(P, stream)
+                    : dispatch_nch<8>(P, stream);
+}
+
 cudaError_t launch_router(const float* x, const uint16_t* w, const float* bias, const uint16_t* w_sg, int m, int E,
                           int H, int top_k, int scoring, int normalize, float scale, int n_group, int topk_group,
                           int32_t* ids, float* weights, float* logits, float* shared_gate, cudaStream_t stream) {
@@ -378,11 +257,7 @@ cudaError_t launch_router(const float* x, const uint16_t* w, const float* bias, 
     P.n_group = scoring == Q4K_ROUTE_SOFTMAX ? 1 : n_group;
     P.topk_group = scoring == Q4K_ROUTE_SOFTMAX ? 1 : topk_group;
     P.per = std::max(1, top_k / std::max(1, P.topk_group));
-    const int nch = (H / 8 + kRThreads - 1) / kRThreads;
-    cudaError_t e = nch <= 1 ? dispatch_nch<1>(P, stream)
-                  : nch <= 2 ? dispatch_nch<2>(P, stream)
-                  : nch <= 4 ? dispatch_nch<4>(P, stream)
-                             : dispatch_nch<8>(P, stream);
+    cudaError_t e = launch_router_logits(x, w, w_sg, m, E, H, logits, shared_gate, stream);
     if (e != cudaSuccess) return e;
     // the choice: tokens per CTA (one warp each) as many as their tables fit
     RouterParams Q = P;

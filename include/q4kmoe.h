@@ -336,6 +336,36 @@ int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_
                    cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * q4k_moe_layer_forward_routed -- the decode MoE block from the layer input: the router
+ * (q4k_moe_router's logits, choice and weights, with d_w_shared_gate giving the shared
+ * expert's gate logit), the layer (q4k_moe_layer_forward) and, when d_w_norm is given, the
+ * next layer's input norm (q4k_rms_norm's formula) into d_normed.
+ *   Arguments: those of q4k_moe_layer_forward without ids, weights and shared_gate, those of
+ *   q4k_moe_router (w_router bf16 [num_experts, hidden], bias, scoring rule); d_w_norm bf16
+ *   [hidden] (8-byte aligned) and eps, or NULL for no norm; d_normed [m, hidden] (may alias
+ *   d_y); d_ids_out / d_weights_out [m, top_k] (both or neither) receive the choice.
+ *   A sigmoid-gated shared expert needs d_w_shared_gate.
+ * Launches: q4k_moe_router's two, q4k_moe_layer_forward's, then q4k_rms_norm's, each a
+ * programmatic dependent of the kernel before it where that is safe (the persistent layer is an
+ * ordinary launch); the ids, weights, y and normed are those of the three calls made one after
+ * the other, bit for bit.
+ * Workspace: q4k_moe_layer_routed_workspace_size(...) bytes, any contents (as the layer's).
+ */
+size_t q4k_moe_layer_routed_workspace_size(int m, int top_k, int num_experts, int hidden, int inter,
+                                           int shared_inter);
+int q4k_moe_layer_forward_routed(const void* d_w_gate, const void* d_w_up, const void* d_w_down,
+                                 int num_experts, const void* d_ws_gate, const void* d_ws_up,
+                                 const void* d_ws_down, int shared_inter, int shared_mode,
+                                 const float* d_h_post, const float* d_h_mid,
+                                 const uint16_t* d_w_router, const float* d_bias,
+                                 const uint16_t* d_w_shared_gate, int scoring, int normalize,
+                                 float scale, int n_group, int topk_group, int m, int top_k,
+                                 int hidden, int inter, float* d_y, const uint16_t* d_w_norm,
+                                 float eps, float* d_normed, int32_t* d_ids_out,
+                                 float* d_weights_out, void* d_workspace, size_t ws_bytes,
+                                 int* d_err_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * q4k_rms_norm -- RMSNorm chained after the combine [P2: ChainToNormed, rms_norm_sum_sq +
  * rms_norm_apply_bf16]: the next layer's normed input from this layer's output.
  *   out[t, h] = x[t, h] / sqrt(sum_h x[t, h]^2 / hidden + eps) * bf16(w[h])   (fp32)
