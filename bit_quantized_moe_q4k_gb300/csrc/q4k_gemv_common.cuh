@@ -386,12 +386,21 @@ __device__ __forceinline__ void item_issue(const GroupDev& G, int e, int tile, i
     }
 }
 
+// A result word of the single-launch layer: the float's bits under the launch's 32-bit tag, so
+// a reader knows from the word alone whether this launch has written it. One relaxed 64-bit
+// store (single-copy atomic).
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag32) {
+    const uint64_t w = ((uint64_t)tag32 << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
 // The item's dot products against the nt staged tokens (pairs s_pairs[0..nt)), the reduction
 // over the lanes of a row, and the write of out[pair, row] (kFused: silu(g) * u; kPair: both
-// rows).
+// rows). out64 != null: the results go as tagged words to out64[pair, row] instead.
 template <int KIND, int TB, bool SMEM = false>
 __device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND, SMEM>& L, const int* s_pairs, int nt,
-                                             const uint8_t* xs, const float2* meta, int lane) {
+                                             const uint8_t* xs, const float2* meta, int lane,
+                                             uint64_t* out64 = nullptr, uint32_t tag32 = 0) {
     constexpr bool TWO = KIND != kOne;
     const int S = L.S, c = L.c;
     const int nsb = G.k / 32;
@@ -448,7 +457,15 @@ __device__ __forceinline__ void item_compute(const GroupDev& G, ItemLane<KIND, S
     if ((lane & (4 * S - 1)) == 0) {
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
-            if (t < nt) {
+            if (t < nt && out64) {
+                uint64_t* o = out64 + (int64_t)s_pairs[t] * G.n;
+                if (KIND == kFused) {
+                    if (L.row_ok) st_tagged(o + L.row, silu(acc[t]) * acc2[t], tag32);
+                } else {
+                    if (L.row_ok) st_tagged(o + L.row, acc[t], tag32);
+                    if (KIND == kPair && L.row2_ok) st_tagged(o + L.row2, acc2[t], tag32);
+                }
+            } else if (t < nt) {
                 float* o = G.out + (int64_t)s_pairs[t] * G.n;
                 if (KIND == kFused) {
                     if (L.row_ok) o[L.row] = silu(acc[t]) * acc2[t];

@@ -117,15 +117,14 @@ size_t tc_image_bytes(int n_pairs, int k, int tc_min);
 bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel's shared memory plan fits
 
 // The small-batch layer in one persistent launch (q4k_layer.cu): gu / dn the groups of the
-// gate|up and down halves (routed, then shared), cb the combine (counters unused). sync:
-// sync_words words of the layer workspace (layer_sync_words), any contents. Returns
+// gate|up and down halves (routed, then shared; their float outputs unused: the results go to
+// tagged words in the sync area), cb the combine (counters unused). sync: sync_words words of
+// the layer workspace (layer_sync_words), any contents. Returns
 // cudaErrorNotSupported, before launching anything, where it does not apply (more than 32
 // pairs in a group, a sync area too small, rows too long for its shared memory).
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
 // Both halves' work items fit one round of the CTAs the device's SMs hold at once.
 bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter);
-// Words at the start of the sync area that hold the generation word and the counter sets.
-size_t layer_sync_head_words(int hidden);
 
 cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
                                     uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream);

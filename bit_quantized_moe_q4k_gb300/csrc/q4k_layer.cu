@@ -12,23 +12,28 @@
 // and can only start once the first launch's CTAs leave the SMs. Here every CTA buckets the
 // pairs of both halves once; moves its gate|up item's activation row and weight tiles, and
 // then its down tile, into shared memory with bulk copies (outside the SM's load queue);
-// starts its down item as soon as the gate|up items of that bucket chunk have landed; and the
-// last down item of a row tile combines that tile.
+// starts its down item as soon as the activations of that bucket chunk are written; and the
+// CTA of each row tile's last down item combines that tile.
 //
-// Hand-off between CTAs without zero-initialised state: every item, when its rows are
-// written, stores a 64-bit tag into its own flag word; a consumer waits until the flags it
-// needs hold the tag. The tag of a launch is next_tag(generation word); the generation word is
-// advanced to the tag at the end of the launch (by CTA 0, once every CTA has recorded that it
-// read the old value), so stale flags of earlier launches never match and nothing needs
-// clearing -- also not on the first call on fresh memory. The combine's per-tile counters come
-// in two sets used by alternate launches: a launch zeroes the set the next one uses and stamps
-// its header with that launch's tag; a launch whose set is not stamped so (the first on this
-// memory, a call of another shape) polls the down items' flags instead. Every wait is bounded
-// in time; one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid
+// Hand-off between CTAs without zero-initialised state. A launch's tag is next_tag(generation
+// word); the generation word is advanced to the tag at the end of the launch (by CTA 0, once
+// every CTA has recorded that it read the old value), and a launch count with it. Every result
+// a CTA hands to another -- an activation of a gate|up row, a row of an expert's down output --
+// is stored as one 64-bit word holding the float under a 32-bit tag made of the launch count
+// (bit 31 set, so never zero; no two of the last 2^31 launches share it). CTA 0
+// also leaves a stamp for the next launch: its tag bound to this launch's shapes. A launch that
+// finds the stamp meant for it (the previous launch on this memory had the same shapes, so it
+// wrote every word this one reads, under another tag) takes a word whose tag matches as
+// written: readers poll the words themselves, one round trip after the last write. Otherwise
+// (the first call on this memory, a call of another shape or after a call with ids out of
+// range, a cleared workspace) the words
+// could hold anything, and every item also publishes a 64-bit tagged flag (a release store)
+// that its readers wait for (acquire) before they read its words. Every wait is bounded in
+// time; one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid
 // resident at once: the grid is capped at what the SMs hold, it is an ordinary launch (it
-// starts on SMs the previous kernel has left), and CTAs never wait on a CTA that
-// is itself waiting (gate|up items never wait; down items wait only on gate|up items; the
-// combine waits only on down items).
+// starts on SMs the previous kernel has left), and CTAs never wait on a CTA that is itself
+// waiting (gate|up items never wait; down items wait only on gate|up items; a combine waits
+// only on down items).
 #include <algorithm>
 #include <cstdlib>
 #include <type_traits>
@@ -42,6 +47,26 @@ namespace q4k {
 constexpr int kLayerMaxCtas = 1024;   // start-tag words in the sync area
 constexpr int kLayerMaxPairs = 32;    // per group: one warp buckets a group
 constexpr uint32_t kLayerMaxPolls = 1u << 26;
+constexpr int kCbRows = 256;          // h_mid elements of a combine tile kept in shared memory
+constexpr int kSyncHead = 4;          // generation word, stamp for the next launch, launch count, pad
+
+// A 4-byte asynchronous copy global -> shared (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_v2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// The 32-bit tag of every result word of a launch: its launch count, bit 31 set (never zero);
+// the words of the last 2^31 launches never carry the tag of this one.
+__device__ __forceinline__ uint32_t word_tag(uint64_t count) { return (uint32_t)count | 0x80000000u; }
+__device__ __forceinline__ bool word_ready(uint64_t w, uint32_t tag32) { return (uint32_t)(w >> 32) == tag32; }
+__device__ __forceinline__ float word_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
 
 struct LayerParams {
     GroupDev a[kMaxGroups];  // gate|up + SwiGLU: routed experts, shared expert
@@ -56,30 +81,21 @@ struct LayerParams {
     int atile_off, atile_bytes;  // ... and a gate|up item's weight tiles, gate then up (use_atile)
     int use_atile;
     CombineSpec cb;           // y, h_mid, weights, shared_gate, shared_mode (no counters)
-    uint64_t* gen;            // generation word
-    uint64_t* cnt_hdr;        // [2] tag for which counter set s is zero (set by the previous launch)
-    unsigned* cnt;            // [2][nt_max] per combine tile: down items done
-    int nt_max;
+    uint64_t* gen;            // [kSyncHead]: generation word, the stamp the previous launch left
+                              // for this one, the launch count
+    uint64_t shape;           // this launch's shapes, hashed
     uint64_t* cta_tag;        // [kLayerMaxCtas] tag each CTA read
-    uint64_t* flag_a;         // [cap_a] one per gate|up item
-    uint64_t* flag_b;         // [cap_b] one per down item
+    uint64_t* flag_a;         // [cap_a] one per gate|up item (flag mode)
+    uint64_t* flag_b;         // [cap_b] one per down item (flag mode)
     int cap_a, cap_b;
+    uint64_t* act64[kMaxGroups];  // gate|up outputs (the down inputs) as tagged words, [pairs, n]
+    uint64_t* out64[kMaxGroups];  // down outputs as tagged words, [pairs, hidden]
     int* err_flag;
     uint64_t wait_ns;         // limit of every wait
 };
 
-// A counter set's header: the tag of the launch it was prepared for, bound to the sets' size
-// (which moves with hidden), so a call of another shape never takes words laid out for
-// another as its zeroed counters.
-__device__ __forceinline__ uint64_t set_stamp(uint64_t tag, int nt_max) {
-    return tag ^ ((uint64_t)(unsigned)nt_max * 0x9E3779B97F4A7C15ull);
-}
-
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
+// The stamp for the launch with the given tag and shapes.
+__device__ __forceinline__ uint64_t launch_stamp(uint64_t tag, uint64_t shape) { return mix64(tag ^ shape); }
 
 // Block-wide: wait until flags[index(j)] == tag for all j < n. Each thread owns j = tid,
 // tid + kThreads, ...; it re-reads only those it has not yet seen set (up to 8 loads per
@@ -112,11 +128,156 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
     }
 }
 
-// Publish an item: its rows were written by this block's threads (the caller synchronised
-// the block); one thread stores the tag with release order at GPU scope, which makes those
-// rows visible first. It is a thread of the last warp: warp 0 locates the next item.
+// Publish an item in flag mode: its words were stored by this block's threads (the caller
+// synchronised the block); one thread stores the tag with release order at GPU scope, which
+// makes those words visible first. It is a thread of the last warp: warp 0 locates the next item.
 __device__ __forceinline__ void publish(uint64_t* flag, uint64_t tag) {
     if (threadIdx.x == kThreads - 32) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(tag) : "memory");
+}
+
+// Stage the activation rows of an item's nt pairs (k values each) from tagged words: a64 holds
+// pair p's row at (p / top_k) * outer + (p % top_k) * inner words. A thread reads four words per
+// float4 of the row and re-reads those not yet written by this launch until all are, then they
+// are quantized as stage_row does. False when a word was still missing after limit_ns (the
+// rows are staged all the same, from what was read). All threads of the block take part.
+__device__ __forceinline__ bool stage_rows_tagged(const uint64_t* a64, int64_t outer, int64_t inner, int top_k,
+                                                  const int* s_pairs, int nt, int k, uint32_t tag32,
+                                                  uint64_t limit_ns, uint8_t* xs, float2* meta) {
+    constexpr int U = 2;  // float4s per thread and pass
+    const int64_t tok_bytes = (int64_t)(k / 64) * kPairBytes;
+    const int nf = k / 4;
+    bool ok = true;
+    const uint64_t t0 = sm100::global_timer_ns();
+    for (int t = 0; t < nt; ++t) {
+        const int p = s_pairs[t];
+        const uint64_t* row = a64 + (int64_t)(p / top_k) * outer + (int64_t)(p % top_k) * inner;
+        for (int f0 = 0; f0 < nf; f0 += kThreads * U) {
+            uint64_t w[U][4];
+            unsigned pending = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int f = f0 + u * kThreads + threadIdx.x;
+                if (f < nf) {
+                    ld_relaxed_v2(row + 4 * f, w[u][0], w[u][1]);
+                    ld_relaxed_v2(row + 4 * f + 2, w[u][2], w[u][3]);
+                    pending |= 1u << u;
+                } else {
+                    w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0;
+                }
+            }
+            for (uint32_t round = 0; pending; ++round) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (((pending >> u) & 1u) && word_ready(w[u][0], tag32) && word_ready(w[u][1], tag32) &&
+                        word_ready(w[u][2], tag32) && word_ready(w[u][3], tag32))
+                        pending &= ~(1u << u);
+                if (!pending) break;
+                if (round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > limit_ns) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if ((pending >> u) & 1u) {
+                        const int f = f0 + u * kThreads + threadIdx.x;
+                        ld_relaxed_v2(row + 4 * f, w[u][0], w[u][1]);
+                        ld_relaxed_v2(row + 4 * f + 2, w[u][2], w[u][3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int f = f0 + u * kThreads + threadIdx.x;  // groups of 8 threads are all in or all out
+                if (f0 + u * kThreads >= nf) break;
+                const float4 v = make_float4(word_value(w[u][0]), word_value(w[u][1]), word_value(w[u][2]),
+                                             word_value(w[u][3]));
+                stage_quad(v, f, f < nf, xs + t * tok_bytes, meta + t * (k / 32));
+            }
+        }
+    }
+    return __syncthreads_and(ok);
+}
+
+// The inputs of a row tile's combine that do not come from this launch (h_mid of the tile's
+// rows for every token, routing weights, ids, shared-expert gate logits), copied into shared
+// memory while the tile's last down item runs, so the combine's only global loads are the
+// expert rows.
+struct CombineStage {
+    float h[kCbRows];       // h_mid[t][r0 + i] at t*span + i, when m*span <= kCbRows
+    float w[kLayerMaxPairs];
+    int id[kLayerMaxPairs];
+    float g[kLayerMaxPairs];  // shared_gate[t]
+};
+
+// Issue the copies of tile [r0, r0 + span) (all threads). The caller waits with
+// cp_async_wait_all and a block barrier before reading.
+__device__ __forceinline__ void combine_stage_issue(const CombineSpec& cb, const int32_t* ids, int n_pairs, int T,
+                                                    int H, bool shared, int r0, int span, CombineStage& S) {
+    const int m = n_pairs / T;
+    if (m * span <= kCbRows)
+        for (int idx = threadIdx.x; idx < m * span; idx += kThreads)
+            cp_async4(&S.h[idx], cb.h_mid + (int64_t)(idx / span) * H + r0 + idx % span);
+    for (int p = threadIdx.x; p < n_pairs; p += kThreads) {
+        cp_async4(&S.w[p], cb.weights + p);
+        if (ids) cp_async4(&S.id[p], ids + p);
+        else S.id[p] = 0;
+    }
+    if (shared)
+        for (int t = threadIdx.x; t < m; t += kThreads) cp_async4(&S.g[t], cb.shared_gate + t);
+}
+
+// The combine of rows [r0, r1) of every token from the tagged expert rows (out0: the routed
+// pairs' rows, out1: the shared expert's, or null) and the staged inputs:
+//   y = h_mid + sum_s w[t*T+s] * out0[t*T+s] + g_t * out1[t]   (slots in order; pairs whose id
+// is out of range contribute nothing and their rows are not read) -- the same sums in the same
+// order as combine_span. A thread re-reads the words not yet written by this launch until all
+// are. False when one was still missing after limit_ns (y is written all the same).
+__device__ __forceinline__ bool combine_tagged(const CombineSpec& cb, const uint64_t* out0, const uint64_t* out1,
+                                               int num_experts, int n_pairs, int T, int H, int r0, int r1,
+                                               const CombineStage& S, uint32_t tag32, uint64_t limit_ns) {
+    const int m = n_pairs / T;
+    const int span = r1 - r0;
+    const bool staged_h = m * span <= kCbRows;
+    bool ok = true;
+    const uint64_t t0 = sm100::global_timer_ns();
+    for (int idx = threadIdx.x; idx < m * span; idx += kThreads) {
+        const int t = idx / span, r = r0 + idx % span;
+        const int64_t o = (int64_t)t * H + r;
+        uint64_t v[Q4K_MAX_TOP_K];
+        uint64_t sh = 0;
+        unsigned need = 0;
+#pragma unroll
+        for (int s = 0; s < Q4K_MAX_TOP_K; ++s) {
+            v[s] = 0;
+            if (s < T && id_valid(S.id[t * T + s], num_experts)) need |= 1u << s;
+        }
+        if (out1) need |= 1u << Q4K_MAX_TOP_K;
+        for (uint32_t round = 0;; ++round) {
+#pragma unroll
+            for (int s = 0; s < Q4K_MAX_TOP_K; ++s)
+                if ((need >> s) & 1u) v[s] = ld_relaxed_u64(out0 + (int64_t)(t * T + s) * H + r);
+            if ((need >> Q4K_MAX_TOP_K) & 1u) sh = ld_relaxed_u64(out1 + o);
+#pragma unroll
+            for (int s = 0; s < Q4K_MAX_TOP_K; ++s)
+                if (((need >> s) & 1u) && word_ready(v[s], tag32)) need &= ~(1u << s);
+            if (((need >> Q4K_MAX_TOP_K) & 1u) && word_ready(sh, tag32)) need &= ~(1u << Q4K_MAX_TOP_K);
+            if (!need) break;
+            if (round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+        float acc = staged_h ? S.h[idx] : cb.h_mid[o];
+#pragma unroll
+        for (int s = 0; s < Q4K_MAX_TOP_K; ++s)
+            if (s < T && id_valid(S.id[t * T + s], num_experts)) acc = fmaf(S.w[t * T + s], word_value(v[s]), acc);
+        if (out1) {
+            const float g = cb.shared_mode == Q4K_SHARED_SIGMOID ? 1.0f / (1.0f + expf(-S.g[t])) : 1.0f;
+            acc = fmaf(g, word_value(sh), acc);
+        }
+        cb.y[o] = acc;
+    }
+    return ok;
 }
 
 // TB: tokens per item; KB: kind of the down items (kOne, or kPair when one-row items would
@@ -133,11 +294,13 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     __shared__ int s_chunk_b[2 * kLayerMaxPairs]; // first down item of every (group, bucket, chunk)
     __shared__ int s_n_chunks;
     __shared__ uint64_t s_tag;
-    __shared__ int s_set, s_cnt_ok, s_per_tile, s_last;  // counter set, it is valid, items per tile
+    __shared__ uint32_t s_tag32;                 // the tag of this launch's result words
+    __shared__ int s_fast_mode;                  // the stamp was meant for this launch: tags suffice
     __shared__ __align__(8) uint64_t s_bar;  // the down tile's copy into shared memory
     __shared__ __align__(8) uint64_t s_xbar; // a gate|up item's activation rows' copy
     __shared__ __align__(8) uint64_t s_abar; // a gate|up item's weight tiles' copy
     __shared__ int s_never;                  // (bounded waits take an abort word; never set)
+    __shared__ CombineStage s_cbs;           // the inputs of this CTA's combine
 
     // (launched as an ordinary launch, so earlier kernels of the stream are complete and the
     // wait returns at once); the next kernel may launch early: it can only take space left
@@ -145,10 +308,10 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // the generation word's load overlaps the bucketing (its value is used after it)
+    // the generation word's, the stamp's and the launch count's loads overlap the bucketing
     const uint64_t gen = threadIdx.x == 0 ? ld_relaxed_u64(P.gen) : 0;
-    const uint64_t hdr0 = threadIdx.x == 0 ? ld_relaxed_u64(P.cnt_hdr) : 0;
-    const uint64_t hdr1 = threadIdx.x == 0 ? ld_relaxed_u64(P.cnt_hdr + 1) : 0;
+    const uint64_t stamp = threadIdx.x == 0 ? ld_relaxed_u64(P.gen + 1) : 0;
+    const uint64_t count = threadIdx.x == 0 ? ld_relaxed_u64(P.gen + 2) : 0;
     {   // bucketing: warp w takes half w >> 1 (gate|up, down), group w & 1
         const int half = warp >> 1, gi = warp & 1;
         if (gi < P.n_groups) {
@@ -172,20 +335,15 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             sm100::fence_mbar_init();
             const uint64_t tag = next_tag(gen);
             s_tag = tag;
-            // the previous launch zeroed this launch's counter set and stamped it with this tag
-            // (else: the first call on this memory, or a call of another shape) -> poll instead
-            s_set = (int)(tag & 1ull);
-            s_cnt_ok = ((tag & 1ull) ? hdr1 : hdr0) == set_stamp(tag, P.nt_max) && P.b[0].tiles <= P.nt_max;
+            s_tag32 = word_tag(count + 1);
+            s_fast_mode = stamp == launch_stamp(tag, P.shape);
             st_relaxed_u64(P.cta_tag + blockIdx.x, tag);  // this CTA has read the generation
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {  // down items per combine tile: every chunk has one on each tile
-        int per_tile = 0;
-        for (int gi = 0; gi < P.n_groups; ++gi) per_tile += (s_items[1][gi + 1] - s_items[1][gi]) / P.b[gi].tiles;
-        s_per_tile = per_tile;  // read after the barriers of the items below
-    }
     const uint64_t tag = s_tag;
+    const uint32_t tag32 = s_tag32;
+    const bool fast = s_fast_mode;
     const int na = s_items[0][P.n_groups], nb = s_items[1][P.n_groups];
     // the caps bound any bucketing (chunks <= pairs); checked all the same
     const bool fits = na <= P.cap_a && nb <= P.cap_b;
@@ -228,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     int staged = -1;  // (half, group, rank, chunk) of the staged activation rows
     // ---- gate|up + SwiGLU items: activation rows and (use_atile) the weight tiles of both slabs
     // arrive by bulk copy, which keeps them out of the SM's load queue
-    auto gate_up_item = [&](auto from_smem, int item, const GroupDev& G, int e, int tile, int nt, int key) -> bool {
+    auto gate_up_item = [&](auto from_smem, int item, int gi, const GroupDev& G, int e, int tile, int nt,
+                            int key) -> bool {
         constexpr bool SM = decltype(from_smem)::value;
         ItemLane<kFused, SM> IL;
         if constexpr (!SM) item_issue<kFused>(G, e, tile, lane, warp, IL);
@@ -252,9 +411,11 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             item_issue<kFused, true>(G, e, tile, lane, warp, IL, atile, atile + P.atile_bytes);
         }
         __syncthreads();
-        item_compute<kFused, TB>(G, IL, s_pairs, nt, xs, meta, lane);
-        __syncthreads();
-        publish(P.flag_a + item, tag);
+        item_compute<kFused, TB>(G, IL, s_pairs, nt, xs, meta, lane, P.act64[gi], tag32);
+        if (!fast) {
+            __syncthreads();
+            publish(P.flag_a + item, tag);
+        }
         return true;
     };
     for (int item = a0; ok && item < a1; ++item) {
@@ -285,40 +446,64 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
                 sm100::bulk_g2s(atile + P.atile_bytes, G.w2 + src, bytes, &s_abar);
             }
         }
-        ok = P.use_atile ? gate_up_item(std::true_type{}, item, G, e, tile, nt, key)
-                         : gate_up_item(std::false_type{}, item, G, e, tile, nt, key);
+        ok = P.use_atile ? gate_up_item(std::true_type{}, item, gi, G, e, tile, nt, key)
+                         : gate_up_item(std::false_type{}, item, gi, G, e, tile, nt, key);
     }
 
-    // ---- down items: each waits for the gate|up items of its chunk (all their row tiles)
-    // (the first from its shared-memory copy when there is one)
+    // ---- down items: each reads the activations of its chunk (all their row tiles) as they are
+    // written (flag mode: after the gate|up items' flags); the first from its shared-memory copy
+    // when there is one. The CTA of a row tile's last down item (the tile's item in the last
+    // chunk: items nb - tiles .. nb - 1) combines that tile.
     const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
     const int tr = item_tile_rows(P.b[0].lg_split, KB);
-    auto combine_tile = [&](int t) {
+    const int n_tiles = P.b[0].tiles;
+    const int first_last = nb - n_tiles;  // first of the items that end a tile
+    if (threadIdx.x == 0 && !fast) {  // down items of tile 0 of every chunk (a combine's wait list)
+        int nc = 0;
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const FastGroup& F = s_fast[1][gi];
+            for (int r = 0; r < F.U; ++r) {
+                const int chunks = (F.start[r + 1] - F.start[r]) / P.b[gi].tiles;
+                for (int c = 0; c < chunks && nc < 2 * kLayerMaxPairs; ++c)
+                    s_chunk_b[nc++] = s_items[1][gi] + F.start[r] + c * P.b[gi].tiles;
+            }
+        }
+        s_n_chunks = nc;
+    }
+    auto combine_tile = [&](int t) -> bool {  // all threads; the inputs were staged
         const GroupDev& R = P.b[0];
-        combine_span(P.cb, R.out, R.ids, R.num_experts, R.n_pairs, R.top_k, R.n, shared ? P.b[1].out : nullptr, t * tr,
-                     min(R.n, (t + 1) * tr), threadIdx.x, kThreads);
+        if (!fast && !wait_tags(P.flag_b, s_n_chunks, tag, P.wait_ns, [t](int j) { return s_chunk_b[j] + t; }))
+            return false;
+        const bool done = combine_tagged(P.cb, P.out64[0], shared ? P.out64[1] : nullptr, R.num_experts, R.n_pairs,
+                                         R.top_k, R.n, t * tr, min(R.n, (t + 1) * tr), s_cbs, tag32, P.wait_ns);
+        return __syncthreads_and(done);
     };
     auto down_item = [&](auto& IL, int item, const GroupDev& G, int gi, int r, int nt, int chunk, int tile) -> bool {
         const int key = ((gi * 32 + r) * 32 + chunk) * 2 + 1;
+        const bool ends_tile = item >= first_last;
+        if (ends_tile) {
+            const GroupDev& R = P.b[0];
+            combine_stage_issue(P.cb, R.ids, R.n_pairs, R.top_k, R.n, shared, tile * tr,
+                                min(R.n, (tile + 1) * tr) - tile * tr, s_cbs);
+        }
         if (key != staged) {
-            const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
-            if (!wait_tags(P.flag_a, P.a[gi].tiles, tag, P.wait_ns, [first](int j) { return first + j; })) return false;
-            stage_rows<true>(G, s_pairs, nt, xs, meta);
+            if (!fast) {
+                const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
+                if (!wait_tags(P.flag_a, P.a[gi].tiles, tag, P.wait_ns, [first](int j) { return first + j; }))
+                    return false;
+            }
+            if (!stage_rows_tagged(P.act64[gi], G.outer, G.inner, G.top_k, s_pairs, nt, G.k, tag32, P.wait_ns, xs, meta))
+                return false;
             staged = key;
         }
         __syncthreads();
-        item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane);
+        item_compute<KB, TB>(G, IL, s_pairs, nt, xs, meta, lane, P.out64[gi], tag32);
         __syncthreads();
-        if (s_cnt_ok) {  // the last down item of the tile combines it
-            // the counter's release makes this item's rows visible (no flag: only the combine
-            // without counters reads the down flags); its acquire, passed on to the block by the
-            // barrier, orders the reads of the other items' rows (from L2) after their releases
-            if (threadIdx.x == kThreads - 32)
-                s_last = atom_add_acq_rel(P.cnt + s_set * P.nt_max + tile, 1u) + 1u == (unsigned)s_per_tile;
+        if (!fast) publish(P.flag_b + item, tag);
+        if (ends_tile) {
+            cp_async_wait_all();
             __syncthreads();
-            if (s_last) combine_tile(tile);
-        } else {
-            publish(P.flag_b + item, tag);
+            return combine_tile(tile);
         }
         return true;
     };
@@ -343,33 +528,24 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
             ok = down_item(IL, item, G, gi, r, nt, chunk, tile);
         }
     }
+    // no down item at all (every id out of range, no shared expert): y = h_mid, tiles split
+    // over the CTAs
+    if (ok && nb == 0) {
+        const GroupDev& R = P.b[0];
+        for (int t = (int)(cta * n_tiles / grid); ok && t < (int)((cta + 1) * n_tiles / grid); ++t) {
+            __syncthreads();
+            combine_stage_issue(P.cb, R.ids, R.n_pairs, R.top_k, R.n, shared, t * tr, min(R.n, (t + 1) * tr) - t * tr,
+                                s_cbs);
+            cp_async_wait_all();
+            __syncthreads();
+            ok = combine_tile(t);
+        }
+    }
     // a copy still in flight must land before the CTA leaves (after an abort)
+    cp_async_wait_all();
     if (slot_issued && !slot_waited) sm100::mbar_wait(&s_bar, 0, &s_never);
     if (cps & 1u) sm100::mbar_wait(&s_xbar, (cps >> 2) & 1u, &s_never);
     if (cps & 2u) sm100::mbar_wait(&s_abar, (cps >> 3) & 1u, &s_never);
-
-    // ---- combine (without valid counters): row tiles of the routed down group, each by a
-    // designated CTA after its down items' flags
-    if (threadIdx.x == 0 && !s_cnt_ok) {  // down items of tile 0 of every chunk (the combine's wait list)
-        int nc = 0;
-        for (int gi = 0; gi < P.n_groups; ++gi) {
-            const FastGroup& F = s_fast[1][gi];
-            for (int r = 0; r < F.U; ++r) {
-                const int chunks = (F.start[r + 1] - F.start[r]) / P.b[gi].tiles;
-                for (int c = 0; c < chunks && nc < 2 * kLayerMaxPairs; ++c)
-                    s_chunk_b[nc++] = s_items[1][gi] + F.start[r] + c * P.b[gi].tiles;
-            }
-        }
-        s_n_chunks = nc;
-    }
-    __syncthreads();
-    const int n_tiles = P.b[0].tiles;
-    const int t0 = (int)(cta * n_tiles / grid), t1 = (int)((cta + 1) * n_tiles / grid);
-    for (int t = t0; ok && !s_cnt_ok && t < t1; ++t) {
-        ok = wait_tags(P.flag_b, s_n_chunks, tag, P.wait_ns, [t](int j) { return s_chunk_b[j] + t; });
-        if (!ok) break;
-        combine_tile(t);
-    }
 
     if (threadIdx.x == 0) {
         if (!fits) raise_flag(P.err_flag, Q4K_ERR_LIMIT);
@@ -379,19 +555,19 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
                 for (int gi = 0; gi < P.n_groups; ++gi)
                     if (s_bad[half][gi]) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
     }
-    // ---- advance the generation once every CTA has read it, and prepare the next launch's
-    // counter set (the one this launch does not use): zero it, then stamp it with its tag
+    // ---- advance the generation and the launch count once every CTA has read them, and leave
+    // the next launch its stamp (this launch's shapes under the next tag). A launch that saw an
+    // id out of range wrote no words for that pair, so it leaves none: the next launch of the
+    // same shapes could read those words.
     if (blockIdx.x == 0) {
         const bool all = wait_tags(P.cta_tag, (int)gridDim.x, tag, P.wait_ns, [](int j) { return j; });
-        if (all) {
-            unsigned* next = P.cnt + (s_set ^ 1) * P.nt_max;
-            for (int i = threadIdx.x; i < P.nt_max; i += kThreads) next[i] = 0u;
-            __syncthreads();
-        }
         if (threadIdx.x == 0) {
+            bool clean = true;
+            for (int half = 0; half < 2; ++half)
+                for (int gi = 0; gi < P.n_groups; ++gi) clean = clean && !s_bad[half][gi];
             if (all) {
-                __threadfence();
-                st_relaxed_u64(P.cnt_hdr + (s_set ^ 1), set_stamp(next_tag(tag), P.nt_max));
+                st_relaxed_u64(P.gen + 1, clean ? launch_stamp(next_tag(tag), P.shape) : 0ull);
+                st_relaxed_u64(P.gen + 2, count + 1);
                 st_relaxed_u64(P.gen, tag);
             } else {
                 raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
@@ -433,16 +609,22 @@ LayerPlan plan_of(const GemvGroup* gu, const GemvGroup* dn, int n_groups, int kb
 
 bool g_layer_attr_set[4][64] = {};
 
-// Combine tiles of the smallest row tile (8 rows), whatever the down items' kind.
-int combine_tiles_max(int hidden) { return (hidden + 7) / 8; }
+// Result words of the single-launch layer: the gate|up outputs of the routed pairs and of the
+// shared expert's tokens, then the down outputs of both (64-bit tagged words, row-major).
+int64_t result_words(int m, int top_k, int hidden, int inter, int shared_inter) {
+    const int64_t pairs = (int64_t)m * top_k;
+    return pairs * inter + (int64_t)m * shared_inter + pairs * hidden + (shared_inter > 0 ? (int64_t)m * hidden : 0);
+}
 
-// Words before the start tags: the generation word, two counter-set headers and two sets of
-// u32 counters. They depend on hidden only, so they stay in place when m changes.
-size_t sync_head_words(int hidden) { return 3 + (size_t)(combine_tiles_max(hidden) + 1) / 2 * 2; }
+// splitmix64's output function on the host (Steele, Lea, Flood 2014), for the shape word.
+uint64_t host_mix64(uint64_t z) {
+    z += 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
 
 }  // namespace
-
-size_t layer_sync_head_words(int hidden) { return sync_head_words(hidden); }
 
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter) {
     if (m < 1 || (int64_t)m * top_k > kLayerMaxPairs || (shared_inter > 0 && m > kLayerMaxPairs)) return 0;
@@ -457,7 +639,9 @@ size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inte
     }
     const LayerPlan L = plan_of(gu, dn, ng, kOne);  // one-row down items: the larger cap
     if (L.cap_a + L.cap_b > (1 << 26)) return 0;
-    return sync_head_words(hidden) + kLayerMaxCtas + (size_t)L.cap_a + (size_t)L.cap_b;
+    // head, start tags, result words, then the flags
+    return kSyncHead + kLayerMaxCtas + (size_t)result_words(m, top_k, hidden, inter, shared_inter) +
+           (size_t)L.cap_a + (size_t)L.cap_b;
 }
 
 bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter) {
@@ -486,8 +670,11 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     const int64_t resident = (int64_t)num_sms() * 3;
     const int kb = plan_of(gu, dn, n_groups, kOne).cap_b > resident ? kPair : kOne;
     const LayerPlan L = plan_of(gu, dn, n_groups, kb);
-    const size_t head = sync_head_words(dn[0].n);
-    if (sync == nullptr || sync_words < head + kLayerMaxCtas + (size_t)(L.cap_a + L.cap_b)) return cudaErrorNotSupported;
+    const int m = gu[0].m, top_k = gu[0].top_k, hidden = dn[0].n, inter = gu[0].n;
+    const int shared_inter = n_groups > 1 ? gu[1].n : 0;
+    const int64_t n_results = result_words(m, top_k, hidden, inter, shared_inter);
+    if (sync == nullptr || sync_words < kSyncHead + kLayerMaxCtas + (size_t)(n_results + L.cap_a + L.cap_b))
+        return cudaErrorNotSupported;
     LayerParams P{};
     P.n_groups = n_groups;
     int kmax = 0, tb = 1;
@@ -535,16 +722,25 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     size_t smem = layout(2 * atile_bytes <= 48 * 1024);
     P.cb = cb;
     P.gen = sync;
-    P.cnt_hdr = sync + 1;
-    P.cnt = reinterpret_cast<unsigned*>(sync + 3);
-    P.nt_max = combine_tiles_max(dn[0].n);
-    P.cta_tag = sync + head;
-    P.flag_a = P.cta_tag + kLayerMaxCtas;
+    P.cta_tag = sync + kSyncHead;
+    uint64_t* words = P.cta_tag + kLayerMaxCtas;  // 16-byte aligned (even word offset)
+    P.act64[0] = words;
+    P.act64[1] = P.act64[0] + (int64_t)m * top_k * inter;
+    P.out64[0] = P.act64[1] + (int64_t)m * shared_inter;
+    P.out64[1] = n_groups > 1 ? P.out64[0] + (int64_t)m * top_k * hidden : nullptr;
+    P.flag_a = words + n_results;
     P.flag_b = P.flag_a + L.cap_a;
     P.cap_a = (int)L.cap_a;
     P.cap_b = (int)L.cap_b;
     P.err_flag = err_flag;
     P.wait_ns = wait_limit_ns();
+
+    // the shapes that decide which result words a launch writes and reads, and where
+    uint64_t shape = host_mix64(0x51A9E0F1A7E2ull);
+    for (const int64_t v : {(int64_t)m, (int64_t)top_k, (int64_t)hidden, (int64_t)inter, (int64_t)shared_inter,
+                            (int64_t)n_groups, (int64_t)kb, (int64_t)tb, (int64_t)(cb.shared_mode != Q4K_SHARED_NONE)})
+        shape = host_mix64(shape ^ (uint64_t)v);
+    P.shape = shape;
 
     void (*kern)(LayerParams) = tb == 1 ? (kb == kPair ? layer_kernel<1, kPair> : layer_kernel<1, kOne>)
                                         : (kb == kPair ? layer_kernel<kTB, kPair> : layer_kernel<kTB, kOne>);

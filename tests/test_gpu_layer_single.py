@@ -4,11 +4,12 @@ combine, routed and shared experts) against the two-launch layer and the oracle.
 The single launch sums every output row in the same order as the two-launch layer (the order
 all kernels share: each lane's block terms folded left to right, then the lane shuffles), so
 the two agree bit for bit; against the oracle the per-row acceptance of helpers.rows_close
-applies. Its CTAs hand work to each other through tagged flag words at the start of the
-workspace, so the tests also run it on a workspace full of garbage, on one workspace call
-after call (and replayed from a CUDA graph), with m changing between calls on one workspace,
-and with a wait limit so short that the waits give up (the error flag reports it, and the
-next call on a cleared workspace is right).
+applies. Its CTAs hand results to each other as words tagged with the launch; a call whose
+previous call on the workspace had the same shapes trusts the tags alone, any other call also
+waits for tagged flags. So the tests also run it on a workspace full of garbage, on one
+workspace call after call with the same shapes and with changing ones (and replayed from a
+CUDA graph), after a call with ids out of range, and with a wait limit so short that the
+waits give up (the error flag reports it, and the next call on a cleared workspace is right).
 """
 import numpy as np
 import pytest
@@ -210,9 +211,9 @@ def test_single_launch_m_changes_on_one_workspace(monkeypatch):
 
 
 def test_single_launch_hidden_changes_on_one_workspace(monkeypatch):
-    """Layers of different hidden sizes share one workspace: the sync area's layout moves with
-    hidden, so a call finds the previous call's counters and flags at other offsets (it falls
-    back to polling, then prepares its counters for the next call of its own shape)."""
+    """Layers of different hidden sizes share one workspace: the result words move with the
+    shapes, so a call whose previous call had other shapes finds no stamp meant for it (it waits
+    for the items' flags before reading their words, and leaves a stamp for the next call)."""
     seq = [Workload("h1", 1024, 512, 64, 8, 1, "uniform", 512, 1, 1701),
            Workload("h2", 2048, 512, 64, 8, 1, "uniform", 512, 2, 1702)]
     layers = [Layer(W, _inputs(W)) for W in seq]
@@ -249,3 +250,66 @@ def test_single_launch_wait_limit_runs_out(monkeypatch):
     layer.run(ws, f)
     assert int(host(f)[0]) == 0
     assert np.array_equal(host(layer.y), ref2)
+    # the same after a call that left its stamp: the next call trusts the words' tags, and its
+    # polls of them give up
+    monkeypatch.setenv("Q4K_WAIT_NS", "1")
+    layer.run(ws, f)
+    assert int(host(f)[0]) == Q4K_ERR_TIMEOUT
+    monkeypatch.delenv("Q4K_WAIT_NS")
+    ws.zero_()
+    f.zero_()
+    layer.y.zero_()
+    layer.run(ws, f)
+    assert int(host(f)[0]) == 0
+    assert np.array_equal(host(layer.y), ref2)
+
+
+def test_single_launch_same_shapes_trust_tags(monkeypatch):
+    """Layers of one shape (different ids, weights and inputs) on one workspace that starts full
+    of garbage: the first call waits for flags, every later one trusts the tags of the words the
+    previous call wrote over. A call with an id out of range writes no words for that pair, so
+    the call after it waits for flags again. Every call equals the two-launch layer bit for
+    bit, eagerly and replayed from a CUDA graph."""
+    W0 = WORKLOADS["qwen3moe_h2048_i768_e128_t8_m1"]
+    layers = []
+    for i in range(4):
+        W = Workload(f"same{i}", W0.hidden, W0.inter, W0.num_experts, W0.top_k, 1, "uniform", W0.shared_inter,
+                     W0.shared_mode, 1900 + i)
+        ids = None
+        if i == 2:  # slot 5 out of range
+            ids = inputs.make_ids(W.seed, W.ids, W.m, W.top_k, W.num_experts).reshape(-1).copy()
+            ids[5] = W.num_experts + 3
+        layers.append(Layer(W, _inputs(W, ids)))
+    refs = [_two_launch(L, monkeypatch) for L in layers]
+    assert [r[1] for r in refs] == [0, 0, Q4K_ERR_EXPERT_ID, 0]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(91)
+    ws = torch.randint(0, 256, (layers[0].ws_bytes(),), dtype=torch.uint8, device="cuda", generator=g)
+    for rep in range(3):
+        for L, (ref, flag) in zip(layers, refs):
+            f = err_flag()
+            L.y.zero_()
+            L.run(ws, f)
+            assert int(host(f)[0]) == flag
+            assert np.array_equal(host(L.y), ref), f"eager pass {rep}, {L.W.name}"
+    clean = [layers[i] for i in (0, 1, 3)]
+    f = err_flag()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for rep in range(2):
+                for L in clean:
+                    L.run(ws, f, stream)
+    stream.synchronize()
+    for rep in range(3):
+        for L in clean:
+            L.y.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        for L, i in zip(clean, (0, 1, 3)):
+            assert np.array_equal(host(L.y), refs[i][0]), f"graph replay {rep}, {L.W.name}"
+    assert int(host(f)[0]) == 0
