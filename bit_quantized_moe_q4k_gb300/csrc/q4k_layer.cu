@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
         }
         slot_issued = true;
     };
-    if (slot_item && (a0 == a1 || !P.slot_shares_raw)) issue_slot();
+    if (slot_item && a0 == a1) issue_slot();
     // the bulk copies of the gate|up items: bit 0 / 1 = a copy on s_xbar / s_abar not yet waited
     // for (drained before the CTA leaves, also after a wait gave up), bit 2 / 3 = the parity of
     // the phase that barrier completes next
@@ -446,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
                 sm100::bulk_g2s(atile + P.atile_bytes, G.w2 + src, bytes, &s_abar);
             }
         }
+        // a down tile with its own space goes into the copy queue right behind the first item's
+        // weight tiles, which are needed first
+        if (slot_item && !slot_issued && !P.slot_shares_raw) issue_slot();
         ok = P.use_atile ? gate_up_item(std::true_type{}, item, gi, G, e, tile, nt, key)
                          : gate_up_item(std::false_type{}, item, gi, G, e, tile, nt, key);
     }
