@@ -99,6 +99,11 @@ bool layer_wants_tc(int m, int top_k, int num_experts, int hidden, int inter, in
            tc_wanted(m * top_k, num_experts, hidden, t) || (sh && tc_wanted(m, 1, hidden, t));
 }
 
+// The two-launch layer fuses the combine into the down launch (the last item of a row tile
+// combines it) up to this many tokens. Beyond, that one CTA's share (tokens x tile rows) grows
+// long and holds the launch up, so the combine runs as a launch of its own over all outputs.
+constexpr int kFusedCombineMaxM = 4;
+
 // The layer runs as one persistent launch (q4k_layer.cu): a few pairs, no tensor-core bucket.
 bool layer_single_launch(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     const int setting = single_launch_setting();
@@ -360,7 +365,7 @@ int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, in
     const int t = tc_min_for(m * top_k, num_experts);
     const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t));
     const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t));
-    return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0);
+    return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0) + (m > kFusedCombineMaxM ? 1 : 0);
 }
 
 int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
@@ -505,14 +510,23 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
         if (e != cudaErrorNotSupported) return cuda_status(e, "layer launch");
     }
     // two launches: gate|up + SwiGLU (routed and shared; it also zeroes the combine counters),
-    // then down (routed and shared) with the combine fused into its last CTA per row tile
+    // then down (routed and shared) with the combine fused into its last CTA per row tile; for
+    // more than kFusedCombineMaxM tokens the combine is a third launch
+    const bool fuse = m <= kFusedCombineMaxM;
     unsigned* counters = reinterpret_cast<unsigned*>(ws + ls.counters);
     st = run_gate_up(d_w_gate, d_w_up, num_experts, d_h_post, d_ids, m, top_k, hidden, inter, act, d_ws_gate, d_ws_up,
-                     shared_inter, act_shared, d_err_flag, stream, ws + ls.tc_gu, counters, ls.n_counters);
+                     shared_inter, act_shared, d_err_flag, stream, ws + ls.tc_gu, fuse ? counters : nullptr,
+                     fuse ? ls.n_counters : 0);
     if (st) return st;
     CombineSpec cb{d_y, d_h_mid, d_weights, d_shared_gate, shared_mode, counters, ls.n_counters};
-    return run_down(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,
-                    act_shared, sout, d_err_flag, stream, ws + ls.tc_dn, &cb, ws + ls.pre, ws + ls.pre_shared);
+    st = run_down(d_w_down, num_experts, act, d_ids, m, top_k, hidden, inter, eout, d_ws_down, shared_inter,
+                  act_shared, sout, d_err_flag, stream, ws + ls.tc_dn, fuse ? &cb : nullptr, ws + ls.pre,
+                  ws + ls.pre_shared);
+    if (st || fuse) return st;
+    return cuda_status(launch_combine(d_h_mid, eout, d_weights, shared_mode != Q4K_SHARED_NONE ? sout : nullptr,
+                                      d_shared_gate, shared_mode, m, top_k, hidden, d_y, true, stream, d_ids,
+                                      num_experts),
+                       "combine launch");
 }
 
 size_t q4k_moe_layer_routed_workspace_size(int m, int top_k, int num_experts, int hidden, int inter,

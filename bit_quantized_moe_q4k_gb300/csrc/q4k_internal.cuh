@@ -32,7 +32,8 @@ cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int3
                           int32_t* offsets, int32_t* perm, int* err_flag, cudaStream_t stream);
 cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
                            const float* shared_out, const float* shared_gate, int shared_mode, int m,
-                           int top_k, int hidden, float* y, bool pdl, cudaStream_t stream);
+                           int top_k, int hidden, float* y, bool pdl, cudaStream_t stream,
+                           const int32_t* ids = nullptr, int num_experts = 0);
 cudaError_t launch_fmt4(int fmt, const uint8_t* w, const uint8_t* w2, uint64_t expert_stride, uint64_t s_off,
                         uint64_t b_off, int gs, int num_experts, const float* a, int64_t outer, int64_t inner,
                         const int32_t* ids, int m, int top_k, int n, int k, float* out, int* err_flag,

@@ -80,21 +80,24 @@ cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int3
 // (moeflux expert_forward.rs, `combine_kernel_name` and
 // `encode_moe_combine_residual_n_tokens`). One thread per 4 consecutive hidden elements
 // of one token; the slot sum runs in slot order. y may alias h_mid (each element is read
-// before it is written by the same thread).
+// before it is written by the same thread). ids != null (the layer's combine): a pair whose
+// id is outside [0, num_experts) contributes nothing, as in the combine fused into the down
+// launch, which gives the same sums bit for bit.
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* h_mid, const float* __restrict__ expert_out, const float* __restrict__ weights,
                const float* __restrict__ shared_out, const float* __restrict__ shared_gate, int shared_mode,
-               int top_k, int hidden, float* y) {
+               int top_k, int hidden, float* y, const int32_t* __restrict__ ids, int num_experts) {
     const int t = blockIdx.y;
     const int h4 = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index within the row
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (h4 * 4 >= hidden) return;
     const int64_t row = (int64_t)t * hidden + h4 * 4;
-    float4 acc = *reinterpret_cast<const float4*>(h_mid + row);
-    // expert and shared outputs come from the previous kernel (programmatic dependent launch)
+    // everything read here may come from earlier kernels (programmatic dependent launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    float4 acc = *reinterpret_cast<const float4*>(h_mid + row);
     for (int s = 0; s < top_k; ++s) {
         const int64_t p = (int64_t)t * top_k + s;
+        if (ids && !id_valid(ids[p], num_experts)) continue;
         const float w = weights[p];
         const float4 e = *reinterpret_cast<const float4*>(expert_out + p * hidden + h4 * 4);
         acc.x = fmaf(w, e.x, acc.x);
@@ -115,7 +118,8 @@ combine_kernel(const float* h_mid, const float* __restrict__ expert_out, const f
 
 cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
                            const float* shared_out, const float* shared_gate, int shared_mode, int m,
-                           int top_k, int hidden, float* y, bool pdl, cudaStream_t stream) {
+                           int top_k, int hidden, float* y, bool pdl, cudaStream_t stream, const int32_t* ids,
+                           int num_experts) {
     const int threads = 256;
     dim3 grid((hidden / 4 + threads - 1) / threads, m);
     cudaLaunchConfig_t cfg = {};
@@ -128,7 +132,7 @@ cudaError_t launch_combine(const float* h_mid, const float* expert_out, const fl
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, combine_kernel, h_mid, expert_out, weights, shared_out, shared_gate,
-                              shared_mode, top_k, hidden, y);
+                              shared_mode, top_k, hidden, y, ids, num_experts);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -195,9 +195,10 @@ int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const 
  * Launches: a layer with at most 32 routed pairs (m*top_k <= 32), no bucket large
  * enough for the tensor-core path, and halves whose work items each fit one round of the
  * CTAs the device holds at once (a decode layer) is ONE persistent launch whose CTAs
- * hand work to each other through tagged flag words and counters at the start of the
+ * hand results to each other as launch-tagged words (and tagged flags) at the start of the
  * workspace; any other layer is a gate|up launch and a down launch with the combine fused
- * into it (+ the tensor-core kernels of a half that uses them). Both give the same
+ * into it (+ the tensor-core kernels of a half that uses them); beyond 4 tokens the combine
+ * is a launch of its own, over all outputs, after the down launch. All give the same
  * results bit for bit. The environment variable Q4K_SINGLE_LAUNCH=1 takes every layer the
  * single launch can run (the first condition alone) that way, =0 none. The workspace
  * needs no initialisation: the flag words of a launch carry a tag derived from a
@@ -243,14 +244,15 @@ size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int sha
 
 /* Number of kernels one q4k_moe_layer_forward call with its full workspace launches for these
  * sizes on the current device (1 for the single-launch layer; else 2, plus 2 per half that
- * takes the tensor-core path). 0 on invalid sizes. */
+ * takes the tensor-core path, plus 1 for the combine beyond 4 tokens). 0 on invalid sizes. */
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
 /* Which kernels one q4k_moe_layer_forward call runs for these sizes on the current device
  * (the environment switches included):
  *   Q4K_PATH_PERSISTENT one persistent launch for the whole layer (a decode layer);
- *   Q4K_PATH_TWO_LAUNCH a gate|up launch and a down launch with the combine fused (plus the
- *                       tensor-core kernels of a half that uses them).
+ *   Q4K_PATH_TWO_LAUNCH a gate|up launch and a down launch with the combine fused, or after
+ *                       it beyond 4 tokens (plus the tensor-core kernels of a half that uses
+ *                       them).
  * Both give the same results bit for bit. -1 on invalid sizes. */
 #define Q4K_PATH_TWO_LAUNCH 0
 #define Q4K_PATH_PERSISTENT 1

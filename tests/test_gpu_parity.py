@@ -270,6 +270,33 @@ def test_layer_full_size_qwen3_like(name):
     rows_close(got, ref, what=name)
 
 
+def test_layer_separate_combine_out_of_range_ids():
+    """Beyond 4 tokens the two-launch layer combines in a launch of its own; pairs whose id is out
+    of range contribute nothing there too (their rows are zero, and the flag is raised)."""
+    from bit_quantized_moe_q4k_gb300.workloads import Workload
+    W = Workload("sepcomb", 512, 256, 12, 3, 12, "uniform", 256, 1, 990)  # 36 pairs: two launches
+    assert q4k.q4k_moe_layer_path(W.m, W.top_k, W.num_experts, W.hidden, W.inter, W.shared_inter) == \
+        q4k.PATH_TWO_LAUNCH
+    args = list(_layer_inputs(W))
+    ids = args[4].reshape(-1).copy()
+    ids[[1, 7, 14]] = [W.num_experts, -2, W.num_experts + 40]
+    args[4] = ids
+    wg, wu, wd, shared, ids, x, hm, rw, gl = args
+    ref, bad = oracle.moe_layer(wg, wu, wd, W.num_experts, shared, W.shared_inter, W.shared_mode, x, hm, ids, rw, gl,
+                                W.m, W.top_k, W.hidden, W.inter)
+    assert bad == 3
+    sh = W.shared_inter
+    ws_bytes = q4k.q4k_moe_layer_workspace_size(W.m, W.top_k, W.num_experts, W.hidden, W.inter, sh)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    y = _empty((W.m, W.hidden))
+    f = err_flag()
+    q4k.q4k_moe_layer_forward(dev(wg), dev(wu), dev(wd), W.num_experts, *(dev(s) for s in shared), sh, W.shared_mode,
+                              dev(x), dev(hm), dev(ids), dev(rw), dev(gl), W.m, W.top_k, W.hidden, W.inter, y, ws,
+                              ws_bytes, f)
+    assert int(host(f)[0]) == 6  # Q4K_ERR_EXPERT_ID
+    rows_close(host(y), ref, what="separate combine, out-of-range ids")
+
+
 def test_layer_top_k_16():
     """The combine at the top_k limit (16 slots per token), with a sigmoid-gated shared expert."""
     from bit_quantized_moe_q4k_gb300.workloads import Workload
