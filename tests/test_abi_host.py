@@ -193,7 +193,7 @@ def test_layer_launch_count_single_launch_rule(monkeypatch):
     assert lib.q4k_moe_layer_launch_count(5, 8, 128, 2048, 768, 768) == 3   # 40 pairs (+ the combine)
     assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 1     # Mixtral-like decode
     assert lib.q4k_moe_layer_launch_count(16, 2, 8, 4096, 14336, 0) == 7    # tensor-core buckets + combine
-    assert lib.q4k_moe_layer_launch_count(4, 2, 8, 4096, 14336, 0) == 6     # combine fused (4 tokens)
+    assert lib.q4k_moe_layer_launch_count(4, 2, 8, 4096, 14336, 0) == 1     # one pair per expert: no TC bucket
     assert lib.q4k_moe_layer_launch_count(33, 1, 4, 256, 256, 256) == 3     # a 33-pair shared expert
     with_flags = lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768)
     monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
