@@ -308,15 +308,74 @@ int num_sms() {
 
 int idgemv_tile_rows(int k) { return kWarps * (8 >> lg_split_for(k)); }
 
+cudaError_t launch_idgemv_kernel(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
+                                 cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
+                                 int n_zero, bool pdl_wait_first, const PreStaged* pre);
+
+// A second stream and two events per device for the calling host thread: the tensor-core
+// kernels of a launch run on it beside the id-GEMV kernel (they take disjoint experts and write
+// disjoint rows). Created on first use; null when creation failed (the launch then stays on
+// one stream).
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+
+static SideStream* side_stream(int dev) {
+    thread_local SideStream t_side[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStream& s = t_side[dev];
+    if (!s.tried) {
+        s.tried = true;
+        if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            s.stream = nullptr;
+        }
+    }
+    return s.stream ? &s : nullptr;
+}
+
 cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
                           unsigned* zero, int n_zero, bool pdl_wait_first, const PreStaged* pre) {
     if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
-    if (tc_min > 0) {
+    // With the tensor-core path the launch forks: its kernels go to the side stream after an
+    // event on `stream` (so they see everything issued before), the id-GEMV kernel stays on
+    // `stream`, and `stream` waits for the side stream's event after it. Not with a fused
+    // combine, which reads the tensor-core rows: then the tensor-core kernels come first.
+    SideStream* side = nullptr;
+    if (tc_min > 0 && !combine) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) side = side_stream(dev);
+    }
+    if (tc_min > 0 && side) {
+        cudaError_t e = cudaEventRecord(side->fork, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+        if (e == cudaSuccess) e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, side->stream);
+        if (e == cudaSuccess) e = cudaEventRecord(side->join, side->stream);
+        if (e != cudaSuccess) return e;
+    } else if (tc_min > 0) {
         cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
         if (e != cudaSuccess) return e;
         pdl = false;  // the tensor-core kernels precede this launch in the stream
     }
+    // (the join: the rest of the launch runs through launch_idgemv_kernel, then `stream` waits)
+    const cudaError_t ke = launch_idgemv_kernel(groups, n_groups, fused_swiglu, pdl, err_flag, stream, tc_min, combine,
+                                                zero, n_zero, pdl_wait_first, pre);
+    if (tc_min > 0 && side) {
+        const cudaError_t je = cudaStreamWaitEvent(stream, side->join, 0);
+        if (ke == cudaSuccess) return je;
+    }
+    return ke;
+}
+
+// The id-GEMV kernel's launch (after any tensor-core launches of the same call).
+cudaError_t launch_idgemv_kernel(const GemvGroup* groups, int n_groups, bool fused_swiglu, bool pdl, int* err_flag,
+                                 cudaStream_t stream, int tc_min, const CombineSpec* combine, unsigned* zero,
+                                 int n_zero, bool pdl_wait_first, const PreStaged* pre) {
     GemvParams P{};
     P.n_groups = n_groups;
     P.err_flag = err_flag;
