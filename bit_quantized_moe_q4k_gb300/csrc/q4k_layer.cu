@@ -103,7 +103,7 @@ __device__ __forceinline__ uint64_t launch_stamp(uint64_t tag, uint64_t shape) {
 // ends the wait, and what any thread of the block does after it is ordered after the
 // flags' releases. True when all are set; false once the wait has run for limit_ns or
 // kLayerMaxPolls rounds. Uniform over the block.
-template <class Index>
+template <int NTHR = kThreads, class Index>
 __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t tag, uint64_t limit_ns, Index index) {
     int j = threadIdx.x;
     const uint64_t t0 = sm100::global_timer_ns();
@@ -111,7 +111,7 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
         uint64_t v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int jj = j + u * kThreads;
+            const int jj = j + u * NTHR;
             v[u] = jj < n ? ld_acquire_u64(flags + index(jj)) : tag;
         }
         int seen = 0;
@@ -120,7 +120,7 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
             if (v[u] != tag) break;
             ++seen;
         }
-        j += seen * kThreads;
+        j += seen * NTHR;
         if (__syncthreads_and(j >= n)) return true;
         const bool late = round >= kLayerMaxPolls || sm100::global_timer_ns() - t0 > limit_ns;
         if (__syncthreads_or(late)) return false;
@@ -131,8 +131,9 @@ __device__ __forceinline__ bool wait_tags(const uint64_t* flags, int n, uint64_t
 // Publish an item in flag mode: its words were stored by this block's threads (the caller
 // synchronised the block); one thread stores the tag with release order at GPU scope, which
 // makes those words visible first. It is a thread of the last warp: warp 0 locates the next item.
+template <int NTHR = kThreads>
 __device__ __forceinline__ void publish(uint64_t* flag, uint64_t tag) {
-    if (threadIdx.x == kThreads - 32) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(tag) : "memory");
+    if (threadIdx.x == NTHR - 32) asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag), "l"(tag) : "memory");
 }
 
 // Stage the activation rows of an item's nt pairs (k values each) from tagged words: a64 holds
@@ -140,6 +141,7 @@ __device__ __forceinline__ void publish(uint64_t* flag, uint64_t tag) {
 // float4 of the row and re-reads those not yet written by this launch until all are, then they
 // are quantized as stage_row does. False when a word was still missing after limit_ns (the
 // rows are staged all the same, from what was read). All threads of the block take part.
+template <int NTHR = kThreads>
 __device__ __forceinline__ bool stage_rows_tagged(const uint64_t* a64, int64_t outer, int64_t inner, int top_k,
                                                   const int* s_pairs, int nt, int k, uint32_t tag32,
                                                   uint64_t limit_ns, uint8_t* xs, float2* meta) {
@@ -151,12 +153,12 @@ __device__ __forceinline__ bool stage_rows_tagged(const uint64_t* a64, int64_t o
     for (int t = 0; t < nt; ++t) {
         const int p = s_pairs[t];
         const uint64_t* row = a64 + (int64_t)(p / top_k) * outer + (int64_t)(p % top_k) * inner;
-        for (int f0 = 0; f0 < nf; f0 += kThreads * U) {
+        for (int f0 = 0; f0 < nf; f0 += NTHR * U) {
             uint64_t w[U][4];
             unsigned pending = 0;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int f = f0 + u * kThreads + threadIdx.x;
+                const int f = f0 + u * NTHR + threadIdx.x;
                 if (f < nf) {
                     ld_relaxed_v2(row + 4 * f, w[u][0], w[u][1]);
                     ld_relaxed_v2(row + 4 * f + 2, w[u][2], w[u][3]);
@@ -179,7 +181,7 @@ __device__ __forceinline__ bool stage_rows_tagged(const uint64_t* a64, int64_t o
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if ((pending >> u) & 1u) {
-                        const int f = f0 + u * kThreads + threadIdx.x;
+                        const int f = f0 + u * NTHR + threadIdx.x;
                         ld_relaxed_v2(row + 4 * f, w[u][0], w[u][1]);
                         ld_relaxed_v2(row + 4 * f + 2, w[u][2], w[u][3]);
                     }
@@ -187,8 +189,8 @@ __device__ __forceinline__ bool stage_rows_tagged(const uint64_t* a64, int64_t o
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int f = f0 + u * kThreads + threadIdx.x;  // groups of 8 threads are all in or all out
-                if (f0 + u * kThreads >= nf) break;
+                const int f = f0 + u * NTHR + threadIdx.x;  // groups of 8 threads are all in or all out
+                if (f0 + u * NTHR >= nf) break;
                 const float4 v = make_float4(word_value(w[u][0]), word_value(w[u][1]), word_value(w[u][2]),
                                              word_value(w[u][3]));
                 stage_quad(v, f, f < nf, xs + t * tok_bytes, meta + t * (k / 32));
@@ -211,19 +213,20 @@ struct CombineStage {
 
 // Issue the copies of tile [r0, r0 + span) (all threads). The caller waits with
 // cp_async_wait_all and a block barrier before reading.
+template <int NTHR = kThreads>
 __device__ __forceinline__ void combine_stage_issue(const CombineSpec& cb, const int32_t* ids, int n_pairs, int T,
                                                     int H, bool shared, int r0, int span, CombineStage& S) {
     const int m = n_pairs / T;
     if (m * span <= kCbRows)
-        for (int idx = threadIdx.x; idx < m * span; idx += kThreads)
+        for (int idx = threadIdx.x; idx < m * span; idx += NTHR)
             cp_async4(&S.h[idx], cb.h_mid + (int64_t)(idx / span) * H + r0 + idx % span);
-    for (int p = threadIdx.x; p < n_pairs; p += kThreads) {
+    for (int p = threadIdx.x; p < n_pairs; p += NTHR) {
         cp_async4(&S.w[p], cb.weights + p);
         if (ids) cp_async4(&S.id[p], ids + p);
         else S.id[p] = 0;
     }
     if (shared)
-        for (int t = threadIdx.x; t < m; t += kThreads) cp_async4(&S.g[t], cb.shared_gate + t);
+        for (int t = threadIdx.x; t < m; t += NTHR) cp_async4(&S.g[t], cb.shared_gate + t);
 }
 
 // The combine of rows [r0, r1) of every token from the tagged expert rows (out0: the routed
@@ -232,6 +235,7 @@ __device__ __forceinline__ void combine_stage_issue(const CombineSpec& cb, const
 // is out of range contribute nothing and their rows are not read) -- the same sums in the same
 // order as combine_span. A thread re-reads the words not yet written by this launch until all
 // are. False when one was still missing after limit_ns (y is written all the same).
+template <int NTHR = kThreads>
 __device__ __forceinline__ bool combine_tagged(const CombineSpec& cb, const uint64_t* out0, const uint64_t* out1,
                                                int num_experts, int n_pairs, int T, int H, int r0, int r1,
                                                const CombineStage& S, uint32_t tag32, uint64_t limit_ns) {
@@ -240,7 +244,7 @@ __device__ __forceinline__ bool combine_tagged(const CombineSpec& cb, const uint
     const bool staged_h = m * span <= kCbRows;
     bool ok = true;
     const uint64_t t0 = sm100::global_timer_ns();
-    for (int idx = threadIdx.x; idx < m * span; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < m * span; idx += NTHR) {
         const int t = idx / span, r = r0 + idx % span;
         const int64_t o = (int64_t)t * H + r;
         uint64_t v[Q4K_MAX_TOP_K];
@@ -580,6 +584,294 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
 }
 
 // ------------------------------------------------------------------------------------------
+// The wide layer kernel: the same layer, items, hand-offs and sums as layer_kernel, for the
+// case where every CTA takes at most one gate|up item and at most one down item, both with
+// their weight tiles in shared memory (the decode layer). Its CTAs have 256 threads: two groups
+// of four warps, h = warp >> 2. In a gate|up item group 0 folds the gate rows and group 1 the
+// up rows of the tile; in a down item (tiles of 64 rows) group 0 folds the first 32 rows and
+// group 1 the rest. Within a group the lanes are laid out as in item_issue, and each lane
+// folds one row of one slab over its blocks in the canonical order, so every sum equals
+// layer_kernel's (and the two-launch layer's) bit for bit. Twice the warps per CTA, each with
+// half the work: the dot products are bound by the latency of each warp's chain, not by the
+// SM's issue rate.
+constexpr int kWideThreads = 256;
+
+// One lane's fold of its row (wrow: the row's blocks in shared memory; zeros when !row_ok)
+// against token 0's staged planes, then the xor reduction over the row's 4*S lanes: the row's
+// sum in each of them.
+__device__ __forceinline__ float row_fold_smem(const uint8_t* wrow, const GroupDev& G, int lane, const uint8_t* xs,
+                                               const float2* meta, bool row_ok) {
+    const int S = 1 << G.lg_split;
+    const int c = lane & 3, sl = (lane >> 2) & (S - 1);
+    const int nb = G.k / kQK;
+    const int nbl = sl < nb ? (nb - sl + S - 1) / S : 0;
+    float acc = 0.0f;
+    for (int i = 0; i < nbl; ++i) {
+        const int b = sl + S * i;
+        uint4 H = make_uint4(0, 0, 0, 0), Q0 = H, Q1 = H;
+        if (row_ok) {
+            const uint8_t* p = wrow + (int64_t)b * kBlockBytes;
+            H = ldw16<true>(p); Q0 = ldw16<true>(p + 16 + 32 * c); Q1 = ldw16<true>(p + 32 + 32 * c);
+        }
+        float sa, ma, sb, mb;
+        block_scales(H, c, sa, ma, sb, mb);
+        const uint4* xp = reinterpret_cast<const uint4*>(xs + (4 * b + c) * kPairBytes);
+        const float4 mt = *reinterpret_cast<const float4*>(meta + 8 * b + 2 * c);
+        int Sa, Sb;
+        dot64(Q0, Q1, xp, Sa, Sb);
+        acc = fold_term(acc, block_term(mt, sa, ma, sb, mb, Sa, Sb), i == 0);
+    }
+    for (int off = 1; off < 4 * S; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    return acc;
+}
+
+__global__ void __launch_bounds__(kWideThreads, 3) layer_wide_kernel(const __grid_constant__ LayerParams P) {
+    constexpr int NT = kWideThreads;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ FastGroup s_fast[2][kMaxGroups];
+    __shared__ int s_items[2][kMaxGroups + 1];
+    __shared__ int s_bad[2][kMaxGroups];
+    __shared__ int s_pairs[kTB];
+    __shared__ int s_info[6];
+    __shared__ int s_chunk_b[2 * kLayerMaxPairs];
+    __shared__ int s_n_chunks;
+    __shared__ uint64_t s_tag;
+    __shared__ uint32_t s_tag32;
+    __shared__ int s_fast_mode;
+    __shared__ __align__(8) uint64_t s_bar;   // the down tile's copy
+    __shared__ __align__(8) uint64_t s_xbar;  // the gate|up item's activation row's copy
+    __shared__ __align__(8) uint64_t s_abar;  // the gate|up item's weight tiles' copy
+    __shared__ int s_never;
+    __shared__ float s_g[32];                 // a gate|up tile's gate sums (group 0 -> group 1)
+    __shared__ CombineStage s_cbs;
+
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, h = warp >> 2, w4 = warp & 3;
+    const uint64_t gen = threadIdx.x == 0 ? ld_relaxed_u64(P.gen) : 0;
+    const uint64_t stamp = threadIdx.x == 0 ? ld_relaxed_u64(P.gen + 1) : 0;
+    const uint64_t count = threadIdx.x == 0 ? ld_relaxed_u64(P.gen + 2) : 0;
+    if (warp < 4) {  // bucketing: warp w takes half w >> 1, group w & 1
+        const int half = warp >> 1, gi = warp & 1;
+        if (gi < P.n_groups) {
+            const GroupDev& G = half ? P.b[gi] : P.a[gi];
+            fast_bucket(G.ids, G.n_pairs, G.num_experts, G.tiles, 1, 0, s_fast[half][gi], &s_bad[half][gi]);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        const int half = threadIdx.x;
+        s_items[half][0] = 0;
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const FastGroup& F = s_fast[half][gi];
+            s_items[half][gi + 1] = s_items[half][gi] + F.start[F.U];
+        }
+        if (half == 0) {
+            s_never = 0;
+            sm100::mbar_init(&s_bar, 1);
+            sm100::mbar_init(&s_xbar, 1);
+            sm100::mbar_init(&s_abar, 1);
+            sm100::fence_mbar_init();
+            const uint64_t tag = next_tag(gen);
+            s_tag = tag;
+            s_tag32 = word_tag(count + 1);
+            s_fast_mode = stamp == launch_stamp(tag, P.shape);
+            st_relaxed_u64(P.cta_tag + blockIdx.x, tag);
+        }
+    }
+    __syncthreads();
+    const uint64_t tag = s_tag;
+    const uint32_t tag32 = s_tag32;
+    const bool fast = s_fast_mode;
+    const int na = s_items[0][P.n_groups], nb = s_items[1][P.n_groups];
+    const int64_t grid = gridDim.x, cta = blockIdx.x;
+    // at most one item of each half per CTA (the caps bound na and nb; checked all the same)
+    const bool fits = na <= P.cap_a && nb <= P.cap_b && na <= grid && nb <= grid;
+    bool ok = fits;
+    const int a0 = (int)(cta * na / grid), a1 = (int)((cta + 1) * na / grid);
+    const int b0 = (int)(cta * nb / grid), b1 = (int)((cta + 1) * nb / grid);
+    uint8_t* xs = smem + P.x_off;
+    float2* meta = reinterpret_cast<float2*>(smem + P.meta_off);
+    uint8_t* slot = smem + P.slot_off;
+    float* raw = reinterpret_cast<float*>(smem + P.raw_off);
+    uint8_t* atile = smem + P.atile_off;
+    const bool has_a = ok && a0 < a1, has_b = ok && b0 < b1;
+    bool slot_issued = false, slot_waited = false;
+    uint32_t cps = 0;  // bit 0 / 1: the x copy / the weight tiles' copy not yet waited for
+    auto issue_slot = [&]() {  // all threads
+        if (warp == 0) {
+            const FastLoc L = fast_locate(s_fast[1], s_items[1], P.b, P.n_groups, 1, b0, nullptr);
+            if (lane == 0) {
+                const GroupDev& G = P.b[L.gi];
+                const int tr = item_tile_rows(G.lg_split, kPair);
+                const int r0 = L.tile * tr, rows = min(tr, G.n - r0);
+                const uint32_t bytes = (uint32_t)((int64_t)rows * G.nb01);
+                sm100::fence_proxy_async_smem();
+                sm100::mbar_arrive_expect_tx(&s_bar, bytes);
+                sm100::bulk_g2s(slot, G.w + (int64_t)L.e * G.nb02 + (int64_t)r0 * G.nb01, bytes, &s_bar);
+            }
+        }
+        slot_issued = true;
+    };
+    if (has_b && !has_a) issue_slot();
+
+    // ---- the gate|up + SwiGLU item
+    if (has_a) {
+        if (warp == 0) {
+            const FastLoc L = fast_locate(s_fast[0], s_items[0], P.a, P.n_groups, 1, a0, s_pairs);
+            if (lane == 0) { s_info[0] = L.gi; s_info[2] = L.e; s_info[3] = L.tile; }
+        }
+        __syncthreads();
+        const int gi = s_info[0], e = s_info[2], tile = s_info[3];
+        const GroupDev& G = P.a[gi];
+        cps = 3u;
+        if (threadIdx.x == 0) {
+            sm100::mbar_arrive_expect_tx(&s_xbar, (uint32_t)(G.k * 4));
+            sm100::bulk_g2s(raw, act_row(G, s_pairs[0]), (uint32_t)(G.k * 4), &s_xbar);
+            const int tra = item_tile_rows(G.lg_split, kFused);
+            const int r0 = tile * tra, rows = min(tra, G.n - r0);
+            const uint32_t bytes = (uint32_t)((int64_t)rows * G.nb01);
+            const int64_t src = (int64_t)e * G.nb02 + (int64_t)r0 * G.nb01;
+            sm100::mbar_arrive_expect_tx(&s_abar, 2 * bytes);
+            sm100::bulk_g2s(atile, G.w + src, bytes, &s_abar);
+            sm100::bulk_g2s(atile + P.atile_bytes, G.w2 + src, bytes, &s_abar);
+        }
+        ok = __syncthreads_and(mbar_wait_for(&s_xbar, 0, &s_never, P.wait_ns));
+        if (ok) {
+            cps &= ~1u;
+            stage_row<2, NT>(raw, G.k, xs, meta, threadIdx.x);
+            __syncthreads();  // the last reads of the raw row: the down tile may take its space
+            if (has_b) issue_slot();
+            ok = __syncthreads_and(mbar_wait_for(&s_abar, 0, &s_never, P.wait_ns));
+        }
+        if (ok) {
+            cps &= ~2u;
+            const int lgS = G.lg_split, S = 1 << lgS, rpw = 8 >> lgS;
+            const int rt = w4 * rpw + (lane >> (2 + lgS));
+            const int row = tile * item_tile_rows(lgS, kFused) + rt;
+            const bool row_ok = row < G.n;
+            const uint8_t* wrow = atile + (h ? P.atile_bytes : 0) + (int64_t)(row_ok ? rt : 0) * G.nb01;
+            const float v = row_fold_smem(wrow, G, lane, xs, meta, row_ok);
+            const bool writer = (lane & (4 * S - 1)) == 0;
+            if (h == 0 && writer) s_g[rt] = v;
+            __syncthreads();
+            if (h == 1 && writer && row_ok)
+                st_tagged(P.act64[gi] + (int64_t)s_pairs[0] * G.n + row, silu(s_g[rt]) * v, tag32);
+            if (!fast) {
+                __syncthreads();
+                publish<NT>(P.flag_a + a0, tag);
+            }
+        }
+    }
+
+    // ---- the down item; the CTA of a row tile's last down item combines the tile
+    const bool shared = P.cb.shared_mode != Q4K_SHARED_NONE && P.n_groups > 1;
+    const int tr = item_tile_rows(P.b[0].lg_split, kPair);
+    const int n_tiles = P.b[0].tiles;
+    if (threadIdx.x == 0 && !fast) {
+        int nc = 0;
+        for (int gi = 0; gi < P.n_groups; ++gi) {
+            const FastGroup& F = s_fast[1][gi];
+            for (int r = 0; r < F.U; ++r) {
+                const int chunks = (F.start[r + 1] - F.start[r]) / P.b[gi].tiles;
+                for (int c = 0; c < chunks && nc < 2 * kLayerMaxPairs; ++c)
+                    s_chunk_b[nc++] = s_items[1][gi] + F.start[r] + c * P.b[gi].tiles;
+            }
+        }
+        s_n_chunks = nc;
+    }
+    auto combine_tile = [&](int t) -> bool {
+        const GroupDev& R = P.b[0];
+        if (!fast && !wait_tags<NT>(P.flag_b, s_n_chunks, tag, P.wait_ns, [t](int j) { return s_chunk_b[j] + t; }))
+            return false;
+        const bool done = combine_tagged<NT>(P.cb, P.out64[0], shared ? P.out64[1] : nullptr, R.num_experts,
+                                             R.n_pairs, R.top_k, R.n, t * tr, min(R.n, (t + 1) * tr), s_cbs, tag32,
+                                             P.wait_ns);
+        return __syncthreads_and(done);
+    };
+    if (ok && has_b) {
+        if (warp == 0) {
+            const FastLoc L = fast_locate(s_fast[1], s_items[1], P.b, P.n_groups, 1, b0, s_pairs);
+            if (lane == 0) { s_info[0] = L.gi; s_info[1] = L.r; s_info[3] = L.tile; s_info[5] = L.chunk; }
+        }
+        __syncthreads();
+        const int gi = s_info[0], r = s_info[1], tile = s_info[3], chunk = s_info[5];
+        const GroupDev& G = P.b[gi];
+        const bool ends_tile = b0 >= nb - n_tiles;
+        if (ends_tile) {
+            const GroupDev& R = P.b[0];
+            combine_stage_issue<NT>(P.cb, R.ids, R.n_pairs, R.top_k, R.n, shared, tile * tr,
+                                    min(R.n, (tile + 1) * tr) - tile * tr, s_cbs);
+        }
+        if (!fast) {
+            const int first = s_items[0][gi] + s_fast[0][gi].start[r] + chunk * P.a[gi].tiles;
+            ok = wait_tags<NT>(P.flag_a, P.a[gi].tiles, tag, P.wait_ns, [first](int j) { return first + j; });
+        }
+        if (ok) ok = stage_rows_tagged<NT>(P.act64[gi], G.outer, G.inner, G.top_k, s_pairs, 1, G.k, tag32, P.wait_ns, xs,
+                                           meta);
+        if (ok) {
+            ok = __syncthreads_and(mbar_wait_for(&s_bar, 0, &s_never, P.wait_ns));
+            slot_waited = ok;
+        }
+        if (ok) {
+            const int lgS = G.lg_split, S = 1 << lgS, rpw = 8 >> lgS;
+            const int rt = h * (kWarps * rpw) + w4 * rpw + (lane >> (2 + lgS));
+            const int row = tile * tr + rt;
+            const bool row_ok = row < G.n;
+            const float v = row_fold_smem(slot + (int64_t)(row_ok ? rt : 0) * G.nb01, G, lane, xs, meta, row_ok);
+            if ((lane & (4 * S - 1)) == 0 && row_ok) st_tagged(P.out64[gi] + (int64_t)s_pairs[0] * G.n + row, v, tag32);
+            __syncthreads();
+            if (!fast) publish<NT>(P.flag_b + b0, tag);
+            if (ends_tile) {
+                cp_async_wait_all();
+                __syncthreads();
+                ok = combine_tile(tile);
+            }
+        }
+    }
+    if (ok && nb == 0) {  // no down item at all: y = h_mid, tiles split over the CTAs
+        const GroupDev& R = P.b[0];
+        for (int t = (int)(cta * n_tiles / grid); ok && t < (int)((cta + 1) * n_tiles / grid); ++t) {
+            __syncthreads();
+            combine_stage_issue<NT>(P.cb, R.ids, R.n_pairs, R.top_k, R.n, shared, t * tr, min(R.n, (t + 1) * tr) - t * tr,
+                                    s_cbs);
+            cp_async_wait_all();
+            __syncthreads();
+            ok = combine_tile(t);
+        }
+    }
+    // copies still in flight land before the CTA leaves (after a wait gave up)
+    cp_async_wait_all();
+    if (slot_issued && !slot_waited) sm100::mbar_wait(&s_bar, 0, &s_never);
+    if (cps & 1u) sm100::mbar_wait(&s_xbar, 0, &s_never);
+    if (cps & 2u) sm100::mbar_wait(&s_abar, 0, &s_never);
+
+    if (threadIdx.x == 0) {
+        if (!fits) raise_flag(P.err_flag, Q4K_ERR_LIMIT);
+        else if (!ok) raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+        if (blockIdx.x == 0)
+            for (int half = 0; half < 2; ++half)
+                for (int gi = 0; gi < P.n_groups; ++gi)
+                    if (s_bad[half][gi]) raise_flag(P.err_flag, Q4K_ERR_EXPERT_ID);
+    }
+    if (blockIdx.x == 0) {
+        const bool all = wait_tags<NT>(P.cta_tag, (int)gridDim.x, tag, P.wait_ns, [](int j) { return j; });
+        if (threadIdx.x == 0) {
+            bool clean = true;
+            for (int half = 0; half < 2; ++half)
+                for (int gi = 0; gi < P.n_groups; ++gi) clean = clean && !s_bad[half][gi];
+            if (all) {
+                st_relaxed_u64(P.gen + 1, clean ? launch_stamp(next_tag(tag), P.shape) : 0ull);
+                st_relaxed_u64(P.gen + 2, count + 1);
+                st_relaxed_u64(P.gen, tag);
+            } else {
+                raise_flag(P.err_flag, Q4K_ERR_TIMEOUT);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
 uint64_t wait_limit_ns() {
     const char* s = getenv("Q4K_WAIT_NS");
     if (s) {
@@ -610,7 +902,7 @@ LayerPlan plan_of(const GemvGroup* gu, const GemvGroup* dn, int n_groups, int kb
     return L;
 }
 
-bool g_layer_attr_set[4][64] = {};
+bool g_layer_attr_set[5][64] = {};
 
 // Result words of the single-launch layer: the gate|up outputs of the routed pairs and of the
 // shared expert's tokens, then the down outputs of both (64-bit tagged words, row-major).
@@ -669,9 +961,33 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     int64_t max_pairs = 0;
     for (int gi = 0; gi < n_groups; ++gi) max_pairs = std::max<int64_t>(max_pairs, (int64_t)gu[gi].m * gu[gi].top_k);
     if (max_pairs > kLayerMaxPairs) return cudaErrorNotSupported;
-    // paired down items when one-row items would outnumber the CTAs the SMs hold
+    // tokens per item: 1 when every bucket holds about one pair (decode with distinct experts),
+    // else up to kTB -- as in the two-launch layer, so both compute alike
+    int kmax = 0, tb = 1;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        kmax = std::max(kmax, std::max(gu[gi].k, dn[gi].k));
+        if ((int64_t)gu[gi].m * gu[gi].top_k > gu[gi].num_experts) tb = kTB;
+    }
+    const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
+    while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;
+    if (tb != 1 && tb != kTB) tb = 1;
+    // paired down items when one-row items would outnumber the CTAs the SMs hold; always for the
+    // wide kernel (one token per item, the gate|up tiles, the down tile and the activation row
+    // in shared memory, one item of each half per CTA; Q4K_LAYER_WIDE=0: never)
     const int64_t resident = (int64_t)num_sms() * 3;
-    const int kb = plan_of(gu, dn, n_groups, kOne).cap_b > resident ? kPair : kOne;
+    const char* wide_env = getenv("Q4K_LAYER_WIDE");
+    bool wide_ok = (wide_env == nullptr || atoi(wide_env) != 0) && tb == 1;
+    for (int gi = 0; wide_ok && gi < n_groups; ++gi) {
+        const int lga = lg_split_for(gu[gi].k), lgb = lg_split_for(dn[0].k);
+        const int64_t nb01a = (int64_t)(gu[gi].k / kQK) * kBlockBytes, nb01b = (int64_t)(dn[gi].k / kQK) * kBlockBytes;
+        wide_ok = 2 * item_tile_rows(lga, kFused) * nb01a <= 48 * 1024 && item_tile_rows(lgb, kPair) * nb01b <= 48 * 1024 &&
+                  (int64_t)gu[gi].k * 4 <= 32 * 1024;
+    }
+    if (wide_ok) {
+        const LayerPlan Lw = plan_of(gu, dn, n_groups, kPair);
+        wide_ok = Lw.cap_a <= resident && Lw.cap_b <= resident;
+    }
+    const int kb = wide_ok || plan_of(gu, dn, n_groups, kOne).cap_b > resident ? kPair : kOne;
     const LayerPlan L = plan_of(gu, dn, n_groups, kb);
     const int m = gu[0].m, top_k = gu[0].top_k, hidden = dn[0].n, inter = gu[0].n;
     const int shared_inter = n_groups > 1 ? gu[1].n : 0;
@@ -680,18 +996,10 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
         return cudaErrorNotSupported;
     LayerParams P{};
     P.n_groups = n_groups;
-    int kmax = 0, tb = 1;
     for (int gi = 0; gi < n_groups; ++gi) {
         P.a[gi] = group_dev(gu[gi], L.lg_a[gi], kFused);
         P.b[gi] = group_dev(dn[gi], L.lg_b[gi], kb);
-        kmax = std::max(kmax, std::max(gu[gi].k, dn[gi].k));
-        // tokens per item: 1 when every bucket holds about one pair (decode with distinct
-        // experts), else up to kTB -- as in the two-launch layer, so both compute alike
-        if ((int64_t)gu[gi].m * gu[gi].top_k > gu[gi].num_experts) tb = kTB;
     }
-    const int64_t per_tok = (int64_t)(kmax / 64) * kPairBytes + (int64_t)(kmax / 32) * 8;
-    while (tb > 1 && per_tok * tb > 150 * 1024) tb >>= 1;
-    if (tb != 1 && tb != kTB) tb = 1;
     P.x_off = 0;
     P.meta_off = (int)(((int64_t)(kmax / 64) * kPairBytes * tb + 15) & ~int64_t(15));
     const size_t base_smem = (size_t)P.meta_off + (size_t)(kmax / 32) * 8 * tb;
@@ -747,24 +1055,42 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
 
     void (*kern)(LayerParams) = tb == 1 ? (kb == kPair ? layer_kernel<1, kPair> : layer_kernel<1, kOne>)
                                         : (kb == kPair ? layer_kernel<kTB, kPair> : layer_kernel<kTB, kOne>);
+    const bool wide = wide_ok && P.use_atile && P.use_slot && P.use_xcopy;
+    int threads = kThreads;
+    if (wide) {
+        kern = layer_wide_kernel;
+        threads = kWideThreads;
+    }
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int kind = (tb == 1 ? 0 : 1) + (kb == kPair ? 2 : 0);
-    if (!g_layer_attr_set[kind][dev]) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        if (err != cudaSuccess) return err;
-        g_layer_attr_set[kind][dev] = true;
-    }
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    // the shared-memory attributes are set once per device and kernel
+    auto prepare = [&](void (*k)(LayerParams), int kind) -> cudaError_t {
+        if (g_layer_attr_set[kind][dev]) return cudaSuccess;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess) g_layer_attr_set[kind][dev] = true;
+        return e;
+    };
+    err = prepare(kern, wide ? 4 : (tb == 1 ? 0 : 1) + (kb == kPair ? 2 : 0));
     if (err != cudaSuccess) return err;
-    if (P.use_atile && per_sm < 3) {  // the weight tiles must not cost residency
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (err != cudaSuccess) return err;
+    if (wide && (int64_t)per_sm * num_sms() < std::max(L.cap_a, L.cap_b)) {
+        // not one item of each half per CTA: the four-warp kernel
+        kern = layer_kernel<1, kPair>;
+        threads = kThreads;
+        err = prepare(kern, 2);
+        if (err != cudaSuccess) return err;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+        if (err != cudaSuccess) return err;
+    }
+    if (P.use_atile && per_sm < 3 && threads == kThreads) {  // the weight tiles must not cost residency
         smem = layout(false);
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
         if (err != cudaSuccess) return err;
     }
     if (smem > 200 * 1024) return cudaErrorNotSupported;
@@ -775,7 +1101,7 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     grid = std::min<int64_t>(grid, std::max<int64_t>(std::max(L.cap_a, L.cap_b), 1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     // an ordinary launch: it starts on idle SMs. As a programmatic dependent its CTAs could be

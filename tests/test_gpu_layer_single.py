@@ -141,6 +141,36 @@ def test_single_launch_duplicate_and_out_of_range_ids(monkeypatch):
     rows_close(got, ref, what="duplicate / out-of-range ids")
 
 
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[5]], ids=["qwen3_m1", "e4_m3", "zipf_ragged"])
+def test_wide_kernel_matches_four_warp_kernel(case, monkeypatch):
+    """The 256-thread kernel (one item of each half per CTA, gate and up rows -- or the two
+    halves of a down tile -- on separate warps) and the 128-thread kernel give the same bits,
+    call after call on one workspace (tags trusted from the second call on) and with an id out
+    of range."""
+    H, I, E, T, m, ids_kind, Is, mode = case
+    W = Workload("wide", H, I, E, T, m, ids_kind, Is, mode, 2100 + sum(case[:5]))
+    ids = inputs.make_ids(W.seed, W.ids, W.m, W.top_k, W.num_experts).reshape(-1).copy()
+    bad_ids = ids.copy()
+    bad_ids[-1] = W.num_experts + 1
+    for ids_now in (ids, bad_ids):
+        layer = Layer(W, _inputs(W, ids_now))
+        outs = {}
+        for wide in ("1", "0"):
+            monkeypatch.setenv("Q4K_LAYER_WIDE", wide)
+            ws = torch.empty(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
+            got = []
+            for _ in range(3):
+                f = err_flag()
+                layer.y.zero_()
+                layer.run(ws, f)
+                got.append((host(layer.y).copy(), int(host(f)[0])))
+            outs[wide] = got
+        for (a, fa), (b, fb) in zip(outs["1"], outs["0"]):
+            assert fa == fb
+            assert np.array_equal(a, b)
+    monkeypatch.delenv("Q4K_LAYER_WIDE")
+
+
 @pytest.mark.parametrize("fill", ["random", "ones", "zeros"])
 def test_single_launch_any_workspace_contents(fill, monkeypatch):
     """The workspace needs no initialisation: whatever it holds, the first call is right."""
