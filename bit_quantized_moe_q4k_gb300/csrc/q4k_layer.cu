@@ -740,12 +740,14 @@ __global__ void __launch_bounds__(kWideThreads, 3) layer_wide_kernel(const __gri
         if (ok) {
             cps &= ~1u;
             stage_row<2, NT>(raw, G.k, xs, meta, threadIdx.x);
-            __syncthreads();  // the last reads of the raw row: the down tile may take its space
-            if (has_b) issue_slot();
             ok = __syncthreads_and(mbar_wait_for(&s_abar, 0, &s_never, P.wait_ns));
         }
         if (ok) {
             cps &= ~2u;
+            // the down tile takes the raw row's space (read before the barrier above); its copy
+            // starts once this CTA's gate|up tiles are in, so those have HBM to themselves
+            // (15.48 against 15.78 us on the Qwen3-like m = 1 layer)
+            if (has_b) issue_slot();
             const int lgS = G.lg_split, S = 1 << lgS, rpw = 8 >> lgS;
             const int rt = w4 * rpw + (lane >> (2 + lgS));
             const int row = tile * item_tile_rows(lgS, kFused) + rt;
