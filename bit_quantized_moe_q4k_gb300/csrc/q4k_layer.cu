@@ -595,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
 // half the work: the dot products are bound by the latency of each warp's chain, not by the
 // SM's issue rate.
 constexpr int kWideThreads = 256;
+constexpr int kWideCopyRows = 8;   // rows per bulk copy of a gate|up weight tile
 
 // One lane's fold of its row (wrow: the row's blocks in shared memory; zeros when !row_ok)
 // against token 0's staged planes, then the xor reduction over the row's 4*S lanes: the row's
@@ -733,8 +734,14 @@ __global__ void __launch_bounds__(kWideThreads, 3) layer_wide_kernel(const __gri
             const uint32_t bytes = (uint32_t)((int64_t)rows * G.nb01);
             const int64_t src = (int64_t)e * G.nb02 + (int64_t)r0 * G.nb01;
             sm100::mbar_arrive_expect_tx(&s_abar, 2 * bytes);
-            sm100::bulk_g2s(atile, G.w + src, bytes, &s_abar);
-            sm100::bulk_g2s(atile + P.atile_bytes, G.w2 + src, bytes, &s_abar);
+            // in copies of a few rows, gate and up alternating: the copy engine of an SM then
+            // serves its CTAs' tiles side by side rather than one CTA's after another's
+            const uint32_t piece = (uint32_t)(kWideCopyRows * G.nb01);
+            for (uint32_t o = 0; o < bytes; o += piece) {
+                const uint32_t n = min(piece, bytes - o);
+                sm100::bulk_g2s(atile + o, G.w + src + o, n, &s_abar);
+                sm100::bulk_g2s(atile + P.atile_bytes + o, G.w2 + src + o, n, &s_abar);
+            }
         }
         ok = __syncthreads_and(mbar_wait_for(&s_xbar, 0, &s_never, P.wait_ns));
         if (ok) {
