@@ -536,7 +536,7 @@ def per_config_records(args, rank, world, local_rank, peak):
                 "layer_bytes": r["layer_bytes"], "layer_hbm_gbs": r["layer_bytes"] / (step_ms * 1e-3) / 1e9,
                 "layer_hbm_frac": r["layer_bytes"] / (step_ms * 1e-3) / 1e9 / peak,
                 "experts_touched_per_step": r["experts_touched"], "launches_per_step": r["launches_per_step"],
-                "roofline": {"kernel": "layer_kernel (one persistent launch)" if r["single"] else
+                "roofline": {"kernel": "layer_wide_kernel / layer_kernel (one persistent launch)" if r["single"] else
                              "idgemv_kernel<fused gate|up+SwiGLU> (routed + shared)",
                              "bound": "hbm", "bytes_per_launch": kbytes, "avg_launch_us": gu_ms * 1e3,
                              "achieved": kbytes / (gu_ms * 1e-3) / 1e9, "peak": peak,
@@ -830,6 +830,7 @@ def measured_peaks():
 KERNEL_SOURCES = {  # the files whose text a kernel's counters depend on
     "idgemv_kernel<true>": ("q4k_gemv.cu", "q4k_gemv_common.cuh"),
     "layer_kernel": ("q4k_layer.cu", "q4k_gemv_common.cuh", "q4k_sync.cuh"),
+    "layer_wide_kernel": ("q4k_layer.cu", "q4k_gemv_common.cuh", "q4k_sync.cuh"),
 }
 
 
@@ -914,8 +915,11 @@ def main():
     gu_ms = float(np.mean(r["gu_ms"]))
     if r["single"]:
         # one kernel per step: the whole layer's bytes over its launch duration
-        kernel, kbytes = "layer_kernel", r["layer_bytes"]
-        kdesc = "layer_kernel (gate|up+SwiGLU, down, combine; routed + shared) in one persistent launch"
+        # the 256-thread kernel where each CTA takes at most one item of each half from tiles in
+        # shared memory (the decode layer), else the 128-thread one (Q4K_LAYER_WIDE=0 forces it)
+        wide = os.environ.get("Q4K_LAYER_WIDE", "1") != "0" and W.pairs <= W.num_experts
+        kernel, kbytes = ("layer_wide_kernel" if wide else "layer_kernel"), r["layer_bytes"]
+        kdesc = (f"{kernel} (gate|up+SwiGLU, down, combine; routed + shared) in one persistent launch")
         ktiming = ("CUDA events around the timed graph: K back-to-back launches of this kernel, one per step, "
                    "on the launching stream")
     else:
