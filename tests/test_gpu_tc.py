@@ -119,6 +119,63 @@ def test_tc_layer_shared_expert_takes_tensor_cores():
     rows_close(got, ref, what="tc layer")
 
 
+def test_tc_side_stream_in_graph_matches_eager():
+    """The tensor-core kernels of a launch run on a second stream beside the id-GEMV kernel (a
+    fork and join on events). Layers with tensor-core buckets and one-pair buckets, called
+    eagerly and then captured in one CUDA graph (two layers, twice each) and replayed three
+    times: the same bits every time, and no error."""
+    from bit_quantized_moe_q4k_gb300.workloads import Workload
+    layers = []
+    for i, (E, T, m, ids_kind) in enumerate([(32, 4, 24, "zipf"), (64, 8, 16, "zipf")]):
+        W = Workload(f"side{i}", 512, 512, E, T, m, ids_kind, 512, 1, 700 + i)
+        seed = W.seed
+        ids = inputs.make_ids(seed, W.ids, W.m, W.top_k, W.num_experts)
+        d = dict(wg=dev(oracle_slab(seed, "gate", E, W.inter, W.hidden)),
+                 wu=dev(oracle_slab(seed, "up", E, W.inter, W.hidden)),
+                 wd=dev(oracle_slab(seed, "down", E, W.hidden, W.inter)),
+                 sg=dev(oracle_slab(seed, "sgate", 1, W.shared_inter, W.hidden)),
+                 su=dev(oracle_slab(seed, "sup", 1, W.shared_inter, W.hidden)),
+                 sd=dev(oracle_slab(seed, "sdown", 1, W.hidden, W.shared_inter)),
+                 x=dev(inputs.normal(seed, "h_post", (W.m, W.hidden))), hm=dev(inputs.normal(seed, "h_mid", (W.m, W.hidden))),
+                 ids=dev(ids), rw=dev(inputs.routing_weights(seed, W.m, W.top_k)),
+                 gl=dev(inputs.normal(seed, "shared_gate", (W.m,))))
+        nbytes = q4k.q4k_moe_layer_workspace_size(W.m, W.top_k, E, W.hidden, W.inter, W.shared_inter)
+        d["ws"], d["nb"] = torch.empty(nbytes, dtype=torch.uint8, device="cuda"), nbytes
+        d["y"] = torch.empty((W.m, W.hidden), dtype=torch.float32, device="cuda")
+        assert q4k.q4k_moe_layer_launch_count(W.m, W.top_k, E, W.hidden, W.inter, W.shared_inter) > 3
+        layers.append((W, d))
+    f = err_flag()
+
+    def run(W, d, stream=None):
+        q4k.q4k_moe_layer_forward(d["wg"], d["wu"], d["wd"], W.num_experts, d["sg"], d["su"], d["sd"], W.shared_inter,
+                                  W.shared_mode, d["x"], d["hm"], d["ids"], d["rw"], d["gl"], W.m, W.top_k, W.hidden,
+                                  W.inter, d["y"], d["ws"], d["nb"], f, stream)
+
+    refs = []
+    for W, d in layers:
+        run(W, d)
+        refs.append(host(d["y"]).copy())
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for _ in range(2):
+                for W, d in layers:
+                    run(W, d, stream)
+    stream.synchronize()
+    for rep in range(3):
+        for _, d in layers:
+            d["y"].zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        for (W, d), ref in zip(layers, refs):
+            assert np.array_equal(host(d["y"]), ref), f"replay {rep}, {W.name}"
+    assert int(host(f)[0]) == 0
+
+
 def test_tc_wait_limit_runs_out(monkeypatch):
     """A wait limit of 1 ns (Q4K_WAIT_NS) makes the tensor-core kernel's pipeline waits give up:
     the roles leave together (abort word), the MMAs already issued and the copies in flight
