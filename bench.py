@@ -917,8 +917,8 @@ def main():
         # one kernel per step: the whole layer's bytes over its launch duration
         # the 256-thread kernel where each CTA takes at most one item of each half from tiles in
         # shared memory (the decode layer), else the 128-thread one (Q4K_LAYER_WIDE=0 forces it)
-        wide = os.environ.get("Q4K_LAYER_WIDE", "1") != "0" and W.pairs <= W.num_experts
-        kernel, kbytes = ("layer_wide_kernel" if wide else "layer_kernel"), r["layer_bytes"]
+        kernel = "layer_wide_kernel" if r["path"] == 2 else "layer_kernel"  # Q4K_PATH_PERSISTENT_WIDE
+        kbytes = r["layer_bytes"]
         kdesc = (f"{kernel} (gate|up+SwiGLU, down, combine; routed + shared) in one persistent launch")
         ktiming = ("CUDA events around the timed graph: K back-to-back launches of this kernel, one per step, "
                    "on the launching stream")

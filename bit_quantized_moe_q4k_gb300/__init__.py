@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     FMT_AFFINE4,
     FMT_Q4TP,
     PATH_PERSISTENT,
+    PATH_PERSISTENT_WIDE,
     PATH_TWO_LAUNCH,
     Q4KError,
     ROUTE_SIGMOID_GROUPED,

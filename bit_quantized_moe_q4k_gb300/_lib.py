@@ -23,7 +23,7 @@ STATUS_NAMES = {
     10: "Q4K_ERR_TIMEOUT",
 }
 SHARED_NONE, SHARED_SIGMOID, SHARED_UNSCALED = 0, 1, 2
-PATH_TWO_LAUNCH, PATH_PERSISTENT = 0, 1
+PATH_TWO_LAUNCH, PATH_PERSISTENT, PATH_PERSISTENT_WIDE = 0, 1, 2
 ROUTE_SOFTMAX, ROUTE_SIGMOID_GROUPED = 0, 1
 FMT_AFFINE4, FMT_Q4TP = 1, 2
 
@@ -258,7 +258,7 @@ def q4k_moe_layer_launch_count(m, top_k, num_experts, hidden, inter, shared_inte
 
 
 def q4k_moe_layer_path(m, top_k, num_experts, hidden, inter, shared_inter) -> int:
-    """PATH_PERSISTENT or PATH_TWO_LAUNCH: the kernels one layer call runs."""
+    """PATH_PERSISTENT_WIDE, PATH_PERSISTENT or PATH_TWO_LAUNCH: the kernels one layer call runs."""
     return int(load().q4k_moe_layer_path(m, top_k, num_experts, hidden, inter, shared_inter))
 
 

@@ -374,7 +374,9 @@ int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter,
     if (m <= 0 || top_k < 1 || top_k > Q4K_MAX_TOP_K || num_experts < 1 || hidden < 1 || inter < 1 ||
         shared_inter < 0)
         return -1;
-    if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) return Q4K_PATH_PERSISTENT;
+    if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter))
+        return layer_kernel_kind(m, top_k, num_experts, hidden, inter, shared_inter) == 2 ? Q4K_PATH_PERSISTENT_WIDE
+                                                                              : Q4K_PATH_PERSISTENT;
     return Q4K_PATH_TWO_LAUNCH;
 }
 

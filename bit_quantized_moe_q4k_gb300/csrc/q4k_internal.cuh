@@ -126,6 +126,9 @@ bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel'
 size_t layer_sync_words(int m, int top_k, int hidden, int inter, int shared_inter);
 // Both halves' work items fit one round of the CTAs the device's SMs hold at once.
 bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter);
+// Which kernel a single-launch layer of these sizes takes on the current device: 2 the wide
+// kernel, 1 the four-warp kernel (or no device to ask), 0 none (the layer takes two launches).
+int layer_kernel_kind(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
 cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
                                     uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream);

@@ -964,8 +964,23 @@ bool layer_one_round(int m, int top_k, int hidden, int inter, int shared_inter) 
     return L.cap_a <= resident && L.cap_b <= resident;
 }
 
-cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
-                                    uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream) {
+namespace {
+
+// A planned launch: the kernel, its block size, shared memory and grid.
+struct LaunchPlan {
+    void (*kern)(LayerParams);
+    int threads;
+    size_t smem;
+    int64_t grid;
+    bool wide;
+};
+
+// Plan a single-launch layer for these groups: P's shapes, shared-memory layout, caps and shape
+// word (not its pointers into the workspace, the combine or the error flag) and the kernel the
+// launch takes. Sets the kernels' shared-memory attributes on the current device on first use.
+// cudaErrorNotSupported where the single launch does not apply.
+cudaError_t plan_layer(const GemvGroup* gu, const GemvGroup* dn, int n_groups, bool shared_term, LayerParams& P,
+                       LaunchPlan& LP) {
     if (n_groups < 1 || n_groups > kMaxGroups) return cudaErrorNotSupported;
     int64_t max_pairs = 0;
     for (int gi = 0; gi < n_groups; ++gi) max_pairs = std::max<int64_t>(max_pairs, (int64_t)gu[gi].m * gu[gi].top_k);
@@ -1000,10 +1015,7 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     const LayerPlan L = plan_of(gu, dn, n_groups, kb);
     const int m = gu[0].m, top_k = gu[0].top_k, hidden = dn[0].n, inter = gu[0].n;
     const int shared_inter = n_groups > 1 ? gu[1].n : 0;
-    const int64_t n_results = result_words(m, top_k, hidden, inter, shared_inter);
-    if (sync == nullptr || sync_words < kSyncHead + kLayerMaxCtas + (size_t)(n_results + L.cap_a + L.cap_b))
-        return cudaErrorNotSupported;
-    LayerParams P{};
+    P = LayerParams{};
     P.n_groups = n_groups;
     for (int gi = 0; gi < n_groups; ++gi) {
         P.a[gi] = group_dev(gu[gi], L.lg_a[gi], kFused);
@@ -1040,31 +1052,18 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
         return off + (size_t)region;
     };
     size_t smem = layout(2 * atile_bytes <= 48 * 1024);
-    P.cb = cb;
-    P.gen = sync;
-    P.cta_tag = sync + kSyncHead;
-    uint64_t* words = P.cta_tag + kLayerMaxCtas;  // 16-byte aligned (even word offset)
-    P.act64[0] = words;
-    P.act64[1] = P.act64[0] + (int64_t)m * top_k * inter;
-    P.out64[0] = P.act64[1] + (int64_t)m * shared_inter;
-    P.out64[1] = n_groups > 1 ? P.out64[0] + (int64_t)m * top_k * hidden : nullptr;
-    P.flag_a = words + n_results;
-    P.flag_b = P.flag_a + L.cap_a;
     P.cap_a = (int)L.cap_a;
     P.cap_b = (int)L.cap_b;
-    P.err_flag = err_flag;
-    P.wait_ns = wait_limit_ns();
-
     // the shapes that decide which result words a launch writes and reads, and where
     uint64_t shape = host_mix64(0x51A9E0F1A7E2ull);
     for (const int64_t v : {(int64_t)m, (int64_t)top_k, (int64_t)hidden, (int64_t)inter, (int64_t)shared_inter,
-                            (int64_t)n_groups, (int64_t)kb, (int64_t)tb, (int64_t)(cb.shared_mode != Q4K_SHARED_NONE)})
+                            (int64_t)n_groups, (int64_t)kb, (int64_t)tb, (int64_t)shared_term})
         shape = host_mix64(shape ^ (uint64_t)v);
     P.shape = shape;
 
     void (*kern)(LayerParams) = tb == 1 ? (kb == kPair ? layer_kernel<1, kPair> : layer_kernel<1, kOne>)
                                         : (kb == kPair ? layer_kernel<kTB, kPair> : layer_kernel<kTB, kOne>);
-    const bool wide = wide_ok && P.use_atile && P.use_slot && P.use_xcopy;
+    bool wide = wide_ok && P.use_atile && P.use_slot && P.use_xcopy;
     int threads = kThreads;
     if (wide) {
         kern = layer_wide_kernel;
@@ -1092,6 +1091,7 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
         // not one item of each half per CTA: the four-warp kernel
         kern = layer_kernel<1, kPair>;
         threads = kThreads;
+        wide = false;
         err = prepare(kern, 2);
         if (err != cudaSuccess) return err;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
@@ -1108,15 +1108,69 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     int64_t grid = (int64_t)num_sms() * per_sm;
     grid = std::min<int64_t>(grid, kLayerMaxCtas);
     grid = std::min<int64_t>(grid, std::max<int64_t>(std::max(L.cap_a, L.cap_b), 1));
+    LP.kern = kern;
+    LP.threads = threads;
+    LP.smem = smem;
+    LP.grid = grid;
+    LP.wide = wide;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int layer_kernel_kind(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
+    if (layer_sync_words(m, top_k, hidden, inter, shared_inter) == 0) return 0;
+    GemvGroup gu[2] = {}, dn[2] = {};
+    gu[0] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, num_experts, m, top_k, inter, hidden};
+    dn[0] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, num_experts, m, top_k, hidden, inter};
+    int ng = 1;
+    if (shared_inter > 0) {
+        gu[1] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, 1, shared_inter, hidden};
+        dn[1] = GemvGroup{nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, 1, m, 1, hidden, shared_inter};
+        ng = 2;
+    }
+    LayerParams P{};
+    LaunchPlan LP{};
+    const cudaError_t e = plan_layer(gu, dn, ng, shared_inter > 0, P, LP);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorNotSupported ? 0 : 1;  // (no device to ask: the kernel is unknown)
+    }
+    return LP.wide ? 2 : 1;
+}
+
+cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, int n_groups, const CombineSpec& cb,
+                                    uint64_t* sync, size_t sync_words, int* err_flag, cudaStream_t stream) {
+    LayerParams P{};
+    LaunchPlan LP{};
+    cudaError_t err = plan_layer(gu, dn, n_groups, cb.shared_mode != Q4K_SHARED_NONE, P, LP);
+    if (err != cudaSuccess) return err;
+    const int m = gu[0].m, top_k = gu[0].top_k, hidden = dn[0].n, inter = gu[0].n;
+    const int shared_inter = n_groups > 1 ? gu[1].n : 0;
+    const int64_t n_results = result_words(m, top_k, hidden, inter, shared_inter);
+    if (sync == nullptr || sync_words < kSyncHead + kLayerMaxCtas + (size_t)(n_results + P.cap_a + P.cap_b))
+        return cudaErrorNotSupported;
+    P.cb = cb;
+    P.gen = sync;
+    P.cta_tag = sync + kSyncHead;
+    uint64_t* words = P.cta_tag + kLayerMaxCtas;  // 16-byte aligned (even word offset)
+    P.act64[0] = words;
+    P.act64[1] = P.act64[0] + (int64_t)m * top_k * inter;
+    P.out64[0] = P.act64[1] + (int64_t)m * shared_inter;
+    P.out64[1] = n_groups > 1 ? P.out64[0] + (int64_t)m * top_k * hidden : nullptr;
+    P.flag_a = words + n_results;
+    P.flag_b = P.flag_a + P.cap_a;
+    P.err_flag = err_flag;
+    P.wait_ns = wait_limit_ns();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3((unsigned)LP.grid);
+    cfg.blockDim = dim3(LP.threads);
+    cfg.dynamicSmemBytes = LP.smem;
     cfg.stream = stream;
     // an ordinary launch: it starts on idle SMs. As a programmatic dependent its CTAs could be
     // placed beside the previous kernel's last CTAs on SMs configured for a smaller shared-memory
     // share, which then hold fewer of them than the grid needs resident at once.
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    return cudaLaunchKernelEx(&cfg, LP.kern, P);
 }
 
 }  // namespace q4k

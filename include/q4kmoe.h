@@ -250,12 +250,16 @@ int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, in
 /* Which kernels one q4k_moe_layer_forward call runs for these sizes on the current device
  * (the environment switches included):
  *   Q4K_PATH_PERSISTENT one persistent launch for the whole layer (a decode layer);
+ *   Q4K_PATH_PERSISTENT_WIDE the same with 256-thread CTAs, each taking at most one work item of
+ *                       each half from tiles in shared memory (decode layers that allow it;
+ *                       Q4K_LAYER_WIDE=0 switches it off);
  *   Q4K_PATH_TWO_LAUNCH a gate|up launch and a down launch with the combine fused, or after
  *                       it beyond 4 tokens (plus the tensor-core kernels of a half that uses
  *                       them).
  * Both give the same results bit for bit. -1 on invalid sizes. */
 #define Q4K_PATH_TWO_LAUNCH 0
 #define Q4K_PATH_PERSISTENT 1
+#define Q4K_PATH_PERSISTENT_WIDE 2
 int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
 /* ---------------------------------------------------------------------------------

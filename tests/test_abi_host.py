@@ -212,7 +212,7 @@ def test_layer_path_query(monkeypatch):
     decode layer, two launches otherwise or when switched off; -1 for invalid sizes."""
     lib = q4k.load()
     monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "1")
-    assert lib.q4k_moe_layer_path(1, 8, 128, 2048, 768, 768) == q4k.PATH_PERSISTENT
+    assert lib.q4k_moe_layer_path(1, 8, 128, 2048, 768, 768) in (q4k.PATH_PERSISTENT, q4k.PATH_PERSISTENT_WIDE)
     assert lib.q4k_moe_layer_path(5, 8, 128, 2048, 768, 768) == q4k.PATH_TWO_LAUNCH  # 40 pairs
     monkeypatch.setenv("Q4K_SINGLE_LAUNCH", "0")
     assert lib.q4k_moe_layer_path(1, 8, 128, 2048, 768, 768) == q4k.PATH_TWO_LAUNCH

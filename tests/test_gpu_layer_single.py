@@ -108,7 +108,7 @@ def test_single_launch_matches_two_launch_and_oracle(case, monkeypatch):
     H, I, E, T, m, ids_kind, Is, mode = case
     W = Workload("single", H, I, E, T, m, ids_kind, Is, mode, 1200 + sum(case[:5]))
     assert q4k.q4k_moe_layer_launch_count(m, T, E, H, I, Is) == 1
-    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) == q4k.PATH_PERSISTENT
+    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) in (q4k.PATH_PERSISTENT, q4k.PATH_PERSISTENT_WIDE)
     layer = Layer(W, _inputs(W))
     ref2, f2 = _two_launch(layer, monkeypatch)
     assert f2 == 0
@@ -141,7 +141,13 @@ def test_single_launch_duplicate_and_out_of_range_ids(monkeypatch):
     rows_close(got, ref, what="duplicate / out-of-range ids")
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[5]], ids=["qwen3_m1", "e4_m3", "zipf_ragged"])
+WIDE_CASES = [CASES[0],                                      # the Qwen3-like decode layer
+              (1024, 512, 64, 8, 1, "uniform", 512, 2),     # k = 1024 / 512: one lane per row
+              (1024, 512, 64, 4, 1, "zipf", 0, 0),          # no shared expert
+              CASES[2]]                                     # 4-token items: the four-warp kernel
+
+
+@pytest.mark.parametrize("case", WIDE_CASES, ids=["qwen3_m1", "k1024", "no_shared", "tb4"])
 def test_wide_kernel_matches_four_warp_kernel(case, monkeypatch):
     """The 256-thread kernel (one item of each half per CTA, gate and up rows -- or the two
     halves of a down tile -- on separate warps) and the 128-thread kernel give the same bits,
@@ -149,6 +155,11 @@ def test_wide_kernel_matches_four_warp_kernel(case, monkeypatch):
     of range."""
     H, I, E, T, m, ids_kind, Is, mode = case
     W = Workload("wide", H, I, E, T, m, ids_kind, Is, mode, 2100 + sum(case[:5]))
+    expect = q4k.PATH_PERSISTENT if case is CASES[2] else q4k.PATH_PERSISTENT_WIDE
+    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) == expect
+    monkeypatch.setenv("Q4K_LAYER_WIDE", "0")
+    assert q4k.q4k_moe_layer_path(m, T, E, H, I, Is) == q4k.PATH_PERSISTENT
+    monkeypatch.delenv("Q4K_LAYER_WIDE")
     ids = inputs.make_ids(W.seed, W.ids, W.m, W.top_k, W.num_experts).reshape(-1).copy()
     bad_ids = ids.copy()
     bad_ids[-1] = W.num_experts + 1
@@ -257,17 +268,19 @@ def test_single_launch_hidden_changes_on_one_workspace(monkeypatch):
     assert int(host(f)[0]) == 0
 
 
-def test_single_launch_wait_limit_runs_out(monkeypatch):
+@pytest.mark.parametrize("wide", ["1", "0"])
+def test_single_launch_wait_limit_runs_out(wide, monkeypatch):
     """A wait limit of 1 ns (Q4K_WAIT_NS) makes the waits give up: the kernel returns with
     Q4K_ERR_TIMEOUT in the device flag after its bulk copies have landed (no fault, no hang, the
     context stays usable), and the next call on a cleared workspace with the default limit is
     right. (Below a millisecond the mbarrier waits poll without suspending, so the first copy
     that has not landed yet makes its wait give up.)"""
+    monkeypatch.setenv("Q4K_LAYER_WIDE", wide)
     W = WORKLOADS["qwen3moe_h2048_i768_e128_t8_m1"]
     layer = Layer(W, _inputs(W))
     ref2, _ = _two_launch(layer, monkeypatch)
     assert q4k.q4k_moe_layer_path(W.m, W.top_k, W.num_experts, W.hidden, W.inter, W.shared_inter) == \
-        q4k.PATH_PERSISTENT
+        (q4k.PATH_PERSISTENT_WIDE if wide == "1" else q4k.PATH_PERSISTENT)
     ws = torch.zeros(layer.ws_bytes(), dtype=torch.uint8, device="cuda")
     f = err_flag()
     monkeypatch.setenv("Q4K_WAIT_NS", "1")

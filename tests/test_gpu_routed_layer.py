@@ -101,7 +101,7 @@ def _call_separate(c, E, H, I, SI, mode, m, K, scoring, ng, tg, scale):
 @pytest.mark.parametrize("name,E,H,I,SI,mode,m,K,scoring,ng,tg,scale", CASES, ids=[c[0] for c in CASES])
 def test_routed_layer_matches_separate_calls_and_oracle(name, E, H, I, SI, mode, m, K, scoring, ng, tg, scale):
     c = _layer_case(800 + m + E, E, H, I, SI, m, scoring == q4k.ROUTE_SIGMOID_GROUPED)
-    single = q4k.q4k_moe_layer_path(m, K, E, H, I, SI) == q4k.PATH_PERSISTENT
+    single = q4k.q4k_moe_layer_path(m, K, E, H, I, SI) in (q4k.PATH_PERSISTENT, q4k.PATH_PERSISTENT_WIDE)
     assert single == ("two-launch" not in name)
     got, ws = _call_routed(c, E, H, I, SI, mode, m, K, scoring, ng, tg, scale)
     sep = _call_separate(c, E, H, I, SI, mode, m, K, scoring, ng, tg, scale)
