@@ -203,6 +203,15 @@ idgemv_kernel(const __grid_constant__ GemvParams P) {
         // ---- start the weight stream before staging (independent of the activations)
         ItemLane<FUSED ? kFused : kOne> L;
         item_issue<FUSED ? kFused : kOne>(G, e, tile, lane, warp, L);
+        // the next item of this CTA is usually the next row tile of the same slab: start its
+        // rows into L2 (copy engine, no registers), so its loads need not wait for HBM
+        if (threadIdx.x == 0 && item + 1 < item_end && tile + 1 < G.tiles) {
+            const int tr = item_tile_rows(G.lg_split, FUSED ? kFused : kOne);
+            const int r1 = (tile + 1) * tr, rows = min(tr, G.n - r1);
+            const int64_t off = (int64_t)e * G.nb02 + (int64_t)r1 * G.nb01;
+            bulk_prefetch_l2(G.w + off, (uint32_t)(rows * G.nb01));
+            if (FUSED) bulk_prefetch_l2(G.w2 + off, (uint32_t)(rows * G.nb01));
+        }
 
         if (!P.fast && warp == 0) {
             const bool have = s_pairs_key[0] == gi && s_pairs_key[1] == e && s_pairs_key[2] == chunk;
