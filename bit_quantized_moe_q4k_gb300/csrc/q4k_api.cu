@@ -528,8 +528,8 @@ int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* 
                   ws + ls.pre_shared);
     if (st || fuse) return st;
     return cuda_status(launch_combine(d_h_mid, eout, d_weights, shared_mode != Q4K_SHARED_NONE ? sout : nullptr,
-                                      d_shared_gate, shared_mode, m, top_k, hidden, d_y, true, stream, d_ids,
-                                      num_experts),
+                                      d_shared_gate, shared_mode, m, top_k, hidden, d_y, !take_after_join(), stream,
+                                      d_ids, num_experts),
                        "combine launch");
 }
 

@@ -331,6 +331,17 @@ struct SideStream {
     bool tried = false;
 };
 
+// Set when a launch has joined its side stream back into the caller's stream: the next launch
+// of this host thread is then an ordinary one, so no programmatic overlap has to be trusted to
+// respect the join (a launch right after a join may read rows the side stream wrote).
+thread_local bool t_after_join = false;
+
+bool take_after_join() {
+    const bool v = t_after_join;
+    t_after_join = false;
+    return v;
+}
+
 static SideStream* side_stream(int dev) {
     thread_local SideStream t_side[kMaxDevices];
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -351,6 +362,8 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
                           cudaStream_t stream, int tc_min, uint8_t* const* tc_img, const CombineSpec* combine,
                           unsigned* zero, int n_zero, bool pdl_wait_first, const PreStaged* pre) {
     if (tc_min > 0 && !tc_fits(groups, n_groups)) tc_min = 0;  // too many experts for its tables
+    const bool after_join = take_after_join();
+    if (after_join) pdl = false;
     // With the tensor-core path the launch forks: its kernels go to the side stream after an
     // event on `stream` (so they see everything issued before), the id-GEMV kernel stays on
     // `stream`, and `stream` waits for the side stream's event after it. Not with a fused
@@ -363,11 +376,21 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
     if (tc_min > 0 && side) {
         cudaError_t e = cudaEventRecord(side->fork, stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-        if (e == cudaSuccess) e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, side->stream);
+        if (e != cudaSuccess) {
+            // the side stream or its events are gone (e.g. after a device reset): make new ones
+            // next time, and run this launch on one stream
+            cudaGetLastError();
+            side->tried = false;
+            side->stream = nullptr;
+            side = nullptr;
+        }
+    }
+    if (tc_min > 0 && side) {
+        cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, side->stream);
         if (e == cudaSuccess) e = cudaEventRecord(side->join, side->stream);
         if (e != cudaSuccess) return e;
     } else if (tc_min > 0) {
-        cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream);
+        cudaError_t e = launch_tc(groups, n_groups, fused_swiglu, tc_min, tc_img, err_flag, stream, !after_join);
         if (e != cudaSuccess) return e;
         pdl = false;  // the tensor-core kernels precede this launch in the stream
     }
@@ -376,6 +399,7 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
                                                 zero, n_zero, pdl_wait_first, pre);
     if (tc_min > 0 && side) {
         const cudaError_t je = cudaStreamWaitEvent(stream, side->join, 0);
+        t_after_join = true;
         if (ke == cudaSuccess) return je;
     }
     return ke;
@@ -540,7 +564,7 @@ cudaError_t launch_prestage(const GemvGroup* groups, int n_groups, const PreStag
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = take_after_join() ? 0 : 1;  // an ordinary launch right after a join
     return cudaLaunchKernelEx(&cfg, prestage_kernel, P);
 }
 

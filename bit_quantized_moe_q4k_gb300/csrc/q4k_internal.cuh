@@ -30,6 +30,9 @@ struct BucketView {
 // Launchers (defined in q4k_misc.cu / q4k_gemv.cu). All return cudaError_t of the launch.
 cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int32_t* counts,
                           int32_t* offsets, int32_t* perm, int* err_flag, cudaStream_t stream);
+// True (once) when the calling thread's last id-GEMV launch joined a side stream back into its
+// stream: the next launch should then not be a programmatic dependent.
+bool take_after_join();
 cudaError_t launch_combine(const float* h_mid, const float* expert_out, const float* weights,
                            const float* shared_out, const float* shared_gate, int shared_mode, int m,
                            int top_k, int hidden, float* y, bool pdl, cudaStream_t stream,
@@ -113,7 +116,7 @@ cudaError_t launch_idgemv(const GemvGroup* groups, int n_groups, bool fused_swig
 // rows per id-GEMV work item for a given k (bucketed kernel)
 int idgemv_tile_rows(int k);
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
-                      int* err_flag, cudaStream_t stream);
+                      int* err_flag, cudaStream_t stream, bool pdl = true);
 size_t tc_image_bytes(int n_pairs, int k, int tc_min);
 bool tc_fits(const GemvGroup* groups, int n_groups);  // the tensor-core kernel's shared memory plan fits
 

@@ -580,7 +580,7 @@ bool tc_fits(const GemvGroup* groups, int n_groups) {
 }
 
 cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_min, uint8_t* const* img,
-                      int* err_flag, cudaStream_t stream) {
+                      int* err_flag, cudaStream_t stream, bool pdl) {
     TcParams P{};
     P.n_groups = n_groups;
     P.tc_min = tc_min;
@@ -626,7 +626,7 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = pdl ? 1 : 0;
         err = cudaLaunchKernelEx(&cfg, tc_prep_kernel, P);
         if (err != cudaSuccess) return err;
     }
