@@ -30,7 +30,11 @@
  *     pointer past the call. The one global device state is the static scratch
  *     array of q4k_expert_ffn_forward_noalloc (4 MiB per device, part of the
  *     library image); after a cudaDeviceReset the process must not call that
- *     entry point again (the address it keeps belongs to the old context).
+ *     entry point again (the address it keeps belongs to the old context). A call
+ *     whose experts take the tensor-core path also keeps, per device and host
+ *     thread, one CUDA stream and two events (created on first use, made anew if
+ *     they stop working): its tensor-core kernels run on that stream beside its
+ *     id-GEMV kernel, joined back into `stream` before anything reads their rows.
  *   - Waits inside a kernel for work of other CTAs of the same launch are bounded
  *     in time: the environment variable Q4K_WAIT_NS (nanoseconds, read at every
  *     call; default 2 s) sets the limit, after which the kernel stops waiting, sets
