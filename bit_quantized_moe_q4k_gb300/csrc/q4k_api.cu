@@ -51,12 +51,13 @@ int check_gemv_shape(int num_experts, int m, int top_k, int n, int k) {
 // Tensor-core path policy: experts whose bucket holds at least t pairs run on the tcgen05
 // grouped GEMM (q4k_tc.cu), the others on the id-GEMV kernel, the tensor-core launch first.
 // t is the environment variable Q4K_TC_MIN when set (0 disables the path); otherwise 2 when
-// the batch averages at least two pairs per expert; else 4 with at least 64 experts (about
+// the batch averages at least two pairs per expert; else 3 with at least 64 experts (about
 // one pair each on average, but routed ids crowd some experts: on the Zipf-distributed
-// Qwen3-like m = 16 layer 126.6 us with 4 against 133 us with 2 or without the path); else 8
-// (few experts with about one pair each: the path's two launches find hardly a bucket to
-// take; Mixtral-like m = 4 209 us against 220 us with 4). A launch uses the path only when
-// some bucket can reach t and the caller's workspace holds the activation images.
+// Qwen3-like m = 16 layer 94.5 us with 3 against 99.9 / 100.7 / 135 us with 2 / 4 / without
+// the path); else 8 (few experts with about one pair each: the path's two launches find
+// hardly a bucket to take; Mixtral-like m = 4 200 us against 220-265 us with 2-4). A launch
+// uses the path only when some bucket can reach t and the caller's workspace holds the
+// activation images.
 int tc_min_env() {
     static int v = [] {
         const char* s = getenv("Q4K_TC_MIN");
@@ -68,7 +69,7 @@ int tc_min_env() {
 int tc_min_for(int routed_pairs, int num_experts) {
     if (tc_min_env() >= 0) return tc_min_env();
     if ((int64_t)routed_pairs >= 2 * (int64_t)num_experts) return 2;
-    return num_experts >= 64 ? 4 : 8;
+    return num_experts >= 64 ? 3 : 8;
 }
 
 // Switch (environment, read at every call): Q4K_SINGLE_LAUNCH=1 runs every layer the single
