@@ -79,10 +79,13 @@ cudaError_t launch_bucket(const int32_t* ids, int n_pairs, int num_experts, int3
 // Combine: hidden_out = h_mid + sum_k w_k * expert_out_k + g * shared_out
 // (moeflux expert_forward.rs, `combine_kernel_name` and
 // `encode_moe_combine_residual_n_tokens`). One thread per 4 consecutive hidden elements
-// of one token; the slot sum runs in slot order. y may alias h_mid (each element is read
-// before it is written by the same thread). ids != null (the layer's combine): a pair whose
-// id is outside [0, num_experts) contributes nothing, as in the combine fused into the down
-// launch, which gives the same sums bit for bit.
+// of one token. All of a thread's loads are issued before any sum (one round trip, not one per
+// slot); the slot sum then runs in slot order. KS: slots the thread holds (8 for top_k <= 8,
+// which keeps it at 64 registers, else 16). y may alias h_mid (each element is read before it
+// is written by the same thread). ids != null (the layer's combine): a pair whose id is outside
+// [0, num_experts) contributes nothing, as in the combine fused into the down launch, which gives
+// the same sums bit for bit.
+template <int KS>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* h_mid, const float* __restrict__ expert_out, const float* __restrict__ weights,
                const float* __restrict__ shared_out, const float* __restrict__ shared_gate, int shared_mode,
@@ -94,20 +97,31 @@ combine_kernel(const float* h_mid, const float* __restrict__ expert_out, const f
     const int64_t row = (int64_t)t * hidden + h4 * 4;
     // everything read here may come from earlier kernels (programmatic dependent launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    float4 acc = *reinterpret_cast<const float4*>(h_mid + row);
-    for (int s = 0; s < top_k; ++s) {
+    float4 e[KS];
+    float w[KS];
+    bool ok[KS];
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {  // independent loads (the rows of bad ids exist, unused)
         const int64_t p = (int64_t)t * top_k + s;
-        if (ids && !id_valid(ids[p], num_experts)) continue;
-        const float w = weights[p];
-        const float4 e = *reinterpret_cast<const float4*>(expert_out + p * hidden + h4 * 4);
-        acc.x = fmaf(w, e.x, acc.x);
-        acc.y = fmaf(w, e.y, acc.y);
-        acc.z = fmaf(w, e.z, acc.z);
-        acc.w = fmaf(w, e.w, acc.w);
+        ok[s] = s < top_k && (!ids || id_valid(ids[p], num_experts));
+        w[s] = s < top_k ? weights[p] : 0.0f;
+        e[s] = s < top_k ? *reinterpret_cast<const float4*>(expert_out + p * hidden + h4 * 4)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (shared_mode != Q4K_SHARED_NONE) {
-        const float g = shared_mode == Q4K_SHARED_SIGMOID ? 1.0f / (1.0f + expf(-shared_gate[t])) : 1.0f;
-        const float4 so = *reinterpret_cast<const float4*>(shared_out + row);
+    const bool sh = shared_mode != Q4K_SHARED_NONE;
+    const float4 so = sh ? *reinterpret_cast<const float4*>(shared_out + row) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float gl = sh && shared_mode == Q4K_SHARED_SIGMOID ? shared_gate[t] : 0.0f;
+    float4 acc = *reinterpret_cast<const float4*>(h_mid + row);
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+        if (!ok[s]) continue;
+        acc.x = fmaf(w[s], e[s].x, acc.x);
+        acc.y = fmaf(w[s], e[s].y, acc.y);
+        acc.z = fmaf(w[s], e[s].z, acc.z);
+        acc.w = fmaf(w[s], e[s].w, acc.w);
+    }
+    if (sh) {
+        const float g = shared_mode == Q4K_SHARED_SIGMOID ? 1.0f / (1.0f + expf(-gl)) : 1.0f;
         acc.x = fmaf(g, so.x, acc.x);
         acc.y = fmaf(g, so.y, acc.y);
         acc.z = fmaf(g, so.z, acc.z);
@@ -131,7 +145,7 @@ cudaError_t launch_combine(const float* h_mid, const float* expert_out, const fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, h_mid, expert_out, weights, shared_out, shared_gate,
+    return cudaLaunchKernelEx(&cfg, top_k <= 8 ? combine_kernel<8> : combine_kernel<Q4K_MAX_TOP_K>, h_mid, expert_out, weights, shared_out, shared_gate,
                               shared_mode, top_k, hidden, y, ids, num_experts);
 }
 
