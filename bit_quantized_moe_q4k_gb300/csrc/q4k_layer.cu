@@ -30,8 +30,8 @@
 // could hold anything, and every item also publishes a 64-bit tagged flag (a release store)
 // that its readers wait for (acquire) before they read its words. Every wait is bounded in
 // time; one that gives up raises Q4K_ERR_TIMEOUT. The waits need every CTA of the grid
-// resident at once: the grid is capped at what the SMs hold, it is an ordinary launch (it
-// starts on SMs the previous kernel has left), and CTAs never wait on a CTA that is itself
+// resident at once: the grid is capped at what the SMs hold, it is a cooperative launch (the
+// driver starts it only with every CTA resident), and CTAs never wait on a CTA that is itself
 // waiting (gate|up items never wait; down items wait only on gate|up items; a combine waits
 // only on down items).
 #include <algorithm>
@@ -306,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 3) layer_kernel(const __grid_constan
     __shared__ int s_never;                  // (bounded waits take an abort word; never set)
     __shared__ CombineStage s_cbs;           // the inputs of this CTA's combine
 
-    // (launched as an ordinary launch, so earlier kernels of the stream are complete and the
-    // wait returns at once); the next kernel may launch early: it can only take space left
-    // over once every CTA of this grid has started, which the trigger implies
+    // (not launched as a programmatic dependent, so earlier kernels of the stream are complete
+    // and the wait returns at once); the next kernel may launch early: it can only take space
+    // left over once every CTA of this grid has started, which the trigger implies
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1167,10 +1167,23 @@ cudaError_t launch_layer_persistent(const GemvGroup* gu, const GemvGroup* dn, in
     cfg.blockDim = dim3(LP.threads);
     cfg.dynamicSmemBytes = LP.smem;
     cfg.stream = stream;
-    // an ordinary launch: it starts on idle SMs. As a programmatic dependent its CTAs could be
-    // placed beside the previous kernel's last CTAs on SMs configured for a smaller shared-memory
-    // share, which then hold fewer of them than the grid needs resident at once.
-    return cudaLaunchKernelEx(&cfg, LP.kern, P);
+    // A cooperative launch: the driver starts the grid only with every CTA resident at once,
+    // which the waits between CTAs need (the grid is at most what the SMs hold). Not a
+    // programmatic dependent: its CTAs could then be placed beside the previous kernel's last
+    // CTAs on SMs configured for a smaller shared-memory share.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, LP.kern, P);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        // fewer CTAs fit than the occupancy query said (e.g. SMs held by another client): the
+        // caller runs the two-launch layer, which gives the same bits
+        cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    return e;
 }
 
 }  // namespace q4k

@@ -209,9 +209,11 @@ int moe_combine_residual(const float* d_h_mid, const float* d_expert_out, const 
  * generation word that the launch advances, so leftovers of earlier calls (or of
  * anything else) never match; its counters are used only when the previous call on the
  * workspace zeroed them and stamped them with this call's tag (else the call polls flags).
- * Concurrent calls on one workspace race, as with any scratch. After a device error
- * flag Q4K_ERR_TIMEOUT (a bounded wait gave up: the grid could not be resident at
- * once, e.g. under an SM partition) zero the workspace before its next use.
+ * Concurrent calls on one workspace race, as with any scratch. The single launch is a
+ * cooperative launch, so the driver starts it only with every CTA resident; when the
+ * driver refuses that grid (fewer CTAs fit than the occupancy query said, e.g. SMs held by
+ * another client) the call runs the two launches instead. After a device error flag
+ * Q4K_ERR_TIMEOUT (a bounded wait gave up) zero the workspace before its next use.
  */
 int q4k_moe_layer_forward(const void* d_w_gate, const void* d_w_up, const void* d_w_down,
                           int num_experts, const void* d_ws_gate, const void* d_ws_up,
@@ -356,8 +358,8 @@ int q4k_moe_router(const float* d_x, const uint16_t* d_w_router, const float* d_
  *   d_y); d_ids_out / d_weights_out [m, top_k] (both or neither) receive the choice.
  *   A sigmoid-gated shared expert needs d_w_shared_gate.
  * Launches: q4k_moe_router's two, q4k_moe_layer_forward's, then q4k_rms_norm's, each a
- * programmatic dependent of the kernel before it where that is safe (the persistent layer is an
- * ordinary launch); the ids, weights, y and normed are those of the three calls made one after
+ * programmatic dependent of the kernel before it where that is safe (the persistent layer is a
+ * cooperative launch); the ids, weights, y and normed are those of the three calls made one after
  * the other, bit for bit.
  * Workspace: q4k_moe_layer_routed_workspace_size(...) bytes, any contents (as the layer's).
  */
