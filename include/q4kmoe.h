@@ -163,7 +163,9 @@ int q4k_expert_ffn_forward(const void* d_w_gate, const void* d_w_up, const void*
  *   - Limit: m*top_k*inter*4 bytes <= q4k_expert_ffn_noalloc_max_scratch_bytes() (4 MiB);
  *     larger sizes return Q4K_ERR_LIMIT.
  *   - The first call on a device looks up the array's device address (with that device
- *     current) and keeps it; make that first call before any stream capture.
+ *     current) and keeps it; make that first call before any stream capture. A device
+ *     reset (cudaDeviceReset) after that first call is not supported: the kept address
+ *     belongs to the context the reset destroyed.
  *   - Every call on a device shares the array and leaves its contents behind; the call
  *     overwrites all it reads, so nothing needs clearing. Calls that overlap on the GPU
  *     (other streams, other host threads) race on it and must be serialised by the caller.
