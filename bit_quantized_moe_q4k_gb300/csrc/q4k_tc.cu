@@ -490,18 +490,24 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     const int ps = pg & 1;
                     const uint32_t pph = (pg >> 1) & 1;
                     if (!mbar_wait_for(&bar_d_full[ps], pph, &s_abort, P.wait_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    uint32_t d1[kHalfTok], d2[kHalfTok], d3[kHalfTok];
-                    tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kHalfTok * half, d1);
-                    tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kTcTok + kHalfTok * half, d3);
-                    tmem_ld16(tmem + lane_base + kColD2 + ps * 32 + kHalfTok * half, d2);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&bar_d_empty[ps]);
+                    // a chunk of at most 16 tokens leaves the second half's columns unused: its
+                    // warps only hand the accumulators back (uniform per item)
+                    if (kHalfTok * half < it.nt) {
+                        tc_fence_after();
+                        uint32_t d1[kHalfTok], d2[kHalfTok], d3[kHalfTok];
+                        tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kHalfTok * half, d1);
+                        tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kTcTok + kHalfTok * half, d3);
+                        tmem_ld16(tmem + lane_base + kColD2 + ps * 32 + kHalfTok * half, d2);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        mbar_arrive(&bar_d_empty[ps]);
 #pragma unroll
-                    for (int t = 0; t < kHalfTok; ++t)
-                        acc[t] = fmaf(d_prev, __uint_as_float(d1[t]) + __uint_as_float(d3[t]),
-                                      fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[t]));
+                        for (int t = 0; t < kHalfTok; ++t)
+                            acc[t] = fmaf(d_prev, __uint_as_float(d1[t]) + __uint_as_float(d3[t]),
+                                          fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[t]));
+                    } else {
+                        mbar_arrive(&bar_d_empty[ps]);
+                    }
                     if (FUSED && s - 1 == nb - 1) {  // the gate slab is complete
 #pragma unroll
                         for (int t = 0; t < kHalfTok; ++t) { accg[t] = acc[t]; acc[t] = 0.f; }
