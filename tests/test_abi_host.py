@@ -231,3 +231,21 @@ def test_bench_traffic_record_keys_on_code_lines():
     sha = bench.source_sha("layer_kernel")
     assert len(sha) == 16 and sha == bench.source_sha("layer_kernel", read=lambda p: open(
         os.path.join(ROOT, p)).read())
+
+
+def test_bench_reports_a_raised_flag_of_a_secondary_record():
+    """A secondary measurement whose device error flag is raised records the flag's meaning
+    instead of stopping the run; a clear flag records nothing."""
+    import bench
+
+    class Flag:
+        def __init__(self, v):
+            self.v = v
+
+        def item(self):
+            return self.v
+
+    assert bench.flag_error(Flag(0)) is None
+    assert "timeout" in bench.flag_error(Flag(10)) and "10" in bench.flag_error(Flag(10))
+    assert "expert id" in bench.flag_error(Flag(6))
+    assert "see q4kmoe.h" in bench.flag_error(Flag(42))
