@@ -51,13 +51,14 @@ int check_gemv_shape(int num_experts, int m, int top_k, int n, int k) {
 // Tensor-core path policy: experts whose bucket holds at least t pairs run on the tcgen05
 // grouped GEMM (q4k_tc.cu), the others on the id-GEMV kernel, the tensor-core launch first.
 // t is the environment variable Q4K_TC_MIN when set (0 disables the path); otherwise 2 when
-// the batch averages at least two pairs per expert; else 3 with at least 64 experts (about
-// one pair each on average, but routed ids crowd some experts: on the Zipf-distributed
-// Qwen3-like m = 16 layer 94.5 us with 3 against 99.9 / 100.7 / 135 us with 2 / 4 / without
-// the path); else 8 (few experts with about one pair each: the path's two launches find
-// hardly a bucket to take; Mixtral-like m = 4 200 us against 220-265 us with 2-4). A launch
-// uses the path only when some bucket can reach t and the caller's workspace holds the
-// activation images.
+// the batch averages at least two pairs per expert; else, with at least 64 experts (about one
+// pair each on average, but routed ids crowd some experts), 3 for gate|up and 2 for down (the
+// down rows are short, and its buckets of two pairs run better on the tensor cores): on the
+// Zipf-distributed Qwen3-like m = 16 layer 90.6 us against 92.9 us with 3 for both halves and
+// 97.4 us with 2 for both (one GB300); else 8 (few experts with about one pair each: the
+// path's two launches find hardly a bucket to take; Mixtral-like m = 4 200 us against
+// 220-265 us with 2-4). A launch uses the path only when some bucket can reach t and the
+// caller's workspace holds the activation images.
 int tc_min_env() {
     static int v = [] {
         const char* s = getenv("Q4K_TC_MIN");
@@ -66,10 +67,11 @@ int tc_min_env() {
     return v;
 }
 
-int tc_min_for(int routed_pairs, int num_experts) {
+int tc_min_for(int routed_pairs, int num_experts, bool down) {
     if (tc_min_env() >= 0) return tc_min_env();
     if ((int64_t)routed_pairs >= 2 * (int64_t)num_experts) return 2;
-    return num_experts >= 64 ? 3 : 8;
+    if (num_experts >= 64) return down ? 2 : 3;
+    return 8;
 }
 
 // Switch (environment, read at every call): Q4K_SINGLE_LAUNCH=1 runs every layer the single
@@ -96,10 +98,10 @@ bool tc_wanted(int n_pairs, int num_experts, int n_rows, int t) {
 
 // Would the two-launch layer send some bucket of either half to the tensor-core path?
 bool layer_wants_tc(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
-    const int t = tc_min_for(m * top_k, num_experts);
+    const int tg = tc_min_for(m * top_k, num_experts, false), td = tc_min_for(m * top_k, num_experts, true);
     const bool sh = shared_inter > 0;
-    return tc_wanted(m * top_k, num_experts, inter, t) || (sh && tc_wanted(m, 1, shared_inter, t)) ||
-           tc_wanted(m * top_k, num_experts, hidden, t) || (sh && tc_wanted(m, 1, hidden, t));
+    return tc_wanted(m * top_k, num_experts, inter, tg) || (sh && tc_wanted(m, 1, shared_inter, tg)) ||
+           tc_wanted(m * top_k, num_experts, hidden, td) || (sh && tc_wanted(m, 1, hidden, td));
 }
 
 // The two-launch layer fuses the combine into the down launch (the last item of a row tile
@@ -256,7 +258,7 @@ int run_gate_up(const void* w_gate, const void* w_up, int num_experts, const flo
                                   ws_up, shared_inter, act_shared, g);
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
-    const int t = tc_min_for(m * top_k, num_experts);
+    const int t = tc_min_for(m * top_k, num_experts, false);
     if (tc_ws && (tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t)))) {
         tc = t;
         img[0] = tc_ws;
@@ -293,7 +295,7 @@ int run_down(const void* w_down, int num_experts, const float* act, const int32_
     }
     int tc = 0;
     uint8_t* img[2] = {nullptr, nullptr};
-    const int t = tc_min_for(m * top_k, num_experts);
+    const int t = tc_min_for(m * top_k, num_experts, true);
     if (tc_ws && (tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t)))) {
         tc = t;
         img[0] = tc_ws;
@@ -365,9 +367,9 @@ size_t q4k_moe_layer_workspace_size(int m, int top_k, int num_experts, int hidde
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {
     if (m <= 0 || top_k < 1 || num_experts < 1) return 0;
     if (layer_single_launch(m, top_k, num_experts, hidden, inter, shared_inter)) return 1;
-    const int t = tc_min_for(m * top_k, num_experts);
-    const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, t) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, t));
-    const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, t) || (shared_inter > 0 && tc_wanted(m, 1, hidden, t));
+    const int tg = tc_min_for(m * top_k, num_experts, false), td = tc_min_for(m * top_k, num_experts, true);
+    const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, tg) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, tg));
+    const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, td) || (shared_inter > 0 && tc_wanted(m, 1, hidden, td));
     return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0) + (m > kFusedCombineMaxM ? 1 : 0);
 }
 
@@ -421,8 +423,8 @@ int q4k_moe_id_gemv(const void* d_w_stacked, uint64_t w_byte_offset, int num_exp
     uint8_t* img[1] = {static_cast<uint8_t*>(d_workspace)};
     const size_t need = tc_scratch(m * top_k, k);
     if (d_workspace && need > 0 && ws_bytes >= need && (reinterpret_cast<uintptr_t>(d_workspace) & 255) == 0 &&
-        tc_wanted(m * top_k, num_experts, n, tc_min_for(m * top_k, num_experts)))
-        tc = tc_min_for(m * top_k, num_experts);
+        tc_wanted(m * top_k, num_experts, n, tc_min_for(m * top_k, num_experts, false)))
+        tc = tc_min_for(m * top_k, num_experts, false);
     return cuda_status(launch_idgemv(&g, 1, false, false, d_err_flag, stream, tc, img), "id-gemv launch");
 }
 
