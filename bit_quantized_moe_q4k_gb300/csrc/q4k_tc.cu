@@ -220,32 +220,42 @@ __device__ __forceinline__ __half2 hfma2_bits(uint32_t a, __half2 b, __half2 c) 
     return __hfma2(*reinterpret_cast<__half2*>(&a), b, c);
 }
 
-// item -> (expert, tile, chunk, tokens): items of expert e are [start[e]*tiles,
-// (start[e] + chunks_e)*tiles), chunk fastest, so the chunks of one row tile run together
-// and share its weight reads in L2
-struct TcItem { int e, tile, chunk, nt; };
-__device__ __forceinline__ TcItem tc_item(const TcGroup& G, const int* cnt, const int* start, int item) {
+// item -> (expert, tile, first chunk, chunks, tokens of each): an item is a row tile of one
+// expert and CPI consecutive 32-token chunks of its bucket (CPI = 2: a pair, the last pair of an
+// odd count holding one, so each block is dequantized once for up to 64 tokens). Items of expert
+// e are [pstart[e]*tiles, (pstart[e] + groups_e)*tiles), chunk group fastest, so the groups of one
+// row tile run together and share its weight reads in L2.
+struct TcItem { int e, tile, c0, nch, nt0, nt1; };
+template <int CPI>
+__device__ __forceinline__ TcItem tc_item(const TcGroup& G, const int* cnt, const int* pstart, int item) {
     int lo = 0, hi = G.num_experts - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (start[mid] * G.tiles <= item) lo = mid; else hi = mid - 1;
+        if (pstart[mid] * G.tiles <= item) lo = mid; else hi = mid - 1;
     }
     TcItem it;
     it.e = lo;
     const int chunks_e = (cnt[lo] + kTcTok - 1) / kTcTok;
-    const int local = item - start[lo] * G.tiles;
-    it.tile = local / chunks_e;
-    it.chunk = local % chunks_e;
-    it.nt = min(kTcTok, cnt[lo] - it.chunk * kTcTok);
+    const int pairs_e = CPI == 1 ? chunks_e : (chunks_e + 1) / 2;
+    const int local = item - pstart[lo] * G.tiles;
+    it.tile = local / pairs_e;
+    it.c0 = CPI * (local % pairs_e);
+    it.nch = CPI == 1 ? 1 : min(2, chunks_e - it.c0);
+    it.nt0 = min(kTcTok, cnt[lo] - it.c0 * kTcTok);
+    it.nt1 = it.nch > 1 ? min(kTcTok, cnt[lo] - (it.c0 + 1) * kTcTok) : 0;
     return it;
 }
 
 // Persistent: grid = (SMs, groups); each CTA walks items grid-stride. A global step counter
-// (one step = one Q4_K block of one slab) carries the stage index and mbarrier parity
-// across items; tensor memory is allocated once per CTA.
-template <bool FUSED>
+// (one step = one Q4_K block of one slab) carries the A stage index and mbarrier parity
+// across items, an image counter (one per step and chunk) the B stages; tensor memory is
+// allocated once per CTA. The two accumulator slots (D1, D2) serve the two chunks of a pair
+// item, or alternate between the steps of a one-chunk item (double buffering); every role
+// counts the uses of each slot the same way.
+template <bool FUSED, int CPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcParams P) {
+    static_assert(CPI == 1 || CPI == 2, "one or two chunks per item");
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* bimg = smem;                          // kNImg x kImgBlock (1024-byte aligned stages)
@@ -256,15 +266,23 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
     __shared__ uint32_t s_tmem;
     __shared__ int s_warp[33];
     __shared__ int s_bad;
-    __shared__ int s_pairs_w[8][kTcTok];  // each worker warp keeps its own copy (no cross-warp barrier)
+    __shared__ int s_pairs_w[8][CPI * kTcTok];  // each worker warp keeps its own copy (no cross-warp barrier)
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gi = blockIdx.y;
     const TcGroup& G = P.g[gi];
     int* cnt = tabs + P.hist_off[gi];
-    int* start = cnt + G.num_experts;
-    const int total_items = tc_chunks(G, P.tc_min, cnt, start, s_warp, &s_bad) * G.tiles;
+    int* start = cnt + G.num_experts;     // first chunk of each expert (its B images)
+    int* pstart = CPI == 1 ? start : start + G.num_experts;  // first chunk group of each expert (its items)
+    int groups = tc_chunks(G, P.tc_min, cnt, start, s_warp, &s_bad);
+    if constexpr (CPI == 2) {
+        for (int e = tid; e < G.num_experts; e += blockDim.x)
+            pstart[e] = cnt[e] >= P.tc_min ? ((cnt[e] + kTcTok - 1) / kTcTok + 1) / 2 : 0;
+        __syncthreads();
+        groups = block_exclusive_scan(pstart, G.num_experts, s_warp);
+    }
+    const int total_items = groups * G.tiles;
     if ((int)blockIdx.x >= total_items) return;  // uniform per CTA: before any allocation
 
     if (warp == kTcMmaWarp) {
@@ -300,14 +318,15 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
 
     if (warp == kTcCopyWarp) {
         // ---------------- copy producer: raw rows of the tile and the block's B image
-        int gs = 0;  // global step
         int raw_issued = 0, b_issued = 0;
         bool ok = true;
+        if constexpr (CPI == 1) {
+        int gs = 0;  // global step
         for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
-            const TcItem it = tc_item(G, cnt, start, item);
+            const TcItem it = tc_item<CPI>(G, cnt, pstart, item);
             const int row0 = it.tile * kTcRows;
             const int rows_valid = min(kTcRows, G.n - row0);
-            const uint8_t* img = G.img + (int64_t)(start[it.e] + it.chunk) * nb * kImgBlock;
+            const uint8_t* img = G.img + (int64_t)(start[it.e] + it.c0) * nb * kImgBlock;
             for (int s = 0; s < steps; ++s, ++gs) {
                 const int rst = gs % kNRaw;
                 const uint32_t rph = (gs / kNRaw) & 1;
@@ -337,6 +356,45 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 b_issued = gs + 1;
             }
         }
+        } else {
+        int gs = 0, gimg = 0;  // global step, global image
+        for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
+            const TcItem it = tc_item<CPI>(G, cnt, pstart, item);
+            const int row0 = it.tile * kTcRows;
+            const uint8_t* img = G.img + (int64_t)(start[it.e] + it.c0) * nb * kImgBlock;
+            for (int s = 0; s < steps && ok; ++s, ++gs) {
+                const int rst = gs % kNRaw;
+                const uint32_t rph = (gs / kNRaw) & 1;
+                const int slab = s / nb, b = s % nb;
+                int okl = 1;
+                if (lane == 0) {
+                    okl = mbar_wait_for(&bar_raw_empty[rst], rph ^ 1, &s_abort, P.wait_ns);
+                    if (okl) {
+                        // one tensor load: 128 rows x 144 bytes of block b (rows past the slab read as zero)
+                        mbar_arrive_expect_tx(&bar_raw_full[rst], kRawStage);
+                        tma_load_2d(raw + rst * kRawStage, &P.tmap[gi][slab], b * kBlockBytes, it.e * G.n + row0,
+                                    &bar_raw_full[rst]);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+                raw_issued = gs + 1;
+                for (int c = 0; c < it.nch; ++c, ++gimg) {  // the block's B image of each chunk
+                    const int bst = gimg % kNImg;
+                    const uint32_t bph = (gimg / kNImg) & 1;
+                    if (lane == 0) {
+                        okl = mbar_wait_for(&bar_b_empty[bst], bph ^ 1, &s_abort, P.wait_ns);
+                        if (okl) {
+                            mbar_arrive_expect_tx(&bar_b_full[bst], kImgBlock);
+                            bulk_g2s(bimg + bst * kImgBlock, img + ((int64_t)c * nb + b) * kImgBlock, kImgBlock,
+                                     &bar_b_full[bst]);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+                    b_issued = gimg + 1;
+                }
+            }
+        }
+        }
         if (!ok && lane == 0) {
             // let the copies already issued land before the CTA leaves (bounded)
             volatile int never = 0;
@@ -353,8 +411,10 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         const uint32_t idesc_min = idesc_f16_f32(kTcRows, kTcTok);
         const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
         const uint32_t bimg_addr = __shfl_sync(0xffffffffu, smem_u32(bimg), 0);
-        int gs = 0, issued = 0;
         bool ok = true;
+        int issued = 0;
+        if constexpr (CPI == 1) {
+        int gs = 0;
         for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
             for (int s = 0; s < steps; ++s, ++gs) {
                 const int st = gs & 1;
@@ -384,6 +444,52 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                 issued = gs + 1;
             }
         }
+        } else {
+        int gs = 0, gimg = 0;
+        int rr = 0, use0 = 0, use1 = 0;  // slot of the next one-chunk step; uses of each slot
+        for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
+            const TcItem it = tc_item<CPI>(G, cnt, pstart, item);
+            for (int s = 0; s < steps && ok; ++s, ++gs) {
+                const int st = gs & 1;
+                const uint32_t ph = (gs >> 1) & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait_for(&bar_a_full[st], ph, &s_abort, P.wait_ns))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a0 = tm + kColA + st * 128;
+                for (int c = 0; c < it.nch; ++c, ++gimg) {
+                    const int slot = it.nch == 2 ? c : rr;
+                    const int bst = gimg % kNImg;
+                    const uint32_t bph = (gimg / kNImg) & 1;
+                    const bool got = mbar_wait_for(&bar_b_full[bst], bph, &s_abort, P.wait_ns) &&
+                                     mbar_wait_for(&bar_d_empty[slot], ((slot ? use1 : use0) & 1) ^ 1, &s_abort,
+                                                   P.wait_ns);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // one descriptor per image; the k steps add constant offsets to its address field
+                    const uint64_t bdesc = desc_sw128_kmajor(bimg_addr + bst * kImgBlock);
+                    const uint32_t d1 = tm + kColD1 + slot * 64;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kPanel + (kk & 3) * 32;
+                        mma_f16_ts_elect(d1, a0 + 8 * kk, bdesc + (koff >> 4), idesc, kk > 0);
+                    }
+                    mma_f16_ts_elect(tm + kColD2 + slot * 32, tm + kColA2 + st * 16, bdesc + (kImgMin >> 4),
+                                     idesc_min, 0);
+                    mma_commit_elect(&bar_b_empty[bst]);
+                    mma_commit_elect(&bar_d_full[slot]);
+                    if (slot) ++use1; else ++use0;
+                    issued = 1;
+                }
+                if (!ok) break;
+                if (it.nch == 1) rr ^= 1;
+                mma_commit_elect(&bar_a_empty[st]);
+            }
+        }
+        }
         if (!ok) {
             if (lane == 0) {
                 s_abort = 1;
@@ -403,18 +509,23 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         constexpr int kHalfTok = kTcTok / 2;
         int gs = 0;
+        int rr = 0, use0 = 0, use1 = 0;  // the same slot bookkeeping as the MMA issuer
         bool ok = true;
         for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
-            const TcItem it = tc_item(G, cnt, start, item);
+            const TcItem it = tc_item<CPI>(G, cnt, pstart, item);
             const int row0 = it.tile * kTcRows;
             const int rows_valid = min(kTcRows, G.n - row0);
-            int* s_pairs = s_pairs_w[warp];
+            const int ntc[2] = {it.nt0, it.nt1};
+            int* s_pairs = s_pairs_w[warp];  // chunk c's pairs at s_pairs[32 c ..]
             __syncwarp();  // this warp's previous outputs are written
-            tc_gather(G, it.e, it.chunk, it.nt, s_pairs);
+            tc_gather(G, it.e, it.c0, it.nt0, s_pairs);
+            if (CPI > 1 && it.nch > 1) tc_gather(G, it.e, it.c0 + 1, it.nt1, s_pairs + (CPI - 1) * kTcTok);
             __syncwarp();
-            float acc[kHalfTok], accg[kHalfTok];
+            float acc[2][kHalfTok], accg[2][kHalfTok];
 #pragma unroll
-            for (int t = 0; t < kHalfTok; ++t) { acc[t] = 0.f; accg[t] = 0.f; }
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int t = 0; t < kHalfTok; ++t) { acc[c][t] = 0.f; accg[c][t] = 0.f; }
             float d_prev = 0.f, dmin_prev = 0.f;
             for (int s = 0; s <= steps; ++s) {
                 const int g_cur = gs + s;
@@ -484,7 +595,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     tc_fence_before();
                     mbar_arrive(&bar_a_full[st]);
                 }
-                if (s >= 1) {
+                if (CPI == 1 && s >= 1) {
                     // epilogue of step s-1 for this half's tokens: acc += d * (D1 hi + D1 lo) - dmin * D2
                     const int pg = g_cur - 1;
                     const int ps = pg & 1;
@@ -492,7 +603,7 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                     if (!mbar_wait_for(&bar_d_full[ps], pph, &s_abort, P.wait_ns)) { ok = false; break; }
                     // a chunk of at most 16 tokens leaves the second half's columns unused: its
                     // warps only hand the accumulators back (uniform per item)
-                    if (kHalfTok * half < it.nt) {
+                    if (kHalfTok * half < it.nt0) {
                         tc_fence_after();
                         uint32_t d1[kHalfTok], d2[kHalfTok], d3[kHalfTok];
                         tmem_ld16(tmem + lane_base + kColD1 + ps * 64 + kHalfTok * half, d1);
@@ -503,14 +614,54 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
                         mbar_arrive(&bar_d_empty[ps]);
 #pragma unroll
                         for (int t = 0; t < kHalfTok; ++t)
-                            acc[t] = fmaf(d_prev, __uint_as_float(d1[t]) + __uint_as_float(d3[t]),
-                                          fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[t]));
+                            acc[0][t] = fmaf(d_prev, __uint_as_float(d1[t]) + __uint_as_float(d3[t]),
+                                             fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[0][t]));
                     } else {
                         mbar_arrive(&bar_d_empty[ps]);
                     }
                     if (FUSED && s - 1 == nb - 1) {  // the gate slab is complete
 #pragma unroll
-                        for (int t = 0; t < kHalfTok; ++t) { accg[t] = acc[t]; acc[t] = 0.f; }
+                        for (int t = 0; t < kHalfTok; ++t) { accg[0][t] = acc[0][t]; acc[0][t] = 0.f; }
+                    }
+                }
+                if (CPI == 2 && s >= 1) {
+                    // epilogue of step s-1 for this half's tokens of each chunk:
+                    // acc += d * (D1 hi + D1 lo) - dmin * D2
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        if (c >= it.nch) break;
+                        const int slot = it.nch == 2 ? c : rr;
+                        if (!mbar_wait_for(&bar_d_full[slot], (slot ? use1 : use0) & 1, &s_abort, P.wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        // a chunk of at most 16 tokens leaves the second half's columns unused:
+                        // its warps only hand the accumulators back (uniform per item)
+                        if (kHalfTok * half < ntc[c]) {
+                            tc_fence_after();
+                            uint32_t d1[kHalfTok], d2[kHalfTok], d3[kHalfTok];
+                            tmem_ld16(tmem + lane_base + kColD1 + slot * 64 + kHalfTok * half, d1);
+                            tmem_ld16(tmem + lane_base + kColD1 + slot * 64 + kTcTok + kHalfTok * half, d3);
+                            tmem_ld16(tmem + lane_base + kColD2 + slot * 32 + kHalfTok * half, d2);
+                            tmem_wait_ld();
+                            tc_fence_before();
+                            mbar_arrive(&bar_d_empty[slot]);
+#pragma unroll
+                            for (int t = 0; t < kHalfTok; ++t)
+                                acc[c][t] = fmaf(d_prev, __uint_as_float(d1[t]) + __uint_as_float(d3[t]),
+                                                 fmaf(-dmin_prev, __uint_as_float(d2[t]), acc[c][t]));
+                        } else {
+                            mbar_arrive(&bar_d_empty[slot]);
+                        }
+                        if (slot) ++use1; else ++use0;
+                    }
+                    if (!ok) break;
+                    if (it.nch == 1) rr ^= 1;
+                    if (FUSED && s - 1 == nb - 1) {  // the gate slab is complete
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int t = 0; t < kHalfTok; ++t) { accg[c][t] = acc[c][t]; acc[c][t] = 0.f; }
                     }
                 }
                 d_prev = d_cur;
@@ -520,12 +671,15 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
             gs += steps;
             if (r < rows_valid) {
 #pragma unroll
-                for (int j = 0; j < kHalfTok; ++j) {
-                    const int t = kHalfTok * half + j;
-                    if (t < it.nt) {
-                        float v = acc[j];
-                        if (FUSED) v = (accg[j] / (1.0f + __expf(-accg[j]))) * acc[j];
-                        G.out[(int64_t)s_pairs[t] * G.n + row0 + r] = v;
+                for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                    for (int j = 0; j < kHalfTok; ++j) {
+                        const int t = kHalfTok * half + j;
+                        if (c < it.nch && t < ntc[c]) {
+                            float v = acc[c][j];
+                            if (FUSED) v = (accg[c][j] / (1.0f + __expf(-accg[c][j]))) * acc[c][j];
+                            G.out[(int64_t)s_pairs[kTcTok * c + t] * G.n + row0 + r] = v;
+                        }
                     }
                 }
             }
@@ -551,7 +705,7 @@ size_t tc_image_bytes(int n_pairs, int k, int tc_min) {
     return (size_t)tc_max_chunks(n_pairs, tc_min) * (size_t)(k / kQK) * kImgBlock;
 }
 
-static bool g_tc_attr_set[2][64] = {};
+static bool g_tc_attr_set[4][64] = {};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -584,9 +738,19 @@ static cudaError_t encode_slab_map(CUtensorMap* map, const uint8_t* w, int num_e
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Whether a launch works on chunk pairs: the routed batch averages at least two 32-token chunks
+// per expert (every group).
+static bool tc_pairs(const GemvGroup* groups, int n_groups) {
+    bool pairs = true;
+    for (int gi = 0; gi < n_groups; ++gi)
+        pairs = pairs && (int64_t)groups[gi].m * groups[gi].top_k >= (int64_t)2 * kTcTok * groups[gi].num_experts;
+    return pairs;
+}
+
 bool tc_fits(const GemvGroup* groups, int n_groups) {
     int ints = 0;
-    for (int gi = 0; gi < n_groups; ++gi) ints += 2 * groups[gi].num_experts;
+    const int per_expert = tc_pairs(groups, n_groups) ? 3 : 2;  // cnt, start[, pstart]
+    for (int gi = 0; gi < n_groups; ++gi) ints += per_expert * groups[gi].num_experts;
     return 1024 + (size_t)(kNImg * kImgBlock + kNRaw * kRawStage) + (size_t)ints * 4 <= 200 * 1024;
 }
 
@@ -597,6 +761,9 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
     P.tc_min = tc_min;
     P.err_flag = err_flag;
     P.wait_ns = wait_limit_ns();
+    // two 32-token chunks per item (one dequantization of each block for both) when the
+    // routed batch averages at least two chunks per expert; else one
+    const bool pairs = tc_pairs(groups, n_groups);
     int ints = 0;
     int64_t max_chunks = 0;
     int max_tiles = 0;
@@ -610,7 +777,7 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
         G.num_experts = S.num_experts; G.n_pairs = S.m * S.top_k; G.top_k = S.top_k; G.n = S.n; G.k = S.k;
         G.tiles = (S.n + kTcRows - 1) / kTcRows;
         P.hist_off[gi] = ints;
-        ints += 2 * S.num_experts;
+        ints += (pairs ? 3 : 2) * S.num_experts;  // cnt, start (chunks)[, pstart (chunk pairs)]
         cudaError_t me = encode_slab_map(&P.tmap[gi][0], S.w, S.num_experts, S.n, G.nb01);
         if (me == cudaSuccess && fused) me = encode_slab_map(&P.tmap[gi][1], S.w2, S.num_experts, S.n, G.nb01);
         if (me != cudaSuccess) return me;
@@ -647,12 +814,14 @@ cudaError_t launch_tc(const GemvGroup* groups, int n_groups, bool fused, int tc_
     size_t smem = 1024 + (size_t)P.tab_off + (size_t)ints * 4;
     if (smem < 120 * 1024) smem = 120 * 1024;
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    auto kern = fused ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+    void (*kern)(TcParams) = fused ? (pairs ? tc_gemm_kernel<true, 2> : tc_gemm_kernel<true, 1>)
+                                   : (pairs ? tc_gemm_kernel<false, 2> : tc_gemm_kernel<false, 1>);
+    const int kind = (fused ? 1 : 0) + (pairs ? 2 : 0);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!g_tc_attr_set[fused ? 1 : 0][dev]) {
+    if (!g_tc_attr_set[kind][dev]) {
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (err != cudaSuccess) return err;
-        g_tc_attr_set[fused ? 1 : 0][dev] = true;
+        g_tc_attr_set[kind][dev] = true;
     }
     if (smem > 200 * 1024) return cudaErrorInvalidValue;
     int64_t grid = (int64_t)max_chunks * max_tiles;
