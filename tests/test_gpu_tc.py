@@ -41,7 +41,10 @@ def _gemv(w, E, a, outer, inner, ids, m, T, n, k, workspace):
 @pytest.mark.parametrize("E,n,k,m,T", [(32, 2048, 512, 48, 4),   # ~6 pairs per expert: small buckets
                                        (4, 2148, 512, 64, 2),    # ~32 pairs per expert, ragged last row tile
                                        (2, 4096, 1024, 40, 2),   # 40 pairs per expert: 2 chunks
-                                       (3, 3072, 256, 70, 1)])   # one block per row
+                                       (3, 3072, 256, 70, 1),    # one block per row
+                                       # 80 pairs per expert (chunks of 32, 32, 16): items of a
+                                       # chunk pair, then of one chunk
+                                       (2, 2048, 512, 80, 2)])
 def test_tc_id_gemv_matches_oracle(mode, E, n, k, m, T):
     seed = 500 + n + k
     w = oracle_slab(seed, "tc", E, n, k)
@@ -89,6 +92,27 @@ def test_tc_ffn_fused_gate_up_matches_oracle():
     got = host(out)
     assert int(host(f)[0]) == 0
     rows_close(got, ref, what="tc ffn")
+
+
+def test_tc_ffn_fused_gate_up_chunk_pairs_match_oracle():
+    """Buckets averaging two or more 32-token chunks: the gate|up GEMM runs items of chunk pairs
+    (each block dequantized once for both chunks); 80 pairs per expert make a pair and a lone
+    chunk of 16 tokens."""
+    E, H, I, m, T = 2, 512, 2048, 80, 2
+    seed = 631
+    wg, wu = oracle_slab(seed, "gate", E, I, H), oracle_slab(seed, "up", E, I, H)
+    wd = oracle_slab(seed, "down", E, H, I)
+    ids = inputs.ids_uniform_distinct(seed, m, T, E)
+    x = inputs.normal(seed, "h_post", (m, H))
+    ref, _ = oracle.expert_ffn(wg, wu, wd, E, x, ids, m, T, H, I)
+    nbytes = q4k.q4k_moe_workspace_size(m, T, E, max(H, I), max(H, I))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((m * T, H), dtype=torch.float32, device="cuda")
+    f = err_flag()
+    q4k.q4k_expert_ffn_forward(dev(wg), dev(wu), dev(wd), E, dev(x), dev(ids), m, T, H, I, out, ws, nbytes, f)
+    got = host(out)
+    assert int(host(f)[0]) == 0
+    rows_close(got, ref, what="tc ffn, chunk pairs")
 
 
 def test_tc_layer_shared_expert_takes_tensor_cores():
