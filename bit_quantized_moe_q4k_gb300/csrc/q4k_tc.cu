@@ -5,6 +5,8 @@
 // contraction per (expert, 128-row tile, chunk of 32 tokens of the expert's bucket):
 //   D[r, t] = sum_k A[r, k] * B[t, k]
 // with A in tensor memory and B in shared memory (tcgen05.mma, kind::f16, fp32 accumulation).
+// When the batch averages at least two chunks per expert, a work item takes two chunks of one
+// row tile, and each block's A serves the MMAs of both.
 //
 // Exactness of the operands. Q4_K gives per 32-weight sub-block j of a 256-weight block
 //   sum_k w_k x_k = d * sum_j sc_j sum_{k in j} q_k x_k  -  dmin * sum_j m_j sum_{k in j} x_k.
