@@ -415,6 +415,8 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         const uint32_t bimg_addr = __shfl_sync(0xffffffffu, smem_u32(bimg), 0);
         bool ok = true;
         int issued = 0;
+        // One chunk per item keeps its own loop (stage = step parity for A, B and D alike): run
+        // through the pair loop below, the same one-chunk items took measurably longer.
         if constexpr (CPI == 1) {
         int gs = 0;
         for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
