@@ -370,7 +370,9 @@ int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, in
     const int tg = tc_min_for(m * top_k, num_experts, false), td = tc_min_for(m * top_k, num_experts, true);
     const bool tc_gu = tc_wanted(m * top_k, num_experts, inter, tg) || (shared_inter > 0 && tc_wanted(m, 1, shared_inter, tg));
     const bool tc_dn = tc_wanted(m * top_k, num_experts, hidden, td) || (shared_inter > 0 && tc_wanted(m, 1, hidden, td));
-    return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0) + (m > kFusedCombineMaxM ? 1 : 0);
+    // the down rows' pre-staging (a launch between the halves) for rows of kPrestageMinK or more
+    const bool pre = inter >= kPrestageMinK || (shared_inter > 0 && shared_inter >= kPrestageMinK);
+    return 2 + (tc_gu ? 2 : 0) + (tc_dn ? 2 : 0) + (pre ? 1 : 0) + (m > kFusedCombineMaxM ? 1 : 0);
 }
 
 int q4k_moe_layer_path(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter) {

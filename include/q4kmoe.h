@@ -252,7 +252,8 @@ size_t q4k_moe_layer_half_workspace_size(int m, int top_k, int k_routed, int sha
 
 /* Number of kernels one q4k_moe_layer_forward call with its full workspace launches for these
  * sizes on the current device (1 for the single-launch layer; else 2, plus 2 per half that
- * takes the tensor-core path, plus 1 for the combine beyond 4 tokens). 0 on invalid sizes. */
+ * takes the tensor-core path, plus 1 for the pre-staging of down rows of 4096 or more
+ * elements, plus 1 for the combine beyond 4 tokens). 0 on invalid sizes. */
 int q4k_moe_layer_launch_count(int m, int top_k, int num_experts, int hidden, int inter, int shared_inter);
 
 /* Which kernels one q4k_moe_layer_forward call runs for these sizes on the current device

@@ -192,7 +192,8 @@ def test_layer_launch_count_single_launch_rule(monkeypatch):
     assert lib.q4k_moe_layer_launch_count(4, 8, 128, 2048, 768, 768) == 1   # 32 pairs
     assert lib.q4k_moe_layer_launch_count(5, 8, 128, 2048, 768, 768) == 3   # 40 pairs (+ the combine)
     assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 1     # Mixtral-like decode
-    assert lib.q4k_moe_layer_launch_count(16, 2, 8, 4096, 14336, 0) == 7    # tensor-core buckets + combine
+    assert lib.q4k_moe_layer_launch_count(16, 2, 8, 4096, 14336, 0) == 8    # tensor-core buckets, pre-staged
+                                                                             # down rows, combine
     assert lib.q4k_moe_layer_launch_count(4, 2, 8, 4096, 14336, 0) == 1     # one pair per expert: no TC bucket
     assert lib.q4k_moe_layer_launch_count(33, 1, 4, 256, 256, 256) == 3     # a 33-pair shared expert
     with_flags = lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768)
@@ -202,7 +203,8 @@ def test_layer_launch_count_single_launch_rule(monkeypatch):
     assert lib.q4k_moe_layer_workspace_size(1, 8, 128, 2048, 768, 768) == with_flags
     monkeypatch.delenv("Q4K_SINGLE_LAUNCH", raising=False)
     assert lib.q4k_moe_layer_launch_count(1, 8, 128, 2048, 768, 768) in (1, 2)
-    assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 2     # 3584 gate|up row tiles
+    assert lib.q4k_moe_layer_launch_count(1, 2, 8, 4096, 14336, 0) == 3     # 3584 gate|up row tiles:
+                                                                             # gate|up, pre-staging, down
     # the activations and expert outputs, plus the generation word and 1024 start tags
     assert with_flags >= (8 * 768 + 768 + 8 * 2048 + 2048) * 4 + 8 * (1 + 1024)
 
