@@ -327,7 +327,6 @@ tc_gemm_kernel(const __grid_constant__ TcParams P) {
         for (int item = blockIdx.x; item < total_items && ok; item += gridDim.x) {
             const TcItem it = tc_item<CPI>(G, cnt, pstart, item);
             const int row0 = it.tile * kTcRows;
-            const int rows_valid = min(kTcRows, G.n - row0);
             const uint8_t* img = G.img + (int64_t)(start[it.e] + it.c0) * nb * kImgBlock;
             for (int s = 0; s < steps; ++s, ++gs) {
                 const int rst = gs % kNRaw;
